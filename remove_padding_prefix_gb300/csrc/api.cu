@@ -1,0 +1,621 @@
+// The C ABI (include/rpp.h): argument validation, prepared-weight layouts, workspace
+// carving and the orchestration of the per-step kernels.  Host code here launches
+// kernels only; it never allocates, synchronises (except rpp_get_device_error) or
+// reads device data, so call sequences are graph-capturable.
+#include <cstring>
+
+#include "kernels.h"
+
+namespace rpp {
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  if (!cached[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+
+inline int esize(rpp_dtype dt) { return dt == RPP_F32 ? 4 : (dt == RPP_I8 ? 1 : 2); }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline rpp_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return RPP_OK;
+  cudaGetLastError();   // clear a sticky launch-configuration error
+  if (e == cudaErrorNotSupported) return RPP_EUNSUPPORTED;
+  if (e == cudaErrorInvalidValue) return RPP_EINVAL;
+  return RPP_ECUDA;
+}
+
+#define RPP_TRY(expr)                         \
+  do {                                        \
+    const rpp_status st_ = from_cuda(expr);   \
+    if (st_ != RPP_OK) return st_;            \
+  } while (0)
+
+// ---------------------------------------------------------------- prepared encoder layer
+struct LayerLayout {
+  size_t wqkv, wo, w1, w2;           // K-major weights (dtype, or bf16-held int8 codes)
+  size_t bqkv, bo, b1, b2;           // fp32
+  size_t g1, be1, g2, be2;           // fp32
+  size_t sqkv, so, s1, s2;           // fp32 per-channel weight scales (int8)
+  size_t total;
+};
+
+bool encoder_cfg_ok(const rpp_encoder_cfg* c) {
+  if (!c) return false;
+  if (c->hidden <= 0 || c->heads <= 0 || c->ffn <= 0 || c->head_dim <= 0) return false;
+  if (c->heads * c->head_dim != c->hidden) return false;
+  if (c->dtype != RPP_F32 && c->dtype != RPP_F16 && c->dtype != RPP_BF16) return false;
+  if (c->int8 && c->dtype != RPP_F16) return false;
+  return true;
+}
+
+rpp_status encoder_cfg_supported(const rpp_encoder_cfg* c) {
+  if (!encoder_cfg_ok(c)) return RPP_EINVAL;
+  const int H = c->hidden, F = c->ffn;
+  if (c->head_dim != 64) return RPP_EUNSUPPORTED;
+  const rpp_dtype dt = static_cast<rpp_dtype>(c->dtype);
+  if (!layernorm_supported(H, dt)) return RPP_EUNSUPPORTED;
+  if (dt == RPP_F32) {
+    if (H % 4 || F % 4) return RPP_EUNSUPPORTED;
+  } else {
+    if (!gemm_tc_supported(3 * H, H) || !gemm_tc_supported(H, H) || !gemm_tc_supported(F, H) ||
+        !gemm_tc_supported(H, F))
+      return RPP_EUNSUPPORTED;
+    if (c->int8 && F > 4096) return RPP_EUNSUPPORTED;
+  }
+  return RPP_OK;
+}
+
+LayerLayout layer_layout(const rpp_encoder_cfg* c) {
+  LayerLayout L{};
+  const size_t H = c->hidden, F = c->ffn;
+  const size_t e = c->int8 ? 2 : esize(static_cast<rpp_dtype>(c->dtype));
+  size_t o = 0;
+  L.wqkv = o; o = align_up(o + 3 * H * H * e);
+  L.wo = o;   o = align_up(o + H * H * e);
+  L.w1 = o;   o = align_up(o + F * H * e);
+  L.w2 = o;   o = align_up(o + H * F * e);
+  L.bqkv = o; o = align_up(o + 3 * H * 4);
+  L.bo = o;   o = align_up(o + H * 4);
+  L.b1 = o;   o = align_up(o + F * 4);
+  L.b2 = o;   o = align_up(o + H * 4);
+  L.g1 = o;   o = align_up(o + H * 4);
+  L.be1 = o;  o = align_up(o + H * 4);
+  L.g2 = o;   o = align_up(o + H * 4);
+  L.be2 = o;  o = align_up(o + H * 4);
+  if (c->int8) {
+    L.sqkv = o; o = align_up(o + 3 * H * 4);
+    L.so = o;   o = align_up(o + H * 4);
+    L.s1 = o;   o = align_up(o + F * 4);
+    L.s2 = o;   o = align_up(o + H * 4);
+  }
+  L.total = o;
+  return L;
+}
+
+struct EncWs {
+  size_t qkv, attn, h, x1, g, cx, ca, cx1, cg, total;
+};
+
+EncWs enc_ws_layout(const rpp_encoder_cfg* c, int T_max) {
+  EncWs w{};
+  const size_t T = T_max, H = c->hidden, F = c->ffn;
+  const size_t e = esize(static_cast<rpp_dtype>(c->dtype));
+  size_t o = 0;
+  w.qkv = o;  o = align_up(o + T * 3 * H * e);
+  w.attn = o; o = align_up(o + T * H * e);
+  w.h = o;    o = align_up(o + T * H * e);
+  w.x1 = o;   o = align_up(o + T * H * e);
+  w.g = o;    o = align_up(o + T * F * e);
+  if (c->int8) {   // bf16-held int8 codes of the four GEMM inputs
+    w.cx = o;  o = align_up(o + T * H * 2);
+    w.ca = o;  o = align_up(o + T * H * 2);
+    w.cx1 = o; o = align_up(o + T * H * 2);
+    w.cg = o;  o = align_up(o + T * F * 2);
+  }
+  w.total = o;
+  return w;
+}
+
+template <typename P>
+inline P* at(void* base, size_t off) {
+  return reinterpret_cast<P*>(static_cast<uint8_t*>(base) + off);
+}
+template <typename P>
+inline const P* at(const void* base, size_t off) {
+  return reinterpret_cast<const P*>(static_cast<const uint8_t*>(base) + off);
+}
+
+// one GEMM of the float path: tensor cores for fp16 / bf16, CUDA cores for fp32
+cudaError_t linear(rpp_dtype dt, const void* a, const void* w_t, const float* bias, const void* residual, void* out,
+                   int M_max, const int32_t* rows, int N, int K, int epi, int32_t* err, cudaStream_t s) {
+  if (dt == RPP_F32)
+    return launch_gemm_f32(static_cast<const float*>(a), static_cast<const float*>(w_t), bias,
+                           static_cast<const float*>(residual), static_cast<float*>(out), M_max, rows, N, K, epi, err,
+                           s);
+  TcGemmArgs g{};
+  g.a = a; g.w_t = w_t; g.bias = bias; g.residual = residual; g.out = out;
+  g.M_max = M_max; g.rows = rows; g.N = N; g.K = K;
+  g.in_dtype = dt; g.out_dtype = dt; g.epi = epi; g.err = err;
+  return launch_gemm_tc(g, s);
+}
+
+// one GEMM of the int8 path (bf16-held codes in, fp16 / codes out)
+cudaError_t linear_i8(const void* a_codes, const void* w_codes, const float* bias, const float* a_scale,
+                      const float* w_scale, const float* q_scale, const void* residual, void* out, rpp_dtype out_dt,
+                      int M_max, const int32_t* rows, int N, int K, int epi, int32_t* err, cudaStream_t s) {
+  TcGemmArgs g{};
+  g.a = a_codes; g.w_t = w_codes; g.bias = bias; g.residual = residual; g.out = out;
+  g.M_max = M_max; g.rows = rows; g.N = N; g.K = K;
+  g.in_dtype = RPP_BF16; g.out_dtype = out_dt; g.epi = epi;
+  g.a_scale = a_scale; g.w_scale = w_scale; g.q_scale = q_scale; g.err = err;
+  return launch_gemm_tc(g, s);
+}
+
+rpp_status encoder_layer_run(const rpp_encoder_cfg* c, const void* layer, const float* act_scales, const void* x,
+                             const int32_t* cu, int B, int T_max, int max_len, void* y, void* ws, size_t ws_bytes,
+                             float* amax, int32_t* err, cudaStream_t s) {
+  rpp_status st = encoder_cfg_supported(c);
+  if (st != RPP_OK) return st;
+  if (!layer || !x || !cu || !y || !ws || B <= 0 || T_max <= 0 || max_len <= 0) return RPP_EINVAL;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(ws) || !aligned16(layer)) return RPP_EINVAL;
+  if (c->int8 && !act_scales) return RPP_EINVAL;
+  const EncWs W = enc_ws_layout(c, T_max);
+  if (ws_bytes < W.total) return RPP_EWORKSPACE;
+  const LayerLayout P = layer_layout(c);
+  const rpp_dtype dt = static_cast<rpp_dtype>(c->dtype);
+  const int H = c->hidden, F = c->ffn, nh = c->heads, d = c->head_dim;
+  const int32_t* rows = cu + B;   // T lives in device memory
+  void* qkv = at<void>(ws, W.qkv);
+  void* attn = at<void>(ws, W.attn);
+  void* h = at<void>(ws, W.h);
+  void* x1 = at<void>(ws, W.x1);
+  void* g = at<void>(ws, W.g);
+  const float* bqkv = at<float>(layer, P.bqkv);
+  const float* bo = at<float>(layer, P.bo);
+  const float* b1 = at<float>(layer, P.b1);
+  const float* b2 = at<float>(layer, P.b2);
+  const float* g1 = at<float>(layer, P.g1);
+  const float* be1 = at<float>(layer, P.be1);
+  const float* g2 = at<float>(layer, P.g2);
+  const float* be2 = at<float>(layer, P.be2);
+
+  if (!c->int8) {
+    if (amax) RPP_TRY(launch_amax(x, T_max, rows, H, dt, amax + 0, err, s));
+    RPP_TRY(linear(dt, x, at<void>(layer, P.wqkv), bqkv, nullptr, qkv, T_max, rows, 3 * H, H, RPP_EPI_BIAS, err, s));
+    RPP_TRY(launch_attention_varlen(qkv, cu, B, T_max, max_len, nh, d, dt, attn, err, s));
+    if (amax) RPP_TRY(launch_amax(attn, T_max, rows, H, dt, amax + 1, err, s));
+    RPP_TRY(linear(dt, attn, at<void>(layer, P.wo), bo, x, h, T_max, rows, H, H, RPP_EPI_BIAS_RESIDUAL, err, s));
+    RPP_TRY(launch_layernorm(h, g1, be1, x1, T_max, rows, H, c->eps, dt, nullptr, nullptr, amax ? amax + 2 : nullptr,
+                             err, s));
+    RPP_TRY(linear(dt, x1, at<void>(layer, P.w1), b1, nullptr, g, T_max, rows, F, H, RPP_EPI_BIAS_GELU, err, s));
+    if (amax) RPP_TRY(launch_amax(g, T_max, rows, F, dt, amax + 3, err, s));
+    RPP_TRY(linear(dt, g, at<void>(layer, P.w2), b2, x1, h, T_max, rows, H, F, RPP_EPI_BIAS_RESIDUAL, err, s));
+    RPP_TRY(launch_layernorm(h, g2, be2, y, T_max, rows, H, c->eps, dt, nullptr, nullptr, nullptr, err, s));
+    return RPP_OK;
+  }
+  // int8: quantise -> int8 GEMM (exact integer accumulation) -> dequantise in the epilogue
+  void* cx = at<void>(ws, W.cx);
+  void* ca = at<void>(ws, W.ca);
+  void* cx1 = at<void>(ws, W.cx1);
+  void* cg = at<void>(ws, W.cg);
+  const float* s0 = act_scales + 0;
+  const float* s1 = act_scales + 1;
+  const float* s2 = act_scales + 2;
+  const float* s3 = act_scales + 3;
+  RPP_TRY(launch_quantize_codes_bf16(x, s0, cx, T_max, rows, H, dt, err, s));
+  RPP_TRY(linear_i8(cx, at<void>(layer, P.wqkv), bqkv, s0, at<float>(layer, P.sqkv), nullptr, nullptr, qkv, dt, T_max,
+                    rows, 3 * H, H, EPI_DQ_BIAS, err, s));
+  RPP_TRY(launch_attention_varlen(qkv, cu, B, T_max, max_len, nh, d, dt, attn, err, s));
+  RPP_TRY(launch_quantize_codes_bf16(attn, s1, ca, T_max, rows, H, dt, err, s));
+  RPP_TRY(linear_i8(ca, at<void>(layer, P.wo), bo, s1, at<float>(layer, P.so), nullptr, x, h, dt, T_max, rows, H, H,
+                    EPI_DQ_BIAS_RESIDUAL, err, s));
+  RPP_TRY(launch_layernorm(h, g1, be1, x1, T_max, rows, H, c->eps, dt, cx1, s2, nullptr, err, s));
+  RPP_TRY(linear_i8(cx1, at<void>(layer, P.w1), b1, s2, at<float>(layer, P.s1), s3, nullptr, cg, RPP_BF16, T_max,
+                    rows, F, H, EPI_DQ_BIAS_GELU_Q, err, s));
+  RPP_TRY(linear_i8(cg, at<void>(layer, P.w2), b2, s3, at<float>(layer, P.s2), nullptr, x1, h, dt, T_max, rows, H, F,
+                    EPI_DQ_BIAS_RESIDUAL, err, s));
+  RPP_TRY(launch_layernorm(h, g2, be2, y, T_max, rows, H, c->eps, dt, nullptr, nullptr, nullptr, err, s));
+  return RPP_OK;
+}
+
+// ---------------------------------------------------------------- prepared Swin block
+struct SwinLayout {
+  size_t wqkv, wo, w1, w2, bqkv, bo, b1, b2, g1, be1, g2, be2, bias, total;
+};
+
+rpp_status swin_cfg_supported(const rpp_swin_cfg* c) {
+  if (!c) return RPP_EINVAL;
+  if (c->img <= 0 || c->channels <= 0 || c->heads <= 0 || c->window <= 0 || c->mlp <= 0) return RPP_EINVAL;
+  if (c->shift < 0 || c->shift >= c->window || c->img % c->window) return RPP_EINVAL;
+  if (c->dtype != RPP_F16 && c->dtype != RPP_BF16) return RPP_EUNSUPPORTED;
+  if (!window_attention_supported(c->channels, c->heads, c->window, c->img, c->shift)) return RPP_EUNSUPPORTED;
+  const int C = c->channels, F = c->mlp;
+  if (!layernorm_supported(C, static_cast<rpp_dtype>(c->dtype))) return RPP_EUNSUPPORTED;
+  if (!gemm_tc_supported(3 * C, C) || !gemm_tc_supported(C, C) || !gemm_tc_supported(F, C) ||
+      !gemm_tc_supported(C, F))
+    return RPP_EUNSUPPORTED;
+  return RPP_OK;
+}
+
+SwinLayout swin_layout(const rpp_swin_cfg* c) {
+  SwinLayout L{};
+  const size_t C = c->channels, F = c->mlp, e = 2, N = c->window * c->window;
+  size_t o = 0;
+  L.wqkv = o; o = align_up(o + 3 * C * C * e);
+  L.wo = o;   o = align_up(o + C * C * e);
+  L.w1 = o;   o = align_up(o + F * C * e);
+  L.w2 = o;   o = align_up(o + C * F * e);
+  L.bqkv = o; o = align_up(o + 3 * C * 4);
+  L.bo = o;   o = align_up(o + C * 4);
+  L.b1 = o;   o = align_up(o + F * 4);
+  L.b2 = o;   o = align_up(o + C * 4);
+  L.g1 = o;   o = align_up(o + C * 4);
+  L.be1 = o;  o = align_up(o + C * 4);
+  L.g2 = o;   o = align_up(o + C * 4);
+  L.be2 = o;  o = align_up(o + C * 4);
+  L.bias = o; o = align_up(o + c->heads * N * N * 4);
+  L.total = o;
+  return L;
+}
+
+struct SwinWs {
+  size_t h, qkv, attn, xa, g, total;
+};
+SwinWs swin_ws_layout(const rpp_swin_cfg* c, int B) {
+  SwinWs w{};
+  const size_t T = static_cast<size_t>(B) * c->img * c->img, C = c->channels, F = c->mlp, e = 2;
+  size_t o = 0;
+  w.h = o;    o = align_up(o + T * C * e);
+  w.qkv = o;  o = align_up(o + T * 3 * C * e);
+  w.attn = o; o = align_up(o + T * C * e);
+  w.xa = o;   o = align_up(o + T * C * e);
+  w.g = o;    o = align_up(o + T * F * e);
+  w.total = o;
+  return w;
+}
+
+}  // namespace
+}  // namespace rpp
+
+using namespace rpp;
+
+extern "C" {
+
+const char* rpp_status_string(int status) {
+  switch (status) {
+    case RPP_OK: return "ok";
+    case RPP_EINVAL: return "invalid argument";
+    case RPP_EUNSUPPORTED: return "unsupported shape or dtype";
+    case RPP_ECUDA: return "CUDA runtime error";
+    case RPP_EWORKSPACE: return "workspace too small";
+    case RPP_EDEVICE: return "device-side error recorded";
+    default: return "unknown status";
+  }
+}
+
+int rpp_version(void) { return 100; }
+
+rpp_status rpp_get_device_error(const int32_t* err, int32_t* host_code, rpp_stream stream) {
+  if (!err || !host_code) return RPP_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, err, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess) return RPP_ECUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return RPP_ECUDA;
+  *host_code = v;
+  return v ? RPP_EDEVICE : RPP_OK;
+}
+
+rpp_status rpp_build_offsets(const int32_t* lengths, int B, int L, int32_t* cu_seqlens, int32_t* padding_offset,
+                             int32_t* err, rpp_stream stream) {
+  if (!lengths || !cu_seqlens || !padding_offset || B <= 0 || L <= 0 || B > 65536) return RPP_EINVAL;
+  if (static_cast<long long>(B) * L > 0x7fffffffLL) return RPP_EINVAL;
+  return from_cuda(launch_build_offsets(lengths, B, L, cu_seqlens, padding_offset, err,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+rpp_status rpp_remove_padding(const void* padded, const int32_t* padding_offset, const int32_t* cu_seqlens, int B,
+                              int L, int H, rpp_dtype dtype, void* packed, int32_t* err, rpp_stream stream) {
+  if (!padded || !padding_offset || !cu_seqlens || !packed || B <= 0 || L <= 0 || H <= 0) return RPP_EINVAL;
+  if (dtype < RPP_F32 || dtype > RPP_I8) return RPP_EINVAL;
+  const long long row_bytes = static_cast<long long>(H) * esize(dtype);
+  if (row_bytes % 16 || !aligned16(padded) || !aligned16(packed)) return RPP_EINVAL;
+  return from_cuda(launch_remove_padding(padded, padding_offset, cu_seqlens, B, L, static_cast<int>(row_bytes), packed,
+                                         err, static_cast<cudaStream_t>(stream)));
+}
+
+rpp_status rpp_rebuild_padding(const void* packed, const int32_t* cu_seqlens, int B, int L, int H, rpp_dtype dtype,
+                               void* padded, int32_t* err, rpp_stream stream) {
+  if (!packed || !cu_seqlens || !padded || B <= 0 || L <= 0 || H <= 0) return RPP_EINVAL;
+  if (dtype < RPP_F32 || dtype > RPP_I8) return RPP_EINVAL;
+  const long long row_bytes = static_cast<long long>(H) * esize(dtype);
+  if (row_bytes % 16 || !aligned16(padded) || !aligned16(packed)) return RPP_EINVAL;
+  return from_cuda(launch_rebuild_padding(packed, cu_seqlens, B, L, static_cast<int>(row_bytes), padded, err,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+rpp_status rpp_linear(const void* a, const void* w_t, const float* bias, const void* residual, void* out, int M_max,
+                      const int32_t* rows, int N, int K, rpp_dtype dtype, rpp_epilogue epilogue, int32_t* err,
+                      rpp_stream stream) {
+  if (!a || !w_t || !bias || !out || M_max <= 0 || N <= 0 || K <= 0) return RPP_EINVAL;
+  if (epilogue != RPP_EPI_BIAS && epilogue != RPP_EPI_BIAS_GELU && epilogue != RPP_EPI_BIAS_RESIDUAL)
+    return RPP_EINVAL;
+  if (epilogue == RPP_EPI_BIAS_RESIDUAL && !residual) return RPP_EINVAL;
+  if (!aligned16(a) || !aligned16(w_t) || !aligned16(out) || !aligned16(bias) || (residual && !aligned16(residual)))
+    return RPP_EINVAL;
+  if (dtype == RPP_F32) {
+    if (K % 4 || N % 4) return RPP_EUNSUPPORTED;
+  } else if (dtype == RPP_F16 || dtype == RPP_BF16) {
+    if (!gemm_tc_supported(N, K)) return RPP_EUNSUPPORTED;
+  } else {
+    return RPP_EUNSUPPORTED;
+  }
+  return from_cuda(linear(dtype, a, w_t, bias, residual, out, M_max, rows, N, K, epilogue, err,
+                          static_cast<cudaStream_t>(stream)));
+}
+
+rpp_status rpp_layernorm(const void* x, const float* gamma, const float* beta, void* y, int M_max, const int32_t* rows,
+                         int H, float eps, rpp_dtype dtype, int32_t* err, rpp_stream stream) {
+  if (!x || !gamma || !beta || !y || M_max <= 0 || H <= 0) return RPP_EINVAL;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(gamma) || !aligned16(beta)) return RPP_EINVAL;
+  if (dtype != RPP_F32 && dtype != RPP_F16 && dtype != RPP_BF16) return RPP_EUNSUPPORTED;
+  if (!layernorm_supported(H, dtype)) return RPP_EUNSUPPORTED;
+  return from_cuda(launch_layernorm(x, gamma, beta, y, M_max, rows, H, eps, dtype, nullptr, nullptr, nullptr, err,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+rpp_status rpp_attention_varlen(const void* qkv, const int32_t* cu_seqlens, int B, int T_max, int max_len, int nh,
+                                int d, rpp_dtype dtype, void* out, int32_t* err, rpp_stream stream) {
+  if (!qkv || !cu_seqlens || !out || B <= 0 || T_max <= 0 || max_len <= 0 || nh <= 0 || d <= 0) return RPP_EINVAL;
+  if (!aligned16(qkv) || !aligned16(out)) return RPP_EINVAL;
+  if (d != 64) return RPP_EUNSUPPORTED;
+  if (dtype != RPP_F32 && dtype != RPP_F16 && dtype != RPP_BF16) return RPP_EUNSUPPORTED;
+  if (B > 65535 || nh > 65535) return RPP_EUNSUPPORTED;
+  return from_cuda(launch_attention_varlen(qkv, cu_seqlens, B, T_max, max_len, nh, d, dtype, out, err,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+size_t rpp_layer_bytes(const rpp_encoder_cfg* cfg) {
+  if (!encoder_cfg_ok(cfg)) return 0;
+  return layer_layout(cfg).total;
+}
+
+rpp_status rpp_prepare_layer(const rpp_encoder_cfg* cfg, const rpp_layer_src* src, void* dst, rpp_stream stream) {
+  rpp_status st = encoder_cfg_supported(cfg);
+  if (st != RPP_OK) return st;
+  if (!src || !dst || !aligned16(dst)) return RPP_EINVAL;
+  const void* ptrs[] = {src->Wq, src->Wk, src->Wv, src->bq, src->bk, src->bv, src->Wo, src->bo, src->W1,
+                        src->b1, src->W2, src->b2, src->gamma1, src->beta1, src->gamma2, src->beta2};
+  for (const void* p : ptrs)
+    if (!p) return RPP_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const LayerLayout P = layer_layout(cfg);
+  const rpp_dtype dt = static_cast<rpp_dtype>(cfg->dtype);
+  const int H = cfg->hidden, F = cfg->ffn, e = esize(dt);
+  if (!cfg->int8) {
+    // Wq | Wk | Wv concatenated as rows of one [3H, H] K-major matrix
+    uint8_t* wqkv = at<uint8_t>(dst, P.wqkv);
+    RPP_TRY(launch_transpose_to_kmajor(src->Wq, H, H, e, wqkv, H, s));
+    RPP_TRY(launch_transpose_to_kmajor(src->Wk, H, H, e, wqkv + static_cast<size_t>(H) * H * e, H, s));
+    RPP_TRY(launch_transpose_to_kmajor(src->Wv, H, H, e, wqkv + 2 * static_cast<size_t>(H) * H * e, H, s));
+    RPP_TRY(launch_transpose_to_kmajor(src->Wo, H, H, e, at<void>(dst, P.wo), H, s));
+    RPP_TRY(launch_transpose_to_kmajor(src->W1, H, F, e, at<void>(dst, P.w1), H, s));
+    RPP_TRY(launch_transpose_to_kmajor(src->W2, F, H, e, at<void>(dst, P.w2), F, s));
+  } else {
+    // int8: the per-channel scales of Wq, Wk, Wv are the per-column scales of the
+    // concatenated [H, 3H] matrix, so each part is quantised on its own
+    __nv_bfloat16* wqkv = at<__nv_bfloat16>(dst, P.wqkv);
+    float* sq = at<float>(dst, P.sqkv);
+    RPP_TRY(launch_quantize_weight(src->Wq, H, H, dt, nullptr, wqkv, sq, s));
+    RPP_TRY(launch_quantize_weight(src->Wk, H, H, dt, nullptr, wqkv + static_cast<size_t>(H) * H, sq + H, s));
+    RPP_TRY(launch_quantize_weight(src->Wv, H, H, dt, nullptr, wqkv + 2 * static_cast<size_t>(H) * H, sq + 2 * H, s));
+    RPP_TRY(launch_quantize_weight(src->Wo, H, H, dt, nullptr, at<void>(dst, P.wo), at<float>(dst, P.so), s));
+    RPP_TRY(launch_quantize_weight(src->W1, H, F, dt, nullptr, at<void>(dst, P.w1), at<float>(dst, P.s1), s));
+    RPP_TRY(launch_quantize_weight(src->W2, F, H, dt, nullptr, at<void>(dst, P.w2), at<float>(dst, P.s2), s));
+  }
+  float* bqkv = at<float>(dst, P.bqkv);
+  RPP_TRY(launch_to_f32(src->bq, dt, H, bqkv, s));
+  RPP_TRY(launch_to_f32(src->bk, dt, H, bqkv + H, s));
+  RPP_TRY(launch_to_f32(src->bv, dt, H, bqkv + 2 * H, s));
+  RPP_TRY(launch_to_f32(src->bo, dt, H, at<float>(dst, P.bo), s));
+  RPP_TRY(launch_to_f32(src->b1, dt, F, at<float>(dst, P.b1), s));
+  RPP_TRY(launch_to_f32(src->b2, dt, H, at<float>(dst, P.b2), s));
+  RPP_TRY(launch_to_f32(src->gamma1, dt, H, at<float>(dst, P.g1), s));
+  RPP_TRY(launch_to_f32(src->beta1, dt, H, at<float>(dst, P.be1), s));
+  RPP_TRY(launch_to_f32(src->gamma2, dt, H, at<float>(dst, P.g2), s));
+  RPP_TRY(launch_to_f32(src->beta2, dt, H, at<float>(dst, P.be2), s));
+  return RPP_OK;
+}
+
+size_t rpp_encoder_workspace_bytes(const rpp_encoder_cfg* cfg, int T_max) {
+  if (!encoder_cfg_ok(cfg) || T_max <= 0) return 0;
+  return enc_ws_layout(cfg, T_max).total;
+}
+
+rpp_status rpp_encoder_layer_forward(const rpp_encoder_cfg* cfg, const void* layer, const float* act_scales,
+                                     const void* x, const int32_t* cu_seqlens, int B, int T_max, int max_len, void* y,
+                                     void* workspace, size_t workspace_bytes, int32_t* err, rpp_stream stream) {
+  return encoder_layer_run(cfg, layer, act_scales, x, cu_seqlens, B, T_max, max_len, y, workspace, workspace_bytes,
+                           nullptr, err, static_cast<cudaStream_t>(stream));
+}
+
+rpp_status rpp_encoder_layer_calibrate(const rpp_encoder_cfg* cfg, const void* layer, const void* x,
+                                       const int32_t* cu_seqlens, int B, int T_max, int max_len, float* amax_out,
+                                       void* workspace, size_t workspace_bytes, int32_t* err, rpp_stream stream) {
+  if (!cfg || cfg->int8 || !amax_out) return RPP_EINVAL;
+  if (cfg->dtype == RPP_F32) return RPP_EUNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(amax_out, 0, 4 * sizeof(float), s) != cudaSuccess) return RPP_ECUDA;
+  const size_t need = enc_ws_layout(cfg, T_max > 0 ? T_max : 1).total;
+  if (workspace_bytes < need) return RPP_EWORKSPACE;
+  // the output of the calibration pass is not needed: write it into the workspace's h buffer
+  void* y = at<void>(workspace, enc_ws_layout(cfg, T_max).h);
+  return encoder_layer_run(cfg, layer, nullptr, x, cu_seqlens, B, T_max, max_len, y, workspace, workspace_bytes,
+                           amax_out, err, s);
+}
+
+rpp_status rpp_encoder_forward(const rpp_encoder_cfg* cfg, const void* const* layers, const float* const* act_scales,
+                               int num_layers, const int32_t* lengths, int B, int L, const void* x_padded,
+                               void* y_padded, int32_t* cu_seqlens, int32_t* padding_offset, void* packed,
+                               void* workspace, size_t workspace_bytes, int32_t* err, rpp_stream stream) {
+  rpp_status st = encoder_cfg_supported(cfg);
+  if (st != RPP_OK) return st;
+  if (!layers || num_layers <= 0 || !lengths || !x_padded || !y_padded || !cu_seqlens || !padding_offset || !packed)
+    return RPP_EINVAL;
+  if (cfg->int8 && !act_scales) return RPP_EINVAL;
+  const rpp_dtype dt = static_cast<rpp_dtype>(cfg->dtype);
+  const int H = cfg->hidden;
+  const int T_max = B * L;
+  if (workspace_bytes < enc_ws_layout(cfg, T_max).total) return RPP_EWORKSPACE;
+  st = rpp_build_offsets(lengths, B, L, cu_seqlens, padding_offset, err, stream);
+  if (st != RPP_OK) return st;
+  st = rpp_remove_padding(x_padded, padding_offset, cu_seqlens, B, L, H, dt, packed, err, stream);
+  if (st != RPP_OK) return st;
+  for (int i = 0; i < num_layers; ++i) {
+    st = encoder_layer_run(cfg, layers[i], cfg->int8 ? act_scales[i] : nullptr, packed, cu_seqlens, B, T_max, L,
+                           packed, workspace, workspace_bytes, nullptr, err, static_cast<cudaStream_t>(stream));
+    if (st != RPP_OK) return st;
+  }
+  return rpp_rebuild_padding(packed, cu_seqlens, B, L, H, dt, y_padded, err, stream);
+}
+
+rpp_status rpp_quantize_weight(const void* w, int K, int N, rpp_dtype dtype, int8_t* wq_t, float* s_w,
+                               rpp_stream stream) {
+  if (!w || !wq_t || !s_w || K <= 0 || N <= 0) return RPP_EINVAL;
+  if (dtype != RPP_F32 && dtype != RPP_F16 && dtype != RPP_BF16) return RPP_EUNSUPPORTED;
+  return from_cuda(launch_quantize_weight(w, K, N, dtype, wq_t, nullptr, s_w, static_cast<cudaStream_t>(stream)));
+}
+
+rpp_status rpp_quantize_activation(const void* x, const float* scale, int8_t* q, int M_max, const int32_t* rows, int H,
+                                   rpp_dtype dtype, int32_t* err, rpp_stream stream) {
+  if (!x || !scale || !q || M_max <= 0 || H <= 0 || H % 8) return RPP_EINVAL;
+  if (!aligned16(x) || (reinterpret_cast<uintptr_t>(q) & 7u)) return RPP_EINVAL;
+  if (dtype != RPP_F32 && dtype != RPP_F16 && dtype != RPP_BF16) return RPP_EUNSUPPORTED;
+  return from_cuda(launch_quantize(x, scale, q, M_max, rows, H, dtype, err, static_cast<cudaStream_t>(stream)));
+}
+
+size_t rpp_gemm_i8_workspace_bytes(int M, int N, int K) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  return align_up(static_cast<size_t>(M) * K * 2) + align_up(static_cast<size_t>(N) * K * 2);
+}
+
+rpp_status rpp_gemm_i8_i32(const int8_t* aq, const int8_t* wq_t, int32_t* acc, int M, int N, int K, void* workspace,
+                           size_t workspace_bytes, int32_t* err, rpp_stream stream) {
+  if (!aq || !wq_t || !acc || !workspace || M <= 0 || N <= 0 || K <= 0) return RPP_EINVAL;
+  if (K % 16 || N % 16 || K > 4096) return RPP_EUNSUPPORTED;
+  if (!aligned16(acc) || !aligned16(workspace)) return RPP_EINVAL;
+  if (workspace_bytes < rpp_gemm_i8_workspace_bytes(M, N, K)) return RPP_EWORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* a_codes = workspace;
+  void* w_codes = at<void>(workspace, align_up(static_cast<size_t>(M) * K * 2));
+  RPP_TRY(launch_i8_to_bf16(aq, a_codes, static_cast<long long>(M) * K, s));
+  RPP_TRY(launch_i8_to_bf16(wq_t, w_codes, static_cast<long long>(N) * K, s));
+  TcGemmArgs g{};
+  g.a = a_codes; g.w_t = w_codes; g.out = acc; g.M_max = M; g.N = N; g.K = K;
+  g.in_dtype = RPP_BF16; g.out_dtype = RPP_F32; g.epi = EPI_I32; g.err = err;
+  return from_cuda(launch_gemm_tc(g, s));
+}
+
+rpp_status rpp_swin_prepare_bias(const rpp_swin_cfg* cfg, const void* table, float* bias, rpp_stream stream) {
+  if (!cfg || !table || !bias || cfg->window <= 0 || cfg->heads <= 0) return RPP_EINVAL;
+  return from_cuda(launch_swin_bias(table, static_cast<rpp_dtype>(cfg->dtype), cfg->window, cfg->heads, bias,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+rpp_status rpp_window_attention_forward(const rpp_swin_cfg* cfg, int B, const void* qkv, const float* bias, void* out,
+                                        int32_t* err, rpp_stream stream) {
+  rpp_status st = swin_cfg_supported(cfg);
+  if (st != RPP_OK) return st;
+  if (B <= 0 || !qkv || !bias || !out || !aligned16(qkv) || !aligned16(out)) return RPP_EINVAL;
+  return from_cuda(launch_window_attention(B, qkv, bias, out, cfg->channels, cfg->heads, cfg->img, cfg->window,
+                                           cfg->shift, static_cast<rpp_dtype>(cfg->dtype), err,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+size_t rpp_swin_block_bytes(const rpp_swin_cfg* cfg) {
+  if (swin_cfg_supported(cfg) == RPP_EINVAL) return 0;
+  return swin_layout(cfg).total;
+}
+
+rpp_status rpp_swin_prepare_block(const rpp_swin_cfg* cfg, const rpp_swin_src* src, void* dst, rpp_stream stream) {
+  rpp_status st = swin_cfg_supported(cfg);
+  if (st != RPP_OK) return st;
+  if (!src || !dst || !aligned16(dst)) return RPP_EINVAL;
+  const void* ptrs[] = {src->gamma1, src->beta1, src->Wqkv, src->bqkv, src->table, src->Wo, src->bo,
+                        src->gamma2, src->beta2, src->W1, src->b1, src->W2, src->b2};
+  for (const void* p : ptrs)
+    if (!p) return RPP_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const SwinLayout P = swin_layout(cfg);
+  const rpp_dtype dt = static_cast<rpp_dtype>(cfg->dtype);
+  const int C = cfg->channels, F = cfg->mlp;
+  RPP_TRY(launch_transpose_to_kmajor(src->Wqkv, C, 3 * C, 2, at<void>(dst, P.wqkv), C, s));
+  RPP_TRY(launch_transpose_to_kmajor(src->Wo, C, C, 2, at<void>(dst, P.wo), C, s));
+  RPP_TRY(launch_transpose_to_kmajor(src->W1, C, F, 2, at<void>(dst, P.w1), C, s));
+  RPP_TRY(launch_transpose_to_kmajor(src->W2, F, C, 2, at<void>(dst, P.w2), F, s));
+  RPP_TRY(launch_to_f32(src->bqkv, dt, 3 * C, at<float>(dst, P.bqkv), s));
+  RPP_TRY(launch_to_f32(src->bo, dt, C, at<float>(dst, P.bo), s));
+  RPP_TRY(launch_to_f32(src->b1, dt, F, at<float>(dst, P.b1), s));
+  RPP_TRY(launch_to_f32(src->b2, dt, C, at<float>(dst, P.b2), s));
+  RPP_TRY(launch_to_f32(src->gamma1, dt, C, at<float>(dst, P.g1), s));
+  RPP_TRY(launch_to_f32(src->beta1, dt, C, at<float>(dst, P.be1), s));
+  RPP_TRY(launch_to_f32(src->gamma2, dt, C, at<float>(dst, P.g2), s));
+  RPP_TRY(launch_to_f32(src->beta2, dt, C, at<float>(dst, P.be2), s));
+  RPP_TRY(launch_swin_bias(src->table, dt, cfg->window, cfg->heads, at<float>(dst, P.bias), s));
+  return RPP_OK;
+}
+
+size_t rpp_swin_workspace_bytes(const rpp_swin_cfg* cfg, int B) {
+  if (swin_cfg_supported(cfg) == RPP_EINVAL || B <= 0) return 0;
+  return swin_ws_layout(cfg, B).total;
+}
+
+rpp_status rpp_swin_block_forward(const rpp_swin_cfg* cfg, const void* block, int B, const void* x, void* y,
+                                  void* workspace, size_t workspace_bytes, int32_t* err, rpp_stream stream) {
+  rpp_status st = swin_cfg_supported(cfg);
+  if (st != RPP_OK) return st;
+  if (!block || !x || !y || !workspace || B <= 0) return RPP_EINVAL;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(workspace) || !aligned16(block)) return RPP_EINVAL;
+  const SwinWs W = swin_ws_layout(cfg, B);
+  if (workspace_bytes < W.total) return RPP_EWORKSPACE;
+  const long long Tl = static_cast<long long>(B) * cfg->img * cfg->img;
+  if (Tl > 0x7fffffffLL) return RPP_EUNSUPPORTED;
+  const int T = static_cast<int>(Tl);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const SwinLayout P = swin_layout(cfg);
+  const rpp_dtype dt = static_cast<rpp_dtype>(cfg->dtype);
+  const int C = cfg->channels, F = cfg->mlp;
+  void* h = at<void>(workspace, W.h);
+  void* qkv = at<void>(workspace, W.qkv);
+  void* attn = at<void>(workspace, W.attn);
+  void* xa = at<void>(workspace, W.xa);
+  void* g = at<void>(workspace, W.g);
+  RPP_TRY(launch_layernorm(x, at<float>(block, P.g1), at<float>(block, P.be1), h, T, nullptr, C, cfg->eps, dt, nullptr,
+                           nullptr, nullptr, err, s));
+  RPP_TRY(linear(dt, h, at<void>(block, P.wqkv), at<float>(block, P.bqkv), nullptr, qkv, T, nullptr, 3 * C, C,
+                 RPP_EPI_BIAS, err, s));
+  RPP_TRY(launch_window_attention(B, qkv, at<float>(block, P.bias), attn, C, cfg->heads, cfg->img, cfg->window,
+                                  cfg->shift, dt, err, s));
+  RPP_TRY(linear(dt, attn, at<void>(block, P.wo), at<float>(block, P.bo), x, xa, T, nullptr, C, C,
+                 RPP_EPI_BIAS_RESIDUAL, err, s));
+  RPP_TRY(launch_layernorm(xa, at<float>(block, P.g2), at<float>(block, P.be2), h, T, nullptr, C, cfg->eps, dt, nullptr,
+                           nullptr, nullptr, err, s));
+  RPP_TRY(linear(dt, h, at<void>(block, P.w1), at<float>(block, P.b1), nullptr, g, T, nullptr, F, C, RPP_EPI_BIAS_GELU,
+                 err, s));
+  RPP_TRY(linear(dt, g, at<void>(block, P.w2), at<float>(block, P.b2), xa, y, T, nullptr, C, F, RPP_EPI_BIAS_RESIDUAL,
+                 err, s));
+  return RPP_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,503 @@
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a with fused epilogues.
+//
+//   out[M, N] = epilogue(A[M, K] @ W[N, K]^T),   A, W fp16 or bf16 (both K-major),
+//   fp32 accumulation in tensor memory, epilogue = bias | bias+GELU | bias+residual.
+//
+// The NVIDIA Swin talk (§3) fuses the bias (and activation) into the GEMM and moves
+// the bias next to the residual add before LayerNorm; the Kuaishou article (Fig. 6,
+// Fig. 11) fuses the elementwise work into the GEMMs and tunes the GEMM tile
+// configuration per shape.  Here the GEMM itself is written for the 5th-generation
+// tensor cores:
+//
+//   warp 0      TMA producer: 2D tiled loads with 128-byte swizzle of a 128 x 64 A
+//               tile and a BN x 64 W tile per pipeline stage (no multicast).
+//   warp 1      allocates tensor memory and issues tcgen05.mma (M = 128, N = BN,
+//               K = 16 per instruction) from one thread; tcgen05.commit releases the
+//               smem stage and, after the last K block, signals the accumulator.
+//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns per warp, bias / GELU /
+//               residual in fp32, 16-byte stores of the converted row segment.
+//
+// The accumulator is double-buffered in tensor memory (2 x BN columns), so the
+// epilogue of tile i overlaps the MMAs of tile i+1.  Tiles are assigned round-robin
+// over a persistent grid of at most one CTA per SM.  The row count M may live in
+// device memory (the packed token count); rows >= M are loaded (they are inside the
+// buffer) but never stored.  Every mbarrier wait is bounded; on a timeout the CTA
+// records RPP_DERR_TIMEOUT, drains its in-flight copies and MMAs, frees its tensor
+// memory and exits.
+//
+// int8 layers: sm_103a has no int8 kind of tcgen05.mma, so the int8 GEMM runs as an
+// exact integer product on the bf16 tensor pipe.  Codes in [-127, 127] are exact in
+// bf16, each product is an integer below 2^14, and K is split into chunks of at most
+// 1024 so every fp32 partial sum is an integer below 2^24 and therefore exact; each
+// chunk accumulates into its own tensor-memory region and the epilogue adds the
+// chunks in int32.  The result equals int32 accumulation bit for bit.
+#include "kernels.h"
+
+namespace rpp {
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;   // 64 x 16-bit = 128 bytes = one swizzle row
+constexpr int kThreads = 192;
+
+constexpr int kChunkBlocks = 16;   // 16 x 64 = 1024 K per exact integer chunk
+
+struct GemmParams {
+  int M_max;
+  const int32_t* rows;   // device row count or null
+  int N;
+  int K;
+  const float* bias;
+  const void* residual;
+  void* out;
+  const float* a_scale;
+  const float* w_scale;
+  const float* q_scale;
+  int32_t* err;
+};
+
+constexpr uint32_t pow2_cols(uint32_t c) {
+  return c <= 32 ? 32 : c <= 64 ? 64 : c <= 128 ? 128 : c <= 256 ? 256 : 512;
+}
+
+template <typename T> struct AbFmt;
+template <> struct AbFmt<__half> { static constexpr int v = 0; };
+template <> struct AbFmt<__nv_bfloat16> { static constexpr int v = 1; };
+
+__device__ __forceinline__ float code_of(float v, float inv_s) {
+  const float t = __fmul_rn(v, inv_s);
+  float q = rintf(t);   // round half to even
+  return fminf(fmaxf(q, -127.f), 127.f);
+}
+
+template <typename TIn, typename TOut, int BN, int STAGES, int EPI, int NCH>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
+  constexpr uint32_t A_BYTES = kBM * kBK * 2;
+  constexpr uint32_t B_BYTES = BN * kBK * 2;
+  constexpr uint32_t B_BYTES_AL = (B_BYTES + 1023u) & ~1023u;
+  constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES;
+  constexpr int NBUF = (2 * NCH * BN <= 512) ? 2 : 1;   // accumulator buffers in tensor memory
+  static_assert(NCH * BN <= 512, "tensor memory columns");
+  constexpr uint32_t TMEM_COLS = pow2_cols(NBUF * NCH * BN);
+  constexpr uint32_t IDESC = idesc_f16(AbFmt<TIn>::v, kBM, BN);
+  constexpr bool kInt = EPI >= EPI_I32;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment for the swizzled tiles
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES_AL);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4 * 32);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  int M = p.M_max;
+  bool skip = device_error_set(p.err);
+  if (p.rows) {
+    M = *p.rows;
+    if (M > p.M_max || M < 0) {
+      if (threadIdx.x == 0) set_device_error(p.err, RPP_DERR_ROWS);
+      skip = true;
+    }
+  }
+  const int num_m = skip ? 0 : (M + kBM - 1) / kBM;
+  const int num_n = p.N / BN;
+  const int num_k = (p.K + kBK - 1) / kBK;
+  const int total = num_m * num_n;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const int m0 = (tile / num_n) * kBM;
+        const int n0 = (tile % num_n) * BN;
+        for (int kb = 0; kb < num_k; ++kb, ++it) {
+          const uint32_t s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (!mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], STAGE_TX);
+          tma_load_2d(sA + s * A_BYTES, &tmA, &full[s], kb * kBK, m0);
+          tma_load_2d(sB + s * B_BYTES_AL, &tmB, &full[s], kb * kBK, n0);
+        }
+      }
+      if (!ok) {
+        set_device_error(p.err, RPP_DERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // wait (bounded) for the copies still in flight: the last min(it, STAGES) loads
+      const uint32_t first = it > STAGES ? it - STAGES : 0;
+      for (uint32_t j = first; j < it; ++j) mbar_wait_bounded(&full[j % STAGES], (j / STAGES) & 1u, nullptr);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, acc_it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++acc_it) {
+        const uint32_t a = NBUF == 2 ? (acc_it & 1u) : 0u;
+        const uint32_t aph = NBUF == 2 ? ((acc_it >> 1) & 1u) : (acc_it & 1u);
+        if (!mbar_wait_bounded(&tempty[a], aph ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < num_k; ++kb, ++it) {
+          const int chunk = NCH > 1 ? kb / kChunkBlocks : 0;
+          const int kb_in = NCH > 1 ? kb - chunk * kChunkBlocks : kb;
+          const uint32_t d_tmem = tmem_base + (a * NCH + chunk) * BN;
+          const uint32_t s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (!mbar_wait_bounded(&full[s], ph, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + s * A_BYTES));
+          const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + s * B_BYTES_AL));
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            // +32 bytes along K inside the swizzled 128-byte row = +2 in the address field
+            tc_mma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, IDESC, (kb_in | k) != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty[s]);
+        }
+        if (ok) tc_commit(&tfull[a]);
+      }
+      if (!ok) {
+        set_device_error(p.err, RPP_DERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // all MMAs issued by this thread complete before tensor memory is released
+      tc_commit(drain);
+      mbar_wait_bounded(drain, 0, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue warps
+    const int q = warp & 3;               // tensor-memory lane quadrant of this warp
+    const int r_in_tile = q * 32 + lane;
+    const int nch = NCH > 1 ? (num_k + kChunkBlocks - 1) / kChunkBlocks : 1;
+    float a_s = 1.f, inv_q = 0.f;
+    if constexpr (EPI == EPI_DQ_BIAS || EPI == EPI_DQ_BIAS_RESIDUAL || EPI == EPI_DQ_BIAS_GELU_Q) a_s = *p.a_scale;
+    if constexpr (EPI == EPI_DQ_BIAS_GELU_Q) inv_q = __fdiv_rn(1.0f, *p.q_scale);
+    uint32_t acc_it = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++acc_it) {
+      const uint32_t a = NBUF == 2 ? (acc_it & 1u) : 0u;
+      const uint32_t aph = NBUF == 2 ? ((acc_it >> 1) & 1u) : (acc_it & 1u);
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait_bounded(&tfull[a], aph, abort_flag) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) {
+          set_device_error(p.err, RPP_DERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      tc_fence_after();
+      const int m0 = (tile / num_n) * kBM;
+      const int n0 = (tile % num_n) * BN;
+      const int row = m0 + r_in_tile;
+      const bool row_ok = row < M;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        float v[32];
+        tmem_ld_32x32b_x32(t_row + (a * NCH) * BN + c * 32, r);
+        tmem_ld_wait();
+        if constexpr (kInt) {
+          // exact: every chunk partial is an integer below 2^24
+          int acc[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc[j] = __float2int_rn(__uint_as_float(r[j]));
+          for (int ch = 1; ch < nch; ++ch) {
+            tmem_ld_32x32b_x32(t_row + (a * NCH + ch) * BN + c * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] += __float2int_rn(__uint_as_float(r[j]));
+          }
+          if constexpr (EPI == EPI_I32) {
+            if (row_ok) {
+              int4* orow = reinterpret_cast<int4*>(static_cast<int32_t*>(p.out) + static_cast<long long>(row) * p.N +
+                                                   n0 + c * 32);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) orow[j] = make_int4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+            }
+            continue;
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = static_cast<float>(acc[j]);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+        }
+        if constexpr (EPI != EPI_I32) {
+          if (row_ok) {
+            const int n = n0 + c * 32;
+            const float4* b4 = reinterpret_cast<const float4*>(p.bias + n);
+            if constexpr (EPI == EPI_DQ_BIAS || EPI == EPI_DQ_BIAS_RESIDUAL || EPI == EPI_DQ_BIAS_GELU_Q) {
+              const float4* s4 = reinterpret_cast<const float4*>(p.w_scale + n);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float4 ss = __ldg(s4 + j);
+                v[4 * j + 0] *= a_s * ss.x;
+                v[4 * j + 1] *= a_s * ss.y;
+                v[4 * j + 2] *= a_s * ss.z;
+                v[4 * j + 3] *= a_s * ss.w;
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float4 bb = __ldg(b4 + j);
+              v[4 * j + 0] += bb.x;
+              v[4 * j + 1] += bb.y;
+              v[4 * j + 2] += bb.z;
+              v[4 * j + 3] += bb.w;
+            }
+            if constexpr (EPI == RPP_EPI_BIAS_GELU || EPI == EPI_DQ_BIAS_GELU_Q) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
+            }
+            if constexpr (EPI == EPI_DQ_BIAS_GELU_Q) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = code_of(v[j], inv_q);
+            }
+            if constexpr (EPI == RPP_EPI_BIAS_RESIDUAL || EPI == EPI_DQ_BIAS_RESIDUAL) {
+              const uint4* rr = reinterpret_cast<const uint4*>(static_cast<const TOut*>(p.residual) +
+                                                               static_cast<long long>(row) * p.N + n);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                float f[8];
+                unpack16<TOut>(rr[j], f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[8 * j + e] += f[e];
+              }
+            }
+            uint4* orow = reinterpret_cast<uint4*>(static_cast<TOut*>(p.out) + static_cast<long long>(row) * p.N + n);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) orow[j] = pack16<TOut>(v + 8 * j);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[a]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+}  // namespace
+
+// 2D row-major [rows, cols] tensor of 2-byte (or 1-byte) elements, box = box_cols x box_rows
+bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int rows, int cols,
+                  int box_rows, int box_cols, CUtensorMapSwizzle swz) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * elem_bytes};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+namespace {
+
+template <typename TIn, typename TOut, int BN, int STAGES, int EPI, int NCH>
+cudaError_t gemm_tc_launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cudaStream_t stream) {
+  constexpr uint32_t A_BYTES = kBM * kBK * 2;
+  constexpr uint32_t B_BYTES_AL = ((BN * kBK * 2) + 1023u) & ~1023u;
+  constexpr size_t SMEM = 1024 + STAGES * (A_BYTES + B_BYTES_AL) + 256;
+  static_assert(SMEM <= 232448, "shared memory per CTA");
+  auto kern = gemm_tc_kernel<TIn, TOut, BN, STAGES, EPI, NCH>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int num_m = (p.M_max + kBM - 1) / kBM;
+  const int tiles = num_m * (p.N / BN);
+  int grid = tiles < num_sms() ? tiles : num_sms();
+  if (grid < 1) grid = 1;
+  kern<<<grid, kThreads, SMEM, stream>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+// Tile width choice (the per-shape GEMM configuration of the Kuaishou article's
+// Fig. 11): minimise waves x (BN + fixed per-tile cost) over the candidates that divide
+// N, ties to the wider tile.
+int choose_bn(int M, int N, int max_bn) {
+  static const int cands[] = {256, 192, 144, 128, 96, 64, 48, 32, 16};
+  const int sms = num_sms();
+  int best = 0;
+  double best_cost = 1e30;
+  const int num_m = (M + kBM - 1) / kBM;
+  for (int bn : cands) {
+    if (N % bn || bn > max_bn) continue;
+    const long long tiles = static_cast<long long>(num_m) * (N / bn);
+    const long long waves = (tiles + sms - 1) / sms;
+    const double cost = static_cast<double>(waves) * (bn + 24.0);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+template <typename TIn, typename TOut, int EPI, int NCH>
+cudaError_t dispatch_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
+                        cudaStream_t stream) {
+  if constexpr (NCH == 1) {
+    switch (bn) {
+      case 256: return gemm_tc_launch<TIn, TOut, 256, 4, EPI, 1>(ta, tb, p, stream);
+      case 192: return gemm_tc_launch<TIn, TOut, 192, 5, EPI, 1>(ta, tb, p, stream);
+      case 144: return gemm_tc_launch<TIn, TOut, 144, 5, EPI, 1>(ta, tb, p, stream);
+      case 128: return gemm_tc_launch<TIn, TOut, 128, 6, EPI, 1>(ta, tb, p, stream);
+      case 96: return gemm_tc_launch<TIn, TOut, 96, 7, EPI, 1>(ta, tb, p, stream);
+      case 64: return gemm_tc_launch<TIn, TOut, 64, 8, EPI, 1>(ta, tb, p, stream);
+      case 48: return gemm_tc_launch<TIn, TOut, 48, 8, EPI, 1>(ta, tb, p, stream);
+      case 32: return gemm_tc_launch<TIn, TOut, 32, 8, EPI, 1>(ta, tb, p, stream);
+      case 16: return gemm_tc_launch<TIn, TOut, 16, 8, EPI, 1>(ta, tb, p, stream);
+      default: return cudaErrorNotSupported;
+    }
+  } else {
+    switch (bn) {   // NCH x BN <= 512 tensor-memory columns
+      case 128: return gemm_tc_launch<TIn, TOut, 128, 6, EPI, NCH>(ta, tb, p, stream);
+      case 96: return gemm_tc_launch<TIn, TOut, 96, 7, EPI, NCH>(ta, tb, p, stream);
+      case 64: return gemm_tc_launch<TIn, TOut, 64, 8, EPI, NCH>(ta, tb, p, stream);
+      case 48: return gemm_tc_launch<TIn, TOut, 48, 8, EPI, NCH>(ta, tb, p, stream);
+      case 32: return gemm_tc_launch<TIn, TOut, 32, 8, EPI, NCH>(ta, tb, p, stream);
+      case 16: return gemm_tc_launch<TIn, TOut, 16, 8, EPI, NCH>(ta, tb, p, stream);
+      default: return cudaErrorNotSupported;
+    }
+  }
+}
+
+template <typename T>
+cudaError_t dispatch_float(int bn, int epi, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
+                           cudaStream_t stream) {
+  switch (epi) {
+    case RPP_EPI_BIAS: return dispatch_bn<T, T, RPP_EPI_BIAS, 1>(bn, ta, tb, p, stream);
+    case RPP_EPI_BIAS_GELU: return dispatch_bn<T, T, RPP_EPI_BIAS_GELU, 1>(bn, ta, tb, p, stream);
+    case RPP_EPI_BIAS_RESIDUAL: return dispatch_bn<T, T, RPP_EPI_BIAS_RESIDUAL, 1>(bn, ta, tb, p, stream);
+    default: return cudaErrorNotSupported;
+  }
+}
+
+template <int NCH>
+cudaError_t dispatch_int(int bn, int epi, rpp_dtype out_dtype, const CUtensorMap& ta, const CUtensorMap& tb,
+                         const GemmParams& p, cudaStream_t stream) {
+  using BF = __nv_bfloat16;
+  switch (epi) {
+    case EPI_I32: return dispatch_bn<BF, int32_t, EPI_I32, NCH>(bn, ta, tb, p, stream);
+    case EPI_DQ_BIAS:
+      if (out_dtype == RPP_F16) return dispatch_bn<BF, __half, EPI_DQ_BIAS, NCH>(bn, ta, tb, p, stream);
+      return dispatch_bn<BF, BF, EPI_DQ_BIAS, NCH>(bn, ta, tb, p, stream);
+    case EPI_DQ_BIAS_RESIDUAL:
+      if (out_dtype == RPP_F16) return dispatch_bn<BF, __half, EPI_DQ_BIAS_RESIDUAL, NCH>(bn, ta, tb, p, stream);
+      return dispatch_bn<BF, BF, EPI_DQ_BIAS_RESIDUAL, NCH>(bn, ta, tb, p, stream);
+    case EPI_DQ_BIAS_GELU_Q: return dispatch_bn<BF, BF, EPI_DQ_BIAS_GELU_Q, NCH>(bn, ta, tb, p, stream);
+    default: return cudaErrorNotSupported;
+  }
+}
+
+}  // namespace
+
+bool gemm_tc_supported(int N, int K) { return K % 8 == 0 && K > 0 && N % 16 == 0 && choose_bn(1, N, 256) != 0; }
+
+cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t stream) {
+  const bool is_int = g.epi >= EPI_I32;
+  const int num_k = (g.K + kBK - 1) / kBK;
+  const int nch = is_int ? (num_k + kChunkBlocks - 1) / kChunkBlocks : 1;
+  if (nch > 4) return cudaErrorNotSupported;
+  const int max_bn = nch > 1 ? 128 : 256;
+  const int bn = g.force_bn ? g.force_bn : choose_bn(g.M_max, g.N, max_bn);
+  if (!bn || g.N % bn || bn > max_bn) return cudaErrorNotSupported;
+  const CUtensorMapDataType dt =
+      (is_int || g.in_dtype == RPP_BF16) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap ta, tb;
+  if (!make_tmap_2d(&ta, g.a, dt, 2, g.M_max, g.K, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+  if (!make_tmap_2d(&tb, g.w_t, dt, 2, g.N, g.K, bn, kBK, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+  GemmParams p{g.M_max, g.rows, g.N, g.K, g.bias, g.residual, g.out, g.a_scale, g.w_scale, g.q_scale, g.err};
+  if (is_int) {
+    if (nch == 1) return dispatch_int<1>(bn, g.epi, g.out_dtype, ta, tb, p, stream);
+    return dispatch_int<4>(bn, g.epi, g.out_dtype, ta, tb, p, stream);
+  }
+  if (g.in_dtype == RPP_BF16) return dispatch_float<__nv_bfloat16>(bn, g.epi, ta, tb, p, stream);
+  if (g.in_dtype == RPP_F16) return dispatch_float<__half>(bn, g.epi, ta, tb, p, stream);
+  return cudaErrorNotSupported;
+}
+
+}  // namespace rpp

@@ -1,0 +1,78 @@
+// Internal launchers shared by the kernel translation units and the C ABI (api.cu).
+#pragma once
+#include <type_traits>
+
+#include "common.cuh"
+
+namespace rpp {
+
+int num_sms();   // SM count of the current device (cached per device)
+
+// epilogue codes beyond the public rpp_epilogue (int8 layer)
+enum InternalEpilogue {
+  EPI_I32 = 3,               // raw int32 accumulators
+  EPI_DQ_BIAS = 4,           // acc * s_a * s_w[n] + b
+  EPI_DQ_BIAS_RESIDUAL = 5,  // acc * s_a * s_w[n] + b + residual
+  EPI_DQ_BIAS_GELU_Q = 6     // int8 code of GELU(acc * s_a * s_w[n] + b), held in a bf16 container
+};
+
+cudaError_t launch_build_offsets(const int32_t* lengths, int B, int L, int32_t* cu, int32_t* po, int32_t* err,
+                                 cudaStream_t stream);
+cudaError_t launch_remove_padding(const void* padded, const int32_t* po, const int32_t* cu, int B, int L,
+                                  int row_bytes, void* packed, int32_t* err, cudaStream_t stream);
+cudaError_t launch_rebuild_padding(const void* packed, const int32_t* cu, int B, int L, int row_bytes, void* padded,
+                                   int32_t* err, cudaStream_t stream);
+
+bool layernorm_supported(int H, rpp_dtype dtype);
+cudaError_t launch_layernorm(const void* x, const float* gamma, const float* beta, void* y, int M_max,
+                             const int32_t* rows, int H, float eps, rpp_dtype dtype, void* q_codes_bf16,
+                             const float* q_scale, float* amax, int32_t* err, cudaStream_t stream);
+cudaError_t launch_quantize(const void* x, const float* scale, int8_t* q, int M_max, const int32_t* rows, int H,
+                            rpp_dtype dtype, int32_t* err, cudaStream_t stream);
+cudaError_t launch_amax(const void* x, int M_max, const int32_t* rows, int H, rpp_dtype dtype, float* amax,
+                        int32_t* err, cudaStream_t stream);
+
+// int8 code helpers (quant.cu)
+cudaError_t launch_quantize_codes_bf16(const void* x, const float* scale, void* codes, int M_max, const int32_t* rows,
+                                       int H, rpp_dtype dtype, int32_t* err, cudaStream_t stream);
+cudaError_t launch_i8_to_bf16(const int8_t* src, void* dst, long long n, cudaStream_t stream);
+cudaError_t launch_quantize_weight(const void* w, int K, int N, rpp_dtype dtype, int8_t* wq_t, void* wq_t_bf16,
+                                   float* s_w, cudaStream_t stream);
+cudaError_t launch_transpose_to_kmajor(const void* w, int K, int N, int elem_bytes, void* dst, int dst_ld,
+                                       cudaStream_t stream);
+cudaError_t launch_to_f32(const void* src, rpp_dtype dtype, long long n, float* dst, cudaStream_t stream);
+
+struct TcGemmArgs {
+  const void* a;           // [M_max, K] operand (fp16 / bf16, or bf16-held int8 codes)
+  const void* w_t;         // [N, K] operand
+  const float* bias;       // [N] or null (EPI_I32)
+  const void* residual;    // [M_max, N] of the output type
+  void* out;               // [M_max, N]
+  int M_max;
+  const int32_t* rows;
+  int N, K;
+  rpp_dtype in_dtype;      // RPP_F16 or RPP_BF16
+  rpp_dtype out_dtype;     // RPP_F16 / RPP_BF16 (or anything for EPI_I32)
+  int epi;                 // rpp_epilogue or InternalEpilogue
+  const float* a_scale;    // device scalar s_a (int8 epilogues)
+  const float* w_scale;    // device [N] s_w (int8 epilogues)
+  const float* q_scale;    // device scalar for the requantised output (EPI_DQ_BIAS_GELU_Q)
+  int32_t* err;
+  int force_bn;            // 0 = heuristic
+};
+bool gemm_tc_supported(int N, int K);
+cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t stream);
+
+cudaError_t launch_gemm_f32(const float* a, const float* w_t, const float* bias, const float* residual, float* out,
+                            int M_max, const int32_t* rows, int N, int K, int epi, int32_t* err, cudaStream_t stream);
+
+cudaError_t launch_attention_varlen(const void* qkv, const int32_t* cu, int B, int T_max, int max_len, int nh, int d,
+                                    rpp_dtype dtype, void* out, int32_t* err, cudaStream_t stream);
+
+bool window_attention_supported(int C, int nh, int w, int I, int s);
+cudaError_t launch_window_attention(int B, const void* qkv, const float* bias, void* out, int C, int nh, int I, int w,
+                                    int s, rpp_dtype dtype, int32_t* err, cudaStream_t stream);
+cudaError_t launch_swin_bias(const void* table, rpp_dtype table_dtype, int w, int nh, float* bias,
+                             cudaStream_t stream);
+
+}  // namespace rpp

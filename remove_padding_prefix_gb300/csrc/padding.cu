@@ -1,0 +1,154 @@
+// Offset mask, padding removal and rebuild ('GPU底層優化 | 如何讓Transformer在GPU上跑得更快？',
+// Fig. 9: an Offset Mask converts between the padded and the padding-removed batch).
+//
+// The offset builder is one CTA: a block-wide exclusive scan of the lengths followed
+// by a cooperative fill of padding_offset.  Removal and rebuild are flat 16-byte
+// vector copies over (row, vector) pairs with a grid-stride loop; the number of valid
+// rows T = cu_seqlens[B] is read on the device so no host synchronisation is needed.
+#include "kernels.h"
+
+namespace rpp {
+
+namespace {
+
+constexpr int kScanThreads = 1024;
+
+__global__ void __launch_bounds__(kScanThreads) build_offsets_kernel(const int32_t* __restrict__ lengths, int B,
+                                                                     int L, int32_t* __restrict__ cu,
+                                                                     int32_t* __restrict__ padding_offset,
+                                                                     int32_t* err) {
+  __shared__ int32_t warp_sums[kScanThreads / 32];
+  __shared__ int32_t s_carry;
+  const int tid = threadIdx.x;
+  if (tid == 0) s_carry = 0;
+  __syncthreads();
+  // chunked block scan: each pass handles kScanThreads lengths
+  for (int base = 0; base < B; base += kScanThreads) {
+    const int b = base + tid;
+    int32_t v = 0;
+    if (b < B) {
+      v = lengths[b];
+      if (v < 0 || v > L) {
+        set_device_error(err, RPP_DERR_LENGTH);
+        v = v < 0 ? 0 : L;
+      }
+    }
+    // inclusive warp scan
+    int32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+      if ((tid & 31) >= o) x += y;
+    }
+    if ((tid & 31) == 31) warp_sums[tid >> 5] = x;
+    __syncthreads();
+    if (tid < 32) {
+      int32_t w = warp_sums[tid];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+        if (tid >= o) w += y;
+      }
+      warp_sums[tid] = w;   // inclusive over warps
+    }
+    __syncthreads();
+    const int32_t carry = s_carry;
+    const int32_t incl = x + ((tid >> 5) ? warp_sums[(tid >> 5) - 1] : 0) + carry;
+    if (b < B) cu[b + 1] = incl;
+    if (b == 0) cu[0] = 0;
+    __syncthreads();
+    if (tid == kScanThreads - 1) s_carry = incl;
+    __syncthreads();
+  }
+  __syncthreads();
+  // padding_offset[i] = b*L - cu[b] for i in [cu[b], cu[b+1]); one pass over the (b, p) slots
+  const long long slots = static_cast<long long>(B) * L;
+  for (long long s = tid; s < slots; s += kScanThreads) {
+    const int b = static_cast<int>(s / L);
+    const int p = static_cast<int>(s - static_cast<long long>(b) * L);
+    const int32_t c0 = cu[b];
+    const int32_t len = cu[b + 1] - c0;
+    if (p < len) padding_offset[c0 + p] = b * L - c0;
+  }
+}
+
+// packed[i] = padded[i + po[i]] for i < T; VPR 16-byte vectors per row
+__global__ void remove_padding_kernel(const uint4* __restrict__ padded, const int32_t* __restrict__ po,
+                                      const int32_t* __restrict__ cu, int B, int T_max, int vpr,
+                                      uint4* __restrict__ packed, int32_t* err) {
+  if (device_error_set(err)) return;
+  int T = cu[B];
+  if (T > T_max || T < 0) {
+    set_device_error(err, RPP_DERR_ROWS);
+    return;
+  }
+  const long long total = static_cast<long long>(T) * vpr;
+  for (long long v = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; v < total;
+       v += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int row = static_cast<int>(v / vpr);
+    const int c = static_cast<int>(v - static_cast<long long>(row) * vpr);
+    const int src_row = row + po[row];
+    if (src_row < 0 || src_row >= T_max) {   // offsets inconsistent with cu_seqlens
+      set_device_error(err, RPP_DERR_ROWS);
+      continue;
+    }
+    packed[v] = __ldg(padded + static_cast<long long>(src_row) * vpr + c);
+  }
+}
+
+// padded[b*L + p] = p < len_b ? packed[cu[b] + p] : 0
+__global__ void rebuild_padding_kernel(const uint4* __restrict__ packed, const int32_t* __restrict__ cu, int B,
+                                       int L, int vpr, uint4* __restrict__ padded, int32_t* err) {
+  if (device_error_set(err)) return;
+  const long long total = static_cast<long long>(B) * L * vpr;
+  for (long long v = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; v < total;
+       v += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = v / vpr;
+    const int c = static_cast<int>(v - row * vpr);
+    const int b = static_cast<int>(row / L);
+    const int p = static_cast<int>(row - static_cast<long long>(b) * L);
+    const int32_t c0 = cu[b];
+    const int32_t len = cu[b + 1] - c0;
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (p < len) val = __ldg(packed + (static_cast<long long>(c0) + p) * vpr + c);
+    padded[v] = val;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_build_offsets(const int32_t* lengths, int B, int L, int32_t* cu, int32_t* po, int32_t* err,
+                                 cudaStream_t stream) {
+  build_offsets_kernel<<<1, kScanThreads, 0, stream>>>(lengths, B, L, cu, po, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_remove_padding(const void* padded, const int32_t* po, const int32_t* cu, int B, int L,
+                                  int row_bytes, void* packed, int32_t* err, cudaStream_t stream) {
+  const int vpr = row_bytes / 16;
+  const long long total = static_cast<long long>(B) * L * vpr;
+  const int threads = 256;
+  long long blocks = (total + threads - 1) / threads;
+  const long long cap = static_cast<long long>(num_sms()) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  remove_padding_kernel<<<static_cast<int>(blocks), threads, 0, stream>>>(
+      static_cast<const uint4*>(padded), po, cu, B, B * L, vpr, static_cast<uint4*>(packed), err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rebuild_padding(const void* packed, const int32_t* cu, int B, int L, int row_bytes,
+                                   void* padded, int32_t* err, cudaStream_t stream) {
+  const int vpr = row_bytes / 16;
+  const long long total = static_cast<long long>(B) * L * vpr;
+  const int threads = 256;
+  long long blocks = (total + threads - 1) / threads;
+  const long long cap = static_cast<long long>(num_sms()) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  rebuild_padding_kernel<<<static_cast<int>(blocks), threads, 0, stream>>>(
+      static_cast<const uint4*>(packed), cu, B, L, vpr, static_cast<uint4*>(padded), err);
+  return cudaGetLastError();
+}
+
+}  // namespace rpp

@@ -1,0 +1,305 @@
+// Shifted-window attention with the cyclic shift, window partition, window reverse
+// and unshift folded into the kernel's loads and stores, plus the relative-position
+// bias lookup done once in preprocessing.
+//
+// NVIDIA Swin talk: §1 (window attention, cyclic window shift, relative position
+// bias), §2 (window shift / partition / merge are pure index mappings; the training
+// timeline spent 4.6 % in roll kernels alone), §3 (bias lookup moved to
+// preprocessing; batch GEMM + softmax + batch GEMM in one fMHA kernel with the
+// transposes in its I/O; the 49-token windows padded to a multiple of 8).
+//
+// One CTA (4 warps) processes whole windows in a persistent loop.  For window
+// (image, wy, wx) token t = ty*w + tx sits at (y, x) = (wy*w + ty, wx*w + tx) in the
+// shifted frame and reads raster row ((y + s) mod I, (x + s) mod I); the output row
+// is written back to the same raster row, which performs reverse + unshift.  The
+// 49 rows are padded to 64 inside shared memory only (padding rows stay zero); warp w
+// owns query rows 16w..16w+15.  S = Q K^T and O = P V use mma.sync.m16n8k16 with fp32
+// accumulation; scores get the bias and, for shifted blocks, exclusion of pairs from
+// different regions of the shifted frame (per axis: c < I-w, c < I-s, else).
+#include "kernels.h"
+
+namespace rpp {
+
+namespace {
+
+constexpr int kWD = 32;     // head dim
+constexpr int kWRows = 64;  // padded window rows
+
+// 64-byte rows (32 x 16-bit): chunk c of row r lives at chunk c ^ ((r >> 1) & 3)
+__device__ __forceinline__ uint32_t swz64(int r, int c) {
+  return static_cast<uint32_t>(r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+}
+
+__device__ __forceinline__ void ldsm_x4w(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4w_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+template <typename T>
+__device__ __forceinline__ void mma_w(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  if constexpr (sizeof(T) == 2 && std::is_same<T, __half>::value) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2w(float lo, float hi) {
+  if constexpr (std::is_same<T, __half>::value) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+__device__ __forceinline__ int region(int c, int I, int w, int s) { return c < I - w ? 0 : (c < I - s ? 1 : 2); }
+
+template <typename T, int NH>
+__global__ void __launch_bounds__(128) window_attention_kernel(const T* __restrict__ qkv,
+                                                               const float* __restrict__ bias, T* __restrict__ out,
+                                                               int B, int I, int w, int s, float scale_log2,
+                                                               int32_t* err) {
+  if (device_error_set(err)) return;
+  constexpr int C = NH * kWD;
+  constexpr int TILE = kWRows * kWD * 2;   // bytes of one 64 x 32 tile
+  extern __shared__ __align__(128) uint8_t wsm[];
+  uint8_t* sQKV = wsm;                                      // [3][NH][64][32]
+  float* sBias = reinterpret_cast<float*>(wsm + 3 * NH * TILE);   // [NH][N][N] (pre-scaled by log2 e)
+  const int N = w * w;
+  int* sRow = reinterpret_cast<int*>(sBias + NH * N * N);   // [64] raster rows of the window
+  int* sLab = sRow + kWRows;                                // [64] region labels
+
+  const int tid = threadIdx.x;
+  const int warp = warp_id();
+  const int lane = lane_id();
+  const float log2e = 1.4426950408889634f;
+  for (int i = tid; i < NH * N * N; i += blockDim.x) sBias[i] = bias[i] * log2e;
+  // padding rows (N..63) of every tile stay zero for the whole kernel
+  for (int i = tid; i < 3 * NH * kWRows * 4; i += blockDim.x) {
+    const int tile = i / (kWRows * 4);
+    const int r = (i / 4) % kWRows;
+    if (r >= N) *reinterpret_cast<uint4*>(sQKV + tile * TILE + swz64(r, i & 3)) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  const int nWs = I / w;
+  const int nW = nWs * nWs;
+  const long long total = static_cast<long long>(B) * nW;
+
+  for (long long wid = blockIdx.x; wid < total; wid += gridDim.x) {
+    const int img = static_cast<int>(wid / nW);
+    const int wr = static_cast<int>(wid - static_cast<long long>(img) * nW);
+    const int wy = wr / nWs, wx = wr - (wr / nWs) * nWs;
+    __syncthreads();   // previous window fully consumed
+    if (tid < N) {
+      const int y = wy * w + tid / w, x = wx * w + tid % w;
+      int ys = y + s, xs = x + s;
+      if (ys >= I) ys -= I;
+      if (xs >= I) xs -= I;
+      sRow[tid] = img * I * I + ys * I + xs;
+      sLab[tid] = s > 0 ? 3 * region(y, I, w, s) + region(x, I, w, s) : 0;
+    }
+    __syncthreads();
+    // gather: N rows x (3 * NH * 4) chunks of 16 bytes
+    const int cpr = 3 * NH * 4;
+    for (int i = tid; i < N * cpr; i += blockDim.x) {
+      const int r = i / cpr;
+      const int cc = i - r * cpr;         // chunk within the qkv row: (part, head, chunk)
+      const int tile = cc >> 2;           // part * NH + head
+      const T* src = qkv + static_cast<long long>(sRow[r]) * (3 * C) + cc * 8;
+      cp_async_16(sQKV + tile * TILE + swz64(r, cc & 3), src, true);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+
+    const int rA = warp * 16 + (lane >> 2);   // this thread's two query rows: rA, rA + 8
+    for (int h = 0; h < NH; ++h) {
+      const uint32_t sQa = smem_u32(sQKV + (0 * NH + h) * TILE);
+      const uint32_t sKa = smem_u32(sQKV + (1 * NH + h) * TILE);
+      const uint32_t sVa = smem_u32(sQKV + (2 * NH + h) * TILE);
+      uint32_t qf[2][4];
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        const int r = warp * 16 + (lane & 15);
+        ldsm_x4w(sQa + swz64(r, kk * 2 + (lane >> 4)), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
+      }
+      float sc[8][4];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+#pragma unroll
+        for (int np = 0; np < 4; ++np) {
+          uint32_t b0, b1, b2, b3;
+          const int r = np * 16 + (lane & 7) + ((lane >> 4) << 3);
+          ldsm_x4w(sKa + swz64(r, kk * 2 + ((lane >> 3) & 1)), b0, b1, b2, b3);
+          mma_w<T>(sc[2 * np], qf[kk], b0, b1);
+          mma_w<T>(sc[2 * np + 1], qf[kk], b2, b3);
+        }
+      }
+      // scores -> log2 domain with bias and region mask; softmax over the N keys
+      float mx[2] = {-INFINITY, -INFINITY};
+      const float* bh = sBias + h * N * N;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = rA + ((e >> 1) << 3);
+          const int u = j * 8 + 2 * (lane & 3) + (e & 1);
+          float v = -INFINITY;
+          if (u < N && t < N && sLab[t] == sLab[u]) v = sc[j][e] * scale_log2 + bh[t * N + u];
+          sc[j][e] = v;
+        }
+        mx[0] = fmaxf(mx[0], fmaxf(sc[j][0], sc[j][1]));
+        mx[1] = fmaxf(mx[1], fmaxf(sc[j][2], sc[j][3]));
+      }
+      float sum[2] = {0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
+        mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
+        if (mx[i] == -INFINITY) mx[i] = 0.f;   // padding query rows
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        sc[j][0] = exp2f(sc[j][0] - mx[0]);
+        sc[j][1] = exp2f(sc[j][1] - mx[0]);
+        sc[j][2] = exp2f(sc[j][2] - mx[1]);
+        sc[j][3] = exp2f(sc[j][3] - mx[1]);
+        sum[0] += sc[j][0] + sc[j][1];
+        sum[1] += sc[j][2] + sc[j][3];
+      }
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], 1);
+        sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], 2);
+        sum[i] = sum[i] > 0.f ? 1.f / sum[i] : 0.f;
+      }
+      float o[4][4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        uint32_t pa[4];
+        pa[0] = pack2w<T>(sc[2 * kk][0], sc[2 * kk][1]);
+        pa[1] = pack2w<T>(sc[2 * kk][2], sc[2 * kk][3]);
+        pa[2] = pack2w<T>(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+        pa[3] = pack2w<T>(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+#pragma unroll
+        for (int dp = 0; dp < 2; ++dp) {
+          uint32_t b0, b1, b2, b3;
+          const int r = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+          ldsm_x4w_t(sVa + swz64(r, dp * 2 + (lane >> 4)), b0, b1, b2, b3);
+          mma_w<T>(o[2 * dp], pa, b0, b1);
+          mma_w<T>(o[2 * dp + 1], pa, b2, b3);
+        }
+      }
+      // write the normalised head output over this warp's own Q rows of head h (no
+      // longer needed); the scatter below reads it back
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = pack2w<T>(o[j][0] * sum[0], o[j][1] * sum[0]);
+        const uint32_t hi = pack2w<T>(o[j][2] * sum[1], o[j][3] * sum[1]);
+        uint8_t* tq = sQKV + (0 * NH + h) * TILE;
+        *reinterpret_cast<uint32_t*>(tq + swz64(rA, j) + (lane & 3) * 4) = lo;
+        *reinterpret_cast<uint32_t*>(tq + swz64(rA + 8, j) + (lane & 3) * 4) = hi;
+      }
+    }
+    __syncthreads();
+    // scatter: N rows x (NH * 4) chunks back to the same raster rows
+    const int opr = NH * 4;
+    for (int i = tid; i < N * opr; i += blockDim.x) {
+      const int r = i / opr;
+      const int cc = i - r * opr;
+      const uint4 v = *reinterpret_cast<const uint4*>(sQKV + (cc >> 2) * TILE + swz64(r, cc & 3));
+      *reinterpret_cast<uint4*>(out + static_cast<long long>(sRow[r]) * C + cc * 8) = v;
+    }
+  }
+}
+
+__global__ void swin_bias_kernel(const void* table, int table_dtype, int w, int nh, float* bias) {
+  const int N = w * w;
+  const int total = nh * N * N;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const int h = i / (N * N);
+    const int t = (i / N) % N;
+    const int u = i % N;
+    const int ty = t / w, tx = t % w, uy = u / w, ux = u % w;
+    const int idx = (ty - uy + w - 1) * (2 * w - 1) + (tx - ux + w - 1);
+    float v;
+    if (table_dtype == RPP_F16) v = __half2float(static_cast<const __half*>(table)[idx * nh + h]);
+    else if (table_dtype == RPP_BF16) v = __bfloat162float(static_cast<const __nv_bfloat16*>(table)[idx * nh + h]);
+    else v = static_cast<const float*>(table)[idx * nh + h];
+    bias[i] = v;
+  }
+}
+
+template <typename T, int NH>
+cudaError_t wa_launch(int B, const void* qkv, const float* bias, void* out, int I, int w, int s, int32_t* err,
+                      cudaStream_t stream) {
+  const int N = w * w;
+  const size_t smem = 3 * NH * kWRows * kWD * 2 + NH * N * N * sizeof(float) + 2 * kWRows * sizeof(int);
+  auto kern = window_attention_kernel<T, NH>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const long long windows = static_cast<long long>(B) * (I / w) * (I / w);
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 128, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  long long grid = static_cast<long long>(num_sms()) * per_sm;
+  if (grid > windows) grid = windows;
+  if (grid < 1) grid = 1;
+  const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kWD));
+  kern<<<static_cast<int>(grid), 128, smem, stream>>>(static_cast<const T*>(qkv), bias, static_cast<T*>(out), B, I, w,
+                                                      s, scale_log2, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool window_attention_supported(int C, int nh, int w, int I, int s) {
+  return nh > 0 && C == nh * kWD && (nh == 3 || nh == 6) && w > 0 && w * w <= kWRows && I % w == 0 && s >= 0 &&
+         s < w;
+}
+
+cudaError_t launch_window_attention(int B, const void* qkv, const float* bias, void* out, int C, int nh, int I, int w,
+                                    int s, rpp_dtype dtype, int32_t* err, cudaStream_t stream) {
+  if (!window_attention_supported(C, nh, w, I, s)) return cudaErrorNotSupported;
+  if (B <= 0) return cudaSuccess;
+  if (dtype == RPP_F16) {
+    if (nh == 3) return wa_launch<__half, 3>(B, qkv, bias, out, I, w, s, err, stream);
+    return wa_launch<__half, 6>(B, qkv, bias, out, I, w, s, err, stream);
+  }
+  if (dtype == RPP_BF16) {
+    if (nh == 3) return wa_launch<__nv_bfloat16, 3>(B, qkv, bias, out, I, w, s, err, stream);
+    return wa_launch<__nv_bfloat16, 6>(B, qkv, bias, out, I, w, s, err, stream);
+  }
+  return cudaErrorNotSupported;
+}
+
+cudaError_t launch_swin_bias(const void* table, rpp_dtype table_dtype, int w, int nh, float* bias,
+                             cudaStream_t stream) {
+  const int total = nh * w * w * w * w;
+  swin_bias_kernel<<<(total + 255) / 256, 256, 0, stream>>>(table, table_dtype, w, nh, bias);
+  return cudaGetLastError();
+}
+
+}  // namespace rpp

@@ -1,0 +1,86 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library loads and exports every entry point include/rpp.h declares; size
+queries and argument validation are pure host logic and return without touching the
+device.
+"""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rpp.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from remove_padding_prefix_gb300 import _abi, build
+    if not os.path.exists(_abi.LIB_PATH):
+        build.build()
+    return _abi.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"^RPP_API\s+[\w\s\*]+?\b(rpp_\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_functions())
+    for must in ("rpp_build_offsets", "rpp_remove_padding", "rpp_rebuild_padding", "rpp_encoder_layer_forward",
+                 "rpp_window_attention_forward", "rpp_swin_block_forward", "rpp_gemm_i8_i32"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from remove_padding_prefix_gb300 import _abi
+    names = declared_functions()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in _abi.SIGNATURES, f"binding lacks {n}"
+    assert set(_abi.SIGNATURES) == set(names)
+
+
+def test_status_strings_and_version(lib):
+    assert lib.rpp_status_string(0) == b"ok"
+    assert lib.rpp_status_string(-4) == b"workspace too small"
+    assert lib.rpp_version() >= 100
+
+
+def test_argument_validation_returns_without_launching(lib):
+    # null pointers and bad sizes are rejected on the host
+    assert lib.rpp_build_offsets(None, 4, 8, None, None, None, None) == -1
+    assert lib.rpp_remove_padding(None, None, None, 1, 1, 8, 1, None, None, None) == -1
+    assert lib.rpp_rebuild_padding(None, None, 1, 1, 8, 1, None, None, None) == -1
+    assert lib.rpp_linear(None, None, None, None, None, 1, None, 16, 16, 1, 0, None, None) == -1
+    assert lib.rpp_attention_varlen(None, None, 1, 1, 1, 1, 64, 1, None, None, None) == -1
+    assert lib.rpp_gemm_i8_i32(None, None, None, 1, 16, 16, None, 0, None, None) == -1
+    # misaligned activation pointer (odd address) is rejected before any launch
+    assert lib.rpp_remove_padding(1, 16, 16, 1, 1, 8, 1, 32, None, None) == -1
+
+
+def test_size_queries(lib):
+    from remove_padding_prefix_gb300 import _abi
+    cfg = _abi.EncoderCfg(768, 12, 64, 3072, 1e-12, _abi.RPP_F16, 0)
+    wbytes = lib.rpp_layer_bytes(C.byref(cfg))
+    H, F = 768, 3072
+    assert wbytes >= (4 * H * H + 2 * H * F) * 2 + (3 * H + 2 * H + F + 4 * H) * 4
+    ws = lib.rpp_encoder_workspace_bytes(C.byref(cfg), 4096)
+    assert ws >= 4096 * (3 * H + 3 * H + F) * 2
+    cfg8 = _abi.EncoderCfg(1024, 16, 64, 4096, 1e-12, _abi.RPP_F16, 1)
+    assert lib.rpp_encoder_workspace_bytes(C.byref(cfg8), 100) > lib.rpp_encoder_workspace_bytes(
+        C.byref(_abi.EncoderCfg(1024, 16, 64, 4096, 1e-12, _abi.RPP_F16, 0)), 100)
+    bad = _abi.EncoderCfg(768, 12, 60, 3072, 1e-12, _abi.RPP_F16, 0)   # heads * head_dim != hidden
+    assert lib.rpp_layer_bytes(C.byref(bad)) == 0
+    int8_bf16 = _abi.EncoderCfg(768, 12, 64, 3072, 1e-12, _abi.RPP_BF16, 1)   # int8 needs fp16 activations
+    assert lib.rpp_layer_bytes(C.byref(int8_bf16)) == 0
+    assert lib.rpp_gemm_i8_workspace_bytes(128, 64, 256) >= (128 + 64) * 256 * 2
+    sw = _abi.SwinCfg(56, 96, 3, 7, 3, 384, 1e-5, _abi.RPP_F16)
+    assert lib.rpp_swin_block_bytes(C.byref(sw)) > 0
+    assert lib.rpp_swin_workspace_bytes(C.byref(sw), 2) >= 2 * 56 * 56 * (96 * 5 + 384) * 2
+    # workspace too small is reported before any launch
+    assert lib.rpp_encoder_layer_forward(C.byref(cfg), 256, None, 256, 256, 4, 512, 128, 256, 256, 16, None,
+                                         None) == -4

@@ -1,0 +1,122 @@
+"""GPU parity of the layer's building blocks against the oracle: the tcgen05 GEMM with
+each fused epilogue, the fp32 GEMM, LayerNorm and the varlen attention kernel.
+
+Sizes span several 128-row tiles plus a ragged tail, every tile width the heuristic
+picks, and the device-side row count used inside the layer."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import remove_padding_prefix_gb300 as rpp
+from workloads import round_to_dtype
+from gpu_util import dev, up, down, assert_close, check_err, TDT
+
+pytestmark = pytest.mark.gpu
+
+
+def _gemm_case(dtype, M, N, K, epi, seed=0, rows=None):
+    rng = np.random.default_rng(seed)
+    a = round_to_dtype(rng.standard_normal((M, K), dtype=np.float32), dtype)
+    W = round_to_dtype(0.02 * rng.standard_normal((K, N), dtype=np.float32), dtype)   # [in, out]
+    b = round_to_dtype(0.02 * rng.standard_normal(N, dtype=np.float32), dtype)
+    r = round_to_dtype(rng.standard_normal((M, N), dtype=np.float32), dtype)
+    err = rpp.new_error_word()
+    rows_t = torch.tensor([rows], dtype=torch.int32, device=dev()) if rows is not None else None
+    out = torch.full((M, N), float("nan"), dtype=TDT[dtype], device=dev())
+    res_t = up(r, dtype) if epi == rpp.RPP_EPI_BIAS_RESIDUAL else None
+    rpp.linear(up(a, dtype), up(W.T, dtype), torch.as_tensor(b, device=dev()), epilogue=epi, residual=res_t,
+               out=out, rows=rows_t, err=err)
+    check_err(err)
+    ref = oracle.linear(a, W, b)
+    if epi == rpp.RPP_EPI_BIAS_GELU:
+        ref = oracle.gelu(ref)
+    if epi == rpp.RPP_EPI_BIAS_RESIDUAL:
+        ref = ref + r
+    m = M if rows is None else rows
+    assert_close(down(out[:m]), ref[:m], dtype, f"linear {dtype} {M}x{N}x{K} epi{epi}")
+    if rows is not None:   # rows past the device count are never written
+        assert torch.isnan(out[m:].float()).all()
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("epi", [0, 1, 2])
+def test_tc_gemm_epilogues(dtype, epi):
+    _gemm_case(dtype, 300, 256, 192, epi, seed=epi)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 16, 8), (129, 2304, 768), (2304, 768, 3072), (517, 3072, 1024),
+                                   (1000, 288, 96), (384, 96, 384), (255, 144, 64)])
+def test_tc_gemm_shapes(M, N, K):
+    _gemm_case("fp16", M, N, K, rpp.RPP_EPI_BIAS, seed=M)
+
+
+def test_tc_gemm_device_row_count():
+    _gemm_case("bf16", 1000, 768, 256, rpp.RPP_EPI_BIAS_RESIDUAL, rows=613)
+    _gemm_case("fp16", 512, 128, 64, rpp.RPP_EPI_BIAS, rows=0)
+
+
+@pytest.mark.parametrize("epi", [0, 1, 2])
+def test_f32_gemm(epi):
+    _gemm_case("fp32", 150, 256, 1024, epi, seed=10 + epi)
+
+
+@pytest.mark.parametrize("dtype,H", [("fp32", 256), ("fp16", 768), ("bf16", 1024), ("fp16", 96), ("bf16", 96)])
+def test_layernorm(dtype, H):
+    rng = np.random.default_rng(H)
+    M = 333
+    x = round_to_dtype(rng.standard_normal((M, H), dtype=np.float32) * 2 + 0.5, dtype)
+    g = round_to_dtype(1 + 0.1 * rng.standard_normal(H, dtype=np.float32), dtype)
+    b = round_to_dtype(0.1 * rng.standard_normal(H, dtype=np.float32), dtype)
+    eps = 1e-5 if H == 96 else 1e-12
+    err = rpp.new_error_word()
+    y = rpp.layernorm(up(x, dtype), torch.as_tensor(g, device=dev()), torch.as_tensor(b, device=dev()), eps, err=err)
+    check_err(err)
+    assert_close(down(y), oracle.layernorm(x, g, b, eps), dtype, f"layernorm {dtype} H={H}")
+
+
+def _attention_case(dtype, lengths, nh, seed=0, max_len=None):
+    rng = np.random.default_rng(seed)
+    lengths = np.asarray(lengths, np.int32)
+    L = int(max_len or max(1, lengths.max()))
+    T = int(lengths.sum())
+    T_max = max(T, 1) + 5   # capacity larger than T: rows past T must be ignored
+    d = 64
+    qkv = round_to_dtype(rng.standard_normal((T_max, 3 * nh * d), dtype=np.float32), dtype)
+    lt = torch.as_tensor(lengths, device=dev())
+    err = rpp.new_error_word()
+    cu, _ = rpp.build_offsets(lt, L, err=err)
+    out = torch.full((T_max, nh * d), float("nan"), dtype=TDT[dtype], device=dev())
+    rpp.attention_varlen(up(qkv, dtype), cu, len(lengths), L, nh, out=out, err=err)
+    check_err(err)
+    cu_ref, _, _ = oracle.build_offsets(lengths, L)
+    H = nh * d
+    ref = oracle.attention_varlen(qkv[:T, :H], qkv[:T, H:2 * H], qkv[:T, 2 * H:], cu_ref, nh)
+    if T:
+        assert_close(down(out[:T]), ref, dtype, f"attention {dtype} lens={lengths.tolist()[:6]}")
+    assert torch.isnan(out[T:].float()).all()
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16", "fp32"])
+def test_attention_ragged(dtype):
+    _attention_case(dtype, [1, 63, 64, 65, 128, 129, 200, 7], nh=4, seed=1)
+
+
+def test_attention_bert_large_lengths():
+    rng = np.random.default_rng(7)
+    lens = np.concatenate([rng.integers(32, 129, 8), rng.integers(256, 385, 8)])
+    _attention_case("bf16", lens, nh=16, seed=2, max_len=384)
+
+
+def test_attention_empty_and_zero_length_sequences():
+    _attention_case("fp16", [0, 5, 0, 0, 70], nh=2, seed=3)
+    _attention_case("fp16", [0, 0], nh=2, seed=4, max_len=8)
+
+
+def test_attention_rejects_length_above_max_len():
+    lengths = np.array([10, 40], np.int32)
+    qkv = torch.zeros(50, 3 * 64, dtype=torch.float16, device=dev())
+    err = rpp.new_error_word()
+    cu, _ = rpp.build_offsets(torch.as_tensor(lengths, device=dev()), 64, err=err)
+    rpp.attention_varlen(qkv, cu, 2, 32, 1, err=err)   # max_len 32 < 40
+    assert rpp.get_device_error(err) == rpp.RPP_DERR_LENGTH
