@@ -78,6 +78,17 @@ RPP_API int rpp_version(void);
  * otherwise; RPP_ECUDA if the copy failed. */
 RPP_API rpp_status rpp_get_device_error(const int32_t* err, int32_t* host_code, rpp_stream stream);
 
+/* Launch-event hook for profiling (the pages profile with Nsight timelines; this
+ * hook lets a caller time each kernel inside the real step with CUDA events).  While
+ * enabled, every kernel the path launches is followed by cudaEventRecord(events[i++])
+ * on its stream, i < capacity, and its label (e.g. "gemm_fc1") is kept.  `events` is
+ * a host array of cudaEvent_t owned by the caller; capacity 0 disables the hook.
+ * Not thread-safe: one profiling caller at a time. */
+RPP_API rpp_status rpp_set_launch_events(void* const* events, int capacity);
+/* Events recorded since the last rpp_set_launch_events; label of the i-th ("" if out of range). */
+RPP_API int rpp_launch_event_count(void);
+RPP_API const char* rpp_launch_event_label(int i);
+
 /* ------------------------------------------------------------------------------
  * Padding removal ([KS] Fig. 9, Fig. 10)
  * ------------------------------------------------------------------------------ */
@@ -164,6 +175,8 @@ typedef struct rpp_encoder_cfg {
   float eps;     /* LayerNorm eps */
   int dtype;     /* rpp_dtype of activations and float weights: RPP_F32, RPP_F16, RPP_BF16 */
   int int8;      /* 1: the four linear GEMMs run on int8 codes (dtype must be RPP_F16) */
+  int tokens_hint; /* expected valid tokens per forward call (0: unknown, the capacity T_max is
+                      assumed); only tile shapes and K splits depend on it, never the result */
 } rpp_encoder_cfg;
 
 /* The caller's float weights (device, dtype of cfg, row-major [in, out] as in x @ W). */

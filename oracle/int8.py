@@ -52,8 +52,16 @@ def quantize_activation(x, s_a):
 
 
 def int8_gemm(aq, bq):
-    """Exact integer product of int8 matrices aq [M, K] and bq [K, N]; int64 result."""
-    return np.asarray(aq, np.int64) @ np.asarray(bq, np.int64)
+    """Exact integer product of int8 matrices aq [M, K] and bq [K, N]; int64 result.
+
+    Computed as a float64 matrix product: every product is an integer of magnitude at
+    most 127^2 and every partial sum stays below 2^53 for K < 2^38, so float64
+    represents all of them exactly whatever the summation order.
+    """
+    aq = np.asarray(aq)
+    bq = np.asarray(bq)
+    assert aq.shape[1] < 2 ** 38
+    return (aq.astype(np.float64) @ bq.astype(np.float64)).astype(np.int64)
 
 
 def int8_linear(x, s_a, Wq, s_w, b):

@@ -146,9 +146,9 @@ def attention_varlen(qkv, cu_seqlens, B: int, max_len: int, nh: int, d: int = 64
 
 
 # ---------------------------------------------------------------- encoder layer
-def encoder_cfg(H, nh, F, eps, dtype, int8=False) -> EncoderCfg:
+def encoder_cfg(H, nh, F, eps, dtype, int8=False, tokens_hint=0) -> EncoderCfg:
     code = dtype_code(dtype) if not isinstance(dtype, int) else dtype
-    return EncoderCfg(H, nh, H // nh, F, float(eps), code, 1 if int8 else 0)
+    return EncoderCfg(H, nh, H // nh, F, float(eps), code, 1 if int8 else 0, int(tokens_hint))
 
 
 class EncoderLayer:

@@ -23,7 +23,7 @@ sz = C.c_size_t
 
 class EncoderCfg(C.Structure):
     _fields_ = [("hidden", i32), ("heads", i32), ("head_dim", i32), ("ffn", i32), ("eps", f32),
-                ("dtype", i32), ("int8", i32)]
+                ("dtype", i32), ("int8", i32), ("tokens_hint", i32)]
 
 
 class LayerSrc(C.Structure):
@@ -45,6 +45,9 @@ class SwinSrc(C.Structure):
 SIGNATURES = {
     "rpp_status_string": (C.c_char_p, [i32]),
     "rpp_version": (i32, []),
+    "rpp_set_launch_events": (i32, [C.POINTER(vp), i32]),
+    "rpp_launch_event_count": (i32, []),
+    "rpp_launch_event_label": (C.c_char_p, [i32]),
     "rpp_get_device_error": (i32, [vp, C.POINTER(C.c_int32), vp]),
     "rpp_build_offsets": (i32, [vp, i32, i32, vp, vp, vp, vp]),
     "rpp_remove_padding": (i32, [vp, vp, vp, i32, i32, i32, i32, vp, vp, vp]),

@@ -36,10 +36,37 @@ inline rpp_status from_cuda(cudaError_t e) {
   return RPP_ECUDA;
 }
 
+// ---------------------------------------------------------------- launch-event hook
+// While enabled (rpp_set_launch_events), every kernel launch of the path is followed
+// by cudaEventRecord of the next caller-provided event on the launch's stream, and its
+// label is kept, so a profiler can time each kernel inside the real step.
+struct LaunchHook {
+  cudaEvent_t* events = nullptr;
+  int capacity = 0;
+  int count = 0;
+  const char* labels[4096];
+};
+LaunchHook g_hook;
+
+inline cudaError_t note(const char* label, cudaStream_t s) {
+  if (g_hook.events && g_hook.count < g_hook.capacity) {
+    if (g_hook.count < 4096) g_hook.labels[g_hook.count] = label;
+    return cudaEventRecord(g_hook.events[g_hook.count++], s);
+  }
+  return cudaSuccess;
+}
+
 #define RPP_TRY(expr)                         \
   do {                                        \
     const rpp_status st_ = from_cuda(expr);   \
     if (st_ != RPP_OK) return st_;            \
+  } while (0)
+
+// launch, then (when profiling) record the event that marks its end
+#define RPP_LAUNCH(label, stream, expr)          \
+  do {                                           \
+    RPP_TRY(expr);                               \
+    RPP_TRY(note(label, stream));                \
   } while (0)
 
 // ---------------------------------------------------------------- prepared encoder layer
@@ -104,9 +131,16 @@ LayerLayout layer_layout(const rpp_encoder_cfg* c) {
   return L;
 }
 
+constexpr int kMaxSplits = 4;   // K splits of the proj / FC2 GEMMs (partials summed by LayerNorm)
+
 struct EncWs {
-  size_t qkv, attn, h, x1, g, cx, ca, cx1, cg, total;
+  size_t qkv, attn, h, x1, x1f, g, cx, ca, cx1, cg, total;
 };
+
+// bf16 layers keep the LN1 output used as the FC2 residual in fp32 as well: with
+// 8 significand bits, rounding that residual would add up to half a bf16 step to the
+// final output on top of the output's own rounding
+inline bool fp32_residual(const rpp_encoder_cfg* c) { return c->dtype == RPP_BF16 && !c->int8; }
 
 EncWs enc_ws_layout(const rpp_encoder_cfg* c, int T_max) {
   EncWs w{};
@@ -115,8 +149,11 @@ EncWs enc_ws_layout(const rpp_encoder_cfg* c, int T_max) {
   size_t o = 0;
   w.qkv = o;  o = align_up(o + T * 3 * H * e);
   w.attn = o; o = align_up(o + T * H * e);
-  w.h = o;    o = align_up(o + T * H * e);
+  w.h = o;    o = align_up(o + kMaxSplits * T * H * 4);   // fp32 pre-LayerNorm sums (split-K slices)
   w.x1 = o;   o = align_up(o + T * H * e);
+  if (fp32_residual(c)) {
+    w.x1f = o; o = align_up(o + T * H * 4);
+  }
   w.g = o;    o = align_up(o + T * F * e);
   if (c->int8) {   // bf16-held int8 codes of the four GEMM inputs
     w.cx = o;  o = align_up(o + T * H * 2);
@@ -139,7 +176,12 @@ inline const P* at(const void* base, size_t off) {
 
 // one GEMM of the float path: tensor cores for fp16 / bf16, CUDA cores for fp32
 cudaError_t linear(rpp_dtype dt, const void* a, const void* w_t, const float* bias, const void* residual, void* out,
-                   int M_max, const int32_t* rows, int N, int K, int epi, int32_t* err, cudaStream_t s) {
+                   int M_max, const int32_t* rows, int N, int K, int epi, int32_t* err, cudaStream_t s,
+                   rpp_dtype out_dt = RPP_I8 /* = dt */, rpp_dtype res_dt = RPP_I8 /* = dt */, int rows_hint = 0,
+                   int max_splits = 1, int* splits_out = nullptr) {
+  if (splits_out) *splits_out = 1;
+  if (out_dt == RPP_I8) out_dt = dt;
+  if (res_dt == RPP_I8) res_dt = dt;
   if (dt == RPP_F32)
     return launch_gemm_f32(static_cast<const float*>(a), static_cast<const float*>(w_t), bias,
                            static_cast<const float*>(residual), static_cast<float*>(out), M_max, rows, N, K, epi, err,
@@ -147,15 +189,18 @@ cudaError_t linear(rpp_dtype dt, const void* a, const void* w_t, const float* bi
   TcGemmArgs g{};
   g.a = a; g.w_t = w_t; g.bias = bias; g.residual = residual; g.out = out;
   g.M_max = M_max; g.rows = rows; g.N = N; g.K = K;
-  g.in_dtype = dt; g.out_dtype = dt; g.epi = epi; g.err = err;
+  g.in_dtype = dt; g.out_dtype = out_dt; g.res_dtype = res_dt; g.epi = epi; g.err = err;
+  g.rows_hint = rows_hint; g.max_splits = max_splits; g.splits_out = splits_out;
   return launch_gemm_tc(g, s);
 }
 
 // one GEMM of the int8 path (bf16-held codes in, fp16 / codes out)
 cudaError_t linear_i8(const void* a_codes, const void* w_codes, const float* bias, const float* a_scale,
                       const float* w_scale, const float* q_scale, const void* residual, void* out, rpp_dtype out_dt,
-                      int M_max, const int32_t* rows, int N, int K, int epi, int32_t* err, cudaStream_t s) {
+                      int M_max, const int32_t* rows, int N, int K, int epi, int32_t* err, cudaStream_t s,
+                      int rows_hint) {
   TcGemmArgs g{};
+  g.rows_hint = rows_hint;
   g.a = a_codes; g.w_t = w_codes; g.bias = bias; g.residual = residual; g.out = out;
   g.M_max = M_max; g.rows = rows; g.N = N; g.K = K;
   g.in_dtype = RPP_BF16; g.out_dtype = out_dt; g.epi = epi;
@@ -177,11 +222,16 @@ rpp_status encoder_layer_run(const rpp_encoder_cfg* c, const void* layer, const 
   const rpp_dtype dt = static_cast<rpp_dtype>(c->dtype);
   const int H = c->hidden, F = c->ffn, nh = c->heads, d = c->head_dim;
   const int32_t* rows = cu + B;   // T lives in device memory
+  const int hint = c->tokens_hint > 0 && c->tokens_hint < T_max ? c->tokens_hint : T_max;
+  const long long hs = static_cast<long long>(T_max) * H;   // elements between split-K slices
+  int sp_proj = 1, sp_fc2 = 1;
   void* qkv = at<void>(ws, W.qkv);
   void* attn = at<void>(ws, W.attn);
   void* h = at<void>(ws, W.h);
   void* x1 = at<void>(ws, W.x1);
   void* g = at<void>(ws, W.g);
+  // the pre-LayerNorm residual sums stay fp32 (fp32 layers: same type)
+  const rpp_dtype hdt = RPP_F32;
   const float* bqkv = at<float>(layer, P.bqkv);
   const float* bo = at<float>(layer, P.bo);
   const float* b1 = at<float>(layer, P.b1);
@@ -192,17 +242,24 @@ rpp_status encoder_layer_run(const rpp_encoder_cfg* c, const void* layer, const 
   const float* be2 = at<float>(layer, P.be2);
 
   if (!c->int8) {
-    if (amax) RPP_TRY(launch_amax(x, T_max, rows, H, dt, amax + 0, err, s));
-    RPP_TRY(linear(dt, x, at<void>(layer, P.wqkv), bqkv, nullptr, qkv, T_max, rows, 3 * H, H, RPP_EPI_BIAS, err, s));
-    RPP_TRY(launch_attention_varlen(qkv, cu, B, T_max, max_len, nh, d, dt, attn, err, s));
-    if (amax) RPP_TRY(launch_amax(attn, T_max, rows, H, dt, amax + 1, err, s));
-    RPP_TRY(linear(dt, attn, at<void>(layer, P.wo), bo, x, h, T_max, rows, H, H, RPP_EPI_BIAS_RESIDUAL, err, s));
-    RPP_TRY(launch_layernorm(h, g1, be1, x1, T_max, rows, H, c->eps, dt, nullptr, nullptr, amax ? amax + 2 : nullptr,
-                             err, s));
-    RPP_TRY(linear(dt, x1, at<void>(layer, P.w1), b1, nullptr, g, T_max, rows, F, H, RPP_EPI_BIAS_GELU, err, s));
-    if (amax) RPP_TRY(launch_amax(g, T_max, rows, F, dt, amax + 3, err, s));
-    RPP_TRY(linear(dt, g, at<void>(layer, P.w2), b2, x1, h, T_max, rows, H, F, RPP_EPI_BIAS_RESIDUAL, err, s));
-    RPP_TRY(launch_layernorm(h, g2, be2, y, T_max, rows, H, c->eps, dt, nullptr, nullptr, nullptr, err, s));
+    if (amax) RPP_LAUNCH("amax", s, launch_amax(x, T_max, rows, H, dt, amax + 0, err, s));
+    RPP_LAUNCH("gemm_qkv", s, linear(dt, x, at<void>(layer, P.wqkv), bqkv, nullptr, qkv, T_max, rows, 3 * H, H,
+                                     RPP_EPI_BIAS, err, s, RPP_I8, RPP_I8, hint));
+    RPP_LAUNCH("attention", s, launch_attention_varlen(qkv, cu, B, T_max, max_len, nh, d, dt, attn, err, s));
+    if (amax) RPP_LAUNCH("amax", s, launch_amax(attn, T_max, rows, H, dt, amax + 1, err, s));
+    RPP_LAUNCH("gemm_proj", s, linear(dt, attn, at<void>(layer, P.wo), bo, x, h, T_max, rows, H, H,
+                                      RPP_EPI_BIAS_RESIDUAL, err, s, hdt, RPP_I8, hint, kMaxSplits, &sp_proj));
+    float* x1f = fp32_residual(c) ? at<float>(ws, W.x1f) : nullptr;
+    RPP_LAUNCH("layernorm1", s, launch_layernorm(h, g1, be1, x1, T_max, rows, H, c->eps, hdt, dt, nullptr, nullptr,
+                                                 amax ? amax + 2 : nullptr, x1f, err, s, sp_proj, hs));
+    RPP_LAUNCH("gemm_fc1", s, linear(dt, x1, at<void>(layer, P.w1), b1, nullptr, g, T_max, rows, F, H,
+                                     RPP_EPI_BIAS_GELU, err, s, RPP_I8, RPP_I8, hint));
+    if (amax) RPP_LAUNCH("amax", s, launch_amax(g, T_max, rows, F, dt, amax + 3, err, s));
+    RPP_LAUNCH("gemm_fc2", s, linear(dt, g, at<void>(layer, P.w2), b2, x1f ? static_cast<const void*>(x1f) : x1, h,
+                                     T_max, rows, H, F, RPP_EPI_BIAS_RESIDUAL, err, s, hdt, x1f ? RPP_F32 : dt, hint,
+                                     kMaxSplits, &sp_fc2));
+    RPP_LAUNCH("layernorm2", s, launch_layernorm(h, g2, be2, y, T_max, rows, H, c->eps, hdt, dt, nullptr, nullptr,
+                                                 nullptr, nullptr, err, s, sp_fc2, hs));
     return RPP_OK;
   }
   // int8: quantise -> int8 GEMM (exact integer accumulation) -> dequantise in the epilogue
@@ -214,19 +271,21 @@ rpp_status encoder_layer_run(const rpp_encoder_cfg* c, const void* layer, const 
   const float* s1 = act_scales + 1;
   const float* s2 = act_scales + 2;
   const float* s3 = act_scales + 3;
-  RPP_TRY(launch_quantize_codes_bf16(x, s0, cx, T_max, rows, H, dt, err, s));
-  RPP_TRY(linear_i8(cx, at<void>(layer, P.wqkv), bqkv, s0, at<float>(layer, P.sqkv), nullptr, nullptr, qkv, dt, T_max,
-                    rows, 3 * H, H, EPI_DQ_BIAS, err, s));
-  RPP_TRY(launch_attention_varlen(qkv, cu, B, T_max, max_len, nh, d, dt, attn, err, s));
-  RPP_TRY(launch_quantize_codes_bf16(attn, s1, ca, T_max, rows, H, dt, err, s));
-  RPP_TRY(linear_i8(ca, at<void>(layer, P.wo), bo, s1, at<float>(layer, P.so), nullptr, x, h, dt, T_max, rows, H, H,
-                    EPI_DQ_BIAS_RESIDUAL, err, s));
-  RPP_TRY(launch_layernorm(h, g1, be1, x1, T_max, rows, H, c->eps, dt, cx1, s2, nullptr, err, s));
-  RPP_TRY(linear_i8(cx1, at<void>(layer, P.w1), b1, s2, at<float>(layer, P.s1), s3, nullptr, cg, RPP_BF16, T_max,
-                    rows, F, H, EPI_DQ_BIAS_GELU_Q, err, s));
-  RPP_TRY(linear_i8(cg, at<void>(layer, P.w2), b2, s3, at<float>(layer, P.s2), nullptr, x1, h, dt, T_max, rows, H, F,
-                    EPI_DQ_BIAS_RESIDUAL, err, s));
-  RPP_TRY(launch_layernorm(h, g2, be2, y, T_max, rows, H, c->eps, dt, nullptr, nullptr, nullptr, err, s));
+  RPP_LAUNCH("quantize_x", s, launch_quantize_codes_bf16(x, s0, cx, T_max, rows, H, dt, err, s));
+  RPP_LAUNCH("gemm_qkv_i8", s, linear_i8(cx, at<void>(layer, P.wqkv), bqkv, s0, at<float>(layer, P.sqkv), nullptr,
+                                          nullptr, qkv, dt, T_max, rows, 3 * H, H, EPI_DQ_BIAS, err, s, hint));
+  RPP_LAUNCH("attention", s, launch_attention_varlen(qkv, cu, B, T_max, max_len, nh, d, dt, attn, err, s));
+  RPP_LAUNCH("quantize_attn", s, launch_quantize_codes_bf16(attn, s1, ca, T_max, rows, H, dt, err, s));
+  RPP_LAUNCH("gemm_proj_i8", s, linear_i8(ca, at<void>(layer, P.wo), bo, s1, at<float>(layer, P.so), nullptr, x, h,
+                                           dt, T_max, rows, H, H, EPI_DQ_BIAS_RESIDUAL, err, s, hint));
+  RPP_LAUNCH("layernorm1", s, launch_layernorm(h, g1, be1, x1, T_max, rows, H, c->eps, hdt, dt, cx1, s2, nullptr,
+                                               nullptr, err, s));
+  RPP_LAUNCH("gemm_fc1_i8", s, linear_i8(cx1, at<void>(layer, P.w1), b1, s2, at<float>(layer, P.s1), s3, nullptr, cg,
+                                          RPP_BF16, T_max, rows, F, H, EPI_DQ_BIAS_GELU_Q, err, s, hint));
+  RPP_LAUNCH("gemm_fc2_i8", s, linear_i8(cg, at<void>(layer, P.w2), b2, s3, at<float>(layer, P.s2), nullptr, x1, h,
+                                          dt, T_max, rows, H, F, EPI_DQ_BIAS_RESIDUAL, err, s, hint));
+  RPP_LAUNCH("layernorm2", s, launch_layernorm(h, g2, be2, y, T_max, rows, H, c->eps, hdt, dt, nullptr, nullptr,
+                                               nullptr, nullptr, err, s));
   return RPP_OK;
 }
 
@@ -307,6 +366,21 @@ const char* rpp_status_string(int status) {
 
 int rpp_version(void) { return 100; }
 
+rpp_status rpp_set_launch_events(void* const* events, int capacity) {
+  if (capacity < 0 || (capacity > 0 && !events)) return RPP_EINVAL;
+  g_hook.events = capacity > 0 ? reinterpret_cast<cudaEvent_t*>(const_cast<void**>(events)) : nullptr;
+  g_hook.capacity = capacity;
+  g_hook.count = 0;
+  return RPP_OK;
+}
+
+int rpp_launch_event_count(void) { return g_hook.count; }
+
+const char* rpp_launch_event_label(int i) {
+  if (i < 0 || i >= g_hook.count || i >= 4096) return "";
+  return g_hook.labels[i];
+}
+
 rpp_status rpp_get_device_error(const int32_t* err, int32_t* host_code, rpp_stream stream) {
   if (!err || !host_code) return RPP_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -321,8 +395,9 @@ rpp_status rpp_build_offsets(const int32_t* lengths, int B, int L, int32_t* cu_s
                              int32_t* err, rpp_stream stream) {
   if (!lengths || !cu_seqlens || !padding_offset || B <= 0 || L <= 0 || B > 65536) return RPP_EINVAL;
   if (static_cast<long long>(B) * L > 0x7fffffffLL) return RPP_EINVAL;
-  return from_cuda(launch_build_offsets(lengths, B, L, cu_seqlens, padding_offset, err,
-                                        static_cast<cudaStream_t>(stream)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  RPP_LAUNCH("build_offsets", s, launch_build_offsets(lengths, B, L, cu_seqlens, padding_offset, err, s));
+  return RPP_OK;
 }
 
 rpp_status rpp_remove_padding(const void* padded, const int32_t* padding_offset, const int32_t* cu_seqlens, int B,
@@ -331,8 +406,10 @@ rpp_status rpp_remove_padding(const void* padded, const int32_t* padding_offset,
   if (dtype < RPP_F32 || dtype > RPP_I8) return RPP_EINVAL;
   const long long row_bytes = static_cast<long long>(H) * esize(dtype);
   if (row_bytes % 16 || !aligned16(padded) || !aligned16(packed)) return RPP_EINVAL;
-  return from_cuda(launch_remove_padding(padded, padding_offset, cu_seqlens, B, L, static_cast<int>(row_bytes), packed,
-                                         err, static_cast<cudaStream_t>(stream)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  RPP_LAUNCH("remove_padding", s, launch_remove_padding(padded, padding_offset, cu_seqlens, B, L,
+                                                        static_cast<int>(row_bytes), packed, err, s));
+  return RPP_OK;
 }
 
 rpp_status rpp_rebuild_padding(const void* packed, const int32_t* cu_seqlens, int B, int L, int H, rpp_dtype dtype,
@@ -341,8 +418,10 @@ rpp_status rpp_rebuild_padding(const void* packed, const int32_t* cu_seqlens, in
   if (dtype < RPP_F32 || dtype > RPP_I8) return RPP_EINVAL;
   const long long row_bytes = static_cast<long long>(H) * esize(dtype);
   if (row_bytes % 16 || !aligned16(padded) || !aligned16(packed)) return RPP_EINVAL;
-  return from_cuda(launch_rebuild_padding(packed, cu_seqlens, B, L, static_cast<int>(row_bytes), padded, err,
-                                          static_cast<cudaStream_t>(stream)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  RPP_LAUNCH("rebuild_padding", s, launch_rebuild_padding(packed, cu_seqlens, B, L, static_cast<int>(row_bytes), padded,
+                                                          err, s));
+  return RPP_OK;
 }
 
 rpp_status rpp_linear(const void* a, const void* w_t, const float* bias, const void* residual, void* out, int M_max,
@@ -371,8 +450,8 @@ rpp_status rpp_layernorm(const void* x, const float* gamma, const float* beta, v
   if (!aligned16(x) || !aligned16(y) || !aligned16(gamma) || !aligned16(beta)) return RPP_EINVAL;
   if (dtype != RPP_F32 && dtype != RPP_F16 && dtype != RPP_BF16) return RPP_EUNSUPPORTED;
   if (!layernorm_supported(H, dtype)) return RPP_EUNSUPPORTED;
-  return from_cuda(launch_layernorm(x, gamma, beta, y, M_max, rows, H, eps, dtype, nullptr, nullptr, nullptr, err,
-                                    static_cast<cudaStream_t>(stream)));
+  return from_cuda(launch_layernorm(x, gamma, beta, y, M_max, rows, H, eps, dtype, dtype, nullptr, nullptr, nullptr,
+                                    nullptr, err, static_cast<cudaStream_t>(stream)));
 }
 
 rpp_status rpp_attention_varlen(const void* qkv, const int32_t* cu_seqlens, int B, int T_max, int max_len, int nh,
@@ -459,8 +538,9 @@ rpp_status rpp_encoder_layer_calibrate(const rpp_encoder_cfg* cfg, const void* l
   if (cudaMemsetAsync(amax_out, 0, 4 * sizeof(float), s) != cudaSuccess) return RPP_ECUDA;
   const size_t need = enc_ws_layout(cfg, T_max > 0 ? T_max : 1).total;
   if (workspace_bytes < need) return RPP_EWORKSPACE;
-  // the output of the calibration pass is not needed: write it into the workspace's h buffer
-  void* y = at<void>(workspace, enc_ws_layout(cfg, T_max).h);
+  // the output of the calibration pass is not needed: it goes to the QKV buffer, which
+  // is dead once attention has run
+  void* y = at<void>(workspace, enc_ws_layout(cfg, T_max).qkv);
   return encoder_layer_run(cfg, layer, nullptr, x, cu_seqlens, B, T_max, max_len, y, workspace, workspace_bytes,
                            amax_out, err, s);
 }
@@ -601,19 +681,19 @@ rpp_status rpp_swin_block_forward(const rpp_swin_cfg* cfg, const void* block, in
   void* attn = at<void>(workspace, W.attn);
   void* xa = at<void>(workspace, W.xa);
   void* g = at<void>(workspace, W.g);
-  RPP_TRY(launch_layernorm(x, at<float>(block, P.g1), at<float>(block, P.be1), h, T, nullptr, C, cfg->eps, dt, nullptr,
-                           nullptr, nullptr, err, s));
-  RPP_TRY(linear(dt, h, at<void>(block, P.wqkv), at<float>(block, P.bqkv), nullptr, qkv, T, nullptr, 3 * C, C,
+  RPP_LAUNCH("layernorm1", s, launch_layernorm(x, at<float>(block, P.g1), at<float>(block, P.be1), h, T, nullptr, C, cfg->eps, dt, dt,
+                           nullptr, nullptr, nullptr, nullptr, err, s));
+  RPP_LAUNCH("gemm_qkv", s, linear(dt, h, at<void>(block, P.wqkv), at<float>(block, P.bqkv), nullptr, qkv, T, nullptr, 3 * C, C,
                  RPP_EPI_BIAS, err, s));
-  RPP_TRY(launch_window_attention(B, qkv, at<float>(block, P.bias), attn, C, cfg->heads, cfg->img, cfg->window,
+  RPP_LAUNCH("window_attention", s, launch_window_attention(B, qkv, at<float>(block, P.bias), attn, C, cfg->heads, cfg->img, cfg->window,
                                   cfg->shift, dt, err, s));
-  RPP_TRY(linear(dt, attn, at<void>(block, P.wo), at<float>(block, P.bo), x, xa, T, nullptr, C, C,
+  RPP_LAUNCH("gemm_proj", s, linear(dt, attn, at<void>(block, P.wo), at<float>(block, P.bo), x, xa, T, nullptr, C, C,
                  RPP_EPI_BIAS_RESIDUAL, err, s));
-  RPP_TRY(launch_layernorm(xa, at<float>(block, P.g2), at<float>(block, P.be2), h, T, nullptr, C, cfg->eps, dt, nullptr,
-                           nullptr, nullptr, err, s));
-  RPP_TRY(linear(dt, h, at<void>(block, P.w1), at<float>(block, P.b1), nullptr, g, T, nullptr, F, C, RPP_EPI_BIAS_GELU,
+  RPP_LAUNCH("layernorm2", s, launch_layernorm(xa, at<float>(block, P.g2), at<float>(block, P.be2), h, T, nullptr, C, cfg->eps, dt, dt,
+                           nullptr, nullptr, nullptr, nullptr, err, s));
+  RPP_LAUNCH("gemm_fc1", s, linear(dt, h, at<void>(block, P.w1), at<float>(block, P.b1), nullptr, g, T, nullptr, F, C, RPP_EPI_BIAS_GELU,
                  err, s));
-  RPP_TRY(linear(dt, g, at<void>(block, P.w2), at<float>(block, P.b2), xa, y, T, nullptr, C, F, RPP_EPI_BIAS_RESIDUAL,
+  RPP_LAUNCH("gemm_fc2", s, linear(dt, g, at<void>(block, P.w2), at<float>(block, P.b2), xa, y, T, nullptr, C, F, RPP_EPI_BIAS_RESIDUAL,
                  err, s));
   return RPP_OK;
 }

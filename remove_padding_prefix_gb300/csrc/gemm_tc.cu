@@ -14,7 +14,8 @@
 //   warp 1      allocates tensor memory and issues tcgen05.mma (M = 128, N = BN,
 //               K = 16 per instruction) from one thread; tcgen05.commit releases the
 //               smem stage and, after the last K block, signals the accumulator.
-//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns per warp, bias / GELU /
+//   warps 2..9  epilogue: two warps per tensor-memory lane quadrant, each taking every
+//               other 32-column slice: tcgen05.ld 32 lanes x 32 columns, bias / GELU /
 //               residual in fp32, 16-byte stores of the converted row segment.
 //
 // The accumulator is double-buffered in tensor memory (2 x BN columns), so the
@@ -24,6 +25,12 @@
 // buffer) but never stored.  Every mbarrier wait is bounded; on a timeout the CTA
 // records RPP_DERR_TIMEOUT, drains its in-flight copies and MMAs, frees its tensor
 // memory and exits.
+//
+// Split-K: when a GEMM has too few output tiles to fill the SMs (narrow N, few
+// tokens), each tile's K range is cut into `splits` parts; part s writes its fp32
+// partial sum into slice s of the output (part 0 also adds bias and residual) and the
+// LayerNorm that follows adds the slices while loading its row -- the reduction costs
+// no extra kernel and stays deterministic.
 //
 // int8 layers: sm_103a has no int8 kind of tcgen05.mma, so the int8 GEMM runs as an
 // exact integer product on the bf16 tensor pipe.  Codes in [-127, 127] are exact in
@@ -39,7 +46,8 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;   // 64 x 16-bit = 128 bytes = one swizzle row
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 
 constexpr int kChunkBlocks = 16;   // 16 x 64 = 1024 K per exact integer chunk
 
@@ -55,6 +63,8 @@ struct GemmParams {
   const float* w_scale;
   const float* q_scale;
   int32_t* err;
+  int splits;               // K splits per tile (1 = none)
+  long long split_stride;   // elements between the fp32 partial slices
 };
 
 constexpr uint32_t pow2_cols(uint32_t c) {
@@ -71,7 +81,99 @@ __device__ __forceinline__ float code_of(float v, float inv_s) {
   return fminf(fmaxf(q, -127.f), 127.f);
 }
 
-template <typename TIn, typename TOut, int BN, int STAGES, int EPI, int NCH>
+// Epilogue of NV (32 or 16) accumulator columns [col, col + NV) of this thread's row:
+// tensor memory -> registers (summing the int8 chunk partials in int32), then bias,
+// dequantisation, GELU, requantisation, residual, conversion and 16-byte stores.
+template <typename TOut, typename TRes, int EPI, int NCH, int ACC, int NV>
+__device__ __forceinline__ void epilogue_cols(const GemmParams& p, uint32_t t_row, uint32_t a, int col, int nch,
+                                              int row, bool row_ok, int n0, float a_s, float inv_q, int split) {
+  constexpr bool kInt = EPI >= EPI_I32;
+  uint32_t r[NV];
+  float v[NV];
+  const uint32_t base = t_row + (a * NCH) * ACC + col;
+  if constexpr (NV == 32) tmem_ld_32x32b_x32(base, r); else tmem_ld_32x32b_x16(base, r);
+  tmem_ld_wait();
+  if constexpr (kInt) {
+    int acc[NV];   // exact: every chunk partial is an integer below 2^24
+#pragma unroll
+    for (int j = 0; j < NV; ++j) acc[j] = __float2int_rn(__uint_as_float(r[j]));
+    for (int ch = 1; ch < nch; ++ch) {
+      if constexpr (NV == 32) tmem_ld_32x32b_x32(base + ch * ACC, r); else tmem_ld_32x32b_x16(base + ch * ACC, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < NV; ++j) acc[j] += __float2int_rn(__uint_as_float(r[j]));
+    }
+    if constexpr (EPI == EPI_I32) {
+      if (row_ok) {
+        int4* orow = reinterpret_cast<int4*>(static_cast<int32_t*>(p.out) + static_cast<long long>(row) * p.N + n0 + col);
+#pragma unroll
+        for (int j = 0; j < NV / 4; ++j) orow[j] = make_int4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+      }
+      return;
+    }
+#pragma unroll
+    for (int j = 0; j < NV; ++j) v[j] = static_cast<float>(acc[j]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < NV; ++j) v[j] = __uint_as_float(r[j]);
+  }
+  if constexpr (EPI != EPI_I32) {
+    if (!row_ok) return;
+    const int n = n0 + col;
+    const bool first = split == 0;   // later K splits carry the raw partial sum only
+    const float4* b4 = reinterpret_cast<const float4*>(p.bias + n);
+    if constexpr (EPI == EPI_DQ_BIAS || EPI == EPI_DQ_BIAS_RESIDUAL || EPI == EPI_DQ_BIAS_GELU_Q) {
+      const float4* s4 = reinterpret_cast<const float4*>(p.w_scale + n);
+#pragma unroll
+      for (int j = 0; j < NV / 4; ++j) {
+        const float4 ss = __ldg(s4 + j);
+        v[4 * j + 0] *= a_s * ss.x;
+        v[4 * j + 1] *= a_s * ss.y;
+        v[4 * j + 2] *= a_s * ss.z;
+        v[4 * j + 3] *= a_s * ss.w;
+      }
+    }
+    if (first) {
+#pragma unroll
+      for (int j = 0; j < NV / 4; ++j) {
+        const float4 bb = __ldg(b4 + j);
+        v[4 * j + 0] += bb.x;
+        v[4 * j + 1] += bb.y;
+        v[4 * j + 2] += bb.z;
+        v[4 * j + 3] += bb.w;
+      }
+    }
+    if constexpr (EPI == RPP_EPI_BIAS_GELU || EPI == EPI_DQ_BIAS_GELU_Q) {
+#pragma unroll
+      for (int j = 0; j < NV; ++j) v[j] = gelu_erf(v[j]);
+    }
+    if constexpr (EPI == EPI_DQ_BIAS_GELU_Q) {
+#pragma unroll
+      for (int j = 0; j < NV; ++j) v[j] = code_of(v[j], inv_q);
+    }
+    if constexpr (EPI == RPP_EPI_BIAS_RESIDUAL || EPI == EPI_DQ_BIAS_RESIDUAL) {
+      if (first) {
+      constexpr int RPV = Vec<TRes>::N;   // residual elements per 16-byte vector
+      const uint4* rr = reinterpret_cast<const uint4*>(static_cast<const TRes*>(p.residual) +
+                                                       static_cast<long long>(row) * p.N + n);
+#pragma unroll
+      for (int j = 0; j < NV / RPV; ++j) {
+        float f[RPV];
+        unpack16<TRes>(rr[j], f);
+#pragma unroll
+        for (int e = 0; e < RPV; ++e) v[RPV * j + e] += f[e];
+      }
+      }
+    }
+    constexpr int EPV = Vec<TOut>::N;   // output elements per 16-byte vector
+    uint4* orow = reinterpret_cast<uint4*>(static_cast<TOut*>(p.out) + split * p.split_stride +
+                                           static_cast<long long>(row) * p.N + n);
+#pragma unroll
+    for (int j = 0; j < NV / EPV; ++j) orow[j] = pack16<TOut>(v + EPV * j);
+  }
+}
+
+template <typename TIn, typename TOut, typename TRes, int BN, int STAGES, int EPI, int NCH>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
@@ -79,9 +181,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   constexpr uint32_t B_BYTES = BN * kBK * 2;
   constexpr uint32_t B_BYTES_AL = (B_BYTES + 1023u) & ~1023u;
   constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES;
-  constexpr int NBUF = (2 * NCH * BN <= 512) ? 2 : 1;   // accumulator buffers in tensor memory
-  static_assert(NCH * BN <= 512, "tensor memory columns");
-  constexpr uint32_t TMEM_COLS = pow2_cols(NBUF * NCH * BN);
+  constexpr int ACC = (BN + 31) / 32 * 32;               // columns per accumulator region
+  constexpr int NBUF = (2 * NCH * ACC <= 512) ? 2 : 1;  // accumulator buffers in tensor memory
+  static_assert(NCH * ACC <= 512, "tensor memory columns");
+  constexpr uint32_t TMEM_COLS = pow2_cols(NBUF * NCH * ACC);
   constexpr uint32_t IDESC = idesc_f16(AbFmt<TIn>::v, kBM, BN);
   constexpr bool kInt = EPI >= EPI_I32;
 
@@ -109,7 +212,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4 * 32);
+      mbar_init(&tempty[a], kEpiWarps * 32);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -138,17 +241,22 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int num_m = skip ? 0 : (M + kBM - 1) / kBM;
   const int num_n = p.N / BN;
   const int num_k = (p.K + kBK - 1) / kBK;
-  const int total = num_m * num_n;
+  const int S = p.splits;
+  const int kps = (num_k + S - 1) / S;          // K blocks per split
+  const int total = num_m * num_n * S;          // work units: (tile, split)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int unit = blockIdx.x; unit < total && ok; unit += gridDim.x) {
+        const int tile = unit / S;
+        const int kb0 = (unit - tile * S) * kps;
+        const int kb1 = min(num_k, kb0 + kps);
         const int m0 = (tile / num_n) * kBM;
         const int n0 = (tile % num_n) * BN;
-        for (int kb = 0; kb < num_k; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const uint32_t s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
           if (!mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag)) {
@@ -173,7 +281,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (lane == 0) {
       uint32_t it = 0, acc_it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++acc_it) {
+      for (int unit = blockIdx.x; unit < total && ok; unit += gridDim.x, ++acc_it) {
+        const int tile = unit / S;
+        const int kb0 = (unit - tile * S) * kps;
+        const int kb1 = min(num_k, kb0 + kps);
         const uint32_t a = NBUF == 2 ? (acc_it & 1u) : 0u;
         const uint32_t aph = NBUF == 2 ? ((acc_it >> 1) & 1u) : (acc_it & 1u);
         if (!mbar_wait_bounded(&tempty[a], aph ^ 1u, abort_flag)) {
@@ -181,10 +292,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           break;
         }
         tc_fence_after();
-        for (int kb = 0; kb < num_k; ++kb, ++it) {
-          const int chunk = NCH > 1 ? kb / kChunkBlocks : 0;
-          const int kb_in = NCH > 1 ? kb - chunk * kChunkBlocks : kb;
-          const uint32_t d_tmem = tmem_base + (a * NCH + chunk) * BN;
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const int chunk = NCH > 1 ? (kb - kb0) / kChunkBlocks : 0;
+          const int kb_in = (kb - kb0) - chunk * kChunkBlocks;
+          const uint32_t d_tmem = tmem_base + (a * NCH + chunk) * ACC;
           const uint32_t s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
           if (!mbar_wait_bounded(&full[s], ph, abort_flag)) {
@@ -214,13 +325,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else {
     // ------------------------------------------------------------ epilogue warps
     const int q = warp & 3;               // tensor-memory lane quadrant of this warp
+    const int half = (warp - 2) >> 2;     // which of the two warps of this quadrant
     const int r_in_tile = q * 32 + lane;
-    const int nch = NCH > 1 ? (num_k + kChunkBlocks - 1) / kChunkBlocks : 1;
     float a_s = 1.f, inv_q = 0.f;
     if constexpr (EPI == EPI_DQ_BIAS || EPI == EPI_DQ_BIAS_RESIDUAL || EPI == EPI_DQ_BIAS_GELU_Q) a_s = *p.a_scale;
     if constexpr (EPI == EPI_DQ_BIAS_GELU_Q) inv_q = __fdiv_rn(1.0f, *p.q_scale);
     uint32_t acc_it = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++acc_it) {
+    for (int unit = blockIdx.x; unit < total; unit += gridDim.x, ++acc_it) {
+      const int tile = unit / S;
+      const int split = unit - tile * S;
+      const int kb0 = split * kps;
+      const int kb1 = min(num_k, kb0 + kps);
+      const int nch = NCH > 1 ? (kb1 - kb0 + kChunkBlocks - 1) / kChunkBlocks : 1;
       const uint32_t a = NBUF == 2 ? (acc_it & 1u) : 0u;
       const uint32_t aph = NBUF == 2 ? ((acc_it >> 1) & 1u) : (acc_it & 1u);
       int ok = 1;
@@ -239,86 +355,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int row = m0 + r_in_tile;
       const bool row_ok = row < M;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      if constexpr (BN >= 32) {
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        float v[32];
-        tmem_ld_32x32b_x32(t_row + (a * NCH) * BN + c * 32, r);
-        tmem_ld_wait();
-        if constexpr (kInt) {
-          // exact: every chunk partial is an integer below 2^24
-          int acc[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) acc[j] = __float2int_rn(__uint_as_float(r[j]));
-          for (int ch = 1; ch < nch; ++ch) {
-            tmem_ld_32x32b_x32(t_row + (a * NCH + ch) * BN + c * 32, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) acc[j] += __float2int_rn(__uint_as_float(r[j]));
-          }
-          if constexpr (EPI == EPI_I32) {
-            if (row_ok) {
-              int4* orow = reinterpret_cast<int4*>(static_cast<int32_t*>(p.out) + static_cast<long long>(row) * p.N +
-                                                   n0 + c * 32);
-#pragma unroll
-              for (int j = 0; j < 8; ++j) orow[j] = make_int4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
-            }
-            continue;
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = static_cast<float>(acc[j]);
-          }
-        } else {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-        }
-        if constexpr (EPI != EPI_I32) {
-          if (row_ok) {
-            const int n = n0 + c * 32;
-            const float4* b4 = reinterpret_cast<const float4*>(p.bias + n);
-            if constexpr (EPI == EPI_DQ_BIAS || EPI == EPI_DQ_BIAS_RESIDUAL || EPI == EPI_DQ_BIAS_GELU_Q) {
-              const float4* s4 = reinterpret_cast<const float4*>(p.w_scale + n);
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const float4 ss = __ldg(s4 + j);
-                v[4 * j + 0] *= a_s * ss.x;
-                v[4 * j + 1] *= a_s * ss.y;
-                v[4 * j + 2] *= a_s * ss.z;
-                v[4 * j + 3] *= a_s * ss.w;
-              }
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float4 bb = __ldg(b4 + j);
-              v[4 * j + 0] += bb.x;
-              v[4 * j + 1] += bb.y;
-              v[4 * j + 2] += bb.z;
-              v[4 * j + 3] += bb.w;
-            }
-            if constexpr (EPI == RPP_EPI_BIAS_GELU || EPI == EPI_DQ_BIAS_GELU_Q) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = gelu_erf(v[j]);
-            }
-            if constexpr (EPI == EPI_DQ_BIAS_GELU_Q) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = code_of(v[j], inv_q);
-            }
-            if constexpr (EPI == RPP_EPI_BIAS_RESIDUAL || EPI == EPI_DQ_BIAS_RESIDUAL) {
-              const uint4* rr = reinterpret_cast<const uint4*>(static_cast<const TOut*>(p.residual) +
-                                                               static_cast<long long>(row) * p.N + n);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                float f[8];
-                unpack16<TOut>(rr[j], f);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[8 * j + e] += f[e];
-              }
-            }
-            uint4* orow = reinterpret_cast<uint4*>(static_cast<TOut*>(p.out) + static_cast<long long>(row) * p.N + n);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) orow[j] = pack16<TOut>(v + 8 * j);
-          }
-        }
+        for (int c = half; c < BN / 32; c += 2)
+          epilogue_cols<TOut, TRes, EPI, NCH, ACC, 32>(p, t_row, a, c * 32, nch, row, row_ok, n0, a_s, inv_q, split);
+      }
+      if constexpr (BN % 32 == 16) {
+        if (half == ((BN / 32) & 1))
+          epilogue_cols<TOut, TRes, EPI, NCH, ACC, 16>(p, t_row, a, BN - 16, nch, row, row_ok, n0, a_s, inv_q, split);
       }
       tc_fence_before();
       mbar_arrive(&tempty[a]);
@@ -373,109 +417,125 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, in
 
 namespace {
 
-template <typename TIn, typename TOut, int BN, int STAGES, int EPI, int NCH>
-cudaError_t gemm_tc_launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cudaStream_t stream) {
+template <typename TIn, typename TOut, typename TRes, int BN, int STAGES, int EPI, int NCH>
+cudaError_t gemm_tc_launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int grid_rows,
+                           cudaStream_t stream) {
   constexpr uint32_t A_BYTES = kBM * kBK * 2;
   constexpr uint32_t B_BYTES_AL = ((BN * kBK * 2) + 1023u) & ~1023u;
   constexpr size_t SMEM = 1024 + STAGES * (A_BYTES + B_BYTES_AL) + 256;
   static_assert(SMEM <= 232448, "shared memory per CTA");
-  auto kern = gemm_tc_kernel<TIn, TOut, BN, STAGES, EPI, NCH>;
+  auto kern = gemm_tc_kernel<TIn, TOut, TRes, BN, STAGES, EPI, NCH>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  const int num_m = (p.M_max + kBM - 1) / kBM;
-  const int tiles = num_m * (p.N / BN);
-  int grid = tiles < num_sms() ? tiles : num_sms();
+  const int num_m = (grid_rows + kBM - 1) / kBM;
+  const long long units = static_cast<long long>(num_m) * (p.N / BN) * p.splits;
+  int grid = units < num_sms() ? static_cast<int>(units) : num_sms();
   if (grid < 1) grid = 1;
   kern<<<grid, kThreads, SMEM, stream>>>(ta, tb, p);
   return cudaGetLastError();
 }
 
-// Tile width choice (the per-shape GEMM configuration of the Kuaishou article's
-// Fig. 11): minimise waves x (BN + fixed per-tile cost) over the candidates that divide
-// N, ties to the wider tile.
-int choose_bn(int M, int N, int max_bn) {
+// Tile shape choice (the per-shape GEMM configuration of the Kuaishou article's
+// Fig. 11): over the tile widths that divide N and the allowed K splits, minimise
+// waves x (K blocks per unit x (BN + 32) + epilogue cost), using the expected number
+// of rows (the caller's token-count hint, else the capacity).
+struct TileChoice {
+  int bn = 0;
+  int splits = 1;
+};
+
+TileChoice choose_tiles(int M, int N, int K, int max_bn, int max_splits) {
   static const int cands[] = {256, 192, 144, 128, 96, 64, 48, 32, 16};
   const int sms = num_sms();
-  int best = 0;
-  double best_cost = 1e30;
   const int num_m = (M + kBM - 1) / kBM;
+  const int num_k = (K + kBK - 1) / kBK;
+  TileChoice best;
+  double best_cost = 1e30;
   for (int bn : cands) {
     if (N % bn || bn > max_bn) continue;
-    const long long tiles = static_cast<long long>(num_m) * (N / bn);
-    const long long waves = (tiles + sms - 1) / sms;
-    const double cost = static_cast<double>(waves) * (bn + 24.0);
-    if (cost < best_cost - 1e-9) {
-      best_cost = cost;
-      best = bn;
+    for (int sp = 1; sp <= max_splits && sp <= num_k; ++sp) {
+      const int kps = (num_k + sp - 1) / sp;
+      const long long units = static_cast<long long>(num_m) * (N / bn) * sp;
+      const long long waves = (units + sms - 1) / sms;
+      const double cost = static_cast<double>(waves) * (kps * (bn + 32.0) + 6.0 * bn) + (sp - 1) * 64.0;
+      if (cost < best_cost - 1e-9) {
+        best_cost = cost;
+        best.bn = bn;
+        best.splits = sp;
+      }
     }
   }
   return best;
 }
 
-template <typename TIn, typename TOut, int EPI, int NCH>
-cudaError_t dispatch_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
+template <typename TIn, typename TOut, typename TRes, int EPI, int NCH>
+cudaError_t dispatch_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int gr,
                         cudaStream_t stream) {
   if constexpr (NCH == 1) {
     switch (bn) {
-      case 256: return gemm_tc_launch<TIn, TOut, 256, 4, EPI, 1>(ta, tb, p, stream);
-      case 192: return gemm_tc_launch<TIn, TOut, 192, 5, EPI, 1>(ta, tb, p, stream);
-      case 144: return gemm_tc_launch<TIn, TOut, 144, 5, EPI, 1>(ta, tb, p, stream);
-      case 128: return gemm_tc_launch<TIn, TOut, 128, 6, EPI, 1>(ta, tb, p, stream);
-      case 96: return gemm_tc_launch<TIn, TOut, 96, 7, EPI, 1>(ta, tb, p, stream);
-      case 64: return gemm_tc_launch<TIn, TOut, 64, 8, EPI, 1>(ta, tb, p, stream);
-      case 48: return gemm_tc_launch<TIn, TOut, 48, 8, EPI, 1>(ta, tb, p, stream);
-      case 32: return gemm_tc_launch<TIn, TOut, 32, 8, EPI, 1>(ta, tb, p, stream);
-      case 16: return gemm_tc_launch<TIn, TOut, 16, 8, EPI, 1>(ta, tb, p, stream);
+      case 256: return gemm_tc_launch<TIn, TOut, TRes, 256, 4, EPI, 1>(ta, tb, p, gr, stream);
+      case 192: return gemm_tc_launch<TIn, TOut, TRes, 192, 5, EPI, 1>(ta, tb, p, gr, stream);
+      case 144: return gemm_tc_launch<TIn, TOut, TRes, 144, 5, EPI, 1>(ta, tb, p, gr, stream);
+      case 128: return gemm_tc_launch<TIn, TOut, TRes, 128, 6, EPI, 1>(ta, tb, p, gr, stream);
+      case 96: return gemm_tc_launch<TIn, TOut, TRes, 96, 7, EPI, 1>(ta, tb, p, gr, stream);
+      case 64: return gemm_tc_launch<TIn, TOut, TRes, 64, 8, EPI, 1>(ta, tb, p, gr, stream);
+      case 48: return gemm_tc_launch<TIn, TOut, TRes, 48, 8, EPI, 1>(ta, tb, p, gr, stream);
+      case 32: return gemm_tc_launch<TIn, TOut, TRes, 32, 8, EPI, 1>(ta, tb, p, gr, stream);
+      case 16: return gemm_tc_launch<TIn, TOut, TRes, 16, 8, EPI, 1>(ta, tb, p, gr, stream);
       default: return cudaErrorNotSupported;
     }
   } else {
     switch (bn) {   // NCH x BN <= 512 tensor-memory columns
-      case 128: return gemm_tc_launch<TIn, TOut, 128, 6, EPI, NCH>(ta, tb, p, stream);
-      case 96: return gemm_tc_launch<TIn, TOut, 96, 7, EPI, NCH>(ta, tb, p, stream);
-      case 64: return gemm_tc_launch<TIn, TOut, 64, 8, EPI, NCH>(ta, tb, p, stream);
-      case 48: return gemm_tc_launch<TIn, TOut, 48, 8, EPI, NCH>(ta, tb, p, stream);
-      case 32: return gemm_tc_launch<TIn, TOut, 32, 8, EPI, NCH>(ta, tb, p, stream);
-      case 16: return gemm_tc_launch<TIn, TOut, 16, 8, EPI, NCH>(ta, tb, p, stream);
+      case 128: return gemm_tc_launch<TIn, TOut, TRes, 128, 6, EPI, NCH>(ta, tb, p, gr, stream);
+      case 96: return gemm_tc_launch<TIn, TOut, TRes, 96, 7, EPI, NCH>(ta, tb, p, gr, stream);
+      case 64: return gemm_tc_launch<TIn, TOut, TRes, 64, 8, EPI, NCH>(ta, tb, p, gr, stream);
+      case 48: return gemm_tc_launch<TIn, TOut, TRes, 48, 8, EPI, NCH>(ta, tb, p, gr, stream);
+      case 32: return gemm_tc_launch<TIn, TOut, TRes, 32, 8, EPI, NCH>(ta, tb, p, gr, stream);
+      case 16: return gemm_tc_launch<TIn, TOut, TRes, 16, 8, EPI, NCH>(ta, tb, p, gr, stream);
       default: return cudaErrorNotSupported;
     }
   }
 }
 
 template <typename T>
-cudaError_t dispatch_float(int bn, int epi, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p,
-                           cudaStream_t stream) {
+cudaError_t dispatch_float(int bn, int epi, rpp_dtype out_dtype, rpp_dtype res_dtype, const CUtensorMap& ta,
+                           const CUtensorMap& tb, const GemmParams& p, int gr, cudaStream_t stream) {
   switch (epi) {
-    case RPP_EPI_BIAS: return dispatch_bn<T, T, RPP_EPI_BIAS, 1>(bn, ta, tb, p, stream);
-    case RPP_EPI_BIAS_GELU: return dispatch_bn<T, T, RPP_EPI_BIAS_GELU, 1>(bn, ta, tb, p, stream);
-    case RPP_EPI_BIAS_RESIDUAL: return dispatch_bn<T, T, RPP_EPI_BIAS_RESIDUAL, 1>(bn, ta, tb, p, stream);
+    case RPP_EPI_BIAS: return dispatch_bn<T, T, T, RPP_EPI_BIAS, 1>(bn, ta, tb, p, gr, stream);
+    case RPP_EPI_BIAS_GELU: return dispatch_bn<T, T, T, RPP_EPI_BIAS_GELU, 1>(bn, ta, tb, p, gr, stream);
+    case RPP_EPI_BIAS_RESIDUAL:
+      // fp32 output: the pre-LayerNorm residual sum of the encoder layer stays in fp32
+      if (out_dtype == RPP_F32 && res_dtype == RPP_F32)
+        return dispatch_bn<T, float, float, RPP_EPI_BIAS_RESIDUAL, 1>(bn, ta, tb, p, gr, stream);
+      if (out_dtype == RPP_F32) return dispatch_bn<T, float, T, RPP_EPI_BIAS_RESIDUAL, 1>(bn, ta, tb, p, gr, stream);
+      return dispatch_bn<T, T, T, RPP_EPI_BIAS_RESIDUAL, 1>(bn, ta, tb, p, gr, stream);
     default: return cudaErrorNotSupported;
   }
 }
 
 template <int NCH>
 cudaError_t dispatch_int(int bn, int epi, rpp_dtype out_dtype, const CUtensorMap& ta, const CUtensorMap& tb,
-                         const GemmParams& p, cudaStream_t stream) {
+                         const GemmParams& p, int gr, cudaStream_t stream) {
   using BF = __nv_bfloat16;
   switch (epi) {
-    case EPI_I32: return dispatch_bn<BF, int32_t, EPI_I32, NCH>(bn, ta, tb, p, stream);
-    case EPI_DQ_BIAS:
-      if (out_dtype == RPP_F16) return dispatch_bn<BF, __half, EPI_DQ_BIAS, NCH>(bn, ta, tb, p, stream);
-      return dispatch_bn<BF, BF, EPI_DQ_BIAS, NCH>(bn, ta, tb, p, stream);
-    case EPI_DQ_BIAS_RESIDUAL:
-      if (out_dtype == RPP_F16) return dispatch_bn<BF, __half, EPI_DQ_BIAS_RESIDUAL, NCH>(bn, ta, tb, p, stream);
-      return dispatch_bn<BF, BF, EPI_DQ_BIAS_RESIDUAL, NCH>(bn, ta, tb, p, stream);
-    case EPI_DQ_BIAS_GELU_Q: return dispatch_bn<BF, BF, EPI_DQ_BIAS_GELU_Q, NCH>(bn, ta, tb, p, stream);
+    case EPI_I32: return dispatch_bn<BF, int32_t, BF, EPI_I32, NCH>(bn, ta, tb, p, gr, stream);
+    case EPI_DQ_BIAS: return dispatch_bn<BF, __half, __half, EPI_DQ_BIAS, NCH>(bn, ta, tb, p, gr, stream);
+    case EPI_DQ_BIAS_RESIDUAL:   // fp32 pre-LayerNorm sum, fp16 residual
+      return dispatch_bn<BF, float, __half, EPI_DQ_BIAS_RESIDUAL, NCH>(bn, ta, tb, p, gr, stream);
+    case EPI_DQ_BIAS_GELU_Q: return dispatch_bn<BF, BF, BF, EPI_DQ_BIAS_GELU_Q, NCH>(bn, ta, tb, p, gr, stream);
     default: return cudaErrorNotSupported;
   }
 }
 
 }  // namespace
 
-bool gemm_tc_supported(int N, int K) { return K % 8 == 0 && K > 0 && N % 16 == 0 && choose_bn(1, N, 256) != 0; }
+bool gemm_tc_supported(int N, int K) {
+  return K % 8 == 0 && K > 0 && N % 16 == 0 && choose_tiles(1, N, K, 256, 1).bn != 0;
+}
 
 cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t stream) {
   const bool is_int = g.epi >= EPI_I32;
@@ -483,20 +543,29 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t stream) {
   const int nch = is_int ? (num_k + kChunkBlocks - 1) / kChunkBlocks : 1;
   if (nch > 4) return cudaErrorNotSupported;
   const int max_bn = nch > 1 ? 128 : 256;
-  const int bn = g.force_bn ? g.force_bn : choose_bn(g.M_max, g.N, max_bn);
+  // splitting K is only possible for the fp32 partial-sum output of the residual epilogue
+  const bool can_split = g.max_splits > 1 && g.epi == RPP_EPI_BIAS_RESIDUAL && g.out_dtype == RPP_F32;
+  const int rows_hint = (g.rows_hint > 0 && g.rows_hint < g.M_max) ? g.rows_hint : g.M_max;
+  TileChoice tc = choose_tiles(rows_hint, g.N, g.K, max_bn, can_split ? g.max_splits : 1);
+  if (g.force_bn) tc.bn = g.force_bn;
+  const int bn = tc.bn;
   if (!bn || g.N % bn || bn > max_bn) return cudaErrorNotSupported;
+  if (g.splits_out) *g.splits_out = tc.splits;
   const CUtensorMapDataType dt =
       (is_int || g.in_dtype == RPP_BF16) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap ta, tb;
   if (!make_tmap_2d(&ta, g.a, dt, 2, g.M_max, g.K, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
   if (!make_tmap_2d(&tb, g.w_t, dt, 2, g.N, g.K, bn, kBK, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
-  GemmParams p{g.M_max, g.rows, g.N, g.K, g.bias, g.residual, g.out, g.a_scale, g.w_scale, g.q_scale, g.err};
+  GemmParams p{g.M_max, g.rows, g.N, g.K, g.bias, g.residual, g.out, g.a_scale, g.w_scale, g.q_scale, g.err,
+               tc.splits, static_cast<long long>(g.M_max) * g.N};
   if (is_int) {
-    if (nch == 1) return dispatch_int<1>(bn, g.epi, g.out_dtype, ta, tb, p, stream);
-    return dispatch_int<4>(bn, g.epi, g.out_dtype, ta, tb, p, stream);
+    if (nch == 1) return dispatch_int<1>(bn, g.epi, g.out_dtype, ta, tb, p, rows_hint, stream);
+    return dispatch_int<4>(bn, g.epi, g.out_dtype, ta, tb, p, rows_hint, stream);
   }
-  if (g.in_dtype == RPP_BF16) return dispatch_float<__nv_bfloat16>(bn, g.epi, ta, tb, p, stream);
-  if (g.in_dtype == RPP_F16) return dispatch_float<__half>(bn, g.epi, ta, tb, p, stream);
+  if (g.in_dtype == RPP_BF16)
+    return dispatch_float<__nv_bfloat16>(bn, g.epi, g.out_dtype, g.res_dtype, ta, tb, p, rows_hint, stream);
+  if (g.in_dtype == RPP_F16)
+    return dispatch_float<__half>(bn, g.epi, g.out_dtype, g.res_dtype, ta, tb, p, rows_hint, stream);
   return cudaErrorNotSupported;
 }
 

@@ -24,15 +24,20 @@ cudaError_t launch_rebuild_padding(const void* packed, const int32_t* cu, int B,
                                    int32_t* err, cudaStream_t stream);
 
 bool layernorm_supported(int H, rpp_dtype dtype);
+// x of in_dtype, y of out_dtype (equal, or fp32 in -> fp16 / bf16 out for the layer's
+// fp32 pre-LayerNorm sums); optional bf16-held int8 codes of y, running max-abs and an
+// fp32 copy of y
 cudaError_t launch_layernorm(const void* x, const float* gamma, const float* beta, void* y, int M_max,
-                             const int32_t* rows, int H, float eps, rpp_dtype dtype, void* q_codes_bf16,
-                             const float* q_scale, float* amax, int32_t* err, cudaStream_t stream);
+                             const int32_t* rows, int H, float eps, rpp_dtype in_dtype, rpp_dtype out_dtype,
+                             void* q_codes_bf16, const float* q_scale, float* amax, float* y32, int32_t* err,
+                             cudaStream_t stream, int n_in = 1, long long in_stride = 0);
+// (n_in > 1: x holds n_in fp32 slices in_stride elements apart whose sum is normalised)
 cudaError_t launch_quantize(const void* x, const float* scale, int8_t* q, int M_max, const int32_t* rows, int H,
                             rpp_dtype dtype, int32_t* err, cudaStream_t stream);
 cudaError_t launch_amax(const void* x, int M_max, const int32_t* rows, int H, rpp_dtype dtype, float* amax,
                         int32_t* err, cudaStream_t stream);
 
-// int8 code helpers (quant.cu)
+// preprocessing and int8 code helpers (prep.cu)
 cudaError_t launch_quantize_codes_bf16(const void* x, const float* scale, void* codes, int M_max, const int32_t* rows,
                                        int H, rpp_dtype dtype, int32_t* err, cudaStream_t stream);
 cudaError_t launch_i8_to_bf16(const int8_t* src, void* dst, long long n, cudaStream_t stream);
@@ -52,13 +57,17 @@ struct TcGemmArgs {
   const int32_t* rows;
   int N, K;
   rpp_dtype in_dtype;      // RPP_F16 or RPP_BF16
-  rpp_dtype out_dtype;     // RPP_F16 / RPP_BF16 (or anything for EPI_I32)
+  rpp_dtype out_dtype;     // RPP_F16 / RPP_BF16 / RPP_F32 (anything for EPI_I32)
+  rpp_dtype res_dtype;     // residual type for the float path: in_dtype (default) or RPP_F32
   int epi;                 // rpp_epilogue or InternalEpilogue
   const float* a_scale;    // device scalar s_a (int8 epilogues)
   const float* w_scale;    // device [N] s_w (int8 epilogues)
   const float* q_scale;    // device scalar for the requantised output (EPI_DQ_BIAS_GELU_Q)
   int32_t* err;
   int force_bn;            // 0 = heuristic
+  int rows_hint;           // expected rows (0 = M_max): tile shapes only, never correctness
+  int max_splits;          // > 1 allows split-K (fp32 partial slices, residual epilogue only)
+  int* splits_out;         // if set, receives the number of K splits used
 };
 bool gemm_tc_supported(int N, int K);
 cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t stream);

@@ -27,12 +27,34 @@ __device__ __forceinline__ void atomic_max_nonneg(float* addr, float v) {
   atomicMax(reinterpret_cast<int*>(addr), __float_as_int(v));
 }
 
-template <typename T, int G, int VPL>
+// EPV floats -> EPV elements of TOut at p (16 or 8 bytes)
+template <typename TOut, int EPV>
+__device__ __forceinline__ void store_vec(TOut* p, const float* o) {
+  if constexpr (sizeof(TOut) * EPV == 16) {
+    *reinterpret_cast<uint4*>(p) = pack16<TOut>(o);
+  } else {
+    static_assert(sizeof(TOut) == 2 && EPV == 4, "8-byte store of four 16-bit values");
+    uint2 v;
+    if constexpr (std::is_same<TOut, __half>::value) {
+      __half2 a = __floats2half2_rn(o[0], o[1]), b = __floats2half2_rn(o[2], o[3]);
+      v.x = *reinterpret_cast<uint32_t*>(&a);
+      v.y = *reinterpret_cast<uint32_t*>(&b);
+    } else {
+      __nv_bfloat162 a = __floats2bfloat162_rn(o[0], o[1]), b = __floats2bfloat162_rn(o[2], o[3]);
+      v.x = *reinterpret_cast<uint32_t*>(&a);
+      v.y = *reinterpret_cast<uint32_t*>(&b);
+    }
+    *reinterpret_cast<uint2*>(p) = v;
+  }
+}
+
+template <typename T, typename TOut, int G, int VPL>
 __global__ void __launch_bounds__(256) layernorm_kernel(const T* __restrict__ x, const float* __restrict__ gamma,
-                                                        const float* __restrict__ beta, T* y, int M_max,
+                                                        const float* __restrict__ beta, TOut* y, int M_max,
                                                         const int32_t* rows, int H, float eps,
                                                         __nv_bfloat16* __restrict__ q_out, const float* q_scale,
-                                                        float* amax, int32_t* err) {
+                                                        float* amax, float* __restrict__ y32, int n_in,
+                                                        long long in_stride, int32_t* err) {
   if (device_error_set(err)) return;
   int M = rows ? *rows : M_max;
   if (M > M_max || M < 0) {
@@ -61,6 +83,19 @@ __global__ void __launch_bounds__(256) layernorm_kernel(const T* __restrict__ x,
       if (valid) raw = xr[i * G + gl];
       unpack16<T>(raw, v[i]);
     }
+    // split-K partial sums of the preceding GEMM: add the other slices of this row
+    for (int sl = 1; sl < n_in; ++sl) {
+      const uint4* xs = reinterpret_cast<const uint4*>(x + sl * in_stride + static_cast<long long>(valid ? row : 0) * H);
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        float f[EPV];
+        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+        if (valid) raw = xs[i * G + gl];
+        unpack16<T>(raw, f);
+#pragma unroll
+        for (int j = 0; j < EPV; ++j) v[i][j] += f[j];
+      }
+    }
     float s = 0.f;
 #pragma unroll
     for (int i = 0; i < VPL; ++i)
@@ -81,7 +116,7 @@ __global__ void __launch_bounds__(256) layernorm_kernel(const T* __restrict__ x,
     for (int o = G / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     const float rstd = rsqrtf(ss / static_cast<float>(H) + eps);
     if (valid) {
-      uint4* yr = reinterpret_cast<uint4*>(y + static_cast<long long>(row) * H);
+      TOut* yr = y + static_cast<long long>(row) * H;
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
         const int col0 = (i * G + gl) * EPV;
@@ -95,18 +130,17 @@ __global__ void __launch_bounds__(256) layernorm_kernel(const T* __restrict__ x,
           o[j + 2] = (v[i][j + 2] - mean) * rstd * g4.z + b4.z;
           o[j + 3] = (v[i][j + 3] - mean) * rstd * g4.w + b4.w;
         }
-        yr[i * G + gl] = pack16<T>(o);
+        store_vec<TOut, EPV>(yr + col0, o);
+        if (y32) {   // fp32 copy of the normalised row (the next residual add reads it)
+          float* yf = y32 + static_cast<long long>(row) * H + col0;
+#pragma unroll
+          for (int j = 0; j < EPV; j += 4) *reinterpret_cast<float4*>(yf + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+        }
         if (q_out) {   // int8 codes of the normalised row, held in bf16 (exact)
           float qv[EPV];
 #pragma unroll
           for (int j = 0; j < EPV; ++j) qv[j] = static_cast<float>(quantize_one(o[j], inv_s));
-          __nv_bfloat16* qr = q_out + static_cast<long long>(row) * H + col0;
-          if constexpr (EPV == 8) {
-            *reinterpret_cast<uint4*>(qr) = pack16<__nv_bfloat16>(qv);
-          } else {
-#pragma unroll
-            for (int j = 0; j < EPV; ++j) qr[j] = __float2bfloat16_rn(qv[j]);
-          }
+          store_vec<__nv_bfloat16, EPV>(q_out + static_cast<long long>(row) * H + col0, qv);
         }
         if (amax) {
 #pragma unroll
@@ -176,29 +210,31 @@ __global__ void amax_kernel(const T* __restrict__ x, int M_max, const int32_t* r
   if (lane_id() == 0) atomic_max_nonneg(amax, m);
 }
 
-template <typename T, int G, int VPL>
+template <typename T, typename TOut, int G, int VPL>
 cudaError_t ln_launch(const void* x, const float* gamma, const float* beta, void* y, int M_max, const int32_t* rows,
-                      int H, float eps, __nv_bfloat16* q_out, const float* q_scale, float* amax, int32_t* err,
-                      cudaStream_t stream) {
+                      int H, float eps, __nv_bfloat16* q_out, const float* q_scale, float* amax, float* y32,
+                      int n_in, long long in_stride, int32_t* err, cudaStream_t stream) {
   const int threads = 256;
   const int rows_per_block = (threads / 32) * (32 / G);
   long long blocks = (static_cast<long long>(M_max) + rows_per_block - 1) / rows_per_block;
   const long long cap = static_cast<long long>(num_sms()) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  layernorm_kernel<T, G, VPL><<<static_cast<int>(blocks), threads, 0, stream>>>(
-      static_cast<const T*>(x), gamma, beta, static_cast<T*>(y), M_max, rows, H, eps, q_out, q_scale, amax, err);
+  layernorm_kernel<T, TOut, G, VPL><<<static_cast<int>(blocks), threads, 0, stream>>>(
+      static_cast<const T*>(x), gamma, beta, static_cast<TOut*>(y), M_max, rows, H, eps, q_out, q_scale, amax, y32,
+      n_in, in_stride, err);
   return cudaGetLastError();
 }
 
-template <typename T>
+template <typename T, typename TOut>
 cudaError_t ln_dispatch(const void* x, const float* gamma, const float* beta, void* y, int M_max, const int32_t* rows,
-                        int H, float eps, __nv_bfloat16* q_out, const float* q_scale, float* amax, int32_t* err,
-                        cudaStream_t stream) {
+                        int H, float eps, __nv_bfloat16* q_out, const float* q_scale, float* amax, float* y32,
+                        int n_in, long long in_stride, int32_t* err, cudaStream_t stream) {
   const int V = H / Vec<T>::N;   // 16-byte vectors per row
 #define RPP_LN_CASE(G_, VPL_)                                                                                  \
   if (V == (G_) * (VPL_))                                                                                      \
-    return ln_launch<T, G_, VPL_>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, err, stream);
+    return ln_launch<T, TOut, G_, VPL_>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, y32, n_in, \
+                                        in_stride, err, stream);
   RPP_LN_CASE(32, 1) RPP_LN_CASE(32, 2) RPP_LN_CASE(32, 3) RPP_LN_CASE(32, 4)
   RPP_LN_CASE(32, 5) RPP_LN_CASE(32, 6) RPP_LN_CASE(32, 8) RPP_LN_CASE(32, 12) RPP_LN_CASE(32, 16)
   RPP_LN_CASE(16, 1) RPP_LN_CASE(16, 3) RPP_LN_CASE(8, 1) RPP_LN_CASE(8, 3) RPP_LN_CASE(8, 5)
@@ -223,16 +259,25 @@ bool layernorm_supported(int H, rpp_dtype dtype) {
 }
 
 cudaError_t launch_layernorm(const void* x, const float* gamma, const float* beta, void* y, int M_max,
-                             const int32_t* rows, int H, float eps, rpp_dtype dtype, void* q_codes,
-                             const float* q_scale, float* amax, int32_t* err, cudaStream_t stream) {
+                             const int32_t* rows, int H, float eps, rpp_dtype in_dtype, rpp_dtype out_dtype,
+                             void* q_codes, const float* q_scale, float* amax, float* y32, int32_t* err,
+                             cudaStream_t stream, int n_in, long long in_stride) {
+  if (n_in > 1 && in_dtype != RPP_F32) return cudaErrorNotSupported;
   __nv_bfloat16* q_out = static_cast<__nv_bfloat16*>(q_codes);
-  switch (dtype) {
-    case RPP_F32: return ln_dispatch<float>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, err, stream);
-    case RPP_F16: return ln_dispatch<__half>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, err, stream);
-    case RPP_BF16:
-      return ln_dispatch<__nv_bfloat16>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, err, stream);
-    default: return cudaErrorNotSupported;
+  using BF = __nv_bfloat16;
+  if (in_dtype == out_dtype) {
+    switch (in_dtype) {
+      case RPP_F32: return ln_dispatch<float, float>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, y32, n_in, in_stride, err, stream);
+      case RPP_F16: return ln_dispatch<__half, __half>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, y32, n_in, in_stride, err, stream);
+      case RPP_BF16: return ln_dispatch<BF, BF>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, y32, n_in, in_stride, err, stream);
+      default: return cudaErrorNotSupported;
+    }
   }
+  if (in_dtype == RPP_F32 && out_dtype == RPP_F16)
+    return ln_dispatch<float, __half>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, y32, n_in, in_stride, err, stream);
+  if (in_dtype == RPP_F32 && out_dtype == RPP_BF16)
+    return ln_dispatch<float, BF>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, y32, n_in, in_stride, err, stream);
+  return cudaErrorNotSupported;
 }
 
 cudaError_t launch_quantize(const void* x, const float* scale, int8_t* q, int M_max, const int32_t* rows, int H,

@@ -17,10 +17,13 @@ from gpu_util import dev, up, down, assert_close, check_err, TOL
 pytestmark = pytest.mark.gpu
 
 
-def _run_path(wl, dtype, layers=None):
+def _run_path(wl, dtype, layers=None, hint=False):
+    """hint=True passes the true token count as the tile-shape hint (the bench's launch
+    configuration: exact-size tiles and split-K with LayerNorm-side reduction)."""
     cfg = wl["cfg"]
     layers = layers if layers is not None else wl["layers"]
-    ecfg = rpp.encoder_cfg(cfg.H, cfg.nh, cfg.F, cfg.eps, dtype)
+    T = int(wl["lengths"].sum())
+    ecfg = rpp.encoder_cfg(cfg.H, cfg.nh, cfg.F, cfg.eps, dtype, tokens_hint=T if hint else 0)
     prepared = [rpp.EncoderLayer(ecfg, l) for l in layers]
     lengths = torch.as_tensor(wl["lengths"], device=dev())
     x = up(wl["x_padded"].reshape(-1, cfg.H), dtype)
@@ -30,16 +33,17 @@ def _run_path(wl, dtype, layers=None):
     return down(y).reshape(cfg.B, cfg.L, cfg.H), prepared
 
 
+@pytest.mark.parametrize("hint", [False, True])
 @pytest.mark.parametrize("idx,B,L,lens", [
     (0, 4, 64, None),                                  # tiny fp32 config as drawn
     (1, 6, 128, [128, 1, 17, 64, 65, 100]),           # BERT-base shapes, fp16
     (2, 3, 384, [384, 129, 33]),                       # BERT-large shapes, bf16
 ])
-def test_layer_small(idx, B, L, lens):
+def test_layer_small(idx, B, L, lens, hint):
     cfg = CONFIGS[idx]
     wl = make_bert_workload(cfg, B=B, L=L, layers=1, lengths=None if lens is None else np.array(lens, np.int32),
                             affine=True)
-    got, _ = _run_path(wl, cfg.dtype)
+    got, _ = _run_path(wl, cfg.dtype, hint=hint)
     ref, _, _ = oracle.bert_forward(wl["x_padded"], wl["lengths"], wl["layers"], cfg.nh, cfg.eps)
     assert_close(got, ref, cfg.dtype, cfg.name)
 
@@ -55,9 +59,10 @@ def test_bert_base_full_config():
     """configs[1] at full size (the bench workload), every output against the oracle."""
     cfg = CONFIGS[1]
     wl = make_bert_workload(cfg)
-    got, _ = _run_path(wl, "fp16")
     ref, _, _ = oracle.bert_forward(wl["x_padded"], wl["lengths"], wl["layers"], cfg.nh, cfg.eps)
-    assert_close(got, ref, "fp16", cfg.name)
+    for hint in (True, False):
+        got, _ = _run_path(wl, "fp16", hint=hint)
+        assert_close(got, ref, "fp16", f"{cfg.name} hint={hint}")
 
 
 def test_tiny_fp32_full_config():
@@ -72,7 +77,7 @@ def _teacher_forced_stack(wl, dtype, n_layers, sample):
     """Run each layer on the GPU and check it against the oracle applied to the exact
     (rounded) input the GPU layer saw, on sampled sequences."""
     cfg = wl["cfg"]
-    ecfg = rpp.encoder_cfg(cfg.H, cfg.nh, cfg.F, cfg.eps, dtype)
+    ecfg = rpp.encoder_cfg(cfg.H, cfg.nh, cfg.F, cfg.eps, dtype, tokens_hint=int(wl["lengths"].sum()))
     lengths = torch.as_tensor(wl["lengths"], device=dev())
     err = rpp.new_error_word()
     cu, po = rpp.build_offsets(lengths, cfg.L, err=err)

@@ -43,10 +43,14 @@ def test_int8_gemm_exact():
     a = rng.integers(-127, 128, size=(33, 1024)).astype(np.int8)
     b = rng.integers(-127, 128, size=(1024, 17)).astype(np.int8)
     acc = oracle.int8_gemm(a, b)
-    ref = a.astype(np.float64) @ b.astype(np.float64)   # exact: |sum| < 2^53
-    assert np.array_equal(acc, ref.astype(np.int64))
+    ref = a.astype(np.int64) @ b.astype(np.int64)     # integer arithmetic route
+    assert acc.dtype == np.int64 and np.array_equal(acc, ref)
     worst = oracle.int8_gemm(np.full((1, 4096), 127, np.int8), np.full((4096, 1), -127, np.int8))
     assert worst[0, 0] == -127 * 127 * 4096
+    # brute force on a tiny case
+    a2, b2 = a[:3, :5].astype(int), b[:5, :2].astype(int)
+    bf = [[sum(a2[i, k] * b2[k, j] for k in range(5)) for j in range(2)] for i in range(3)]
+    assert oracle.int8_gemm(a2, b2).tolist() == bf
 
 
 def test_int8_linear_lossless_on_grid():
