@@ -277,6 +277,31 @@ RPP_API size_t rpp_gemm_i8_workspace_bytes(int M, int N, int K);
 RPP_API rpp_status rpp_gemm_i8_i32(const int8_t* aq, const int8_t* wq_t, int32_t* acc, int M, int N, int K,
                            void* workspace, size_t workspace_bytes, int32_t* err, rpp_stream stream);
 
+/* Allocation-free int8 GEMM (no counterpart on the pages; an addition for callers
+ * that cannot allocate device memory).
+ *
+ * Same result as rpp_gemm_i8_i32 -- acc[M, N] = aq[M, K] @ wq_t[N, K]^T exactly, int32 --
+ * but the bf16 re-encoding of the operands lives in a scratch array that is part of
+ * the library (device global memory, RPP_GEMM_I8_NOALLOC_SCRATCH_BYTES on every GPU
+ * that loads the library, held until the process exits) instead of a caller buffer.
+ * Meant for callers that cannot allocate: plugins whose host framework owns all device
+ * memory and offers no allocator, latency-critical paths that must not call cudaMalloc
+ * (it may synchronise the device), or foreign-function callers that cannot manage
+ * device buffer lifetimes.  The caller still passes the inputs and the output; the
+ * call itself allocates nothing (no cudaMalloc / cudaFree, no allocating library).
+ *  - Sizes: as rpp_gemm_i8_i32 (K % 16 == 0, N % 16 == 0, K <= 4096), and the
+ *    re-encoded operands, round256(M*K*2) + round256(N*K*2) bytes, must fit the
+ *    scratch; larger problems return RPP_EWORKSPACE and launch nothing.
+ *  - All calls share the one scratch array, which keeps the previous call's contents;
+ *    each call writes every byte it reads, so nothing needs clearing, but calls whose
+ *    kernels overlap on the GPU (unordered streams) race on it.
+ *  - The first call on each device looks up the scratch array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call before
+ *    any stream capture. */
+#define RPP_GEMM_I8_NOALLOC_SCRATCH_BYTES (8u << 20) /* 8 MiB */
+RPP_API rpp_status rpp_gemm_i8_i32_noalloc(const int8_t* aq, const int8_t* wq_t, int32_t* acc, int M,
+                                           int N, int K, int32_t* err, rpp_stream stream);
+
 /* ------------------------------------------------------------------------------
  * Swin shifted-window block ([SW] §1-§3)
  * ------------------------------------------------------------------------------ */

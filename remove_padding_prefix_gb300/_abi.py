@@ -66,6 +66,7 @@ SIGNATURES = {
     "rpp_quantize_activation": (i32, [vp, vp, vp, i32, vp, i32, i32, vp, vp]),
     "rpp_gemm_i8_workspace_bytes": (sz, [i32, i32, i32]),
     "rpp_gemm_i8_i32": (i32, [vp, vp, vp, i32, i32, i32, vp, sz, vp, vp]),
+    "rpp_gemm_i8_i32_noalloc": (i32, [vp, vp, vp, i32, i32, i32, vp, vp]),
     "rpp_swin_prepare_bias": (i32, [C.POINTER(SwinCfg), vp, vp, vp]),
     "rpp_window_attention_forward": (i32, [C.POINTER(SwinCfg), i32, vp, vp, vp, vp, vp]),
     "rpp_swin_block_bytes": (sz, [C.POINTER(SwinCfg)]),
