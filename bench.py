@@ -52,6 +52,7 @@ def parse():
     p.add_argument("--workload", default="bert_base_fp16")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-graph", action="store_true")
     return p.parse_args()
 
 
@@ -281,35 +282,60 @@ def main():
     if rpp.get_device_error(err):
         raise SystemExit(f"device error {rpp.get_device_error(err)}")
 
-    # ---- timed region
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    # ---- timed region: K steps, each bracketed by its own events; L2 flushed between
+    def timed(run_step, label):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            run_step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        tot = sum(a.elapsed_time(b) for a, b in ev) / 1e3
+        if world > 1:
+            t = torch.tensor([tot], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            tot = float(t.item())
+        return tot
+
+    eager_s = timed(step, "eager")
+    y_eager = y.clone()
+    # one step captured into a CUDA graph (the calls allocate nothing and never sync)
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph):
+            step()
+        torch.cuda.synchronize()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
     clk_path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv") if os.path.isdir(
         os.path.join(ROOT, "gpurun_out")) else f"/tmp/rpp_clocks_{rank}.csv"
     proc, fh = clocks_sampler_start(clk_path)
     time.sleep(0.3)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        flush.fill_(float(i))
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+    total_s = timed(graph.replay if graph is not None else step, "graph")
     clocks = clocks_sampler_stop(proc, fh, clk_path, local)
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_s = sum(step_ms) / 1e3
-    if world > 1:
-        t = torch.tensor([total_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_s = float(t.item())
     code = rpp.get_device_error(err)
     if code:
         raise SystemExit(f"device error {code}")
+    if not torch.equal(y, y_eager):
+        raise SystemExit("graph replay output differs from the eager step")
     tokens_per_step = T * len(layers)   # valid tokens x layers: tokens/s per encoder layer
     value = tokens_per_step * args.steps * world / total_s
+    value_eager = tokens_per_step * args.steps * world / eager_s
 
     # ---- per-kernel durations inside the real step (launch-event hook)
     lib = rpp.lib()
@@ -428,6 +454,8 @@ def main():
                 "data": "synthetic", "config": workload_config(cfg), "roofline": roof, "cpu_baseline": cpu,
                 "e2e": e2e, "gpu_launches": int(n_launch_step * args.steps) if n_launch_step else None,
                 "clocks": clocks, "tokens_per_step": T, "layers": len(layers),
+                "launch": "CUDA graph of one step" if graph is not None else "eager C-ABI calls",
+                "value_eager": value_eager, "ms_per_step_eager": 1e3 * eager_s / args.steps,
                 "kernels": per_launch}
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -242,24 +242,43 @@ rpp_status encoder_layer_run(const rpp_encoder_cfg* c, const void* layer, const 
   const float* be2 = at<float>(layer, P.be2);
 
   if (!c->int8) {
+    // proj / FC2 write raw fp32 accumulators (split-K slices); the LayerNorm after each
+    // adds the slices, the GEMM's bias and the residual while it reads the row
+    // ([SW] §3: bias split off the GEMM and fused into the next op).  The fp32 layer
+    // runs its GEMMs on CUDA cores, with bias and residual in the GEMM epilogue.
+    const bool tc = dt != RPP_F32;
+    float* x1f = fp32_residual(c) ? at<float>(ws, W.x1f) : nullptr;
     if (amax) RPP_LAUNCH("amax", s, launch_amax(x, T_max, rows, H, dt, amax + 0, err, s));
     RPP_LAUNCH("gemm_qkv", s, linear(dt, x, at<void>(layer, P.wqkv), bqkv, nullptr, qkv, T_max, rows, 3 * H, H,
                                      RPP_EPI_BIAS, err, s, RPP_I8, RPP_I8, hint));
     RPP_LAUNCH("attention", s, launch_attention_varlen(qkv, cu, B, T_max, max_len, nh, d, dt, attn, err, s));
     if (amax) RPP_LAUNCH("amax", s, launch_amax(attn, T_max, rows, H, dt, amax + 1, err, s));
-    RPP_LAUNCH("gemm_proj", s, linear(dt, attn, at<void>(layer, P.wo), bo, x, h, T_max, rows, H, H,
-                                      RPP_EPI_BIAS_RESIDUAL, err, s, hdt, RPP_I8, hint, kMaxSplits, &sp_proj));
-    float* x1f = fp32_residual(c) ? at<float>(ws, W.x1f) : nullptr;
-    RPP_LAUNCH("layernorm1", s, launch_layernorm(h, g1, be1, x1, T_max, rows, H, c->eps, hdt, dt, nullptr, nullptr,
-                                                 amax ? amax + 2 : nullptr, x1f, err, s, sp_proj, hs));
+    if (tc) {
+      RPP_LAUNCH("gemm_proj", s, linear(dt, attn, at<void>(layer, P.wo), nullptr, nullptr, h, T_max, rows, H, H,
+                                        EPI_ACC, err, s, hdt, RPP_I8, hint, kMaxSplits, &sp_proj));
+      RPP_LAUNCH("layernorm1", s, launch_layernorm(h, g1, be1, x1, T_max, rows, H, c->eps, hdt, dt, nullptr, nullptr,
+                                                   amax ? amax + 2 : nullptr, x1f, err, s, sp_proj, hs, bo, x, dt));
+    } else {
+      RPP_LAUNCH("gemm_proj", s, linear(dt, attn, at<void>(layer, P.wo), bo, x, h, T_max, rows, H, H,
+                                        RPP_EPI_BIAS_RESIDUAL, err, s));
+      RPP_LAUNCH("layernorm1", s, launch_layernorm(h, g1, be1, x1, T_max, rows, H, c->eps, hdt, dt, nullptr, nullptr,
+                                                   amax ? amax + 2 : nullptr, nullptr, err, s));
+    }
     RPP_LAUNCH("gemm_fc1", s, linear(dt, x1, at<void>(layer, P.w1), b1, nullptr, g, T_max, rows, F, H,
                                      RPP_EPI_BIAS_GELU, err, s, RPP_I8, RPP_I8, hint));
     if (amax) RPP_LAUNCH("amax", s, launch_amax(g, T_max, rows, F, dt, amax + 3, err, s));
-    RPP_LAUNCH("gemm_fc2", s, linear(dt, g, at<void>(layer, P.w2), b2, x1f ? static_cast<const void*>(x1f) : x1, h,
-                                     T_max, rows, H, F, RPP_EPI_BIAS_RESIDUAL, err, s, hdt, x1f ? RPP_F32 : dt, hint,
-                                     kMaxSplits, &sp_fc2));
-    RPP_LAUNCH("layernorm2", s, launch_layernorm(h, g2, be2, y, T_max, rows, H, c->eps, hdt, dt, nullptr, nullptr,
-                                                 nullptr, nullptr, err, s, sp_fc2, hs));
+    if (tc) {
+      RPP_LAUNCH("gemm_fc2", s, linear(dt, g, at<void>(layer, P.w2), nullptr, nullptr, h, T_max, rows, H, F, EPI_ACC,
+                                       err, s, hdt, RPP_I8, hint, kMaxSplits, &sp_fc2));
+      RPP_LAUNCH("layernorm2", s, launch_layernorm(h, g2, be2, y, T_max, rows, H, c->eps, hdt, dt, nullptr, nullptr,
+                                                   nullptr, nullptr, err, s, sp_fc2, hs, b2,
+                                                   x1f ? static_cast<const void*>(x1f) : x1, x1f ? RPP_F32 : dt));
+    } else {
+      RPP_LAUNCH("gemm_fc2", s, linear(dt, g, at<void>(layer, P.w2), b2, x1, h, T_max, rows, H, F,
+                                       RPP_EPI_BIAS_RESIDUAL, err, s));
+      RPP_LAUNCH("layernorm2", s, launch_layernorm(h, g2, be2, y, T_max, rows, H, c->eps, hdt, dt, nullptr, nullptr,
+                                                   nullptr, nullptr, err, s));
+    }
     return RPP_OK;
   }
   // int8: quantise -> int8 GEMM (exact integer accumulation) -> dequantise in the epilogue
@@ -276,16 +295,16 @@ rpp_status encoder_layer_run(const rpp_encoder_cfg* c, const void* layer, const 
                                           nullptr, qkv, dt, T_max, rows, 3 * H, H, EPI_DQ_BIAS, err, s, hint));
   RPP_LAUNCH("attention", s, launch_attention_varlen(qkv, cu, B, T_max, max_len, nh, d, dt, attn, err, s));
   RPP_LAUNCH("quantize_attn", s, launch_quantize_codes_bf16(attn, s1, ca, T_max, rows, H, dt, err, s));
-  RPP_LAUNCH("gemm_proj_i8", s, linear_i8(ca, at<void>(layer, P.wo), bo, s1, at<float>(layer, P.so), nullptr, x, h,
-                                           dt, T_max, rows, H, H, EPI_DQ_BIAS_RESIDUAL, err, s, hint));
+  RPP_LAUNCH("gemm_proj_i8", s, linear_i8(ca, at<void>(layer, P.wo), nullptr, s1, at<float>(layer, P.so), nullptr,
+                                           nullptr, h, RPP_F32, T_max, rows, H, H, EPI_DQ_ACC, err, s, hint));
   RPP_LAUNCH("layernorm1", s, launch_layernorm(h, g1, be1, x1, T_max, rows, H, c->eps, hdt, dt, cx1, s2, nullptr,
-                                               nullptr, err, s));
+                                               nullptr, err, s, 1, hs, bo, x, dt));
   RPP_LAUNCH("gemm_fc1_i8", s, linear_i8(cx1, at<void>(layer, P.w1), b1, s2, at<float>(layer, P.s1), s3, nullptr, cg,
                                           RPP_BF16, T_max, rows, F, H, EPI_DQ_BIAS_GELU_Q, err, s, hint));
-  RPP_LAUNCH("gemm_fc2_i8", s, linear_i8(cg, at<void>(layer, P.w2), b2, s3, at<float>(layer, P.s2), nullptr, x1, h,
-                                          dt, T_max, rows, H, F, EPI_DQ_BIAS_RESIDUAL, err, s, hint));
+  RPP_LAUNCH("gemm_fc2_i8", s, linear_i8(cg, at<void>(layer, P.w2), nullptr, s3, at<float>(layer, P.s2), nullptr,
+                                          nullptr, h, RPP_F32, T_max, rows, H, F, EPI_DQ_ACC, err, s, hint));
   RPP_LAUNCH("layernorm2", s, launch_layernorm(h, g2, be2, y, T_max, rows, H, c->eps, hdt, dt, nullptr, nullptr,
-                                               nullptr, nullptr, err, s));
+                                               nullptr, nullptr, err, s, 1, hs, b2, x1, dt));
   return RPP_OK;
 }
 

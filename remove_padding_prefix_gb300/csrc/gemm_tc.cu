@@ -1,13 +1,13 @@
 // Persistent, warp-specialised tcgen05 GEMM for sm_103a with fused epilogues.
 //
 //   out[M, N] = epilogue(A[M, K] @ W[N, K]^T),   A, W fp16 or bf16 (both K-major),
-//   fp32 accumulation in tensor memory, epilogue = bias | bias+GELU | bias+residual.
+//   fp32 accumulation in tensor memory.
 //
-// The NVIDIA Swin talk (§3) fuses the bias (and activation) into the GEMM and moves
-// the bias next to the residual add before LayerNorm; the Kuaishou article (Fig. 6,
-// Fig. 11) fuses the elementwise work into the GEMMs and tunes the GEMM tile
-// configuration per shape.  Here the GEMM itself is written for the 5th-generation
-// tensor cores:
+// The NVIDIA Swin talk (§3) fuses the bias (and activation) into the GEMM and, when
+// the op after the GEMM is LayerNorm, splits the bias off the GEMM and fuses it into
+// that next op; the Kuaishou article (Fig. 6, Fig. 11) fuses the elementwise work
+// into the GEMMs and tunes the GEMM tile configuration per shape.  Here the GEMM is
+// written for the 5th-generation tensor cores:
 //
 //   warp 0      TMA producer: 2D tiled loads with 128-byte swizzle of a 128 x 64 A
 //               tile and a BN x 64 W tile per pipeline stage (no multicast).
@@ -15,22 +15,28 @@
 //               K = 16 per instruction) from one thread; tcgen05.commit releases the
 //               smem stage and, after the last K block, signals the accumulator.
 //   warps 2..9  epilogue: two warps per tensor-memory lane quadrant, each taking every
-//               other 32-column slice: tcgen05.ld 32 lanes x 32 columns, bias / GELU /
-//               residual in fp32, 16-byte stores of the converted row segment.
+//               other 32-column slice: tcgen05.ld 32 lanes x 32 columns (one row per
+//               thread), the epilogue arithmetic in fp32, then the 32 x 32 block goes
+//               to a swizzled staging buffer in shared memory and leaves with one TMA
+//               bulk-tensor store -- coalesced, asynchronous, no per-row scatter.
+//               Tiles that straddle the row count M (the ragged last tile), 16-column
+//               tails and the residual epilogue use per-row 16-byte stores instead.
 //
-// The accumulator is double-buffered in tensor memory (2 x BN columns), so the
-// epilogue of tile i overlaps the MMAs of tile i+1.  Tiles are assigned round-robin
-// over a persistent grid of at most one CTA per SM.  The row count M may live in
-// device memory (the packed token count); rows >= M are loaded (they are inside the
-// buffer) but never stored.  Every mbarrier wait is bounded; on a timeout the CTA
-// records RPP_DERR_TIMEOUT, drains its in-flight copies and MMAs, frees its tensor
-// memory and exits.
+// Epilogues: bias | bias + GELU | bias + residual | raw fp32 accumulator (the encoder
+// layer's proj / FC2: bias and residual are added by the LayerNorm that reads the
+// rows next) and the int8 variants below.
+//
+// The accumulator is double-buffered in tensor memory, so the epilogue of tile i
+// overlaps the MMAs of tile i+1.  Work units are assigned round-robin over a
+// persistent grid of at most one CTA per SM.  The row count M may live in device
+// memory (the packed token count).  Every mbarrier wait is bounded; on a timeout the
+// CTA records RPP_DERR_TIMEOUT, drains its in-flight copies and MMAs, frees its
+// tensor memory and exits.
 //
 // Split-K: when a GEMM has too few output tiles to fill the SMs (narrow N, few
-// tokens), each tile's K range is cut into `splits` parts; part s writes its fp32
-// partial sum into slice s of the output (part 0 also adds bias and residual) and the
-// LayerNorm that follows adds the slices while loading its row -- the reduction costs
-// no extra kernel and stays deterministic.
+// tokens), each tile's K range is cut into `splits` parts; part s writes its raw fp32
+// partial sum into slice s of the output and the LayerNorm that follows adds the
+// slices while loading its row: no extra kernel, deterministic.
 //
 // int8 layers: sm_103a has no int8 kind of tcgen05.mma, so the int8 GEMM runs as an
 // exact integer product on the bf16 tensor pipe.  Codes in [-127, 127] are exact in
@@ -38,6 +44,8 @@
 // 1024 so every fp32 partial sum is an integer below 2^24 and therefore exact; each
 // chunk accumulates into its own tensor-memory region and the epilogue adds the
 // chunks in int32.  The result equals int32 accumulation bit for bit.
+#include <cstring>
+
 #include "kernels.h"
 
 namespace rpp {
@@ -48,8 +56,8 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;   // 64 x 16-bit = 128 bytes = one swizzle row
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;
-
 constexpr int kChunkBlocks = 16;   // 16 x 64 = 1024 K per exact integer chunk
+constexpr size_t kSmemLimit = 232448;   // 227 KB per CTA
 
 struct GemmParams {
   int M_max;
@@ -75,65 +83,53 @@ template <typename T> struct AbFmt;
 template <> struct AbFmt<__half> { static constexpr int v = 0; };
 template <> struct AbFmt<__nv_bfloat16> { static constexpr int v = 1; };
 
+// epilogues whose full 32 x 32 blocks leave through the TMA store path
+template <int EPI>
+constexpr bool tma_store_epi() {
+  return EPI != RPP_EPI_BIAS_RESIDUAL;
+}
+template <int EPI>
+constexpr bool is_int_epi() {
+  return EPI >= EPI_I32 && EPI <= EPI_DQ_BIAS_GELU_Q;
+}
+
 __device__ __forceinline__ float code_of(float v, float inv_s) {
   const float t = __fmul_rn(v, inv_s);
   float q = rintf(t);   // round half to even
   return fminf(fmaxf(q, -127.f), 127.f);
 }
 
-// Epilogue of NV (32 or 16) accumulator columns [col, col + NV) of this thread's row:
-// tensor memory -> registers (summing the int8 chunk partials in int32), then bias,
-// dequantisation, GELU, requantisation, residual, conversion and 16-byte stores.
-template <typename TOut, typename TRes, int EPI, int NCH, int ACC, int NV>
-__device__ __forceinline__ void epilogue_cols(const GemmParams& p, uint32_t t_row, uint32_t a, int col, int nch,
-                                              int row, bool row_ok, int n0, float a_s, float inv_q, int split) {
-  constexpr bool kInt = EPI >= EPI_I32;
-  uint32_t r[NV];
-  float v[NV];
-  const uint32_t base = t_row + (a * NCH) * ACC + col;
-  if constexpr (NV == 32) tmem_ld_32x32b_x32(base, r); else tmem_ld_32x32b_x16(base, r);
-  tmem_ld_wait();
-  if constexpr (kInt) {
-    int acc[NV];   // exact: every chunk partial is an integer below 2^24
+// TMA store of a 2D box from shared memory (bulk group)
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Epilogue arithmetic on NV columns of this thread's row (v holds the accumulator;
+// for int8 epilogues the exact integer sum converted to float).
+template <typename TOut, typename TRes, int EPI, int NV>
+__device__ __forceinline__ void epi_math(const GemmParams& p, float* v, int row, int n, bool first, float a_s,
+                                         float inv_q) {
+  if constexpr (EPI == EPI_I32 || EPI == EPI_ACC) return;
+  if constexpr (EPI == EPI_DQ_BIAS || EPI == EPI_DQ_ACC || EPI == EPI_DQ_BIAS_GELU_Q) {
+    const float4* s4 = reinterpret_cast<const float4*>(p.w_scale + n);
 #pragma unroll
-    for (int j = 0; j < NV; ++j) acc[j] = __float2int_rn(__uint_as_float(r[j]));
-    for (int ch = 1; ch < nch; ++ch) {
-      if constexpr (NV == 32) tmem_ld_32x32b_x32(base + ch * ACC, r); else tmem_ld_32x32b_x16(base + ch * ACC, r);
-      tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < NV; ++j) acc[j] += __float2int_rn(__uint_as_float(r[j]));
+    for (int j = 0; j < NV / 4; ++j) {
+      const float4 ss = __ldg(s4 + j);
+      v[4 * j + 0] *= a_s * ss.x;
+      v[4 * j + 1] *= a_s * ss.y;
+      v[4 * j + 2] *= a_s * ss.z;
+      v[4 * j + 3] *= a_s * ss.w;
     }
-    if constexpr (EPI == EPI_I32) {
-      if (row_ok) {
-        int4* orow = reinterpret_cast<int4*>(static_cast<int32_t*>(p.out) + static_cast<long long>(row) * p.N + n0 + col);
-#pragma unroll
-        for (int j = 0; j < NV / 4; ++j) orow[j] = make_int4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
-      }
-      return;
-    }
-#pragma unroll
-    for (int j = 0; j < NV; ++j) v[j] = static_cast<float>(acc[j]);
-  } else {
-#pragma unroll
-    for (int j = 0; j < NV; ++j) v[j] = __uint_as_float(r[j]);
   }
-  if constexpr (EPI != EPI_I32) {
-    if (!row_ok) return;
-    const int n = n0 + col;
-    const bool first = split == 0;   // later K splits carry the raw partial sum only
-    const float4* b4 = reinterpret_cast<const float4*>(p.bias + n);
-    if constexpr (EPI == EPI_DQ_BIAS || EPI == EPI_DQ_BIAS_RESIDUAL || EPI == EPI_DQ_BIAS_GELU_Q) {
-      const float4* s4 = reinterpret_cast<const float4*>(p.w_scale + n);
-#pragma unroll
-      for (int j = 0; j < NV / 4; ++j) {
-        const float4 ss = __ldg(s4 + j);
-        v[4 * j + 0] *= a_s * ss.x;
-        v[4 * j + 1] *= a_s * ss.y;
-        v[4 * j + 2] *= a_s * ss.z;
-        v[4 * j + 3] *= a_s * ss.w;
-      }
-    }
+  if constexpr (EPI != EPI_DQ_ACC) {
     if (first) {
+      const float4* b4 = reinterpret_cast<const float4*>(p.bias + n);
 #pragma unroll
       for (int j = 0; j < NV / 4; ++j) {
         const float4 bb = __ldg(b4 + j);
@@ -143,19 +139,20 @@ __device__ __forceinline__ void epilogue_cols(const GemmParams& p, uint32_t t_ro
         v[4 * j + 3] += bb.w;
       }
     }
-    if constexpr (EPI == RPP_EPI_BIAS_GELU || EPI == EPI_DQ_BIAS_GELU_Q) {
+  }
+  if constexpr (EPI == RPP_EPI_BIAS_GELU || EPI == EPI_DQ_BIAS_GELU_Q) {
 #pragma unroll
-      for (int j = 0; j < NV; ++j) v[j] = gelu_erf(v[j]);
-    }
-    if constexpr (EPI == EPI_DQ_BIAS_GELU_Q) {
+    for (int j = 0; j < NV; ++j) v[j] = gelu_erf(v[j]);
+  }
+  if constexpr (EPI == EPI_DQ_BIAS_GELU_Q) {
 #pragma unroll
-      for (int j = 0; j < NV; ++j) v[j] = code_of(v[j], inv_q);
-    }
-    if constexpr (EPI == RPP_EPI_BIAS_RESIDUAL || EPI == EPI_DQ_BIAS_RESIDUAL) {
-      if (first) {
-      constexpr int RPV = Vec<TRes>::N;   // residual elements per 16-byte vector
-      const uint4* rr = reinterpret_cast<const uint4*>(static_cast<const TRes*>(p.residual) +
-                                                       static_cast<long long>(row) * p.N + n);
+    for (int j = 0; j < NV; ++j) v[j] = code_of(v[j], inv_q);
+  }
+  if constexpr (EPI == RPP_EPI_BIAS_RESIDUAL) {
+    if (first) {
+      constexpr int RPV = Vec<TRes>::N;
+      const uint4* rr =
+          reinterpret_cast<const uint4*>(static_cast<const TRes*>(p.residual) + static_cast<long long>(row) * p.N + n);
 #pragma unroll
       for (int j = 0; j < NV / RPV; ++j) {
         float f[RPV];
@@ -163,19 +160,97 @@ __device__ __forceinline__ void epilogue_cols(const GemmParams& p, uint32_t t_ro
 #pragma unroll
         for (int e = 0; e < RPV; ++e) v[RPV * j + e] += f[e];
       }
-      }
     }
-    constexpr int EPV = Vec<TOut>::N;   // output elements per 16-byte vector
-    uint4* orow = reinterpret_cast<uint4*>(static_cast<TOut*>(p.out) + split * p.split_stride +
-                                           static_cast<long long>(row) * p.N + n);
-#pragma unroll
-    for (int j = 0; j < NV / EPV; ++j) orow[j] = pack16<TOut>(v + EPV * j);
   }
+}
+
+// tensor memory -> registers: NV fp32 columns, or for int8 epilogues the exact sum of
+// the K-chunk partials (each an integer below 2^24)
+template <int EPI, int NCH, int ACC, int NV>
+__device__ __forceinline__ void load_acc(uint32_t base, int nch, float* v, int* acc) {
+  uint32_t r[NV];
+  if constexpr (NV == 32) tmem_ld_32x32b_x32(base, r); else tmem_ld_32x32b_x16(base, r);
+  tmem_ld_wait();
+  if constexpr (is_int_epi<EPI>()) {
+#pragma unroll
+    for (int j = 0; j < NV; ++j) acc[j] = __float2int_rn(__uint_as_float(r[j]));
+    for (int ch = 1; ch < nch; ++ch) {
+      if constexpr (NV == 32) tmem_ld_32x32b_x32(base + ch * ACC, r); else tmem_ld_32x32b_x16(base + ch * ACC, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < NV; ++j) acc[j] += __float2int_rn(__uint_as_float(r[j]));
+    }
+#pragma unroll
+    for (int j = 0; j < NV; ++j) v[j] = static_cast<float>(acc[j]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < NV; ++j) v[j] = __uint_as_float(r[j]);
+  }
+}
+
+// per-row 16-byte stores of NV columns (ragged tiles, tails, residual epilogue)
+template <typename TOut, int EPI, int NV>
+__device__ __forceinline__ void store_row(const GemmParams& p, const float* v, const int* acc, int row, int n,
+                                          int split) {
+  if constexpr (EPI == EPI_I32) {
+    int4* o = reinterpret_cast<int4*>(static_cast<int32_t*>(p.out) + static_cast<long long>(row) * p.N + n);
+#pragma unroll
+    for (int j = 0; j < NV / 4; ++j) o[j] = make_int4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+  } else {
+    constexpr int EPV = Vec<TOut>::N;
+    uint4* o = reinterpret_cast<uint4*>(static_cast<TOut*>(p.out) + split * p.split_stride +
+                                        static_cast<long long>(row) * p.N + n);
+#pragma unroll
+    for (int j = 0; j < NV / EPV; ++j) o[j] = pack16<TOut>(v + EPV * j);
+  }
+}
+
+// Write this thread's row (32 values) into the swizzled 32 x 32 staging block: rows of
+// 32 * sizeof(TOut) bytes; 16-byte chunk c of row r sits at chunk c ^ f(r), which is
+// the TMA 64-byte swizzle (2-byte types, 64-byte rows) or 128-byte swizzle (4-byte
+// types, 128-byte rows).  Eight consecutive lanes cover all 32 banks: no conflicts.
+template <typename TOut, int EPI>
+__device__ __forceinline__ void stage_row(uint8_t* stage, int r, const float* v, const int* acc) {
+  if constexpr (sizeof(TOut) == 2) {
+    const int x = (r >> 1) & 3;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      *reinterpret_cast<uint4*>(stage + r * 64 + ((c ^ x) << 4)) = pack16<TOut>(v + 8 * c);
+  } else {
+    const int x = r & 7;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint4 w;
+      if constexpr (EPI == EPI_I32)
+        w = make_uint4(static_cast<uint32_t>(acc[4 * c]), static_cast<uint32_t>(acc[4 * c + 1]),
+                       static_cast<uint32_t>(acc[4 * c + 2]), static_cast<uint32_t>(acc[4 * c + 3]));
+      else
+        w = pack16<float>(v + 4 * c);
+      *reinterpret_cast<uint4*>(stage + r * 128 + ((c ^ x) << 4)) = w;
+    }
+  }
+}
+
+constexpr size_t stage_bytes(int bn) { return kBM * kBK * 2 + ((bn * kBK * 2 + 1023) & ~1023); }
+constexpr size_t smem_bytes(int bn, int stages, size_t epi_total) {
+  return 1024 + stages * stage_bytes(bn) + epi_total + 256;
+}
+template <typename TOut, int EPI>
+constexpr size_t epi_stage_total() {
+  return tma_store_epi<EPI>() ? kEpiWarps * 32 * 32 * sizeof(TOut) : 0;
+}
+// pipeline depth: as many stages (<= 8) as fit next to the epilogue staging blocks
+template <typename TOut, int BN, int EPI>
+constexpr int stages_for() {
+  const size_t avail = kSmemLimit - 1024 - 256 - epi_stage_total<TOut, EPI>();
+  const size_t s = avail / stage_bytes(BN);
+  return s > 8 ? 8 : static_cast<int>(s);
 }
 
 template <typename TIn, typename TOut, typename TRes, int BN, int STAGES, int EPI, int NCH>
 __global__ void __launch_bounds__(kThreads, 1)
-gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const __grid_constant__ CUtensorMap tmC, GemmParams p) {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
   constexpr uint32_t A_BYTES = kBM * kBK * 2;
   constexpr uint32_t B_BYTES = BN * kBK * 2;
@@ -186,14 +261,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   static_assert(NCH * ACC <= 512, "tensor memory columns");
   constexpr uint32_t TMEM_COLS = pow2_cols(NBUF * NCH * ACC);
   constexpr uint32_t IDESC = idesc_f16(AbFmt<TIn>::v, kBM, BN);
-  constexpr bool kInt = EPI >= EPI_I32;
+  constexpr bool kTma = tma_store_epi<EPI>();
+  constexpr uint32_t EPI_STAGE = kTma ? 32 * 32 * sizeof(TOut) : 0;   // per epilogue warp
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled tiles
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES_AL);
+  uint8_t* sEpi = sB + STAGES * B_BYTES_AL;   // kEpiWarps staging blocks (1024-aligned)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + kEpiWarps * EPI_STAGE);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* tfull = bars + 2 * STAGES;
@@ -219,6 +296,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     fence_mbarrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if constexpr (kTma) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
@@ -327,10 +405,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int q = warp & 3;               // tensor-memory lane quadrant of this warp
     const int half = (warp - 2) >> 2;     // which of the two warps of this quadrant
     const int r_in_tile = q * 32 + lane;
+    uint8_t* stage = sEpi + (warp - 2) * EPI_STAGE;
     float a_s = 1.f, inv_q = 0.f;
-    if constexpr (EPI == EPI_DQ_BIAS || EPI == EPI_DQ_BIAS_RESIDUAL || EPI == EPI_DQ_BIAS_GELU_Q) a_s = *p.a_scale;
+    if constexpr (EPI == EPI_DQ_BIAS || EPI == EPI_DQ_ACC || EPI == EPI_DQ_BIAS_GELU_Q) a_s = *p.a_scale;
     if constexpr (EPI == EPI_DQ_BIAS_GELU_Q) inv_q = __fdiv_rn(1.0f, *p.q_scale);
     uint32_t acc_it = 0;
+    bool pending_store = false;
     for (int unit = blockIdx.x; unit < total; unit += gridDim.x, ++acc_it) {
       const int tile = unit / S;
       const int split = unit - tile * S;
@@ -354,19 +434,53 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int n0 = (tile % num_n) * BN;
       const int row = m0 + r_in_tile;
       const bool row_ok = row < M;
-      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      const bool full_tile = m0 + kBM <= M;
+      const bool first = split == 0;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + (a * NCH) * ACC;
       if constexpr (BN >= 32) {
 #pragma unroll 1
-        for (int c = half; c < BN / 32; c += 2)
-          epilogue_cols<TOut, TRes, EPI, NCH, ACC, 32>(p, t_row, a, c * 32, nch, row, row_ok, n0, a_s, inv_q, split);
+        for (int c = half; c < BN / 32; c += 2) {
+          float v[32];
+          int acc[32];
+          load_acc<EPI, NCH, ACC, 32>(t_row + c * 32, nch, v, acc);
+          const int n = n0 + c * 32;
+          if (kTma && full_tile) {
+            epi_math<TOut, TRes, EPI, 32>(p, v, row, n, first, a_s, inv_q);
+            if (pending_store) {   // the previous TMA store has finished reading the staging block
+              if (lane == 0) bulk_wait_read0();
+              __syncwarp();
+            }
+            stage_row<TOut, EPI>(stage, lane, v, acc);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmC, stage, n, split * p.M_max + m0 + q * 32);
+              bulk_commit();
+            }
+            pending_store = true;
+          } else if (row_ok) {
+            epi_math<TOut, TRes, EPI, 32>(p, v, row, n, first, a_s, inv_q);
+            store_row<TOut, EPI, 32>(p, v, acc, row, n, split);
+          }
+        }
       }
       if constexpr (BN % 32 == 16) {
-        if (half == ((BN / 32) & 1))
-          epilogue_cols<TOut, TRes, EPI, NCH, ACC, 16>(p, t_row, a, BN - 16, nch, row, row_ok, n0, a_s, inv_q, split);
+        if (half == ((BN / 32) & 1)) {
+          float v[16];
+          int acc[16];
+          load_acc<EPI, NCH, ACC, 16>(t_row + (BN - 16), nch, v, acc);
+          if (row_ok) {
+            const int n = n0 + BN - 16;
+            epi_math<TOut, TRes, EPI, 16>(p, v, row, n, first, a_s, inv_q);
+            store_row<TOut, EPI, 16>(p, v, acc, row, n, split);
+          }
+        }
       }
       tc_fence_before();
       mbar_arrive(&tempty[a]);
     }
+    if (pending_store && lane == 0) bulk_wait0();   // stores complete before the CTA exits
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -401,9 +515,9 @@ EncodeTiledFn get_encode_fn() {
 
 }  // namespace
 
-// 2D row-major [rows, cols] tensor of 2-byte (or 1-byte) elements, box = box_cols x box_rows
-bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, int rows, int cols,
-                  int box_rows, int box_cols, CUtensorMapSwizzle swz) {
+// 2D row-major [rows, cols] tensor, box = box_cols x box_rows
+bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, long long rows,
+                  int cols, int box_rows, int box_cols, CUtensorMapSwizzle swz) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -417,13 +531,28 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, in
 
 namespace {
 
-template <typename TIn, typename TOut, typename TRes, int BN, int STAGES, int EPI, int NCH>
+template <typename T> struct MapType;
+template <> struct MapType<__half> { static constexpr CUtensorMapDataType v = CU_TENSOR_MAP_DATA_TYPE_FLOAT16; };
+template <> struct MapType<__nv_bfloat16> { static constexpr CUtensorMapDataType v = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; };
+template <> struct MapType<float> { static constexpr CUtensorMapDataType v = CU_TENSOR_MAP_DATA_TYPE_FLOAT32; };
+template <> struct MapType<int32_t> { static constexpr CUtensorMapDataType v = CU_TENSOR_MAP_DATA_TYPE_INT32; };
+
+template <typename TIn, typename TOut, typename TRes, int BN, int EPI, int NCH>
 cudaError_t gemm_tc_launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int grid_rows,
                            cudaStream_t stream) {
-  constexpr uint32_t A_BYTES = kBM * kBK * 2;
-  constexpr uint32_t B_BYTES_AL = ((BN * kBK * 2) + 1023u) & ~1023u;
-  constexpr size_t SMEM = 1024 + STAGES * (A_BYTES + B_BYTES_AL) + 256;
-  static_assert(SMEM <= 232448, "shared memory per CTA");
+  constexpr int STAGES = stages_for<TOut, BN, EPI>();
+  static_assert(STAGES >= 2, "pipeline depth");
+  constexpr size_t SMEM = smem_bytes(BN, STAGES, epi_stage_total<TOut, EPI>());
+  static_assert(SMEM <= kSmemLimit, "shared memory per CTA");
+  CUtensorMap tc;
+  std::memset(&tc, 0, sizeof(tc));
+  if constexpr (tma_store_epi<EPI>()) {
+    // output as [splits * M_max, N]; 32 x 32 boxes, swizzle matching the staging rows
+    const CUtensorMapSwizzle swz = sizeof(TOut) == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+    if (!make_tmap_2d(&tc, p.out, MapType<TOut>::v, sizeof(TOut), static_cast<long long>(p.splits) * p.M_max, p.N,
+                      32, 32, swz))
+      return cudaErrorInvalidValue;
+  }
   auto kern = gemm_tc_kernel<TIn, TOut, TRes, BN, STAGES, EPI, NCH>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -435,7 +564,7 @@ cudaError_t gemm_tc_launch(const CUtensorMap& ta, const CUtensorMap& tb, const G
   const long long units = static_cast<long long>(num_m) * (p.N / BN) * p.splits;
   int grid = units < num_sms() ? static_cast<int>(units) : num_sms();
   if (grid < 1) grid = 1;
-  kern<<<grid, kThreads, SMEM, stream>>>(ta, tb, p);
+  kern<<<grid, kThreads, SMEM, stream>>>(ta, tb, tc, p);
   return cudaGetLastError();
 }
 
@@ -477,25 +606,25 @@ cudaError_t dispatch_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb, co
                         cudaStream_t stream) {
   if constexpr (NCH == 1) {
     switch (bn) {
-      case 256: return gemm_tc_launch<TIn, TOut, TRes, 256, 4, EPI, 1>(ta, tb, p, gr, stream);
-      case 192: return gemm_tc_launch<TIn, TOut, TRes, 192, 5, EPI, 1>(ta, tb, p, gr, stream);
-      case 144: return gemm_tc_launch<TIn, TOut, TRes, 144, 5, EPI, 1>(ta, tb, p, gr, stream);
-      case 128: return gemm_tc_launch<TIn, TOut, TRes, 128, 6, EPI, 1>(ta, tb, p, gr, stream);
-      case 96: return gemm_tc_launch<TIn, TOut, TRes, 96, 7, EPI, 1>(ta, tb, p, gr, stream);
-      case 64: return gemm_tc_launch<TIn, TOut, TRes, 64, 8, EPI, 1>(ta, tb, p, gr, stream);
-      case 48: return gemm_tc_launch<TIn, TOut, TRes, 48, 8, EPI, 1>(ta, tb, p, gr, stream);
-      case 32: return gemm_tc_launch<TIn, TOut, TRes, 32, 8, EPI, 1>(ta, tb, p, gr, stream);
-      case 16: return gemm_tc_launch<TIn, TOut, TRes, 16, 8, EPI, 1>(ta, tb, p, gr, stream);
+      case 256: return gemm_tc_launch<TIn, TOut, TRes, 256, EPI, 1>(ta, tb, p, gr, stream);
+      case 192: return gemm_tc_launch<TIn, TOut, TRes, 192, EPI, 1>(ta, tb, p, gr, stream);
+      case 144: return gemm_tc_launch<TIn, TOut, TRes, 144, EPI, 1>(ta, tb, p, gr, stream);
+      case 128: return gemm_tc_launch<TIn, TOut, TRes, 128, EPI, 1>(ta, tb, p, gr, stream);
+      case 96: return gemm_tc_launch<TIn, TOut, TRes, 96, EPI, 1>(ta, tb, p, gr, stream);
+      case 64: return gemm_tc_launch<TIn, TOut, TRes, 64, EPI, 1>(ta, tb, p, gr, stream);
+      case 48: return gemm_tc_launch<TIn, TOut, TRes, 48, EPI, 1>(ta, tb, p, gr, stream);
+      case 32: return gemm_tc_launch<TIn, TOut, TRes, 32, EPI, 1>(ta, tb, p, gr, stream);
+      case 16: return gemm_tc_launch<TIn, TOut, TRes, 16, EPI, 1>(ta, tb, p, gr, stream);
       default: return cudaErrorNotSupported;
     }
   } else {
     switch (bn) {   // NCH x BN <= 512 tensor-memory columns
-      case 128: return gemm_tc_launch<TIn, TOut, TRes, 128, 6, EPI, NCH>(ta, tb, p, gr, stream);
-      case 96: return gemm_tc_launch<TIn, TOut, TRes, 96, 7, EPI, NCH>(ta, tb, p, gr, stream);
-      case 64: return gemm_tc_launch<TIn, TOut, TRes, 64, 8, EPI, NCH>(ta, tb, p, gr, stream);
-      case 48: return gemm_tc_launch<TIn, TOut, TRes, 48, 8, EPI, NCH>(ta, tb, p, gr, stream);
-      case 32: return gemm_tc_launch<TIn, TOut, TRes, 32, 8, EPI, NCH>(ta, tb, p, gr, stream);
-      case 16: return gemm_tc_launch<TIn, TOut, TRes, 16, 8, EPI, NCH>(ta, tb, p, gr, stream);
+      case 128: return gemm_tc_launch<TIn, TOut, TRes, 128, EPI, NCH>(ta, tb, p, gr, stream);
+      case 96: return gemm_tc_launch<TIn, TOut, TRes, 96, EPI, NCH>(ta, tb, p, gr, stream);
+      case 64: return gemm_tc_launch<TIn, TOut, TRes, 64, EPI, NCH>(ta, tb, p, gr, stream);
+      case 48: return gemm_tc_launch<TIn, TOut, TRes, 48, EPI, NCH>(ta, tb, p, gr, stream);
+      case 32: return gemm_tc_launch<TIn, TOut, TRes, 32, EPI, NCH>(ta, tb, p, gr, stream);
+      case 16: return gemm_tc_launch<TIn, TOut, TRes, 16, EPI, NCH>(ta, tb, p, gr, stream);
       default: return cudaErrorNotSupported;
     }
   }
@@ -508,24 +637,23 @@ cudaError_t dispatch_float(int bn, int epi, rpp_dtype out_dtype, rpp_dtype res_d
     case RPP_EPI_BIAS: return dispatch_bn<T, T, T, RPP_EPI_BIAS, 1>(bn, ta, tb, p, gr, stream);
     case RPP_EPI_BIAS_GELU: return dispatch_bn<T, T, T, RPP_EPI_BIAS_GELU, 1>(bn, ta, tb, p, gr, stream);
     case RPP_EPI_BIAS_RESIDUAL:
-      // fp32 output: the pre-LayerNorm residual sum of the encoder layer stays in fp32
       if (out_dtype == RPP_F32 && res_dtype == RPP_F32)
         return dispatch_bn<T, float, float, RPP_EPI_BIAS_RESIDUAL, 1>(bn, ta, tb, p, gr, stream);
       if (out_dtype == RPP_F32) return dispatch_bn<T, float, T, RPP_EPI_BIAS_RESIDUAL, 1>(bn, ta, tb, p, gr, stream);
       return dispatch_bn<T, T, T, RPP_EPI_BIAS_RESIDUAL, 1>(bn, ta, tb, p, gr, stream);
+    case EPI_ACC: return dispatch_bn<T, float, T, EPI_ACC, 1>(bn, ta, tb, p, gr, stream);
     default: return cudaErrorNotSupported;
   }
 }
 
 template <int NCH>
-cudaError_t dispatch_int(int bn, int epi, rpp_dtype out_dtype, const CUtensorMap& ta, const CUtensorMap& tb,
-                         const GemmParams& p, int gr, cudaStream_t stream) {
+cudaError_t dispatch_int(int bn, int epi, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int gr,
+                         cudaStream_t stream) {
   using BF = __nv_bfloat16;
   switch (epi) {
     case EPI_I32: return dispatch_bn<BF, int32_t, BF, EPI_I32, NCH>(bn, ta, tb, p, gr, stream);
     case EPI_DQ_BIAS: return dispatch_bn<BF, __half, __half, EPI_DQ_BIAS, NCH>(bn, ta, tb, p, gr, stream);
-    case EPI_DQ_BIAS_RESIDUAL:   // fp32 pre-LayerNorm sum, fp16 residual
-      return dispatch_bn<BF, float, __half, EPI_DQ_BIAS_RESIDUAL, NCH>(bn, ta, tb, p, gr, stream);
+    case EPI_DQ_ACC: return dispatch_bn<BF, float, __half, EPI_DQ_ACC, NCH>(bn, ta, tb, p, gr, stream);
     case EPI_DQ_BIAS_GELU_Q: return dispatch_bn<BF, BF, BF, EPI_DQ_BIAS_GELU_Q, NCH>(bn, ta, tb, p, gr, stream);
     default: return cudaErrorNotSupported;
   }
@@ -538,13 +666,13 @@ bool gemm_tc_supported(int N, int K) {
 }
 
 cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t stream) {
-  const bool is_int = g.epi >= EPI_I32;
+  const bool is_int = g.epi >= EPI_I32 && g.epi <= EPI_DQ_BIAS_GELU_Q;
   const int num_k = (g.K + kBK - 1) / kBK;
   const int nch = is_int ? (num_k + kChunkBlocks - 1) / kChunkBlocks : 1;
   if (nch > 4) return cudaErrorNotSupported;
   const int max_bn = nch > 1 ? 128 : 256;
-  // splitting K is only possible for the fp32 partial-sum output of the residual epilogue
-  const bool can_split = g.max_splits > 1 && g.epi == RPP_EPI_BIAS_RESIDUAL && g.out_dtype == RPP_F32;
+  // splitting K is only possible for the raw fp32 accumulator output
+  const bool can_split = g.max_splits > 1 && g.epi == EPI_ACC;
   const int rows_hint = (g.rows_hint > 0 && g.rows_hint < g.M_max) ? g.rows_hint : g.M_max;
   TileChoice tc = choose_tiles(rows_hint, g.N, g.K, max_bn, can_split ? g.max_splits : 1);
   if (g.force_bn) tc.bn = g.force_bn;
@@ -559,8 +687,8 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t stream) {
   GemmParams p{g.M_max, g.rows, g.N, g.K, g.bias, g.residual, g.out, g.a_scale, g.w_scale, g.q_scale, g.err,
                tc.splits, static_cast<long long>(g.M_max) * g.N};
   if (is_int) {
-    if (nch == 1) return dispatch_int<1>(bn, g.epi, g.out_dtype, ta, tb, p, rows_hint, stream);
-    return dispatch_int<4>(bn, g.epi, g.out_dtype, ta, tb, p, rows_hint, stream);
+    if (nch == 1) return dispatch_int<1>(bn, g.epi, ta, tb, p, rows_hint, stream);
+    return dispatch_int<4>(bn, g.epi, ta, tb, p, rows_hint, stream);
   }
   if (g.in_dtype == RPP_BF16)
     return dispatch_float<__nv_bfloat16>(bn, g.epi, g.out_dtype, g.res_dtype, ta, tb, p, rows_hint, stream);

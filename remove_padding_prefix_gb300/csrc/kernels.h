@@ -12,8 +12,9 @@ int num_sms();   // SM count of the current device (cached per device)
 enum InternalEpilogue {
   EPI_I32 = 3,               // raw int32 accumulators
   EPI_DQ_BIAS = 4,           // acc * s_a * s_w[n] + b
-  EPI_DQ_BIAS_RESIDUAL = 5,  // acc * s_a * s_w[n] + b + residual
-  EPI_DQ_BIAS_GELU_Q = 6     // int8 code of GELU(acc * s_a * s_w[n] + b), held in a bf16 container
+  EPI_DQ_ACC = 5,            // acc * s_a * s_w[n] (fp32; bias and residual added by the next LayerNorm)
+  EPI_DQ_BIAS_GELU_Q = 6,    // int8 code of GELU(acc * s_a * s_w[n] + b), held in a bf16 container
+  EPI_ACC = 7                // raw fp32 accumulator (split-K slices; bias and residual added by LayerNorm)
 };
 
 cudaError_t launch_build_offsets(const int32_t* lengths, int B, int L, int32_t* cu, int32_t* po, int32_t* err,
@@ -30,8 +31,11 @@ bool layernorm_supported(int H, rpp_dtype dtype);
 cudaError_t launch_layernorm(const void* x, const float* gamma, const float* beta, void* y, int M_max,
                              const int32_t* rows, int H, float eps, rpp_dtype in_dtype, rpp_dtype out_dtype,
                              void* q_codes_bf16, const float* q_scale, float* amax, float* y32, int32_t* err,
-                             cudaStream_t stream, int n_in = 1, long long in_stride = 0);
-// (n_in > 1: x holds n_in fp32 slices in_stride elements apart whose sum is normalised)
+                             cudaStream_t stream, int n_in = 1, long long in_stride = 0,
+                             const float* add_bias = nullptr, const void* residual = nullptr,
+                             rpp_dtype res_dtype = RPP_F32);
+// (n_in > 1: x holds n_in fp32 slices in_stride elements apart; the row normalised is
+//  sum of slices + add_bias + residual, the last two optional)
 cudaError_t launch_quantize(const void* x, const float* scale, int8_t* q, int M_max, const int32_t* rows, int H,
                             rpp_dtype dtype, int32_t* err, cudaStream_t stream);
 cudaError_t launch_amax(const void* x, int M_max, const int32_t* rows, int H, rpp_dtype dtype, float* amax,

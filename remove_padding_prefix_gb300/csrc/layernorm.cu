@@ -22,6 +22,25 @@ __device__ __forceinline__ int8_t quantize_one(float v, float inv_s) {
   return static_cast<int8_t>(q);
 }
 
+// four residual values of a 16-bit or fp32 row segment (kind: 1 fp32, 2 fp16, 3 bf16)
+__device__ __forceinline__ void load_res4(const void* base, int kind, long long off, float* f) {
+  if (kind == 1) {
+    const float4 r = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
+    f[0] = r.x; f[1] = r.y; f[2] = r.z; f[3] = r.w;
+  } else {
+    const uint2 r = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + off);
+    if (kind == 2) {
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&r.x));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&r.y));
+      f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    } else {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.y));
+      f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    }
+  }
+}
+
 __device__ __forceinline__ void atomic_max_nonneg(float* addr, float v) {
   // non-negative floats order like their bit patterns
   atomicMax(reinterpret_cast<int*>(addr), __float_as_int(v));
@@ -54,7 +73,9 @@ __global__ void __launch_bounds__(256) layernorm_kernel(const T* __restrict__ x,
                                                         const int32_t* rows, int H, float eps,
                                                         __nv_bfloat16* __restrict__ q_out, const float* q_scale,
                                                         float* amax, float* __restrict__ y32, int n_in,
-                                                        long long in_stride, int32_t* err) {
+                                                        long long in_stride, const float* __restrict__ add_bias,
+                                                        const void* __restrict__ residual, int res_kind,
+                                                        int32_t* err) {
   if (device_error_set(err)) return;
   int M = rows ? *rows : M_max;
   if (M > M_max || M < 0) {
@@ -94,6 +115,30 @@ __global__ void __launch_bounds__(256) layernorm_kernel(const T* __restrict__ x,
         unpack16<T>(raw, f);
 #pragma unroll
         for (int j = 0; j < EPV; ++j) v[i][j] += f[j];
+      }
+    }
+    // the GEMM's bias and the residual branch, split off the GEMM and added here
+    if (add_bias) {
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const int col0 = (i * G + gl) * EPV;
+#pragma unroll
+        for (int j = 0; j < EPV; j += 4) {
+          const float4 b4 = *reinterpret_cast<const float4*>(add_bias + col0 + j);
+          v[i][j] += b4.x; v[i][j + 1] += b4.y; v[i][j + 2] += b4.z; v[i][j + 3] += b4.w;
+        }
+      }
+    }
+    if (residual && valid) {
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const long long off = static_cast<long long>(row) * H + (i * G + gl) * EPV;
+#pragma unroll
+        for (int j = 0; j < EPV; j += 4) {
+          float f[4];
+          load_res4(residual, res_kind, off + j, f);
+          v[i][j] += f[0]; v[i][j + 1] += f[1]; v[i][j + 2] += f[2]; v[i][j + 3] += f[3];
+        }
       }
     }
     float s = 0.f;
@@ -213,7 +258,8 @@ __global__ void amax_kernel(const T* __restrict__ x, int M_max, const int32_t* r
 template <typename T, typename TOut, int G, int VPL>
 cudaError_t ln_launch(const void* x, const float* gamma, const float* beta, void* y, int M_max, const int32_t* rows,
                       int H, float eps, __nv_bfloat16* q_out, const float* q_scale, float* amax, float* y32,
-                      int n_in, long long in_stride, int32_t* err, cudaStream_t stream) {
+                      int n_in, long long in_stride, const float* add_bias, const void* residual, int res_kind,
+                      int32_t* err, cudaStream_t stream) {
   const int threads = 256;
   const int rows_per_block = (threads / 32) * (32 / G);
   long long blocks = (static_cast<long long>(M_max) + rows_per_block - 1) / rows_per_block;
@@ -222,19 +268,20 @@ cudaError_t ln_launch(const void* x, const float* gamma, const float* beta, void
   if (blocks < 1) blocks = 1;
   layernorm_kernel<T, TOut, G, VPL><<<static_cast<int>(blocks), threads, 0, stream>>>(
       static_cast<const T*>(x), gamma, beta, static_cast<TOut*>(y), M_max, rows, H, eps, q_out, q_scale, amax, y32,
-      n_in, in_stride, err);
+      n_in, in_stride, add_bias, residual, res_kind, err);
   return cudaGetLastError();
 }
 
 template <typename T, typename TOut>
 cudaError_t ln_dispatch(const void* x, const float* gamma, const float* beta, void* y, int M_max, const int32_t* rows,
                         int H, float eps, __nv_bfloat16* q_out, const float* q_scale, float* amax, float* y32,
-                        int n_in, long long in_stride, int32_t* err, cudaStream_t stream) {
+                        int n_in, long long in_stride, const float* add_bias, const void* residual, int res_kind,
+                        int32_t* err, cudaStream_t stream) {
   const int V = H / Vec<T>::N;   // 16-byte vectors per row
 #define RPP_LN_CASE(G_, VPL_)                                                                                  \
   if (V == (G_) * (VPL_))                                                                                      \
     return ln_launch<T, TOut, G_, VPL_>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, y32, n_in, \
-                                        in_stride, err, stream);
+                                        in_stride, add_bias, residual, res_kind, err, stream);
   RPP_LN_CASE(32, 1) RPP_LN_CASE(32, 2) RPP_LN_CASE(32, 3) RPP_LN_CASE(32, 4)
   RPP_LN_CASE(32, 5) RPP_LN_CASE(32, 6) RPP_LN_CASE(32, 8) RPP_LN_CASE(32, 12) RPP_LN_CASE(32, 16)
   RPP_LN_CASE(16, 1) RPP_LN_CASE(16, 3) RPP_LN_CASE(8, 1) RPP_LN_CASE(8, 3) RPP_LN_CASE(8, 5)
@@ -261,22 +308,24 @@ bool layernorm_supported(int H, rpp_dtype dtype) {
 cudaError_t launch_layernorm(const void* x, const float* gamma, const float* beta, void* y, int M_max,
                              const int32_t* rows, int H, float eps, rpp_dtype in_dtype, rpp_dtype out_dtype,
                              void* q_codes, const float* q_scale, float* amax, float* y32, int32_t* err,
-                             cudaStream_t stream, int n_in, long long in_stride) {
+                             cudaStream_t stream, int n_in, long long in_stride, const float* add_bias,
+                             const void* residual, rpp_dtype res_dtype) {
   if (n_in > 1 && in_dtype != RPP_F32) return cudaErrorNotSupported;
+  const int res_kind = !residual ? 0 : (res_dtype == RPP_F32 ? 1 : (res_dtype == RPP_F16 ? 2 : 3));
   __nv_bfloat16* q_out = static_cast<__nv_bfloat16*>(q_codes);
   using BF = __nv_bfloat16;
   if (in_dtype == out_dtype) {
     switch (in_dtype) {
-      case RPP_F32: return ln_dispatch<float, float>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, y32, n_in, in_stride, err, stream);
-      case RPP_F16: return ln_dispatch<__half, __half>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, y32, n_in, in_stride, err, stream);
-      case RPP_BF16: return ln_dispatch<BF, BF>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, y32, n_in, in_stride, err, stream);
+      case RPP_F32: return ln_dispatch<float, float>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, y32, n_in, in_stride, add_bias, residual, res_kind, err, stream);
+      case RPP_F16: return ln_dispatch<__half, __half>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, y32, n_in, in_stride, add_bias, residual, res_kind, err, stream);
+      case RPP_BF16: return ln_dispatch<BF, BF>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, y32, n_in, in_stride, add_bias, residual, res_kind, err, stream);
       default: return cudaErrorNotSupported;
     }
   }
   if (in_dtype == RPP_F32 && out_dtype == RPP_F16)
-    return ln_dispatch<float, __half>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, y32, n_in, in_stride, err, stream);
+    return ln_dispatch<float, __half>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, y32, n_in, in_stride, add_bias, residual, res_kind, err, stream);
   if (in_dtype == RPP_F32 && out_dtype == RPP_BF16)
-    return ln_dispatch<float, BF>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, y32, n_in, in_stride, err, stream);
+    return ln_dispatch<float, BF>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, y32, n_in, in_stride, add_bias, residual, res_kind, err, stream);
   return cudaErrorNotSupported;
 }
 
