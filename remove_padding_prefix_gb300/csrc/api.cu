@@ -208,9 +208,16 @@ cudaError_t linear_i8(const void* a_codes, const void* w_codes, const float* bia
   return launch_gemm_tc(g, s);
 }
 
+// Padded output of the last layer: LN2 writes y straight into the padded [B*L, H]
+// layout with zero pad slots (the padding rebuild, fused into the last kernel).
+struct PaddedOut {
+  void* y = nullptr;
+  int L = 0;
+};
+
 rpp_status encoder_layer_run(const rpp_encoder_cfg* c, const void* layer, const float* act_scales, const void* x,
                              const int32_t* cu, int B, int T_max, int max_len, void* y, void* ws, size_t ws_bytes,
-                             float* amax, int32_t* err, cudaStream_t s) {
+                             float* amax, int32_t* err, cudaStream_t s, PaddedOut pad = PaddedOut{}) {
   rpp_status st = encoder_cfg_supported(c);
   if (st != RPP_OK) return st;
   if (!layer || !x || !cu || !y || !ws || B <= 0 || T_max <= 0 || max_len <= 0) return RPP_EINVAL;
@@ -241,6 +248,30 @@ rpp_status encoder_layer_run(const rpp_encoder_cfg* c, const void* layer, const 
   const float* g2 = at<float>(layer, P.g2);
   const float* be2 = at<float>(layer, P.be2);
 
+  // LayerNorm launches: LN(x_sum) with x_sum = slices of h + bias + residual
+  auto ln_args = [&](const float* gamma, const float* beta) {
+    LnArgs a{};
+    a.x = h;
+    a.in_dtype = hdt;
+    a.gamma = gamma;
+    a.beta = beta;
+    a.out_dtype = dt;
+    a.M_max = T_max;
+    a.rows = rows;
+    a.H = H;
+    a.eps = c->eps;
+    a.err = err;
+    return a;
+  };
+  auto final_ln = [&](LnArgs a) {   // LN2: optionally straight into the padded output
+    if (pad.y) {
+      a.y = pad.y;
+      a.pad_cu = cu;
+      a.pad_B = B;
+      a.pad_L = pad.L;
+    }
+    return a;
+  };
   if (!c->int8) {
     // proj / FC2 write raw fp32 accumulators (split-K slices); the LayerNorm after each
     // adds the slices, the GEMM's bias and the residual while it reads the row
@@ -253,32 +284,41 @@ rpp_status encoder_layer_run(const rpp_encoder_cfg* c, const void* layer, const 
                                      RPP_EPI_BIAS, err, s, RPP_I8, RPP_I8, hint));
     RPP_LAUNCH("attention", s, launch_attention_varlen(qkv, cu, B, T_max, max_len, nh, d, dt, attn, err, s));
     if (amax) RPP_LAUNCH("amax", s, launch_amax(attn, T_max, rows, H, dt, amax + 1, err, s));
+    LnArgs l1 = ln_args(g1, be1);
+    l1.y = x1;
+    l1.y32 = x1f;
+    l1.amax = amax ? amax + 2 : nullptr;
     if (tc) {
       RPP_LAUNCH("gemm_proj", s, linear(dt, attn, at<void>(layer, P.wo), nullptr, nullptr, h, T_max, rows, H, H,
                                         EPI_ACC, err, s, hdt, RPP_I8, hint, kMaxSplits, &sp_proj));
-      RPP_LAUNCH("layernorm1", s, launch_layernorm(h, g1, be1, x1, T_max, rows, H, c->eps, hdt, dt, nullptr, nullptr,
-                                                   amax ? amax + 2 : nullptr, x1f, err, s, sp_proj, hs, bo, x, dt));
+      l1.n_in = sp_proj;
+      l1.in_stride = hs;
+      l1.add_bias = bo;
+      l1.residual = x;
+      l1.res_dtype = dt;
     } else {
       RPP_LAUNCH("gemm_proj", s, linear(dt, attn, at<void>(layer, P.wo), bo, x, h, T_max, rows, H, H,
                                         RPP_EPI_BIAS_RESIDUAL, err, s));
-      RPP_LAUNCH("layernorm1", s, launch_layernorm(h, g1, be1, x1, T_max, rows, H, c->eps, hdt, dt, nullptr, nullptr,
-                                                   amax ? amax + 2 : nullptr, nullptr, err, s));
     }
+    RPP_LAUNCH("layernorm1", s, launch_layernorm(l1, s));
     RPP_LAUNCH("gemm_fc1", s, linear(dt, x1, at<void>(layer, P.w1), b1, nullptr, g, T_max, rows, F, H,
                                      RPP_EPI_BIAS_GELU, err, s, RPP_I8, RPP_I8, hint));
     if (amax) RPP_LAUNCH("amax", s, launch_amax(g, T_max, rows, F, dt, amax + 3, err, s));
+    LnArgs l2 = ln_args(g2, be2);
+    l2.y = y;
     if (tc) {
       RPP_LAUNCH("gemm_fc2", s, linear(dt, g, at<void>(layer, P.w2), nullptr, nullptr, h, T_max, rows, H, F, EPI_ACC,
                                        err, s, hdt, RPP_I8, hint, kMaxSplits, &sp_fc2));
-      RPP_LAUNCH("layernorm2", s, launch_layernorm(h, g2, be2, y, T_max, rows, H, c->eps, hdt, dt, nullptr, nullptr,
-                                                   nullptr, nullptr, err, s, sp_fc2, hs, b2,
-                                                   x1f ? static_cast<const void*>(x1f) : x1, x1f ? RPP_F32 : dt));
+      l2.n_in = sp_fc2;
+      l2.in_stride = hs;
+      l2.add_bias = b2;
+      l2.residual = x1f ? static_cast<const void*>(x1f) : x1;
+      l2.res_dtype = x1f ? RPP_F32 : dt;
     } else {
       RPP_LAUNCH("gemm_fc2", s, linear(dt, g, at<void>(layer, P.w2), b2, x1, h, T_max, rows, H, F,
                                        RPP_EPI_BIAS_RESIDUAL, err, s));
-      RPP_LAUNCH("layernorm2", s, launch_layernorm(h, g2, be2, y, T_max, rows, H, c->eps, hdt, dt, nullptr, nullptr,
-                                                   nullptr, nullptr, err, s));
     }
+    RPP_LAUNCH(pad.y ? "layernorm2_rebuild" : "layernorm2", s, launch_layernorm(final_ln(l2), s));
     return RPP_OK;
   }
   // int8: quantise -> int8 GEMM (exact integer accumulation) -> dequantise in the epilogue
@@ -297,14 +337,24 @@ rpp_status encoder_layer_run(const rpp_encoder_cfg* c, const void* layer, const 
   RPP_LAUNCH("quantize_attn", s, launch_quantize_codes_bf16(attn, s1, ca, T_max, rows, H, dt, err, s));
   RPP_LAUNCH("gemm_proj_i8", s, linear_i8(ca, at<void>(layer, P.wo), nullptr, s1, at<float>(layer, P.so), nullptr,
                                            nullptr, h, RPP_F32, T_max, rows, H, H, EPI_DQ_ACC, err, s, hint));
-  RPP_LAUNCH("layernorm1", s, launch_layernorm(h, g1, be1, x1, T_max, rows, H, c->eps, hdt, dt, cx1, s2, nullptr,
-                                               nullptr, err, s, 1, hs, bo, x, dt));
+  LnArgs l1 = ln_args(g1, be1);
+  l1.add_bias = bo;
+  l1.residual = x;
+  l1.res_dtype = dt;
+  l1.y = x1;
+  l1.q_codes = cx1;
+  l1.q_scale = s2;
+  RPP_LAUNCH("layernorm1", s, launch_layernorm(l1, s));
   RPP_LAUNCH("gemm_fc1_i8", s, linear_i8(cx1, at<void>(layer, P.w1), b1, s2, at<float>(layer, P.s1), s3, nullptr, cg,
                                           RPP_BF16, T_max, rows, F, H, EPI_DQ_BIAS_GELU_Q, err, s, hint));
   RPP_LAUNCH("gemm_fc2_i8", s, linear_i8(cg, at<void>(layer, P.w2), nullptr, s3, at<float>(layer, P.s2), nullptr,
                                           nullptr, h, RPP_F32, T_max, rows, H, F, EPI_DQ_ACC, err, s, hint));
-  RPP_LAUNCH("layernorm2", s, launch_layernorm(h, g2, be2, y, T_max, rows, H, c->eps, hdt, dt, nullptr, nullptr,
-                                               nullptr, nullptr, err, s, 1, hs, b2, x1, dt));
+  LnArgs l2 = ln_args(g2, be2);
+  l2.add_bias = b2;
+  l2.residual = x1;
+  l2.res_dtype = dt;
+  l2.y = y;
+  RPP_LAUNCH(pad.y ? "layernorm2_rebuild" : "layernorm2", s, launch_layernorm(final_ln(l2), s));
   return RPP_OK;
 }
 
@@ -469,8 +519,19 @@ rpp_status rpp_layernorm(const void* x, const float* gamma, const float* beta, v
   if (!aligned16(x) || !aligned16(y) || !aligned16(gamma) || !aligned16(beta)) return RPP_EINVAL;
   if (dtype != RPP_F32 && dtype != RPP_F16 && dtype != RPP_BF16) return RPP_EUNSUPPORTED;
   if (!layernorm_supported(H, dtype)) return RPP_EUNSUPPORTED;
-  return from_cuda(launch_layernorm(x, gamma, beta, y, M_max, rows, H, eps, dtype, dtype, nullptr, nullptr, nullptr,
-                                    nullptr, err, static_cast<cudaStream_t>(stream)));
+  LnArgs a{};
+  a.x = x;
+  a.in_dtype = dtype;
+  a.gamma = gamma;
+  a.beta = beta;
+  a.y = y;
+  a.out_dtype = dtype;
+  a.M_max = M_max;
+  a.rows = rows;
+  a.H = H;
+  a.eps = eps;
+  a.err = err;
+  return from_cuda(launch_layernorm(a, static_cast<cudaStream_t>(stream)));
 }
 
 rpp_status rpp_attention_varlen(const void* qkv, const int32_t* cu_seqlens, int B, int T_max, int max_len, int nh,
@@ -577,16 +638,28 @@ rpp_status rpp_encoder_forward(const rpp_encoder_cfg* cfg, const void* const* la
   const int H = cfg->hidden;
   const int T_max = B * L;
   if (workspace_bytes < enc_ws_layout(cfg, T_max).total) return RPP_EWORKSPACE;
-  st = rpp_build_offsets(lengths, B, L, cu_seqlens, padding_offset, err, stream);
-  if (st != RPP_OK) return st;
-  st = rpp_remove_padding(x_padded, padding_offset, cu_seqlens, B, L, H, dt, packed, err, stream);
-  if (st != RPP_OK) return st;
-  for (int i = 0; i < num_layers; ++i) {
-    st = encoder_layer_run(cfg, layers[i], cfg->int8 ? act_scales[i] : nullptr, packed, cu_seqlens, B, T_max, L,
-                           packed, workspace, workspace_bytes, nullptr, err, static_cast<cudaStream_t>(stream));
+  if (offsets_remove_fusable(B) && aligned16(x_padded) && aligned16(packed) && (H * esize(dt)) % 16 == 0 &&
+      static_cast<long long>(B) * L <= 0x7fffffffLL) {
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    RPP_LAUNCH("offsets_remove", cs, launch_offsets_remove(lengths, B, L, H * esize(dt), x_padded, cu_seqlens,
+                                                           padding_offset, packed, err, cs));
+  } else {
+    st = rpp_build_offsets(lengths, B, L, cu_seqlens, padding_offset, err, stream);
+    if (st != RPP_OK) return st;
+    st = rpp_remove_padding(x_padded, padding_offset, cu_seqlens, B, L, H, dt, packed, err, stream);
     if (st != RPP_OK) return st;
   }
-  return rpp_rebuild_padding(packed, cu_seqlens, B, L, H, dt, y_padded, err, stream);
+  // the last layer's LN2 writes the padded output directly (rebuild fused)
+  PaddedOut pad;
+  pad.y = y_padded;
+  pad.L = L;
+  for (int i = 0; i < num_layers; ++i) {
+    st = encoder_layer_run(cfg, layers[i], cfg->int8 ? act_scales[i] : nullptr, packed, cu_seqlens, B, T_max, L,
+                           packed, workspace, workspace_bytes, nullptr, err, static_cast<cudaStream_t>(stream),
+                           i + 1 == num_layers ? pad : PaddedOut{});
+    if (st != RPP_OK) return st;
+  }
+  return RPP_OK;
 }
 
 rpp_status rpp_quantize_weight(const void* w, int K, int N, rpp_dtype dtype, int8_t* wq_t, float* s_w,
@@ -700,16 +773,29 @@ rpp_status rpp_swin_block_forward(const rpp_swin_cfg* cfg, const void* block, in
   void* attn = at<void>(workspace, W.attn);
   void* xa = at<void>(workspace, W.xa);
   void* g = at<void>(workspace, W.g);
-  RPP_LAUNCH("layernorm1", s, launch_layernorm(x, at<float>(block, P.g1), at<float>(block, P.be1), h, T, nullptr, C, cfg->eps, dt, dt,
-                           nullptr, nullptr, nullptr, nullptr, err, s));
+  LnArgs l1{};
+  l1.x = x;
+  l1.in_dtype = dt;
+  l1.gamma = at<float>(block, P.g1);
+  l1.beta = at<float>(block, P.be1);
+  l1.y = h;
+  l1.out_dtype = dt;
+  l1.M_max = T;
+  l1.H = C;
+  l1.eps = cfg->eps;
+  l1.err = err;
+  RPP_LAUNCH("layernorm1", s, launch_layernorm(l1, s));
   RPP_LAUNCH("gemm_qkv", s, linear(dt, h, at<void>(block, P.wqkv), at<float>(block, P.bqkv), nullptr, qkv, T, nullptr, 3 * C, C,
                  RPP_EPI_BIAS, err, s));
   RPP_LAUNCH("window_attention", s, launch_window_attention(B, qkv, at<float>(block, P.bias), attn, C, cfg->heads, cfg->img, cfg->window,
                                   cfg->shift, dt, err, s));
   RPP_LAUNCH("gemm_proj", s, linear(dt, attn, at<void>(block, P.wo), at<float>(block, P.bo), x, xa, T, nullptr, C, C,
                  RPP_EPI_BIAS_RESIDUAL, err, s));
-  RPP_LAUNCH("layernorm2", s, launch_layernorm(xa, at<float>(block, P.g2), at<float>(block, P.be2), h, T, nullptr, C, cfg->eps, dt, dt,
-                           nullptr, nullptr, nullptr, nullptr, err, s));
+  LnArgs l2 = l1;
+  l2.x = xa;
+  l2.gamma = at<float>(block, P.g2);
+  l2.beta = at<float>(block, P.be2);
+  RPP_LAUNCH("layernorm2", s, launch_layernorm(l2, s));
   RPP_LAUNCH("gemm_fc1", s, linear(dt, h, at<void>(block, P.w1), at<float>(block, P.b1), nullptr, g, T, nullptr, F, C, RPP_EPI_BIAS_GELU,
                  err, s));
   RPP_LAUNCH("gemm_fc2", s, linear(dt, g, at<void>(block, P.w2), at<float>(block, P.b2), xa, y, T, nullptr, C, F, RPP_EPI_BIAS_RESIDUAL,

@@ -21,21 +21,46 @@ cudaError_t launch_build_offsets(const int32_t* lengths, int B, int L, int32_t* 
                                  cudaStream_t stream);
 cudaError_t launch_remove_padding(const void* padded, const int32_t* po, const int32_t* cu, int B, int L,
                                   int row_bytes, void* packed, int32_t* err, cudaStream_t stream);
+bool offsets_remove_fusable(int B);
+// offset builder + padding removal in one launch (B <= 1024)
+cudaError_t launch_offsets_remove(const int32_t* lengths, int B, int L, int row_bytes, const void* padded,
+                                  int32_t* cu, int32_t* po, void* packed, int32_t* err, cudaStream_t stream);
 cudaError_t launch_rebuild_padding(const void* packed, const int32_t* cu, int B, int L, int row_bytes, void* padded,
                                    int32_t* err, cudaStream_t stream);
 
 bool layernorm_supported(int H, rpp_dtype dtype);
-// x of in_dtype, y of out_dtype (equal, or fp32 in -> fp16 / bf16 out for the layer's
-// fp32 pre-LayerNorm sums); optional bf16-held int8 codes of y, running max-abs and an
-// fp32 copy of y
-cudaError_t launch_layernorm(const void* x, const float* gamma, const float* beta, void* y, int M_max,
-                             const int32_t* rows, int H, float eps, rpp_dtype in_dtype, rpp_dtype out_dtype,
-                             void* q_codes_bf16, const float* q_scale, float* amax, float* y32, int32_t* err,
-                             cudaStream_t stream, int n_in = 1, long long in_stride = 0,
-                             const float* add_bias = nullptr, const void* residual = nullptr,
-                             rpp_dtype res_dtype = RPP_F32);
-// (n_in > 1: x holds n_in fp32 slices in_stride elements apart; the row normalised is
-//  sum of slices + add_bias + residual, the last two optional)
+// Row LayerNorm over H columns of [rows, H]; the row normalised is x (or the sum of
+// n_in fp32 split-K slices) + add_bias + residual, the last two optional.  Outputs: y
+// (out_dtype), optional fp32 copy, optional bf16-held int8 codes, optional running
+// max-abs.  With pad_cu set, the grid walks the padded [pad_B, pad_L] slots and writes
+// y at padded rows, zeros in pad slots (the padding rebuild, fused).
+struct LnArgs {
+  const void* x = nullptr;
+  rpp_dtype in_dtype = RPP_F32;
+  int n_in = 1;
+  long long in_stride = 0;
+  const float* add_bias = nullptr;
+  const void* residual = nullptr;
+  rpp_dtype res_dtype = RPP_F32;
+  int res_kind = 0;            // set by launch_layernorm
+  const float* gamma = nullptr;
+  const float* beta = nullptr;
+  void* y = nullptr;
+  rpp_dtype out_dtype = RPP_F32;
+  float* y32 = nullptr;
+  void* q_codes = nullptr;
+  const float* q_scale = nullptr;
+  float* amax = nullptr;
+  int M_max = 0;
+  const int32_t* rows = nullptr;
+  int H = 0;
+  float eps = 0.f;
+  const int32_t* pad_cu = nullptr;
+  int pad_B = 0;
+  int pad_L = 0;
+  int32_t* err = nullptr;
+};
+cudaError_t launch_layernorm(const LnArgs& a, cudaStream_t stream);
 cudaError_t launch_quantize(const void* x, const float* scale, int8_t* q, int M_max, const int32_t* rows, int H,
                             rpp_dtype dtype, int32_t* err, cudaStream_t stream);
 cudaError_t launch_amax(const void* x, int M_max, const int32_t* rows, int H, rpp_dtype dtype, float* amax,

@@ -22,25 +22,6 @@ __device__ __forceinline__ int8_t quantize_one(float v, float inv_s) {
   return static_cast<int8_t>(q);
 }
 
-// four residual values of a 16-bit or fp32 row segment (kind: 1 fp32, 2 fp16, 3 bf16)
-__device__ __forceinline__ void load_res4(const void* base, int kind, long long off, float* f) {
-  if (kind == 1) {
-    const float4 r = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
-    f[0] = r.x; f[1] = r.y; f[2] = r.z; f[3] = r.w;
-  } else {
-    const uint2 r = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + off);
-    if (kind == 2) {
-      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&r.x));
-      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&r.y));
-      f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-    } else {
-      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.x));
-      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.y));
-      f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-    }
-  }
-}
-
 __device__ __forceinline__ void atomic_max_nonneg(float* addr, float v) {
   // non-negative floats order like their bit patterns
   atomicMax(reinterpret_cast<int*>(addr), __float_as_int(v));
@@ -67,88 +48,143 @@ __device__ __forceinline__ void store_vec(TOut* p, const float* o) {
   }
 }
 
+// One row (group of G lanes) per iteration.  All of the row's global loads -- the
+// input (and the split-K slices), the residual -- are issued before any arithmetic,
+// so a row costs one memory round trip; gamma, beta and the GEMM bias live in shared
+// memory, loaded once per CTA.  In padded-output mode the grid walks the padded
+// [B, L] slots: a valid slot normalises its packed row and writes it in place, a pad
+// slot is written as zeros (the padding rebuild of the last layer, fused).
 template <typename T, typename TOut, int G, int VPL>
-__global__ void __launch_bounds__(256) layernorm_kernel(const T* __restrict__ x, const float* __restrict__ gamma,
-                                                        const float* __restrict__ beta, TOut* y, int M_max,
-                                                        const int32_t* rows, int H, float eps,
-                                                        __nv_bfloat16* __restrict__ q_out, const float* q_scale,
-                                                        float* amax, float* __restrict__ y32, int n_in,
-                                                        long long in_stride, const float* __restrict__ add_bias,
-                                                        const void* __restrict__ residual, int res_kind,
-                                                        int32_t* err) {
-  if (device_error_set(err)) return;
-  int M = rows ? *rows : M_max;
-  if (M > M_max || M < 0) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) set_device_error(err, RPP_DERR_ROWS);
+__global__ void __launch_bounds__(128) layernorm_kernel(LnArgs a) {
+  if (device_error_set(a.err)) return;
+  const int H = a.H;
+  int M = a.rows ? *a.rows : a.M_max;
+  if (M > a.M_max || M < 0) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) set_device_error(a.err, RPP_DERR_ROWS);
     return;
   }
+  extern __shared__ float ln_smem[];
+  float* s_gamma = ln_smem;
+  float* s_beta = ln_smem + H;
+  float* s_bias = ln_smem + 2 * H;
+  for (int i = threadIdx.x; i < H; i += blockDim.x) {
+    s_gamma[i] = a.gamma[i];
+    s_beta[i] = a.beta[i];
+    if (a.add_bias) s_bias[i] = a.add_bias[i];
+  }
+  __syncthreads();
+
   constexpr int EPV = Vec<T>::N;
   constexpr int GPW = 32 / G;   // groups (rows) per warp
+  const T* x = static_cast<const T*>(a.x);
+  TOut* y = static_cast<TOut*>(a.y);
   const int lane = lane_id();
   const int gl = lane % G;      // lane inside the group
   const int gw = lane / G;      // group inside the warp
   const int warps_total = gridDim.x * (blockDim.x >> 5);
   const int wglob = blockIdx.x * (blockDim.x >> 5) + warp_id();
+  const bool padded = a.pad_cu != nullptr;
+  const long long n_iter = padded ? static_cast<long long>(a.pad_B) * a.pad_L : M;
   float inv_s = 0.f;
-  if (q_out) inv_s = __fdiv_rn(1.0f, *q_scale);
+  if (a.q_codes) inv_s = __fdiv_rn(1.0f, *a.q_scale);
   float local_amax = 0.f;
 
-  for (int row0 = wglob * GPW; row0 < M; row0 += warps_total * GPW) {
-    const int row = row0 + gw;
-    const bool valid = row < M;
-    float v[VPL][EPV];
-    const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<long long>(valid ? row : 0) * H);
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-      if (valid) raw = xr[i * G + gl];
-      unpack16<T>(raw, v[i]);
+  for (long long it0 = static_cast<long long>(wglob) * GPW; it0 < n_iter;
+       it0 += static_cast<long long>(warps_total) * GPW) {
+    const long long it = it0 + gw;
+    int src = -1;              // packed row normalised by this group (-1: none)
+    long long dst = -1;        // output row
+    if (it < n_iter) {
+      if (padded) {
+        const int b = static_cast<int>(it / a.pad_L);
+        const int p = static_cast<int>(it - static_cast<long long>(b) * a.pad_L);
+        const int c0 = a.pad_cu[b];
+        if (p < a.pad_cu[b + 1] - c0) src = c0 + p;
+        dst = it;
+      } else {
+        src = static_cast<int>(it);
+        dst = it;
+      }
     }
-    // split-K partial sums of the preceding GEMM: add the other slices of this row
-    for (int sl = 1; sl < n_in; ++sl) {
-      const uint4* xs = reinterpret_cast<const uint4*>(x + sl * in_stride + static_cast<long long>(valid ? row : 0) * H);
+    const bool valid = src >= 0;
+    // ---- loads: input, residual (issued together)
+    uint4 rx[VPL];
+    uint4 rr[VPL][EPV / 4];
+    const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<long long>(valid ? src : 0) * H);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) rx[i] = valid ? xr[i * G + gl] : make_uint4(0u, 0u, 0u, 0u);
+    const bool has_res = a.residual != nullptr && valid;
+    if (has_res) {
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+#pragma unroll
+        for (int j = 0; j < EPV / 4; ++j) {
+          const long long off = static_cast<long long>(src) * H + (i * G + gl) * EPV + 4 * j;
+          if (a.res_kind == 1) {
+            rr[i][j] = *reinterpret_cast<const uint4*>(static_cast<const float*>(a.residual) + off);
+          } else {
+            const uint2 t = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.residual) + off);
+            rr[i][j] = make_uint4(t.x, t.y, 0u, 0u);
+          }
+        }
+      }
+    }
+    float v[VPL][EPV];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) unpack16<T>(rx[i], v[i]);
+    // split-K partial sums of the preceding GEMM: the other slices of this row
+    for (int sl = 1; sl < a.n_in; ++sl) {
+      const uint4* xs =
+          reinterpret_cast<const uint4*>(x + sl * a.in_stride + static_cast<long long>(valid ? src : 0) * H);
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
         float f[EPV];
-        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-        if (valid) raw = xs[i * G + gl];
-        unpack16<T>(raw, f);
+        unpack16<T>(valid ? xs[i * G + gl] : make_uint4(0u, 0u, 0u, 0u), f);
 #pragma unroll
         for (int j = 0; j < EPV; ++j) v[i][j] += f[j];
       }
     }
     // the GEMM's bias and the residual branch, split off the GEMM and added here
-    if (add_bias) {
+    if (a.add_bias) {
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
         const int col0 = (i * G + gl) * EPV;
 #pragma unroll
-        for (int j = 0; j < EPV; j += 4) {
-          const float4 b4 = *reinterpret_cast<const float4*>(add_bias + col0 + j);
-          v[i][j] += b4.x; v[i][j + 1] += b4.y; v[i][j + 2] += b4.z; v[i][j + 3] += b4.w;
-        }
+        for (int j = 0; j < EPV; ++j) v[i][j] += s_bias[col0 + j];
       }
     }
-    if (residual && valid) {
+    if (has_res) {
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
-        const long long off = static_cast<long long>(row) * H + (i * G + gl) * EPV;
 #pragma unroll
-        for (int j = 0; j < EPV; j += 4) {
+        for (int j = 0; j < EPV / 4; ++j) {
           float f[4];
-          load_res4(residual, res_kind, off + j, f);
-          v[i][j] += f[0]; v[i][j + 1] += f[1]; v[i][j + 2] += f[2]; v[i][j + 3] += f[3];
+          const uint4 t = rr[i][j];
+          if (a.res_kind == 1) {
+            f[0] = __uint_as_float(t.x); f[1] = __uint_as_float(t.y);
+            f[2] = __uint_as_float(t.z); f[3] = __uint_as_float(t.w);
+          } else if (a.res_kind == 2) {
+            const float2 p0 = __half22float2(*reinterpret_cast<const __half2*>(&t.x));
+            const float2 p1 = __half22float2(*reinterpret_cast<const __half2*>(&t.y));
+            f[0] = p0.x; f[1] = p0.y; f[2] = p1.x; f[3] = p1.y;
+          } else {
+            const float2 p0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&t.x));
+            const float2 p1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&t.y));
+            f[0] = p0.x; f[1] = p0.y; f[2] = p1.x; f[3] = p1.y;
+          }
+          v[i][4 * j + 0] += f[0]; v[i][4 * j + 1] += f[1]; v[i][4 * j + 2] += f[2]; v[i][4 * j + 3] += f[3];
         }
       }
     }
-    float s = 0.f;
+    // ---- statistics (biased variance, two passes over the registers)
+    float sum = 0.f;
 #pragma unroll
     for (int i = 0; i < VPL; ++i)
 #pragma unroll
-      for (int j = 0; j < EPV; ++j) s += v[i][j];
+      for (int j = 0; j < EPV; ++j) sum += v[i][j];
 #pragma unroll
-    for (int o = G / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    const float mean = s / static_cast<float>(H);
+    for (int o = G / 2; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float mean = sum / static_cast<float>(H);
     float ss = 0.f;
 #pragma unroll
     for (int i = 0; i < VPL; ++i)
@@ -159,45 +195,44 @@ __global__ void __launch_bounds__(256) layernorm_kernel(const T* __restrict__ x,
       }
 #pragma unroll
     for (int o = G / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float rstd = rsqrtf(ss / static_cast<float>(H) + eps);
-    if (valid) {
-      TOut* yr = y + static_cast<long long>(row) * H;
+    const float rstd = rsqrtf(ss / static_cast<float>(H) + a.eps);
+    if (dst < 0) continue;
+    TOut* yr = y + dst * H;
 #pragma unroll
-      for (int i = 0; i < VPL; ++i) {
-        const int col0 = (i * G + gl) * EPV;
-        float o[EPV];
+    for (int i = 0; i < VPL; ++i) {
+      const int col0 = (i * G + gl) * EPV;
+      float o[EPV];
+      if (valid) {
 #pragma unroll
-        for (int j = 0; j < EPV; j += 4) {
-          const float4 g4 = *reinterpret_cast<const float4*>(gamma + col0 + j);
-          const float4 b4 = *reinterpret_cast<const float4*>(beta + col0 + j);
-          o[j + 0] = (v[i][j + 0] - mean) * rstd * g4.x + b4.x;
-          o[j + 1] = (v[i][j + 1] - mean) * rstd * g4.y + b4.y;
-          o[j + 2] = (v[i][j + 2] - mean) * rstd * g4.z + b4.z;
-          o[j + 3] = (v[i][j + 3] - mean) * rstd * g4.w + b4.w;
-        }
-        store_vec<TOut, EPV>(yr + col0, o);
-        if (y32) {   // fp32 copy of the normalised row (the next residual add reads it)
-          float* yf = y32 + static_cast<long long>(row) * H + col0;
+        for (int j = 0; j < EPV; ++j) o[j] = (v[i][j] - mean) * rstd * s_gamma[col0 + j] + s_beta[col0 + j];
+      } else {
 #pragma unroll
-          for (int j = 0; j < EPV; j += 4) *reinterpret_cast<float4*>(yf + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
-        }
-        if (q_out) {   // int8 codes of the normalised row, held in bf16 (exact)
-          float qv[EPV];
+        for (int j = 0; j < EPV; ++j) o[j] = 0.f;   // pad slot of the padded output
+      }
+      store_vec<TOut, EPV>(yr + col0, o);
+      if (!valid) continue;
+      if (a.y32) {   // fp32 copy of the normalised row (the next residual add reads it)
+        float* yf = a.y32 + dst * H + col0;
 #pragma unroll
-          for (int j = 0; j < EPV; ++j) qv[j] = static_cast<float>(quantize_one(o[j], inv_s));
-          store_vec<__nv_bfloat16, EPV>(q_out + static_cast<long long>(row) * H + col0, qv);
-        }
-        if (amax) {
+        for (int j = 0; j < EPV; j += 4)
+          *reinterpret_cast<float4*>(yf + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+      }
+      if (a.q_codes) {   // int8 codes of the normalised row, held in bf16 (exact)
+        float qv[EPV];
 #pragma unroll
-          for (int j = 0; j < EPV; ++j) local_amax = fmaxf(local_amax, fabsf(o[j]));
-        }
+        for (int j = 0; j < EPV; ++j) qv[j] = static_cast<float>(quantize_one(o[j], inv_s));
+        store_vec<__nv_bfloat16, EPV>(static_cast<__nv_bfloat16*>(a.q_codes) + dst * H + col0, qv);
+      }
+      if (a.amax) {
+#pragma unroll
+        for (int j = 0; j < EPV; ++j) local_amax = fmaxf(local_amax, fabsf(o[j]));
       }
     }
   }
-  if (amax) {
+  if (a.amax) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) local_amax = fmaxf(local_amax, __shfl_xor_sync(0xffffffffu, local_amax, o));
-    if (lane == 0) atomic_max_nonneg(amax, local_amax);
+    if (lane == 0) atomic_max_nonneg(a.amax, local_amax);
   }
 }
 
@@ -256,32 +291,24 @@ __global__ void amax_kernel(const T* __restrict__ x, int M_max, const int32_t* r
 }
 
 template <typename T, typename TOut, int G, int VPL>
-cudaError_t ln_launch(const void* x, const float* gamma, const float* beta, void* y, int M_max, const int32_t* rows,
-                      int H, float eps, __nv_bfloat16* q_out, const float* q_scale, float* amax, float* y32,
-                      int n_in, long long in_stride, const float* add_bias, const void* residual, int res_kind,
-                      int32_t* err, cudaStream_t stream) {
-  const int threads = 256;
+cudaError_t ln_launch(const LnArgs& a, cudaStream_t stream) {
+  const int threads = 128;
   const int rows_per_block = (threads / 32) * (32 / G);
-  long long blocks = (static_cast<long long>(M_max) + rows_per_block - 1) / rows_per_block;
-  const long long cap = static_cast<long long>(num_sms()) * 8;
+  const long long n_iter = a.pad_cu ? static_cast<long long>(a.pad_B) * a.pad_L : a.M_max;
+  long long blocks = (n_iter + rows_per_block - 1) / rows_per_block;
+  const long long cap = static_cast<long long>(num_sms()) * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  layernorm_kernel<T, TOut, G, VPL><<<static_cast<int>(blocks), threads, 0, stream>>>(
-      static_cast<const T*>(x), gamma, beta, static_cast<TOut*>(y), M_max, rows, H, eps, q_out, q_scale, amax, y32,
-      n_in, in_stride, add_bias, residual, res_kind, err);
+  const size_t smem = 3 * static_cast<size_t>(a.H) * sizeof(float);
+  layernorm_kernel<T, TOut, G, VPL><<<static_cast<int>(blocks), threads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
 template <typename T, typename TOut>
-cudaError_t ln_dispatch(const void* x, const float* gamma, const float* beta, void* y, int M_max, const int32_t* rows,
-                        int H, float eps, __nv_bfloat16* q_out, const float* q_scale, float* amax, float* y32,
-                        int n_in, long long in_stride, const float* add_bias, const void* residual, int res_kind,
-                        int32_t* err, cudaStream_t stream) {
-  const int V = H / Vec<T>::N;   // 16-byte vectors per row
-#define RPP_LN_CASE(G_, VPL_)                                                                                  \
-  if (V == (G_) * (VPL_))                                                                                      \
-    return ln_launch<T, TOut, G_, VPL_>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, y32, n_in, \
-                                        in_stride, add_bias, residual, res_kind, err, stream);
+cudaError_t ln_dispatch(const LnArgs& a, cudaStream_t stream) {
+  const int V = a.H / Vec<T>::N;   // 16-byte vectors per row
+#define RPP_LN_CASE(G_, VPL_) \
+  if (V == (G_) * (VPL_)) return ln_launch<T, TOut, G_, VPL_>(a, stream);
   RPP_LN_CASE(32, 1) RPP_LN_CASE(32, 2) RPP_LN_CASE(32, 3) RPP_LN_CASE(32, 4)
   RPP_LN_CASE(32, 5) RPP_LN_CASE(32, 6) RPP_LN_CASE(32, 8) RPP_LN_CASE(32, 12) RPP_LN_CASE(32, 16)
   RPP_LN_CASE(16, 1) RPP_LN_CASE(16, 3) RPP_LN_CASE(8, 1) RPP_LN_CASE(8, 3) RPP_LN_CASE(8, 5)
@@ -305,27 +332,23 @@ bool layernorm_supported(int H, rpp_dtype dtype) {
   return false;
 }
 
-cudaError_t launch_layernorm(const void* x, const float* gamma, const float* beta, void* y, int M_max,
-                             const int32_t* rows, int H, float eps, rpp_dtype in_dtype, rpp_dtype out_dtype,
-                             void* q_codes, const float* q_scale, float* amax, float* y32, int32_t* err,
-                             cudaStream_t stream, int n_in, long long in_stride, const float* add_bias,
-                             const void* residual, rpp_dtype res_dtype) {
-  if (n_in > 1 && in_dtype != RPP_F32) return cudaErrorNotSupported;
-  const int res_kind = !residual ? 0 : (res_dtype == RPP_F32 ? 1 : (res_dtype == RPP_F16 ? 2 : 3));
-  __nv_bfloat16* q_out = static_cast<__nv_bfloat16*>(q_codes);
+cudaError_t launch_layernorm(const LnArgs& args, cudaStream_t stream) {
+  LnArgs a = args;
+  if (a.n_in > 1 && a.in_dtype != RPP_F32) return cudaErrorNotSupported;
+  a.res_kind = !a.residual ? 0 : (a.res_dtype == RPP_F32 ? 1 : (a.res_dtype == RPP_F16 ? 2 : 3));
+  if (a.residual && a.in_dtype != RPP_F32) return cudaErrorNotSupported;   // residual adds use 4-element groups
+  if (a.pad_cu && (a.pad_B <= 0 || a.pad_L <= 0)) return cudaErrorInvalidValue;
   using BF = __nv_bfloat16;
-  if (in_dtype == out_dtype) {
-    switch (in_dtype) {
-      case RPP_F32: return ln_dispatch<float, float>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, y32, n_in, in_stride, add_bias, residual, res_kind, err, stream);
-      case RPP_F16: return ln_dispatch<__half, __half>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, y32, n_in, in_stride, add_bias, residual, res_kind, err, stream);
-      case RPP_BF16: return ln_dispatch<BF, BF>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, y32, n_in, in_stride, add_bias, residual, res_kind, err, stream);
+  if (a.in_dtype == a.out_dtype) {
+    switch (a.in_dtype) {
+      case RPP_F32: return ln_dispatch<float, float>(a, stream);
+      case RPP_F16: return ln_dispatch<__half, __half>(a, stream);
+      case RPP_BF16: return ln_dispatch<BF, BF>(a, stream);
       default: return cudaErrorNotSupported;
     }
   }
-  if (in_dtype == RPP_F32 && out_dtype == RPP_F16)
-    return ln_dispatch<float, __half>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, y32, n_in, in_stride, add_bias, residual, res_kind, err, stream);
-  if (in_dtype == RPP_F32 && out_dtype == RPP_BF16)
-    return ln_dispatch<float, BF>(x, gamma, beta, y, M_max, rows, H, eps, q_out, q_scale, amax, y32, n_in, in_stride, add_bias, residual, res_kind, err, stream);
+  if (a.in_dtype == RPP_F32 && a.out_dtype == RPP_F16) return ln_dispatch<float, __half>(a, stream);
+  if (a.in_dtype == RPP_F32 && a.out_dtype == RPP_BF16) return ln_dispatch<float, BF>(a, stream);
   return cudaErrorNotSupported;
 }
 

@@ -115,7 +115,101 @@ __global__ void rebuild_padding_kernel(const uint4* __restrict__ packed, const i
   }
 }
 
+// Offsets and removal in one launch (B <= kFusedMaxB): every CTA scans the lengths
+// itself in shared memory -- B is small, so the redundant scan costs less than a
+// second launch -- then copies its share of the valid padded rows to their packed
+// slots and writes their padding offsets; CTA 0 also writes cu_seqlens.
+constexpr int kFusedMaxB = 1024;
+constexpr int kFusedThreads = 256;
+
+__global__ void __launch_bounds__(kFusedThreads) offsets_remove_kernel(const int32_t* __restrict__ lengths, int B,
+                                                                       int L, int vpr, const uint4* __restrict__ padded,
+                                                                       int32_t* __restrict__ cu,
+                                                                       int32_t* __restrict__ po,
+                                                                       uint4* __restrict__ packed, int32_t* err) {
+  __shared__ int32_t s_cu[kFusedMaxB + 1];
+  __shared__ int32_t s_warp[kFusedThreads / 32];
+  const int tid = threadIdx.x;
+  constexpr int PER = kFusedMaxB / kFusedThreads;   // lengths per thread
+  int32_t v[PER];
+  int32_t run = 0;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int b = tid * PER + j;
+    int32_t len = 0;
+    if (b < B) {
+      len = lengths[b];
+      if (len < 0 || len > L) {
+        if (blockIdx.x == 0) set_device_error(err, RPP_DERR_LENGTH);
+        len = len < 0 ? 0 : L;
+      }
+    }
+    run += len;
+    v[j] = run;   // inclusive within the thread
+  }
+  // exclusive scan of the per-thread totals across the block
+  int32_t x = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t t = __shfl_up_sync(0xffffffffu, x, o);
+    if ((tid & 31) >= o) x += t;
+  }
+  if ((tid & 31) == 31) s_warp[tid >> 5] = x;
+  __syncthreads();
+  if (tid < 32) {
+    int32_t w = tid < kFusedThreads / 32 ? s_warp[tid] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t t = __shfl_up_sync(0xffffffffu, w, o);
+      if (tid >= o) w += t;
+    }
+    if (tid < kFusedThreads / 32) s_warp[tid] = w;
+  }
+  __syncthreads();
+  const int32_t base = x - run + ((tid >> 5) ? s_warp[(tid >> 5) - 1] : 0);
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int b = tid * PER + j;
+    if (b < B) s_cu[b + 1] = base + v[j];
+  }
+  if (tid == 0) s_cu[0] = 0;
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int b = tid; b <= B; b += kFusedThreads) cu[b] = s_cu[b];
+  if (device_error_set(err)) return;
+  // copy the valid rows; padded row r = b*L + p goes to packed row cu[b] + p
+  const long long total = static_cast<long long>(B) * L * vpr;
+  for (long long i = blockIdx.x * static_cast<long long>(kFusedThreads) + tid; i < total;
+       i += static_cast<long long>(gridDim.x) * kFusedThreads) {
+    const long long r = i / vpr;
+    const int c = static_cast<int>(i - r * vpr);
+    const int b = static_cast<int>(r / L);
+    const int p = static_cast<int>(r - static_cast<long long>(b) * L);
+    const int32_t c0 = s_cu[b];
+    if (p < s_cu[b + 1] - c0) {
+      packed[(static_cast<long long>(c0) + p) * vpr + c] = __ldg(padded + i);
+      if (c == 0) po[c0 + p] = b * L - c0;
+    }
+  }
+}
+
 }  // namespace
+
+bool offsets_remove_fusable(int B) { return B > 0 && B <= kFusedMaxB; }
+
+cudaError_t launch_offsets_remove(const int32_t* lengths, int B, int L, int row_bytes, const void* padded,
+                                  int32_t* cu, int32_t* po, void* packed, int32_t* err, cudaStream_t stream) {
+  if (!offsets_remove_fusable(B)) return cudaErrorNotSupported;
+  const int vpr = row_bytes / 16;
+  const long long total = static_cast<long long>(B) * L * vpr;
+  long long blocks = (total + kFusedThreads - 1) / kFusedThreads;
+  const long long cap = static_cast<long long>(num_sms()) * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  offsets_remove_kernel<<<static_cast<int>(blocks), kFusedThreads, 0, stream>>>(
+      lengths, B, L, vpr, static_cast<const uint4*>(padded), cu, po, static_cast<uint4*>(packed), err);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_build_offsets(const int32_t* lengths, int B, int L, int32_t* cu, int32_t* po, int32_t* err,
                                  cudaStream_t stream) {

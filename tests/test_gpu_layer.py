@@ -30,6 +30,10 @@ def _run_path(wl, dtype, layers=None, hint=False):
     err = rpp.new_error_word()
     y, cu, po = rpp.encoder_forward(prepared, lengths, x, cfg.L, err=err)
     check_err(err)
+    # the fused offsets + removal of the whole-path call: offsets bit-exact
+    cu_ref, po_ref, T = oracle.build_offsets(wl["lengths"], cfg.L)
+    assert np.array_equal(cu.cpu().numpy(), cu_ref)
+    assert np.array_equal(po.cpu().numpy()[:T], po_ref)
     return down(y).reshape(cfg.B, cfg.L, cfg.H), prepared
 
 
