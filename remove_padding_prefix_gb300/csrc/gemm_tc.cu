@@ -83,10 +83,15 @@ template <typename T> struct AbFmt;
 template <> struct AbFmt<__half> { static constexpr int v = 0; };
 template <> struct AbFmt<__nv_bfloat16> { static constexpr int v = 1; };
 
-// epilogues whose full 32 x 32 blocks leave through the TMA store path
+// epilogues whose full 32 x 32 blocks leave through the TMA store path (all of them)
 template <int EPI>
 constexpr bool tma_store_epi() {
-  return EPI != RPP_EPI_BIAS_RESIDUAL;
+  return true;
+}
+// 16-byte vectors of residual per 32 columns
+template <typename TRes>
+constexpr int res_vecs32() {
+  return 32 * static_cast<int>(sizeof(TRes)) / 16;
 }
 template <int EPI>
 constexpr bool is_int_epi() {
@@ -114,7 +119,7 @@ __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_
 // for int8 epilogues the exact integer sum converted to float).
 template <typename TOut, typename TRes, int EPI, int NV>
 __device__ __forceinline__ void epi_math(const GemmParams& p, float* v, int row, int n, bool first, float a_s,
-                                         float inv_q) {
+                                         float inv_q, const uint4* rres = nullptr) {
   if constexpr (EPI == EPI_I32 || EPI == EPI_ACC) return;
   if constexpr (EPI == EPI_DQ_BIAS || EPI == EPI_DQ_ACC || EPI == EPI_DQ_BIAS_GELU_Q) {
     const float4* s4 = reinterpret_cast<const float4*>(p.w_scale + n);
@@ -152,7 +157,8 @@ __device__ __forceinline__ void epi_math(const GemmParams& p, float* v, int row,
     if (first) {
       constexpr int RPV = Vec<TRes>::N;
       const uint4* rr =
-          reinterpret_cast<const uint4*>(static_cast<const TRes*>(p.residual) + static_cast<long long>(row) * p.N + n);
+          rres ? rres
+               : reinterpret_cast<const uint4*>(static_cast<const TRes*>(p.residual) + static_cast<long long>(row) * p.N + n);
 #pragma unroll
       for (int j = 0; j < NV / RPV; ++j) {
         float f[RPV];
@@ -419,6 +425,20 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int nch = NCH > 1 ? (kb1 - kb0 + kChunkBlocks - 1) / kChunkBlocks : 1;
       const uint32_t a = NBUF == 2 ? (acc_it & 1u) : 0u;
       const uint32_t aph = NBUF == 2 ? ((acc_it >> 1) & 1u) : (acc_it & 1u);
+      // residual of this warp's first 32-column slice, requested before the accumulator wait
+      constexpr int RV = res_vecs32<TRes>();
+      uint4 rnext[RV];
+      const int pre_m0 = (unit / S / num_n) * kBM;
+      const int pre_n0 = (unit / S % num_n) * BN;
+      const int pre_row = pre_m0 + r_in_tile;
+      if constexpr (EPI == RPP_EPI_BIAS_RESIDUAL && BN >= 32) {
+        if (pre_row < M && half < BN / 32) {
+          const uint4* rr = reinterpret_cast<const uint4*>(static_cast<const TRes*>(p.residual) +
+                                                           static_cast<long long>(pre_row) * p.N + pre_n0 + half * 32);
+#pragma unroll
+          for (int j = 0; j < RV; ++j) rnext[j] = rr[j];
+        }
+      }
       int ok = 1;
       if (lane == 0) ok = mbar_wait_bounded(&tfull[a], aph, abort_flag) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -440,12 +460,24 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if constexpr (BN >= 32) {
 #pragma unroll 1
         for (int c = half; c < BN / 32; c += 2) {
+          uint4 rcur[RV];
+          if constexpr (EPI == RPP_EPI_BIAS_RESIDUAL) {
+#pragma unroll
+            for (int j = 0; j < RV; ++j) rcur[j] = rnext[j];
+            if (row_ok && c + 2 < BN / 32) {   // next slice's residual while this one is processed
+              const uint4* rr = reinterpret_cast<const uint4*>(static_cast<const TRes*>(p.residual) +
+                                                               static_cast<long long>(row) * p.N + n0 + (c + 2) * 32);
+#pragma unroll
+              for (int j = 0; j < RV; ++j) rnext[j] = rr[j];
+            }
+          }
+          const uint4* rres = EPI == RPP_EPI_BIAS_RESIDUAL ? rcur : nullptr;
           float v[32];
           int acc[32];
           load_acc<EPI, NCH, ACC, 32>(t_row + c * 32, nch, v, acc);
           const int n = n0 + c * 32;
           if (kTma && full_tile) {
-            epi_math<TOut, TRes, EPI, 32>(p, v, row, n, first, a_s, inv_q);
+            epi_math<TOut, TRes, EPI, 32>(p, v, row, n, first, a_s, inv_q, rres);
             if (pending_store) {   // the previous TMA store has finished reading the staging block
               if (lane == 0) bulk_wait_read0();
               __syncwarp();
@@ -459,7 +491,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
             pending_store = true;
           } else if (row_ok) {
-            epi_math<TOut, TRes, EPI, 32>(p, v, row, n, first, a_s, inv_q);
+            epi_math<TOut, TRes, EPI, 32>(p, v, row, n, first, a_s, inv_q, rres);
             store_row<TOut, EPI, 32>(p, v, acc, row, n, split);
           }
         }

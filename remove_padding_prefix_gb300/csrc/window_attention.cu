@@ -8,7 +8,7 @@
 // preprocessing; batch GEMM + softmax + batch GEMM in one fMHA kernel with the
 // transposes in its I/O; the 49-token windows padded to a multiple of 8).
 //
-// One CTA (4 warps) processes whole windows in a persistent loop.  For window
+// One CTA (4 warps) processes one head of one window.  For window
 // (image, wy, wx) token t = ty*w + tx sits at (y, x) = (wy*w + ty, wx*w + tx) in the
 // shifted frame and reads raster row ((y + s) mod I, (x + s) mod I); the output row
 // is written back to the same raster row, which performs reverse + unshift.  The
@@ -71,166 +71,160 @@ __device__ __forceinline__ uint32_t pack2w(float lo, float hi) {
 
 __device__ __forceinline__ int region(int c, int I, int w, int s) { return c < I - w ? 0 : (c < I - s ? 1 : 2); }
 
-template <typename T, int NH>
+// One CTA (4 warps) per (window, head): 12 KB of shared memory, so many CTAs share an
+// SM and one CTA's gather latency hides behind another's arithmetic.  The bias of the
+// head (fp32, preprocessed) is read through the L1 cache; every window reuses it.
+template <typename T>
 __global__ void __launch_bounds__(128) window_attention_kernel(const T* __restrict__ qkv,
                                                                const float* __restrict__ bias, T* __restrict__ out,
-                                                               int B, int I, int w, int s, float scale_log2,
+                                                               int I, int w, int s, int nh, float scale_log2,
                                                                int32_t* err) {
   if (device_error_set(err)) return;
-  constexpr int C = NH * kWD;
   constexpr int TILE = kWRows * kWD * 2;   // bytes of one 64 x 32 tile
-  extern __shared__ __align__(128) uint8_t wsm[];
-  uint8_t* sQKV = wsm;                                      // [3][NH][64][32]
-  float* sBias = reinterpret_cast<float*>(wsm + 3 * NH * TILE);   // [NH][N][N] (pre-scaled by log2 e)
+  __shared__ __align__(128) uint8_t sQKV[3 * TILE];
+  __shared__ int sRow[kWRows];   // raster rows of the window's tokens
+  __shared__ int sLab[kWRows];   // region labels in the shifted frame
+  const int C = nh * kWD;
   const int N = w * w;
-  int* sRow = reinterpret_cast<int*>(sBias + NH * N * N);   // [64] raster rows of the window
-  int* sLab = sRow + kWRows;                                // [64] region labels
-
+  const int h = blockIdx.y;
+  const int nWs = I / w;
+  const int nW = nWs * nWs;
+  const long long wid = blockIdx.x;
+  const int img = static_cast<int>(wid / nW);
+  const int wr = static_cast<int>(wid - static_cast<long long>(img) * nW);
+  const int wy = wr / nWs, wx = wr - (wr / nWs) * nWs;
   const int tid = threadIdx.x;
   const int warp = warp_id();
   const int lane = lane_id();
-  const float log2e = 1.4426950408889634f;
-  for (int i = tid; i < NH * N * N; i += blockDim.x) sBias[i] = bias[i] * log2e;
-  // padding rows (N..63) of every tile stay zero for the whole kernel
-  for (int i = tid; i < 3 * NH * kWRows * 4; i += blockDim.x) {
-    const int tile = i / (kWRows * 4);
-    const int r = (i / 4) % kWRows;
-    if (r >= N) *reinterpret_cast<uint4*>(sQKV + tile * TILE + swz64(r, i & 3)) = make_uint4(0u, 0u, 0u, 0u);
+
+  // padding rows (N..63) of Q, K and V are zero (V's must be: P = 0 there, and 0 * junk
+  // could be NaN)
+  for (int i = tid; i < 3 * (kWRows - N) * 4; i += blockDim.x) {
+    const int tile = i / ((kWRows - N) * 4);
+    const int r = N + (i / 4) % (kWRows - N);
+    *reinterpret_cast<uint4*>(sQKV + tile * TILE + swz64(r, i & 3)) = make_uint4(0u, 0u, 0u, 0u);
   }
-  const int nWs = I / w;
-  const int nW = nWs * nWs;
-  const long long total = static_cast<long long>(B) * nW;
+  if (tid < N) {
+    const int y = wy * w + tid / w, x = wx * w + tid % w;
+    int ys = y + s, xs = x + s;
+    if (ys >= I) ys -= I;
+    if (xs >= I) xs -= I;
+    sRow[tid] = img * I * I + ys * I + xs;
+    sLab[tid] = s > 0 ? 3 * region(y, I, w, s) + region(x, I, w, s) : 0;
+  }
+  __syncthreads();
+  // gather this head's Q, K and V rows: N rows x 3 parts x 4 chunks of 16 bytes
+  for (int i = tid; i < N * 12; i += blockDim.x) {
+    const int r = i / 12;
+    const int cc = i - r * 12;
+    const int part = cc >> 2;
+    const T* src = qkv + static_cast<long long>(sRow[r]) * (3 * C) + part * C + h * kWD + (cc & 3) * 8;
+    cp_async_16(sQKV + part * TILE + swz64(r, cc & 3), src, true);
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
 
-  for (long long wid = blockIdx.x; wid < total; wid += gridDim.x) {
-    const int img = static_cast<int>(wid / nW);
-    const int wr = static_cast<int>(wid - static_cast<long long>(img) * nW);
-    const int wy = wr / nWs, wx = wr - (wr / nWs) * nWs;
-    __syncthreads();   // previous window fully consumed
-    if (tid < N) {
-      const int y = wy * w + tid / w, x = wx * w + tid % w;
-      int ys = y + s, xs = x + s;
-      if (ys >= I) ys -= I;
-      if (xs >= I) xs -= I;
-      sRow[tid] = img * I * I + ys * I + xs;
-      sLab[tid] = s > 0 ? 3 * region(y, I, w, s) + region(x, I, w, s) : 0;
+  const uint32_t sQa = smem_u32(sQKV);
+  const uint32_t sKa = smem_u32(sQKV + TILE);
+  const uint32_t sVa = smem_u32(sQKV + 2 * TILE);
+  const int rA = warp * 16 + (lane >> 2);   // this thread's two query rows: rA, rA + 8
+  uint32_t qf[2][4];
+#pragma unroll
+  for (int kk = 0; kk < 2; ++kk) {
+    const int r = warp * 16 + (lane & 15);
+    ldsm_x4w(sQa + swz64(r, kk * 2 + (lane >> 4)), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
+  }
+  float sc[8][4];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < 2; ++kk) {
+#pragma unroll
+    for (int np = 0; np < 4; ++np) {
+      uint32_t b0, b1, b2, b3;
+      const int r = np * 16 + (lane & 7) + ((lane >> 4) << 3);
+      ldsm_x4w(sKa + swz64(r, kk * 2 + ((lane >> 3) & 1)), b0, b1, b2, b3);
+      mma_w<T>(sc[2 * np], qf[kk], b0, b1);
+      mma_w<T>(sc[2 * np + 1], qf[kk], b2, b3);
     }
-    __syncthreads();
-    // gather: N rows x (3 * NH * 4) chunks of 16 bytes
-    const int cpr = 3 * NH * 4;
-    for (int i = tid; i < N * cpr; i += blockDim.x) {
-      const int r = i / cpr;
-      const int cc = i - r * cpr;         // chunk within the qkv row: (part, head, chunk)
-      const int tile = cc >> 2;           // part * NH + head
-      const T* src = qkv + static_cast<long long>(sRow[r]) * (3 * C) + cc * 8;
-      cp_async_16(sQKV + tile * TILE + swz64(r, cc & 3), src, true);
+  }
+  // scores -> log2 domain with bias and region mask; softmax over the N keys
+  const float log2e = 1.4426950408889634f;
+  const float* bh = bias + static_cast<long long>(h) * N * N;
+  const int labA = rA < N ? sLab[rA] : -1;
+  const int labB = rA + 8 < N ? sLab[rA + 8] : -1;
+  float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int t = rA + ((e >> 1) << 3);
+      const int u = j * 8 + 2 * (lane & 3) + (e & 1);
+      const int lt = (e >> 1) ? labB : labA;
+      float v = -INFINITY;
+      if (u < N && t < N && lt == sLab[u]) v = sc[j][e] * scale_log2 + __ldg(bh + t * N + u) * log2e;
+      sc[j][e] = v;
     }
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();
-
-    const int rA = warp * 16 + (lane >> 2);   // this thread's two query rows: rA, rA + 8
-    for (int h = 0; h < NH; ++h) {
-      const uint32_t sQa = smem_u32(sQKV + (0 * NH + h) * TILE);
-      const uint32_t sKa = smem_u32(sQKV + (1 * NH + h) * TILE);
-      const uint32_t sVa = smem_u32(sQKV + (2 * NH + h) * TILE);
-      uint32_t qf[2][4];
+    mx[0] = fmaxf(mx[0], fmaxf(sc[j][0], sc[j][1]));
+    mx[1] = fmaxf(mx[1], fmaxf(sc[j][2], sc[j][3]));
+  }
+  float sum[2] = {0.f, 0.f};
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        const int r = warp * 16 + (lane & 15);
-        ldsm_x4w(sQa + swz64(r, kk * 2 + (lane >> 4)), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
-      }
-      float sc[8][4];
+  for (int i = 0; i < 2; ++i) {
+    mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
+    mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
+    if (mx[i] == -INFINITY) mx[i] = 0.f;   // padding query rows
+  }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+  for (int j = 0; j < 8; ++j) {
+    sc[j][0] = exp2f(sc[j][0] - mx[0]);
+    sc[j][1] = exp2f(sc[j][1] - mx[0]);
+    sc[j][2] = exp2f(sc[j][2] - mx[1]);
+    sc[j][3] = exp2f(sc[j][3] - mx[1]);
+    sum[0] += sc[j][0] + sc[j][1];
+    sum[1] += sc[j][2] + sc[j][3];
+  }
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
+  for (int i = 0; i < 2; ++i) {
+    sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], 1);
+    sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], 2);
+    sum[i] = sum[i] > 0.f ? 1.f / sum[i] : 0.f;
+  }
+  float o[4][4];
 #pragma unroll
-        for (int np = 0; np < 4; ++np) {
-          uint32_t b0, b1, b2, b3;
-          const int r = np * 16 + (lane & 7) + ((lane >> 4) << 3);
-          ldsm_x4w(sKa + swz64(r, kk * 2 + ((lane >> 3) & 1)), b0, b1, b2, b3);
-          mma_w<T>(sc[2 * np], qf[kk], b0, b1);
-          mma_w<T>(sc[2 * np + 1], qf[kk], b2, b3);
-        }
-      }
-      // scores -> log2 domain with bias and region mask; softmax over the N keys
-      float mx[2] = {-INFINITY, -INFINITY};
-      const float* bh = sBias + h * N * N;
+  for (int j = 0; j < 4; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+  for (int kk = 0; kk < 4; ++kk) {
+    uint32_t pa[4];
+    pa[0] = pack2w<T>(sc[2 * kk][0], sc[2 * kk][1]);
+    pa[1] = pack2w<T>(sc[2 * kk][2], sc[2 * kk][3]);
+    pa[2] = pack2w<T>(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+    pa[3] = pack2w<T>(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int t = rA + ((e >> 1) << 3);
-          const int u = j * 8 + 2 * (lane & 3) + (e & 1);
-          float v = -INFINITY;
-          if (u < N && t < N && sLab[t] == sLab[u]) v = sc[j][e] * scale_log2 + bh[t * N + u];
-          sc[j][e] = v;
-        }
-        mx[0] = fmaxf(mx[0], fmaxf(sc[j][0], sc[j][1]));
-        mx[1] = fmaxf(mx[1], fmaxf(sc[j][2], sc[j][3]));
-      }
-      float sum[2] = {0.f, 0.f};
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
-        mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
-        if (mx[i] == -INFINITY) mx[i] = 0.f;   // padding query rows
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        sc[j][0] = exp2f(sc[j][0] - mx[0]);
-        sc[j][1] = exp2f(sc[j][1] - mx[0]);
-        sc[j][2] = exp2f(sc[j][2] - mx[1]);
-        sc[j][3] = exp2f(sc[j][3] - mx[1]);
-        sum[0] += sc[j][0] + sc[j][1];
-        sum[1] += sc[j][2] + sc[j][3];
-      }
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], 1);
-        sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], 2);
-        sum[i] = sum[i] > 0.f ? 1.f / sum[i] : 0.f;
-      }
-      float o[4][4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        uint32_t pa[4];
-        pa[0] = pack2w<T>(sc[2 * kk][0], sc[2 * kk][1]);
-        pa[1] = pack2w<T>(sc[2 * kk][2], sc[2 * kk][3]);
-        pa[2] = pack2w<T>(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-        pa[3] = pack2w<T>(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
-#pragma unroll
-        for (int dp = 0; dp < 2; ++dp) {
-          uint32_t b0, b1, b2, b3;
-          const int r = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-          ldsm_x4w_t(sVa + swz64(r, dp * 2 + (lane >> 4)), b0, b1, b2, b3);
-          mma_w<T>(o[2 * dp], pa, b0, b1);
-          mma_w<T>(o[2 * dp + 1], pa, b2, b3);
-        }
-      }
-      // write the normalised head output over this warp's own Q rows of head h (no
-      // longer needed); the scatter below reads it back
-      __syncwarp();
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t lo = pack2w<T>(o[j][0] * sum[0], o[j][1] * sum[0]);
-        const uint32_t hi = pack2w<T>(o[j][2] * sum[1], o[j][3] * sum[1]);
-        uint8_t* tq = sQKV + (0 * NH + h) * TILE;
-        *reinterpret_cast<uint32_t*>(tq + swz64(rA, j) + (lane & 3) * 4) = lo;
-        *reinterpret_cast<uint32_t*>(tq + swz64(rA + 8, j) + (lane & 3) * 4) = hi;
-      }
+    for (int dp = 0; dp < 2; ++dp) {
+      uint32_t b0, b1, b2, b3;
+      const int r = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+      ldsm_x4w_t(sVa + swz64(r, dp * 2 + (lane >> 4)), b0, b1, b2, b3);
+      mma_w<T>(o[2 * dp], pa, b0, b1);
+      mma_w<T>(o[2 * dp + 1], pa, b2, b3);
     }
-    __syncthreads();
-    // scatter: N rows x (NH * 4) chunks back to the same raster rows
-    const int opr = NH * 4;
-    for (int i = tid; i < N * opr; i += blockDim.x) {
-      const int r = i / opr;
-      const int cc = i - r * opr;
-      const uint4 v = *reinterpret_cast<const uint4*>(sQKV + (cc >> 2) * TILE + swz64(r, cc & 3));
-      *reinterpret_cast<uint4*>(out + static_cast<long long>(sRow[r]) * C + cc * 8) = v;
-    }
+  }
+  // normalised output over this warp's own Q rows, then scattered back to the raster rows
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t lo = pack2w<T>(o[j][0] * sum[0], o[j][1] * sum[0]);
+    const uint32_t hi = pack2w<T>(o[j][2] * sum[1], o[j][3] * sum[1]);
+    *reinterpret_cast<uint32_t*>(sQKV + swz64(rA, j) + (lane & 3) * 4) = lo;
+    *reinterpret_cast<uint32_t*>(sQKV + swz64(rA + 8, j) + (lane & 3) * 4) = hi;
+  }
+  __syncthreads();
+  for (int i = tid; i < N * 4; i += blockDim.x) {
+    const int r = i >> 2;
+    const int cc = i & 3;
+    const uint4 v = *reinterpret_cast<const uint4*>(sQKV + swz64(r, cc));
+    *reinterpret_cast<uint4*>(out + static_cast<long long>(sRow[r]) * C + h * kWD + cc * 8) = v;
   }
 }
 
@@ -251,47 +245,30 @@ __global__ void swin_bias_kernel(const void* table, int table_dtype, int w, int 
   }
 }
 
-template <typename T, int NH>
-cudaError_t wa_launch(int B, const void* qkv, const float* bias, void* out, int I, int w, int s, int32_t* err,
+template <typename T>
+cudaError_t wa_launch(int B, const void* qkv, const float* bias, void* out, int nh, int I, int w, int s, int32_t* err,
                       cudaStream_t stream) {
-  const int N = w * w;
-  const size_t smem = 3 * NH * kWRows * kWD * 2 + NH * N * N * sizeof(float) + 2 * kWRows * sizeof(int);
-  auto kern = window_attention_kernel<T, NH>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
   const long long windows = static_cast<long long>(B) * (I / w) * (I / w);
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 128, smem);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) per_sm = 1;
-  long long grid = static_cast<long long>(num_sms()) * per_sm;
-  if (grid > windows) grid = windows;
-  if (grid < 1) grid = 1;
+  if (windows > 0x7fffffffLL || nh > 65535) return cudaErrorNotSupported;
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kWD));
-  kern<<<static_cast<int>(grid), 128, smem, stream>>>(static_cast<const T*>(qkv), bias, static_cast<T*>(out), B, I, w,
-                                                      s, scale_log2, err);
+  dim3 grid(static_cast<unsigned>(windows), nh);
+  window_attention_kernel<T><<<grid, 128, 0, stream>>>(static_cast<const T*>(qkv), bias, static_cast<T*>(out), I, w,
+                                                       s, nh, scale_log2, err);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 bool window_attention_supported(int C, int nh, int w, int I, int s) {
-  return nh > 0 && C == nh * kWD && (nh == 3 || nh == 6) && w > 0 && w * w <= kWRows && I % w == 0 && s >= 0 &&
-         s < w;
+  return nh > 0 && C == nh * kWD && w > 0 && w * w <= kWRows && I % w == 0 && s >= 0 && s < w;
 }
 
 cudaError_t launch_window_attention(int B, const void* qkv, const float* bias, void* out, int C, int nh, int I, int w,
                                     int s, rpp_dtype dtype, int32_t* err, cudaStream_t stream) {
   if (!window_attention_supported(C, nh, w, I, s)) return cudaErrorNotSupported;
   if (B <= 0) return cudaSuccess;
-  if (dtype == RPP_F16) {
-    if (nh == 3) return wa_launch<__half, 3>(B, qkv, bias, out, I, w, s, err, stream);
-    return wa_launch<__half, 6>(B, qkv, bias, out, I, w, s, err, stream);
-  }
-  if (dtype == RPP_BF16) {
-    if (nh == 3) return wa_launch<__nv_bfloat16, 3>(B, qkv, bias, out, I, w, s, err, stream);
-    return wa_launch<__nv_bfloat16, 6>(B, qkv, bias, out, I, w, s, err, stream);
-  }
+  if (dtype == RPP_F16) return wa_launch<__half>(B, qkv, bias, out, nh, I, w, s, err, stream);
+  if (dtype == RPP_BF16) return wa_launch<__nv_bfloat16>(B, qkv, bias, out, nh, I, w, s, err, stream);
   return cudaErrorNotSupported;
 }
 

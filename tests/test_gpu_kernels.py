@@ -121,3 +121,18 @@ def test_attention_rejects_length_above_max_len():
     cu, _ = rpp.build_offsets(torch.as_tensor(lengths, device=dev()), 64, err=err)
     rpp.attention_varlen(qkv, cu, 2, 32, 1, err=err)   # max_len 32 < 40
     assert rpp.get_device_error(err) == rpp.RPP_DERR_LENGTH
+
+
+def test_device_gelu_against_exact_definition():
+    """The GEMM epilogue's GELU (exp of a fitted log-erfcx polynomial) against the fp64
+    definition x * Phi(x): an fp32 GEMM with identity weights makes the accumulator
+    exactly x, so the output is the device GELU of x itself."""
+    x = np.concatenate([np.linspace(-8, 8, 64 * 1000), [0.0, -0.0, 1e-20, -1e-20, 3.9 * 2 ** 0.5, -30.0, 30.0,
+                                                         1e4, -1e4] + [0.0] * 55]).astype(np.float32)
+    a = x.reshape(-1, 64)
+    eye = np.eye(64, dtype=np.float32)
+    out = rpp.linear(up(a, "fp32"), up(eye, "fp32"), torch.zeros(64, device=dev()), epilogue=rpp.RPP_EPI_BIAS_GELU)
+    got = down(out).reshape(-1)
+    ref = oracle.gelu(x.astype(np.float64))
+    err = np.abs(got - ref)
+    assert np.all(err <= 5e-7 * (1.0 + np.abs(x))), (err.max(), x[np.argmax(err)])
