@@ -90,6 +90,8 @@ __global__ void __launch_bounds__(128) attention_varlen_kernel(const T* __restri
                                                                const int32_t* __restrict__ cu, int T_max,
                                                                int max_len, int nh, T* __restrict__ out,
                                                                float scale_log2, int32_t* err) {
+  pdl_wait();
+  pdl_trigger();
   if (device_error_set(err)) return;
   const int b = blockIdx.z;
   const int h = blockIdx.y;
@@ -267,6 +269,8 @@ __global__ void __launch_bounds__(kF32Rows) attention_varlen_f32_kernel(const fl
                                                                         int max_len, int nh,
                                                                         float* __restrict__ out, float scale,
                                                                         int32_t* err) {
+  pdl_wait();
+  pdl_trigger();
   if (device_error_set(err)) return;
   const int b = blockIdx.z;
   const int h = blockIdx.y;
@@ -335,23 +339,22 @@ cudaError_t launch_attention_varlen(const void* qkv, const int32_t* cu, int B, i
   const float scale = 1.0f / sqrtf(static_cast<float>(d));
   if (dtype == RPP_F32) {
     dim3 grid((max_len + kF32Rows - 1) / kF32Rows, nh, B);
-    attention_varlen_f32_kernel<<<grid, kF32Rows, 0, stream>>>(static_cast<const float*>(qkv), cu, T_max, max_len,
-                                                                 nh, static_cast<float*>(out), scale, err);
-    return cudaGetLastError();
+    return launch_pdl(attention_varlen_f32_kernel, grid, dim3(kF32Rows), 0, stream, static_cast<const float*>(qkv), cu,
+                      T_max, max_len, nh, static_cast<float*>(out), scale, err);
   }
   dim3 grid((max_len + kBMq - 1) / kBMq, nh, B);
   const float scale_log2 = scale * 1.4426950408889634f;
   if (dtype == RPP_F16) {
-    attention_varlen_kernel<__half><<<grid, kWarps * 32, 0, stream>>>(
-        static_cast<const __half*>(qkv), cu, T_max, max_len, nh, static_cast<__half*>(out), scale_log2, err);
-  } else if (dtype == RPP_BF16) {
-    attention_varlen_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(qkv), cu, T_max, max_len, nh, static_cast<__nv_bfloat16*>(out), scale_log2,
-        err);
-  } else {
-    return cudaErrorNotSupported;
+    return launch_pdl(attention_varlen_kernel<__half>, grid, dim3(kWarps * 32), 0, stream,
+                      static_cast<const __half*>(qkv), cu, T_max, max_len, nh, static_cast<__half*>(out), scale_log2,
+                      err);
   }
-  return cudaGetLastError();
+  if (dtype == RPP_BF16) {
+    return launch_pdl(attention_varlen_kernel<__nv_bfloat16>, grid, dim3(kWarps * 32), 0, stream,
+                      static_cast<const __nv_bfloat16*>(qkv), cu, T_max, max_len, nh,
+                      static_cast<__nv_bfloat16*>(out), scale_log2, err);
+  }
+  return cudaErrorNotSupported;
 }
 
 }  // namespace rpp

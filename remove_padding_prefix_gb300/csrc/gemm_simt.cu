@@ -18,6 +18,8 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(const float* __restrict__
                                                        const float* __restrict__ bias, const float* residual,
                                                        float* out, int M_max, const int32_t* rows, int N, int K,
                                                        int32_t* err) {
+  pdl_wait();
+  pdl_trigger();
   if (device_error_set(err)) return;
   int M = rows ? *rows : M_max;
   if (M > M_max || M < 0) {
@@ -87,18 +89,16 @@ cudaError_t launch_gemm_f32(const float* a, const float* w_t, const float* bias,
   if (grid.y == 0) grid.y = 1;
   switch (epi) {
     case RPP_EPI_BIAS:
-      gemm_f32_kernel<RPP_EPI_BIAS><<<grid, 256, 0, stream>>>(a, w_t, bias, residual, out, M_max, rows, N, K, err);
-      break;
+      return launch_pdl(gemm_f32_kernel<RPP_EPI_BIAS>, grid, dim3(256), 0, stream, a, w_t, bias, residual, out, M_max,
+                        rows, N, K, err);
     case RPP_EPI_BIAS_GELU:
-      gemm_f32_kernel<RPP_EPI_BIAS_GELU><<<grid, 256, 0, stream>>>(a, w_t, bias, residual, out, M_max, rows, N, K, err);
-      break;
+      return launch_pdl(gemm_f32_kernel<RPP_EPI_BIAS_GELU>, grid, dim3(256), 0, stream, a, w_t, bias, residual, out,
+                        M_max, rows, N, K, err);
     case RPP_EPI_BIAS_RESIDUAL:
-      gemm_f32_kernel<RPP_EPI_BIAS_RESIDUAL><<<grid, 256, 0, stream>>>(a, w_t, bias, residual, out, M_max, rows, N, K,
-                                                                       err);
-      break;
+      return launch_pdl(gemm_f32_kernel<RPP_EPI_BIAS_RESIDUAL>, grid, dim3(256), 0, stream, a, w_t, bias, residual,
+                        out, M_max, rows, N, K, err);
     default: return cudaErrorNotSupported;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace rpp

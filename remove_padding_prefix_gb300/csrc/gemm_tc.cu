@@ -308,10 +308,26 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
   }
+  if (threadIdx.x == 32) {
+    // The weights are never written by the preceding kernel: warm L2 with this CTA's
+    // first weight boxes while that kernel drains.  The (tile, split) order puts the
+    // column block of unit blockIdx.x at (unit / S) % num_n regardless of M.
+    const int nn = p.N / BN;
+    const int nk = (p.K + kBK - 1) / kBK;
+    const int kps0 = (nk + p.splits - 1) / p.splits;
+    const int t0 = blockIdx.x / p.splits;
+    const int kb0 = (blockIdx.x - t0 * p.splits) * kps0;
+    const int n0 = (t0 % nn) * BN;
+    const int kb1 = min(nk, kb0 + min(kps0, STAGES));
+    for (int kb = kb0; kb < kb1; ++kb) tma_prefetch_l2_2d(&tmB, kb * kBK, n0);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // everything below may read what the preceding kernel wrote
+  pdl_wait();
+  pdl_trigger();
 
   int M = p.M_max;
   bool skip = device_error_set(p.err);
@@ -596,8 +612,7 @@ cudaError_t gemm_tc_launch(const CUtensorMap& ta, const CUtensorMap& tb, const G
   const long long units = static_cast<long long>(num_m) * (p.N / BN) * p.splits;
   int grid = units < num_sms() ? static_cast<int>(units) : num_sms();
   if (grid < 1) grid = 1;
-  kern<<<grid, kThreads, SMEM, stream>>>(ta, tb, tc, p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), SMEM, stream, ta, tb, tc, p);
 }
 
 // Tile shape choice (the per-shape GEMM configuration of the Kuaishou article's

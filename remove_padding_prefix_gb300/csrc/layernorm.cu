@@ -56,6 +56,8 @@ __device__ __forceinline__ void store_vec(TOut* p, const float* o) {
 // slot is written as zeros (the padding rebuild of the last layer, fused).
 template <typename T, typename TOut, int G, int VPL>
 __global__ void __launch_bounds__(128) layernorm_kernel(LnArgs a) {
+  pdl_wait();
+  pdl_trigger();
   if (device_error_set(a.err)) return;
   const int H = a.H;
   int M = a.rows ? *a.rows : a.M_max;
@@ -240,6 +242,8 @@ __global__ void __launch_bounds__(128) layernorm_kernel(LnArgs a) {
 template <typename T>
 __global__ void quantize_kernel(const T* __restrict__ x, const float* scale, int8_t* __restrict__ q, int M_max,
                                 const int32_t* rows, int H, int32_t* err) {
+  pdl_wait();
+  pdl_trigger();
   if (device_error_set(err)) return;
   int M = rows ? *rows : M_max;
   if (M > M_max || M < 0) {
@@ -268,6 +272,8 @@ __global__ void quantize_kernel(const T* __restrict__ x, const float* scale, int
 template <typename T>
 __global__ void amax_kernel(const T* __restrict__ x, int M_max, const int32_t* rows, int H, float* amax,
                             int32_t* err) {
+  pdl_wait();
+  pdl_trigger();
   if (device_error_set(err)) return;
   int M = rows ? *rows : M_max;
   if (M > M_max || M < 0) M = 0;
@@ -300,8 +306,8 @@ cudaError_t ln_launch(const LnArgs& a, cudaStream_t stream) {
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   const size_t smem = 3 * static_cast<size_t>(a.H) * sizeof(float);
-  layernorm_kernel<T, TOut, G, VPL><<<static_cast<int>(blocks), threads, smem, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(layernorm_kernel<T, TOut, G, VPL>, dim3(static_cast<unsigned>(blocks)), dim3(threads), smem,
+                    stream, a);
 }
 
 template <typename T, typename TOut>
@@ -359,22 +365,17 @@ cudaError_t launch_quantize(const void* x, const float* scale, int8_t* q, int M_
   const long long cap = static_cast<long long>(num_sms()) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
+  const dim3 grid(static_cast<unsigned>(blocks));
   switch (dtype) {
     case RPP_F32:
-      quantize_kernel<float><<<static_cast<int>(blocks), 256, 0, stream>>>(static_cast<const float*>(x), scale, q,
-                                                                            M_max, rows, H, err);
-      break;
+      return launch_pdl(quantize_kernel<float>, grid, dim3(256), 0, stream, static_cast<const float*>(x), scale, q, M_max, rows, H, err);
     case RPP_F16:
-      quantize_kernel<__half><<<static_cast<int>(blocks), 256, 0, stream>>>(static_cast<const __half*>(x), scale, q,
-                                                                             M_max, rows, H, err);
-      break;
+      return launch_pdl(quantize_kernel<__half>, grid, dim3(256), 0, stream, static_cast<const __half*>(x), scale, q, M_max, rows, H, err);
     case RPP_BF16:
-      quantize_kernel<__nv_bfloat16><<<static_cast<int>(blocks), 256, 0, stream>>>(
-          static_cast<const __nv_bfloat16*>(x), scale, q, M_max, rows, H, err);
-      break;
+      return launch_pdl(quantize_kernel<__nv_bfloat16>, grid, dim3(256), 0, stream, static_cast<const __nv_bfloat16*>(x),
+                        scale, q, M_max, rows, H, err);
     default: return cudaErrorNotSupported;
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_amax(const void* x, int M_max, const int32_t* rows, int H, rpp_dtype dtype, float* amax,
@@ -384,22 +385,17 @@ cudaError_t launch_amax(const void* x, int M_max, const int32_t* rows, int H, rp
   const long long cap = static_cast<long long>(num_sms()) * 4;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
+  const dim3 grid(static_cast<unsigned>(blocks));
   switch (dtype) {
     case RPP_F32:
-      amax_kernel<float><<<static_cast<int>(blocks), 256, 0, stream>>>(static_cast<const float*>(x), M_max, rows, H,
-                                                                        amax, err);
-      break;
+      return launch_pdl(amax_kernel<float>, grid, dim3(256), 0, stream, static_cast<const float*>(x), M_max, rows, H, amax, err);
     case RPP_F16:
-      amax_kernel<__half><<<static_cast<int>(blocks), 256, 0, stream>>>(static_cast<const __half*>(x), M_max, rows,
-                                                                         H, amax, err);
-      break;
+      return launch_pdl(amax_kernel<__half>, grid, dim3(256), 0, stream, static_cast<const __half*>(x), M_max, rows, H, amax, err);
     case RPP_BF16:
-      amax_kernel<__nv_bfloat16><<<static_cast<int>(blocks), 256, 0, stream>>>(
-          static_cast<const __nv_bfloat16*>(x), M_max, rows, H, amax, err);
-      break;
+      return launch_pdl(amax_kernel<__nv_bfloat16>, grid, dim3(256), 0, stream, static_cast<const __nv_bfloat16*>(x),
+                        M_max, rows, H, amax, err);
     default: return cudaErrorNotSupported;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace rpp

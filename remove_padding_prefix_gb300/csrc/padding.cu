@@ -17,6 +17,8 @@ __global__ void __launch_bounds__(kScanThreads) build_offsets_kernel(const int32
                                                                      int L, int32_t* __restrict__ cu,
                                                                      int32_t* __restrict__ padding_offset,
                                                                      int32_t* err) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int32_t warp_sums[kScanThreads / 32];
   __shared__ int32_t s_carry;
   const int tid = threadIdx.x;
@@ -76,6 +78,8 @@ __global__ void __launch_bounds__(kScanThreads) build_offsets_kernel(const int32
 __global__ void remove_padding_kernel(const uint4* __restrict__ padded, const int32_t* __restrict__ po,
                                       const int32_t* __restrict__ cu, int B, int T_max, int vpr,
                                       uint4* __restrict__ packed, int32_t* err) {
+  pdl_wait();
+  pdl_trigger();
   if (device_error_set(err)) return;
   int T = cu[B];
   if (T > T_max || T < 0) {
@@ -99,6 +103,8 @@ __global__ void remove_padding_kernel(const uint4* __restrict__ padded, const in
 // padded[b*L + p] = p < len_b ? packed[cu[b] + p] : 0
 __global__ void rebuild_padding_kernel(const uint4* __restrict__ packed, const int32_t* __restrict__ cu, int B,
                                        int L, int vpr, uint4* __restrict__ padded, int32_t* err) {
+  pdl_wait();
+  pdl_trigger();
   if (device_error_set(err)) return;
   const long long total = static_cast<long long>(B) * L * vpr;
   for (long long v = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; v < total;
@@ -127,6 +133,8 @@ __global__ void __launch_bounds__(kFusedThreads) offsets_remove_kernel(const int
                                                                        int32_t* __restrict__ cu,
                                                                        int32_t* __restrict__ po,
                                                                        uint4* __restrict__ packed, int32_t* err) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int32_t s_cu[kFusedMaxB + 1];
   __shared__ int32_t s_warp[kFusedThreads / 32];
   const int tid = threadIdx.x;
@@ -176,6 +184,8 @@ __global__ void __launch_bounds__(kFusedThreads) offsets_remove_kernel(const int
   __syncthreads();
   if (blockIdx.x == 0)
     for (int b = tid; b <= B; b += kFusedThreads) cu[b] = s_cu[b];
+  pdl_wait();
+  pdl_trigger();
   if (device_error_set(err)) return;
   // copy the valid rows; padded row r = b*L + p goes to packed row cu[b] + p
   const long long total = static_cast<long long>(B) * L * vpr;
@@ -206,15 +216,13 @@ cudaError_t launch_offsets_remove(const int32_t* lengths, int B, int L, int row_
   const long long cap = static_cast<long long>(num_sms()) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  offsets_remove_kernel<<<static_cast<int>(blocks), kFusedThreads, 0, stream>>>(
-      lengths, B, L, vpr, static_cast<const uint4*>(padded), cu, po, static_cast<uint4*>(packed), err);
-  return cudaGetLastError();
+  return launch_pdl(offsets_remove_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kFusedThreads), 0, stream,
+                    lengths, B, L, vpr, static_cast<const uint4*>(padded), cu, po, static_cast<uint4*>(packed), err);
 }
 
 cudaError_t launch_build_offsets(const int32_t* lengths, int B, int L, int32_t* cu, int32_t* po, int32_t* err,
                                  cudaStream_t stream) {
-  build_offsets_kernel<<<1, kScanThreads, 0, stream>>>(lengths, B, L, cu, po, err);
-  return cudaGetLastError();
+  return launch_pdl(build_offsets_kernel, dim3(1), dim3(kScanThreads), 0, stream, lengths, B, L, cu, po, err);
 }
 
 cudaError_t launch_remove_padding(const void* padded, const int32_t* po, const int32_t* cu, int B, int L,
@@ -226,9 +234,8 @@ cudaError_t launch_remove_padding(const void* padded, const int32_t* po, const i
   const long long cap = static_cast<long long>(num_sms()) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  remove_padding_kernel<<<static_cast<int>(blocks), threads, 0, stream>>>(
-      static_cast<const uint4*>(padded), po, cu, B, B * L, vpr, static_cast<uint4*>(packed), err);
-  return cudaGetLastError();
+  return launch_pdl(remove_padding_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream,
+                    static_cast<const uint4*>(padded), po, cu, B, B * L, vpr, static_cast<uint4*>(packed), err);
 }
 
 cudaError_t launch_rebuild_padding(const void* packed, const int32_t* cu, int B, int L, int row_bytes,
@@ -240,9 +247,8 @@ cudaError_t launch_rebuild_padding(const void* packed, const int32_t* cu, int B,
   const long long cap = static_cast<long long>(num_sms()) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  rebuild_padding_kernel<<<static_cast<int>(blocks), threads, 0, stream>>>(
-      static_cast<const uint4*>(packed), cu, B, L, vpr, static_cast<uint4*>(padded), err);
-  return cudaGetLastError();
+  return launch_pdl(rebuild_padding_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream,
+                    static_cast<const uint4*>(packed), cu, B, L, vpr, static_cast<uint4*>(padded), err);
 }
 
 }  // namespace rpp

@@ -73,6 +73,8 @@ __global__ void weight_quant_kernel(const void* w, rpp_dtype dt, int K, int N, c
 template <typename T>
 __global__ void codes_bf16_kernel(const T* __restrict__ x, const float* scale, __nv_bfloat16* __restrict__ codes,
                                   int M_max, const int32_t* rows, int H, int32_t* err) {
+  pdl_wait();
+  pdl_trigger();
   if (device_error_set(err)) return;
   int M = rows ? *rows : M_max;
   if (M > M_max || M < 0) {
@@ -141,20 +143,19 @@ cudaError_t launch_quantize_codes_bf16(const void* x, const float* scale, void* 
                                        int H, rpp_dtype dtype, int32_t* err, cudaStream_t stream) {
   const int g = grid_for(static_cast<long long>(M_max) * H, 256, 8);
   auto* c = static_cast<__nv_bfloat16*>(codes);
+  const dim3 grid(static_cast<unsigned>(g));
   switch (dtype) {
     case RPP_F16:
-      codes_bf16_kernel<__half><<<g, 256, 0, stream>>>(static_cast<const __half*>(x), scale, c, M_max, rows, H, err);
-      break;
+      return launch_pdl(codes_bf16_kernel<__half>, grid, dim3(256), 0, stream, static_cast<const __half*>(x), scale, c,
+                        M_max, rows, H, err);
     case RPP_BF16:
-      codes_bf16_kernel<__nv_bfloat16><<<g, 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(x), scale, c, M_max,
-                                                              rows, H, err);
-      break;
+      return launch_pdl(codes_bf16_kernel<__nv_bfloat16>, grid, dim3(256), 0, stream,
+                        static_cast<const __nv_bfloat16*>(x), scale, c, M_max, rows, H, err);
     case RPP_F32:
-      codes_bf16_kernel<float><<<g, 256, 0, stream>>>(static_cast<const float*>(x), scale, c, M_max, rows, H, err);
-      break;
+      return launch_pdl(codes_bf16_kernel<float>, grid, dim3(256), 0, stream, static_cast<const float*>(x), scale, c,
+                        M_max, rows, H, err);
     default: return cudaErrorNotSupported;
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_i8_to_bf16(const int8_t* src, void* dst, long long n, cudaStream_t stream) {

@@ -79,6 +79,8 @@ __global__ void __launch_bounds__(128) window_attention_kernel(const T* __restri
                                                                const float* __restrict__ bias, T* __restrict__ out,
                                                                int I, int w, int s, int nh, float scale_log2,
                                                                int32_t* err) {
+  pdl_wait();
+  pdl_trigger();
   if (device_error_set(err)) return;
   constexpr int TILE = kWRows * kWD * 2;   // bytes of one 64 x 32 tile
   __shared__ __align__(128) uint8_t sQKV[3 * TILE];
@@ -252,9 +254,8 @@ cudaError_t wa_launch(int B, const void* qkv, const float* bias, void* out, int 
   if (windows > 0x7fffffffLL || nh > 65535) return cudaErrorNotSupported;
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kWD));
   dim3 grid(static_cast<unsigned>(windows), nh);
-  window_attention_kernel<T><<<grid, 128, 0, stream>>>(static_cast<const T*>(qkv), bias, static_cast<T*>(out), I, w,
-                                                       s, nh, scale_log2, err);
-  return cudaGetLastError();
+  return launch_pdl(window_attention_kernel<T>, grid, dim3(128), 0, stream, static_cast<const T*>(qkv), bias,
+                    static_cast<T*>(out), I, w, s, nh, scale_log2, err);
 }
 
 }  // namespace
