@@ -68,9 +68,13 @@ def load_peaks():
     return PEAKS_FALLBACK, "fallback"
 
 
-def src_hash(rel):
-    with open(os.path.join(ROOT, rel), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def src_hash(rels):
+    """Short hash of the sources a traffic figure was measured on (a path or a list)."""
+    h = hashlib.sha256()
+    for rel in ([rels] if isinstance(rels, str) else rels):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def load_traffic():
@@ -447,7 +451,9 @@ def main():
     value = wk.tokens_per_step * args.steps * world / total_s
     value_eager = wk.tokens_per_step * args.steps * world / eager_s
 
-    # ---- per-kernel durations inside the real step (launch-event hook), eager
+    # ---- per-kernel durations inside the real step (launch-event hook).  With graphs
+    # on, the hooked step is captured too (the event records become graph nodes) and
+    # timed on replay, so host launch gaps stay out of the per-kernel times.
     lib = rpp.lib()
     cap = 4096
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(cap)]
@@ -459,23 +465,50 @@ def main():
         raise SystemExit("could not create CUDA events for the launch-event hook")
     reps = max(3, min(args.steps, 10))
     kernels, n_launch_step = {}, None
-    for r in range(reps):
-        flush.fill_(float(r))
-        start = torch.cuda.Event(enable_timing=True)
-        start.record(stream)
+    hook_graph, start, start_inside = None, None, False
+    if graph is not None:
+        try:
+            start = torch.cuda.Event(enable_timing=True, external=True)
+            start_inside = True
+        except TypeError:   # older torch: the start mark is recorded before each replay
+            start = torch.cuda.Event(enable_timing=True)
+        hook_graph = torch.cuda.CUDAGraph()
         lib.rpp_set_launch_events(handles, cap)
         try:
-            wk.step()
+            with torch.cuda.graph(hook_graph):
+                if start_inside:
+                    start.record()
+                wk.step()
         finally:
             n = lib.rpp_launch_event_count()
             labels = [lib.rpp_launch_event_label(i).decode() for i in range(n)]
             lib.rpp_set_launch_events(None, 0)
+        torch.cuda.synchronize()
+        hook_graph.replay()
+        torch.cuda.synchronize()
+    for r in range(reps):
+        flush.fill_(float(r))
+        if hook_graph is not None:
+            if not start_inside:
+                start.record(stream)
+            hook_graph.replay()
+        else:
+            start = torch.cuda.Event(enable_timing=True)
+            start.record(stream)
+            lib.rpp_set_launch_events(handles, cap)
+            try:
+                wk.step()
+            finally:
+                n = lib.rpp_launch_event_count()
+                labels = [lib.rpp_launch_event_label(i).decode() for i in range(n)]
+                lib.rpp_set_launch_events(None, 0)
         torch.cuda.synchronize()
         n_launch_step = n
         prev = start
         for i, lab in enumerate(labels):
             kernels.setdefault(lab, []).append(prev.elapsed_time(evs[i]))
             prev = evs[i]
+    del hook_graph
     peaks, peak_kind = load_peaks()
     per_launch = {}
     for lab, vals in kernels.items():
@@ -494,10 +527,46 @@ def main():
         d.update({"launches_per_step": cnt, "ms_per_launch": ms, "ms_per_step": ms * cnt, "flops": f_, "bytes": b_})
         per_launch[lab] = d
     dom = max(per_launch, key=lambda k: per_launch[k]["ms_per_step"])
-    dd = per_launch[dom]
+    # The dominant kernel alone: events just before and after each of its launches
+    # (the hook's label filter), so the rest of the step keeps its launch overlap and
+    # only this kernel's boundaries carry event records.
+    dom_ms = None
+    if graph is not None:
+        lib.rpp_set_launch_event_filter(dom.encode())
+        lib.rpp_set_launch_events(handles, cap)
+        g3 = torch.cuda.CUDAGraph()
+        try:
+            with torch.cuda.graph(g3):
+                wk.step()
+        finally:
+            n3 = lib.rpp_launch_event_count()
+            lib.rpp_set_launch_events(None, 0)
+            lib.rpp_set_launch_event_filter(None)
+        torch.cuda.synchronize()
+        g3.replay()
+        torch.cuda.synchronize()
+        vals = []
+        for r in range(reps):
+            flush.fill_(float(r))
+            g3.replay()
+            torch.cuda.synchronize()
+            vals += [evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(n3 // 2)]
+        del g3
+        if vals:
+            dom_ms = float(np.mean(vals))
+    dd = dict(per_launch[dom])
+    if dom_ms is not None:
+        f_, b_ = wk.work(dom)
+        dd["ms_per_launch"] = dom_ms
+        if dd["bound"] == "tensor":
+            dd["achieved"] = f_ / (dom_ms * 1e-3) / 1e12
+            dd["frac"] = dd["achieved"] / peaks["bf16_tflops"]
+        else:
+            dd["achieved"] = b_ / (dom_ms * 1e-3) / 1e9
+            dd["frac"] = dd["achieved"] / peaks["hbm_gbs"] if b_ else None
     traffic = None
     ent = load_traffic().get(f"{wk.cfg.name}:{dom}")
-    if ent and ent.get("src_sha") == src_hash(ent["src"]):
+    if ent and ent.get("src_sha") == src_hash(ent["srcs"]):
         traffic = ent["bytes_per_launch"]
     roof = {"kernel": dom, "bound": dd["bound"], "achieved": dd["achieved"],
             "peak": peaks["bf16_tflops"] if dd["bound"] == "tensor" else peaks["hbm_gbs"], "unit": dd["unit"],
@@ -505,7 +574,10 @@ def main():
             "peak_source": (f"{peak_kind} bf16 dense burst (fp16 runs at the same nominal rate)"
                             if dd["bound"] == "tensor" else f"{peak_kind} HBM copy bandwidth"),
             "work_per_launch": dd["flops"] if dd["bound"] == "tensor" else dd["bytes"],
-            "ms_per_launch": dd["ms_per_launch"]}
+            "ms_per_launch": dd["ms_per_launch"],
+            "timing": ("CUDA events just before and after each launch of this kernel inside the captured step "
+                       "(other launches unmarked), graph replays with L2 flushed between them"
+                       if dom_ms is not None else "CUDA events after every launch of an eager step")}
 
     # ---- end to end through host buffers (eager calls of the public API)
     e2e = None
@@ -545,7 +617,10 @@ def main():
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": int(n_launch_step * args.steps) if n_launch_step else None, "clocks": clocks,
                 "value_eager": value_eager, "ms_per_step_eager": 1e3 * eager_s / args.steps,
-                "kernels": per_launch}
+                "kernels": per_launch,
+                "kernel_timing": ("CUDA events recorded as graph nodes after every launch, replayed after the timed "
+                                  "region with the same L2 flush" if graph is not None else
+                                  "CUDA events recorded after every launch of an eager step")}
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

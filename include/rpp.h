@@ -81,10 +81,17 @@ RPP_API rpp_status rpp_get_device_error(const int32_t* err, int32_t* host_code, 
 /* Launch-event hook for profiling (the pages profile with Nsight timelines; this
  * hook lets a caller time each kernel inside the real step with CUDA events).  While
  * enabled, every kernel the path launches is followed by cudaEventRecord(events[i++])
- * on its stream, i < capacity, and its label (e.g. "gemm_fc1") is kept.  `events` is
+ * on its stream, i < capacity, and its label (e.g. "gemm_fc1") is kept; on a stream
+ * under capture the record is an external event node of the graph, so the times can
+ * be read after each replay.  `events` is
  * a host array of cudaEvent_t owned by the caller; capacity 0 disables the hook.
  * Not thread-safe: one profiling caller at a time. */
 RPP_API rpp_status rpp_set_launch_events(void* const* events, int capacity);
+/* Restrict the hook to launches labelled `label` (NULL: every launch, the default).
+ * With a filter, an event is recorded just BEFORE and just after each matching
+ * launch (pairs: even index = start, odd = end), so the rest of the step keeps its
+ * programmatic launch overlap.  RPP_EINVAL if the label is empty or 64+ bytes. */
+RPP_API rpp_status rpp_set_launch_event_filter(const char* label);
 /* Events recorded since the last rpp_set_launch_events; label of the i-th ("" if out of range). */
 RPP_API int rpp_launch_event_count(void);
 RPP_API const char* rpp_launch_event_label(int i);

@@ -39,20 +39,45 @@ inline rpp_status from_cuda(cudaError_t e) {
 // ---------------------------------------------------------------- launch-event hook
 // While enabled (rpp_set_launch_events), every kernel launch of the path is followed
 // by cudaEventRecord of the next caller-provided event on the launch's stream, and its
-// label is kept, so a profiler can time each kernel inside the real step.
+// label is kept, so a profiler can time each kernel inside the real step (eagerly or
+// on replay of a captured graph).
+// With a label filter set, events are recorded only around launches of that label:
+// one just before the launch and one just after, so the other launches of the step
+// keep their programmatic overlap.
 struct LaunchHook {
   cudaEvent_t* events = nullptr;
   int capacity = 0;
   int count = 0;
   const char* labels[4096];
+  char filter[64] = {0};
 };
 LaunchHook g_hook;
 
-inline cudaError_t note(const char* label, cudaStream_t s) {
+inline bool hook_matches(const char* label) {
+  return g_hook.filter[0] == 0 || std::strncmp(label, g_hook.filter, sizeof(g_hook.filter)) == 0;
+}
+
+inline cudaError_t record_next(const char* label, cudaStream_t s) {
   if (g_hook.events && g_hook.count < g_hook.capacity) {
     if (g_hook.count < 4096) g_hook.labels[g_hook.count] = label;
+    // inside stream capture the record becomes an event node of the graph, so the
+    // kernels can be timed on graph replay, free of host launch gaps
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return cudaErrorUnknown;
+    if (cs == cudaStreamCaptureStatusActive)
+      return cudaEventRecordWithFlags(g_hook.events[g_hook.count++], s, cudaEventRecordExternal);
     return cudaEventRecord(g_hook.events[g_hook.count++], s);
   }
+  return cudaSuccess;
+}
+
+inline cudaError_t note_before(const char* label, cudaStream_t s) {
+  if (g_hook.events && g_hook.filter[0] && hook_matches(label)) return record_next(label, s);
+  return cudaSuccess;
+}
+
+inline cudaError_t note(const char* label, cudaStream_t s) {
+  if (g_hook.events && hook_matches(label)) return record_next(label, s);
   return cudaSuccess;
 }
 
@@ -65,6 +90,7 @@ inline cudaError_t note(const char* label, cudaStream_t s) {
 // launch, then (when profiling) record the event that marks its end
 #define RPP_LAUNCH(label, stream, expr)          \
   do {                                           \
+    RPP_TRY(note_before(label, stream));         \
     RPP_TRY(expr);                               \
     RPP_TRY(note(label, stream));                \
   } while (0)
@@ -440,6 +466,17 @@ rpp_status rpp_set_launch_events(void* const* events, int capacity) {
   g_hook.events = capacity > 0 ? reinterpret_cast<cudaEvent_t*>(const_cast<void**>(events)) : nullptr;
   g_hook.capacity = capacity;
   g_hook.count = 0;
+  return RPP_OK;
+}
+
+rpp_status rpp_set_launch_event_filter(const char* label) {
+  if (!label) {
+    g_hook.filter[0] = 0;
+    return RPP_OK;
+  }
+  const size_t n = std::strlen(label);
+  if (n == 0 || n >= sizeof(g_hook.filter)) return RPP_EINVAL;
+  std::memcpy(g_hook.filter, label, n + 1);
   return RPP_OK;
 }
 

@@ -77,21 +77,24 @@ __device__ __forceinline__ int region(int c, int I, int w, int s) { return c < I
 template <typename T>
 __global__ void __launch_bounds__(128) window_attention_kernel(const T* __restrict__ qkv,
                                                                const float* __restrict__ bias, T* __restrict__ out,
-                                                               int I, int w, int s, int nh, float scale_log2,
-                                                               int32_t* err) {
+                                                               int I, int w, int s, int nh, long long n_win,
+                                                               float scale_log2, int32_t* err) {
   pdl_wait();
   pdl_trigger();
   if (device_error_set(err)) return;
+  const long long wid = blockIdx.y + static_cast<long long>(gridDim.y) * blockIdx.z;
+  if (wid >= n_win) return;
   constexpr int TILE = kWRows * kWD * 2;   // bytes of one 64 x 32 tile
   __shared__ __align__(128) uint8_t sQKV[3 * TILE];
   __shared__ int sRow[kWRows];   // raster rows of the window's tokens
   __shared__ int sLab[kWRows];   // region labels in the shifted frame
   const int C = nh * kWD;
   const int N = w * w;
-  const int h = blockIdx.y;
+  // the heads of one window are neighbouring CTAs (x fastest), so the rows they each
+  // read a 64-byte piece of are still in L2 for the others
+  const int h = blockIdx.x;
   const int nWs = I / w;
   const int nW = nWs * nWs;
-  const long long wid = blockIdx.x;
   const int img = static_cast<int>(wid / nW);
   const int wr = static_cast<int>(wid - static_cast<long long>(img) * nW);
   const int wy = wr / nWs, wx = wr - (wr / nWs) * nWs;
@@ -251,11 +254,13 @@ template <typename T>
 cudaError_t wa_launch(int B, const void* qkv, const float* bias, void* out, int nh, int I, int w, int s, int32_t* err,
                       cudaStream_t stream) {
   const long long windows = static_cast<long long>(B) * (I / w) * (I / w);
-  if (windows > 0x7fffffffLL || nh > 65535) return cudaErrorNotSupported;
+  if (windows > 65535LL * 65535LL || nh > 1024) return cudaErrorNotSupported;
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kWD));
-  dim3 grid(static_cast<unsigned>(windows), nh);
+  if (windows == 0) return cudaSuccess;
+  const long long gy = windows < 65535 ? windows : 65535;
+  dim3 grid(nh, static_cast<unsigned>(gy), static_cast<unsigned>((windows + gy - 1) / gy));
   return launch_pdl(window_attention_kernel<T>, grid, dim3(128), 0, stream, static_cast<const T*>(qkv), bias,
-                    static_cast<T*>(out), I, w, s, nh, scale_log2, err);
+                    static_cast<T*>(out), I, w, s, nh, windows, scale_log2, err);
 }
 
 }  // namespace
