@@ -64,6 +64,7 @@ typedef enum rpp_dtype { RPP_F32 = 0, RPP_F16 = 1, RPP_BF16 = 2, RPP_I8 = 3 } rp
 #define RPP_DERR_LENGTH 1   /* a sequence length outside [0, L] or [0, max_len] */
 #define RPP_DERR_TIMEOUT 2  /* a bounded wait inside a kernel gave up (pipeline stall) */
 #define RPP_DERR_ROWS 3     /* cu_seqlens[B] larger than the packed capacity T_max */
+#define RPP_DERR_TMEM 4     /* the CTAs of a paired GEMM got different tensor-memory columns */
 
 typedef void* rpp_stream; /* cudaStream_t */
 
@@ -87,6 +88,15 @@ RPP_API rpp_status rpp_get_device_error(const int32_t* err, int32_t* host_code, 
  * a host array of cudaEvent_t owned by the caller; capacity 0 disables the hook.
  * Not thread-safe: one profiling caller at a time. */
 RPP_API rpp_status rpp_set_launch_events(void* const* events, int capacity);
+/* Tuning knob of the fp16/bf16 tensor-core GEMMs (no counterpart in the pages):
+ * 0 (default) pairs CTAs on neighbouring 128-row tiles into a thread-block cluster
+ * whenever the expected row count exceeds one tile -- each CTA of the pair loads half
+ * of the shared weight tile and multicasts it to both; 1 never pairs; 2 always pairs.
+ * The arithmetic per output element is the same in every mode, except that the
+ * tile shape and K split are chosen per mode, and a different K split changes the
+ * fp32 summation order.  Process-wide, not thread-safe; RPP_EINVAL outside 0..2. */
+RPP_API rpp_status rpp_set_gemm_cluster_mode(int mode);
+
 /* Restrict the hook to launches labelled `label` (NULL: every launch, the default).
  * With a filter, an event is recorded just BEFORE and just after each matching
  * launch (pairs: even index = start, odd = end), so the rest of the step keeps its

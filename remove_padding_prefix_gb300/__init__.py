@@ -17,7 +17,7 @@ import torch
 
 from . import _abi
 from ._abi import (RPP_F32, RPP_F16, RPP_BF16, RPP_I8, RPP_EPI_BIAS, RPP_EPI_BIAS_GELU,  # noqa: F401
-                   RPP_EPI_BIAS_RESIDUAL, RPP_DERR_LENGTH, RPP_DERR_TIMEOUT, RPP_DERR_ROWS, EncoderCfg, LayerSrc,
+                   RPP_EPI_BIAS_RESIDUAL, RPP_DERR_LENGTH, RPP_DERR_TIMEOUT, RPP_DERR_ROWS, RPP_DERR_TMEM, EncoderCfg, LayerSrc,
                    SwinCfg, SwinSrc)
 
 __all__ = [

@@ -13,7 +13,7 @@ LIB_PATH = os.path.join(_PKG, "lib", "librpp.so")
 RPP_OK, RPP_EINVAL, RPP_EUNSUPPORTED, RPP_ECUDA, RPP_EWORKSPACE, RPP_EDEVICE = 0, -1, -2, -3, -4, -5
 RPP_F32, RPP_F16, RPP_BF16, RPP_I8 = 0, 1, 2, 3
 RPP_EPI_BIAS, RPP_EPI_BIAS_GELU, RPP_EPI_BIAS_RESIDUAL = 0, 1, 2
-RPP_DERR_LENGTH, RPP_DERR_TIMEOUT, RPP_DERR_ROWS = 1, 2, 3
+RPP_DERR_LENGTH, RPP_DERR_TIMEOUT, RPP_DERR_ROWS, RPP_DERR_TMEM = 1, 2, 3, 4
 
 vp = C.c_void_p
 i32 = C.c_int
@@ -47,6 +47,7 @@ SIGNATURES = {
     "rpp_version": (i32, []),
     "rpp_set_launch_events": (i32, [C.POINTER(vp), i32]),
     "rpp_set_launch_event_filter": (i32, [C.c_char_p]),
+    "rpp_set_gemm_cluster_mode": (i32, [i32]),
     "rpp_launch_event_count": (i32, []),
     "rpp_launch_event_label": (C.c_char_p, [i32]),
     "rpp_get_device_error": (i32, [vp, C.POINTER(C.c_int32), vp]),

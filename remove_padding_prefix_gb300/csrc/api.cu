@@ -469,6 +469,12 @@ rpp_status rpp_set_launch_events(void* const* events, int capacity) {
   return RPP_OK;
 }
 
+rpp_status rpp_set_gemm_cluster_mode(int mode) {
+  if (mode < 0 || mode > 2) return RPP_EINVAL;
+  set_gemm_cluster_mode(mode);
+  return RPP_OK;
+}
+
 rpp_status rpp_set_launch_event_filter(const char* label) {
   if (!label) {
     g_hook.filter[0] = 0;

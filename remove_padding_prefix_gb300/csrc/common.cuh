@@ -72,31 +72,32 @@ template <> __device__ __forceinline__ uint4 pack16<__nv_bfloat16>(const float* 
 
 // Exact-form GELU, x * Phi(x), evaluated through the complementary error function:
 // with t = |x| / sqrt(2), Phi(x) = 1 - erfc(t) / 2 for x >= 0 and erfc(t) / 2 for x < 0,
-// and erfc(t) = exp(P(t) - t^2), where P is a degree-9 least-squares Chebyshev fit of
-// log(erfcx(t)) = log(exp(t^2) erfc(t)) on [0, 3.9] (fit_gelu.py next to this file).
-// Beyond t = 3.9, erfc < 3.5e-8 and t is clamped.  One exp2 and ten FMAs per element;
-// against the fp64 definition the error is at most 2.4e-7 absolute on [-8, 8] (the fp32
-// rounding of the result itself), far below fp16/bf16 output rounding.
+// so x Phi(x) = x / 2 + |x| (1/2 - e) with e = erfc(t) / 2 for either sign.  And
+// erfc(t) = exp(P(t) - t^2), P a degree-7 least-squares Chebyshev fit of
+// log(erfcx(t)) = log(exp(t^2) erfc(t)) on [0, 3.9]; the base-2 change, the -t^2 and
+// the halving are folded into the coefficients (Q = log2(e) (P - t^2) - 1, from
+// fit_gelu.py next to this file), so e = 2^Q(t).  Beyond t = 3.9, erfc < 3.5e-8 and t
+// is clamped.  One exp2, eight FMAs and three other operations per element; against
+// the fp64 definition the error is at most 6.8e-7 absolute on [-8, 8], far below
+// fp16/bf16 output rounding.
 __device__ __forceinline__ float ex2_approx(float v) {
   float r;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
   return r;
 }
 __device__ __forceinline__ float gelu_erf(float x) {
-  const float t = fminf(fabsf(x) * 0.70710678118654752f, 3.9f);
-  float p = 1.133116712e-06f;
-  p = fmaf(p, t, -2.094374395e-05f);
-  p = fmaf(p, t, 1.468409901e-04f);
-  p = fmaf(p, t, -3.269368608e-04f);
-  p = fmaf(p, t, -2.036793623e-03f);
-  p = fmaf(p, t, 2.131437883e-02f);
-  p = fmaf(p, t, -1.039965749e-01f);
-  p = fmaf(p, t, 3.637310565e-01f);
-  p = fmaf(p, t, -1.128418565e+00f);
-  p = fmaf(p, t, 7.335769396e-07f);
-  const float ec = ex2_approx((p - t * t) * 1.4426950408889634f);   // erfc(t)
-  const float h = 0.5f * x * ec;
-  return x > 0.f ? x - h : h;
+  const float ax = fabsf(x);
+  const float t = fminf(ax * 0.70710678118654752f, 3.9f);
+  float q = -2.174795191e-05f;
+  q = fmaf(q, t, 5.064556026e-04f);
+  q = fmaf(q, t, -5.337523762e-03f);
+  q = fmaf(q, t, 3.422686458e-02f);
+  q = fmaf(q, t, -1.528851390e-01f);
+  q = fmaf(q, t, -9.167622924e-01f);
+  q = fmaf(q, t, -1.628153682e+00f);
+  q = fmaf(q, t, -9.999938607e-01f);
+  const float e = ex2_approx(q);   // erfc(t) / 2
+  return fmaf(ax, 0.5f - e, 0.5f * x);
 }
 
 // ---------------------------------------------------------------- shared memory / mbarrier
@@ -170,7 +171,108 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// Load for a CTA pair (cta_group::2): the data lands in this CTA's shared memory,
+// the complete_tx goes to `bar_cluster`, an mbarrier in either CTA of the pair
+// (a shared::cluster address, e.g. from mapa).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar_cluster, int x,
+                                                 int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
+}
+
+// ---------------------------------------------------------------- thread-block clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// every thread of every CTA of the cluster; release/acquire orders shared-memory
+// writes (and mbarrier inits) before the barrier with reads after it
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// shared::cluster address of the object at the offset of `local`, in CTA `rank`
+__device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  return remote;
+}
+// 32-bit store into the shared memory of CTA `rank` of the cluster, at the offset
+// of `local` in this CTA
+__device__ __forceinline__ void st_shared_remote(const void* local, uint32_t rank, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr(local, rank)), "r"(v) : "memory");
+}
+// arrive (relaxed, cluster scope) on an mbarrier given by its shared::cluster address:
+// for signals that order no memory accesses of this thread (e.g. tensor-memory reads
+// already waited for and fenced with tcgen05.fence::before_thread_sync)
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
+// Every tcgen05 instruction of a kernel uses one cta_group: 1 (this CTA) or 2 (a CTA
+// pair of a cluster: the allocation is collective over one warp of each CTA, and an
+// MMA issued by the even CTA spans both CTAs' shared and tensor memory).
+template <int CG>
+__device__ __forceinline__ void tmem_alloc_cg(uint32_t* dst_smem, uint32_t ncols) {   // whole warp
+  if constexpr (CG == 1)
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+template <int CG>
+__device__ __forceinline__ void tmem_relinquish_cg() {   // whole warp
+  if constexpr (CG == 1)
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  else
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+template <int CG>
+__device__ __forceinline__ void tmem_dealloc_cg(uint32_t taddr, uint32_t ncols) {   // whole warp
+  if constexpr (CG == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+template <int CG>
+__device__ __forceinline__ void tc_mma_f16_cg(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  if constexpr (CG == 1)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// arrive on the mbarrier at this offset in every CTA of cta_mask (CG == 2) or in this
+// CTA (CG == 1) once the tcgen05 ops issued so far by this thread have completed
+template <int CG>
+__device__ __forceinline__ void tc_commit_cg(uint64_t* bar, uint16_t cta_mask) {
+  if constexpr (CG == 1)
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+  else
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {   // whole warp
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
                "r"(ncols)

@@ -10,17 +10,27 @@
 // written for the 5th-generation tensor cores:
 //
 //   warp 0      TMA producer: 2D tiled loads with 128-byte swizzle of a 128 x 64 A
-//               tile and a BN x 64 W tile per pipeline stage (no multicast).
+//               tile and a BN x 64 W tile per pipeline stage.
 //   warp 1      allocates tensor memory and issues tcgen05.mma (M = 128, N = BN,
 //               K = 16 per instruction) from one thread; tcgen05.commit releases the
 //               smem stage and, after the last K block, signals the accumulator.
-//   warps 2..9  epilogue: two warps per tensor-memory lane quadrant, each taking every
-//               other 32-column slice: tcgen05.ld 32 lanes x 32 columns (one row per
-//               thread), the epilogue arithmetic in fp32, then the 32 x 32 block goes
-//               to a swizzled staging buffer in shared memory and leaves with one TMA
-//               bulk-tensor store -- coalesced, asynchronous, no per-row scatter.
-//               Tiles that straddle the row count M (the ragged last tile), 16-column
-//               tails and the residual epilogue use per-row 16-byte stores instead.
+
+//   warps 2..   epilogue: 8 or 16 warps, two or four per tensor-memory lane quadrant,
+//               each taking every second or fourth 32-column slice: tcgen05.ld 32 lanes
+//               x 32 columns (one row per thread), the epilogue arithmetic in fp32, then
+//               the 32 x 32 block goes to a swizzled staging buffer in shared memory and
+//               leaves with one TMA bulk-tensor store -- coalesced, asynchronous, no
+//               per-row scatter.  Tiles that straddle the row count M (the ragged last
+//               tile) and 16-column tails use per-row 16-byte stores instead.
+//
+// CTA pairs: for long-K GEMMs over many row tiles, two CTAs of a cluster compute a
+// 256 x BN tile with cta_group::2 MMAs.  Each CTA loads its own 128 A rows and half of
+// the W tile (BN / 2 rows), both completing on the even CTA's barrier; the even CTA
+// issues M = 256 MMAs that read both CTAs' shared memory and write each CTA's 128
+// accumulator rows into its own tensor memory; commits are multicast to both CTAs'
+// barriers and both CTAs' epilogue warps release the accumulator on the even CTA's
+// barrier.  Shared-memory operand traffic per MMA drops from (128 + BN) to
+// (128 + BN / 2) rows per CTA.
 //
 // Epilogues: bias | bias + GELU | bias + residual | raw fp32 accumulator (the encoder
 // layer's proj / FC2: bias and residual are added by the LayerNorm that reads the
@@ -54,10 +64,22 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;   // 64 x 16-bit = 128 bytes = one swizzle row
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+// epilogue warps: 16 for the arithmetic-heavy bias + GELU epilogue (four per
+// tensor-memory lane quadrant: its per-element math is issue-bound), 8 for the others
+template <int EPI>
+constexpr int epi_warps() {
+  return EPI == RPP_EPI_BIAS_GELU ? 16 : 8;
+}
+template <int EPI>
+constexpr bool kHoistBias = EPI == RPP_EPI_BIAS || EPI == RPP_EPI_BIAS_GELU;
+template <int EPI>
+constexpr int gemm_threads() {
+  return 64 + 32 * epi_warps<EPI>();
+}
 constexpr int kChunkBlocks = 16;   // 16 x 64 = 1024 K per exact integer chunk
 constexpr size_t kSmemLimit = 232448;   // 227 KB per CTA
+constexpr uint16_t kPairMask = 0x3;      // both CTAs of a pair
+constexpr int kPairTmemCols = 512;       // tensor-memory columns a CTA pair allocates at most
 
 struct GemmParams {
   int M_max;
@@ -112,14 +134,24 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// wait until at most N of this thread's bulk store groups are still reading shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Epilogue arithmetic on NV columns of this thread's row (v holds the accumulator;
 // for int8 epilogues the exact integer sum converted to float).
+template <int EPI>
+constexpr bool has_bias() {
+  return EPI == RPP_EPI_BIAS || EPI == RPP_EPI_BIAS_GELU || EPI == RPP_EPI_BIAS_RESIDUAL || EPI == EPI_DQ_BIAS ||
+         EPI == EPI_DQ_BIAS_GELU_Q;
+}
+
 template <typename TOut, typename TRes, int EPI, int NV>
 __device__ __forceinline__ void epi_math(const GemmParams& p, float* v, int row, int n, bool first, float a_s,
-                                         float inv_q, const uint4* rres = nullptr) {
+                                         float inv_q, const uint4* rres = nullptr, const float4* bpre = nullptr) {
   if constexpr (EPI == EPI_I32 || EPI == EPI_ACC) return;
   if constexpr (EPI == EPI_DQ_BIAS || EPI == EPI_DQ_ACC || EPI == EPI_DQ_BIAS_GELU_Q) {
     const float4* s4 = reinterpret_cast<const float4*>(p.w_scale + n);
@@ -132,12 +164,12 @@ __device__ __forceinline__ void epi_math(const GemmParams& p, float* v, int row,
       v[4 * j + 3] *= a_s * ss.w;
     }
   }
-  if constexpr (EPI != EPI_DQ_ACC) {
+  if constexpr (has_bias<EPI>()) {
     if (first) {
       const float4* b4 = reinterpret_cast<const float4*>(p.bias + n);
 #pragma unroll
       for (int j = 0; j < NV / 4; ++j) {
-        const float4 bb = __ldg(b4 + j);
+        const float4 bb = bpre ? bpre[j] : __ldg(b4 + j);
         v[4 * j + 0] += bb.x;
         v[4 * j + 1] += bb.y;
         v[4 * j + 2] += bb.z;
@@ -237,46 +269,61 @@ __device__ __forceinline__ void stage_row(uint8_t* stage, int r, const float* v,
   }
 }
 
-constexpr size_t stage_bytes(int bn) { return kBM * kBK * 2 + ((bn * kBK * 2 + 1023) & ~1023); }
-constexpr size_t smem_bytes(int bn, int stages, size_t epi_total) {
-  return 1024 + stages * stage_bytes(bn) + epi_total + 256;
+// one pipeline stage: the 128-row A tile and this CTA's part of the W tile (all of it,
+// or half of it in a CTA pair)
+constexpr size_t stage_bytes(int bn, int cl) { return kBM * kBK * 2 + ((bn / cl * kBK * 2 + 1023) & ~1023); }
+constexpr size_t smem_bytes(int bn, int cl, int stages, size_t epi_total) {
+  return 1024 + stages * stage_bytes(bn, cl) + epi_total + 256;
+}
+// staging blocks per epilogue warp: two for 2-byte outputs with 8 epilogue warps (a
+// block is refilled while the store of the other is still reading it), else one
+template <typename TOut, int EPI>
+constexpr int epi_bufs() {
+  return (sizeof(TOut) == 2 && epi_warps<EPI>() == 8) ? 2 : 1;
 }
 template <typename TOut, int EPI>
 constexpr size_t epi_stage_total() {
-  return tma_store_epi<EPI>() ? kEpiWarps * 32 * 32 * sizeof(TOut) : 0;
+  return tma_store_epi<EPI>() ? epi_warps<EPI>() * epi_bufs<TOut, EPI>() * 32 * 32 * sizeof(TOut) : 0;
 }
 // pipeline depth: as many stages (<= 8) as fit next to the epilogue staging blocks
-template <typename TOut, int BN, int EPI>
+template <typename TOut, int BN, int EPI, int CL>
 constexpr int stages_for() {
   const size_t avail = kSmemLimit - 1024 - 256 - epi_stage_total<TOut, EPI>();
-  const size_t s = avail / stage_bytes(BN);
+  const size_t s = avail / stage_bytes(BN, CL);
   return s > 8 ? 8 : static_cast<int>(s);
 }
 
-template <typename TIn, typename TOut, typename TRes, int BN, int STAGES, int EPI, int NCH>
-__global__ void __launch_bounds__(kThreads, 1)
+template <typename TIn, typename TOut, typename TRes, int BN, int STAGES, int EPI, int NCH, int CL>
+__global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmC, GemmParams p) {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
+  static_assert(CL == 1 || CL == 2, "one CTA or a CTA pair");
   constexpr uint32_t A_BYTES = kBM * kBK * 2;
-  constexpr uint32_t B_BYTES = BN * kBK * 2;
-  constexpr uint32_t B_BYTES_AL = (B_BYTES + 1023u) & ~1023u;
-  constexpr uint32_t STAGE_TX = A_BYTES + B_BYTES;
+  constexpr uint32_t B_PART = BN / CL * kBK * 2;   // bytes of the W tile held by this CTA
+  static_assert(CL == 1 || B_PART % 1024 == 0, "each CTA's half of the W tile is whole 8-row swizzle atoms");
+  constexpr uint32_t B_BYTES_AL = (B_PART + 1023u) & ~1023u;
+  // bytes the (leader's) full barrier of a stage waits for: every CTA's A tile and W part
+  constexpr uint32_t STAGE_TX = CL * (A_BYTES + B_PART);
   constexpr int ACC = (BN + 31) / 32 * 32;               // columns per accumulator region
-  constexpr int NBUF = (2 * NCH * ACC <= 512) ? 2 : 1;  // accumulator buffers in tensor memory
-  static_assert(NCH * ACC <= 512, "tensor memory columns");
+  constexpr int TMEM_LIMIT = CL == 1 ? 512 : kPairTmemCols;
+  constexpr int NBUF = (2 * NCH * ACC <= TMEM_LIMIT) ? 2 : 1;  // accumulator buffers in tensor memory
+  static_assert(NCH * ACC <= TMEM_LIMIT, "tensor memory columns");
   constexpr uint32_t TMEM_COLS = pow2_cols(NBUF * NCH * ACC);
-  constexpr uint32_t IDESC = idesc_f16(AbFmt<TIn>::v, kBM, BN);
+  constexpr uint32_t IDESC = idesc_f16(AbFmt<TIn>::v, kBM * CL, BN);   // M = 256 across a CTA pair
   constexpr bool kTma = tma_store_epi<EPI>();
-  constexpr uint32_t EPI_STAGE = kTma ? 32 * 32 * sizeof(TOut) : 0;   // per epilogue warp
+  constexpr uint32_t EPI_STAGE = kTma ? 32 * 32 * sizeof(TOut) : 0;   // one staging block
+  constexpr int EPI_BUFS = epi_bufs<TOut, EPI>();
+  constexpr int EW = epi_warps<EPI>();
+  constexpr int WPQ = EW / 4;   // epilogue warps per tensor-memory lane quadrant
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled tiles
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  uint8_t* sEpi = sB + STAGES * B_BYTES_AL;   // kEpiWarps staging blocks (1024-aligned)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + kEpiWarps * EPI_STAGE);
+  uint8_t* sEpi = sB + STAGES * B_BYTES_AL;   // EW x EPI_BUFS staging blocks (1024-aligned)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + EW * EPI_BUFS * EPI_STAGE);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* tfull = bars + 2 * STAGES;
@@ -284,40 +331,47 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // [M, skip, tensor-memory base] as decided by CTA rank 0 of the pair; [3]: mismatch seen
+  int* cl_info = const_cast<int*>(abort_flag) + 1;
 
   const int warp = warp_id();
   const int lane = lane_id();
+  const uint32_t rank = CL > 1 ? cluster_ctarank() : 0u;
+  const int cid = blockIdx.x / CL;         // pair (cluster) index
+  const int ncl = gridDim.x / CL;          // pairs in the grid
+  const bool leader = rank == 0;           // issues the MMAs of the pair
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&full[s], 1);     // in a pair only the leader's is used
+      mbar_init(&empty[s], 1);    // released by the (leader's) MMA commit
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], kEpiWarps * 32);
+      mbar_init(&tempty[a], CL * EW);   // one arrival per epilogue warp of the pair
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
+    cl_info[3] = 0;
     fence_mbarrier_init();
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if constexpr (kTma) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_cg<CL>(tmem_slot, TMEM_COLS);
+    tmem_relinquish_cg<CL>();
   }
   if (threadIdx.x == 32) {
     // The weights are never written by the preceding kernel: warm L2 with this CTA's
     // first weight boxes while that kernel drains.  The (tile, split) order puts the
-    // column block of unit blockIdx.x at (unit / S) % num_n regardless of M.
+    // column block of unit `cid` at (unit / S) % num_n regardless of M.
     const int nn = p.N / BN;
     const int nk = (p.K + kBK - 1) / kBK;
     const int kps0 = (nk + p.splits - 1) / p.splits;
-    const int t0 = blockIdx.x / p.splits;
-    const int kb0 = (blockIdx.x - t0 * p.splits) * kps0;
-    const int n0 = (t0 % nn) * BN;
+    const int t0 = cid / p.splits;
+    const int kb0 = (cid - t0 * p.splits) * kps0;
+    const int n0 = (t0 % nn) * BN + static_cast<int>(rank) * (BN / CL);
     const int kb1 = min(nk, kb0 + min(kps0, STAGES));
     for (int kb = kb0; kb < kb1; ++kb) tma_prefetch_l2_2d(&tmB, kb * kBK, n0);
   }
@@ -330,31 +384,62 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   pdl_trigger();
 
   int M = p.M_max;
-  bool skip = device_error_set(p.err);
-  if (p.rows) {
-    M = *p.rows;
-    if (M > p.M_max || M < 0) {
-      if (threadIdx.x == 0) set_device_error(p.err, RPP_DERR_ROWS);
-      skip = true;
+  bool skip = false;
+  if (CL == 1 || rank == 0) {
+    skip = device_error_set(p.err);
+    if (p.rows) {
+      M = *p.rows;
+      if (M > p.M_max || M < 0) {
+        if (threadIdx.x == 0) set_device_error(p.err, RPP_DERR_ROWS);
+        skip = true;
+      }
     }
   }
+  if constexpr (CL > 1) {
+    // One decision for the pair (both CTAs must run the same units): rank 0 publishes
+    // M and skip into both CTAs' shared memory.  The first barrier also makes the
+    // leader's mbarrier inits visible before the partner's loads signal them.
+    cluster_sync();
+    if (rank == 0 && threadIdx.x == 0) {
+      for (uint32_t r = 0; r < CL; ++r) {
+        st_shared_remote(cl_info, r, static_cast<uint32_t>(M));
+        st_shared_remote(cl_info + 1, r, skip ? 1u : 0u);
+        st_shared_remote(cl_info + 2, r, tmem_base);
+      }
+    }
+    cluster_sync();
+    M = cl_info[0];
+    skip = cl_info[1] != 0;
+    // the leader's MMAs write both CTAs' tensor memory at the leader's column address:
+    // the collective allocation must have given both CTAs the same one
+    if (rank != 0 && threadIdx.x == 0 && static_cast<uint32_t>(cl_info[2]) != tmem_base) {
+      set_device_error(p.err, RPP_DERR_TMEM);
+      for (uint32_t r = 0; r < CL; ++r) st_shared_remote(cl_info + 3, r, 1u);
+    }
+    cluster_sync();
+    if (cl_info[3]) skip = true;
+  }
   const int num_m = skip ? 0 : (M + kBM - 1) / kBM;
+  const int num_mc = (num_m + CL - 1) / CL;     // row-tile groups (one 128-row tile per CTA of a pair)
   const int num_n = p.N / BN;
   const int num_k = (p.K + kBK - 1) / kBK;
   const int S = p.splits;
   const int kps = (num_k + S - 1) / S;          // K blocks per split
-  const int total = num_m * num_n * S;          // work units: (tile, split)
+  const int total = num_mc * num_n * S;         // work units of a pair: (row-tile group, column tile, split)
+  // row tile of this CTA in unit u's group; the last group of an odd count has an
+  // empty second tile (its rows are >= M: loaded, computed, never stored)
+  auto m_tile = [&](int u) { return ((u / S) / num_n) * CL + static_cast<int>(rank); };
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int unit = blockIdx.x; unit < total && ok; unit += gridDim.x) {
+      for (int unit = cid; unit < total && ok; unit += ncl) {
         const int tile = unit / S;
         const int kb0 = (unit - tile * S) * kps;
         const int kb1 = min(num_k, kb0 + kps);
-        const int m0 = (tile / num_n) * kBM;
+        const int m0 = m_tile(unit) * kBM;
         const int n0 = (tile % num_n) * BN;
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const uint32_t s = it % STAGES;
@@ -363,9 +448,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[s], STAGE_TX);
-          tma_load_2d(sA + s * A_BYTES, &tmA, &full[s], kb * kBK, m0);
-          tma_load_2d(sB + s * B_BYTES_AL, &tmB, &full[s], kb * kBK, n0);
+          if constexpr (CL == 1) {
+            mbar_arrive_expect_tx(&full[s], STAGE_TX);
+            tma_load_2d(sA + s * A_BYTES, &tmA, &full[s], kb * kBK, m0);
+            tma_load_2d(sB + s * B_BYTES_AL, &tmB, &full[s], kb * kBK, n0);
+          } else {
+            // both CTAs load their A tile and their half of the W tile into their own
+            // shared memory; every copy completes on the leader's full barrier
+            if (leader) mbar_arrive_expect_tx(&full[s], STAGE_TX);
+            const uint32_t fb = cluster_addr(&full[s], 0);
+            tma_load_2d_pair(sA + s * A_BYTES, &tmA, fb, kb * kBK, m0);
+            tma_load_2d_pair(sB + s * B_BYTES_AL, &tmB, fb, kb * kBK, n0 + static_cast<int>(rank) * (BN / CL));
+          }
         }
       }
       if (!ok) {
@@ -373,15 +467,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         *abort_flag = 1;
       }
       // wait (bounded) for the copies still in flight: the last min(it, STAGES) loads
-      const uint32_t first = it > STAGES ? it - STAGES : 0;
-      for (uint32_t j = first; j < it; ++j) mbar_wait_bounded(&full[j % STAGES], (j / STAGES) & 1u, nullptr);
+      // (a pair's partner: the leader waits for them, and the pair meets at the end)
+      if (leader) {
+        const uint32_t first = it > STAGES ? it - STAGES : 0;
+        for (uint32_t j = first; j < it; ++j) mbar_wait_bounded(&full[j % STAGES], (j / STAGES) & 1u, nullptr);
+      }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer (the leader's)
+    if (lane == 0 && leader) {
       uint32_t it = 0, acc_it = 0;
       bool ok = true;
-      for (int unit = blockIdx.x; unit < total && ok; unit += gridDim.x, ++acc_it) {
+      for (int unit = cid; unit < total && ok; unit += ncl, ++acc_it) {
         const int tile = unit / S;
         const int kb0 = (unit - tile * S) * kps;
         const int kb1 = min(num_k, kb0 + kps);
@@ -408,32 +505,34 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             // +32 bytes along K inside the swizzled 128-byte row = +2 in the address field
-            tc_mma_f16(d_tmem, adesc + 2u * k, bdesc + 2u * k, IDESC, (kb_in | k) != 0 ? 1u : 0u);
+            tc_mma_f16_cg<CL>(d_tmem, adesc + 2u * k, bdesc + 2u * k, IDESC, (kb_in | k) != 0 ? 1u : 0u);
           }
-          tc_commit(&empty[s]);
+          // the stage is free in every CTA of the pair once these MMAs are done
+          tc_commit_cg<CL>(&empty[s], kPairMask);
         }
-        if (ok) tc_commit(&tfull[a]);
+        if (ok) tc_commit_cg<CL>(&tfull[a], kPairMask);
       }
       if (!ok) {
         set_device_error(p.err, RPP_DERR_TIMEOUT);
         *abort_flag = 1;
       }
       // all MMAs issued by this thread complete before tensor memory is released
-      tc_commit(drain);
+      tc_commit_cg<CL>(drain, 1u);
       mbar_wait_bounded(drain, 0, nullptr);
     }
   } else {
     // ------------------------------------------------------------ epilogue warps
     const int q = warp & 3;               // tensor-memory lane quadrant of this warp
-    const int half = (warp - 2) >> 2;     // which of the two warps of this quadrant
+    const int part = (warp - 2) >> 2;     // which of the WPQ warps of this quadrant
     const int r_in_tile = q * 32 + lane;
-    uint8_t* stage = sEpi + (warp - 2) * EPI_STAGE;
+    uint8_t* stage0 = sEpi + (warp - 2) * EPI_BUFS * EPI_STAGE;
+    int sb = 0;   // staging block of the next store
     float a_s = 1.f, inv_q = 0.f;
     if constexpr (EPI == EPI_DQ_BIAS || EPI == EPI_DQ_ACC || EPI == EPI_DQ_BIAS_GELU_Q) a_s = *p.a_scale;
     if constexpr (EPI == EPI_DQ_BIAS_GELU_Q) inv_q = __fdiv_rn(1.0f, *p.q_scale);
     uint32_t acc_it = 0;
     bool pending_store = false;
-    for (int unit = blockIdx.x; unit < total; unit += gridDim.x, ++acc_it) {
+    for (int unit = cid; unit < total; unit += ncl, ++acc_it) {
       const int tile = unit / S;
       const int split = unit - tile * S;
       const int kb0 = split * kps;
@@ -444,13 +543,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       // residual of this warp's first 32-column slice, requested before the accumulator wait
       constexpr int RV = res_vecs32<TRes>();
       uint4 rnext[RV];
-      const int pre_m0 = (unit / S / num_n) * kBM;
+      const int pre_m0 = m_tile(unit) * kBM;
       const int pre_n0 = (unit / S % num_n) * BN;
       const int pre_row = pre_m0 + r_in_tile;
       if constexpr (EPI == RPP_EPI_BIAS_RESIDUAL && BN >= 32) {
-        if (pre_row < M && half < BN / 32) {
+        if (pre_row < M && part < BN / 32) {
           const uint4* rr = reinterpret_cast<const uint4*>(static_cast<const TRes*>(p.residual) +
-                                                           static_cast<long long>(pre_row) * p.N + pre_n0 + half * 32);
+                                                           static_cast<long long>(pre_row) * p.N + pre_n0 + part * 32);
 #pragma unroll
           for (int j = 0; j < RV; ++j) rnext[j] = rr[j];
         }
@@ -466,7 +565,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         break;
       }
       tc_fence_after();
-      const int m0 = (tile / num_n) * kBM;
+      const int m0 = m_tile(unit) * kBM;
       const int n0 = (tile % num_n) * BN;
       const int row = m0 + r_in_tile;
       const bool row_ok = row < M;
@@ -475,27 +574,36 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + (a * NCH) * ACC;
       if constexpr (BN >= 32) {
 #pragma unroll 1
-        for (int c = half; c < BN / 32; c += 2) {
+        for (int c = part; c < BN / 32; c += WPQ) {
           uint4 rcur[RV];
           if constexpr (EPI == RPP_EPI_BIAS_RESIDUAL) {
 #pragma unroll
             for (int j = 0; j < RV; ++j) rcur[j] = rnext[j];
-            if (row_ok && c + 2 < BN / 32) {   // next slice's residual while this one is processed
+            if (row_ok && c + WPQ < BN / 32) {   // next slice's residual while this one is processed
               const uint4* rr = reinterpret_cast<const uint4*>(static_cast<const TRes*>(p.residual) +
-                                                               static_cast<long long>(row) * p.N + n0 + (c + 2) * 32);
+                                                               static_cast<long long>(row) * p.N + n0 + (c + WPQ) * 32);
 #pragma unroll
               for (int j = 0; j < RV; ++j) rnext[j] = rr[j];
             }
           }
           const uint4* rres = EPI == RPP_EPI_BIAS_RESIDUAL ? rcur : nullptr;
+          const int n = n0 + c * 32;
+          // the bias loads go out before the tensor-memory wait and overlap it
+          float4 bpre[kHoistBias<EPI> ? 8 : 1];
+          if constexpr (kHoistBias<EPI>) {
+            if (first) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) bpre[j] = __ldg(reinterpret_cast<const float4*>(p.bias + n) + j);
+            }
+          }
           float v[32];
           int acc[32];
           load_acc<EPI, NCH, ACC, 32>(t_row + c * 32, nch, v, acc);
-          const int n = n0 + c * 32;
           if (kTma && full_tile) {
-            epi_math<TOut, TRes, EPI, 32>(p, v, row, n, first, a_s, inv_q, rres);
-            if (pending_store) {   // the previous TMA store has finished reading the staging block
-              if (lane == 0) bulk_wait_read0();
+            epi_math<TOut, TRes, EPI, 32>(p, v, row, n, first, a_s, inv_q, rres, kHoistBias<EPI> ? bpre : nullptr);
+            uint8_t* stage = stage0 + sb * EPI_STAGE;
+            if (pending_store) {   // the store that last used this block has finished reading it
+              if (lane == 0) bulk_wait_read<EPI_BUFS - 1>();
               __syncwarp();
             }
             stage_row<TOut, EPI>(stage, lane, v, acc);
@@ -506,14 +614,15 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               bulk_commit();
             }
             pending_store = true;
+            sb = EPI_BUFS > 1 ? sb ^ 1 : 0;
           } else if (row_ok) {
-            epi_math<TOut, TRes, EPI, 32>(p, v, row, n, first, a_s, inv_q, rres);
+            epi_math<TOut, TRes, EPI, 32>(p, v, row, n, first, a_s, inv_q, rres, kHoistBias<EPI> ? bpre : nullptr);
             store_row<TOut, EPI, 32>(p, v, acc, row, n, split);
           }
         }
       }
       if constexpr (BN % 32 == 16) {
-        if (half == ((BN / 32) & 1)) {
+        if (part == (BN / 32) % WPQ) {
           float v[16];
           int acc[16];
           load_acc<EPI, NCH, ACC, 16>(t_row + (BN - 16), nch, v, acc);
@@ -524,8 +633,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
         }
       }
+      // this warp is done with accumulator a (in a pair: tell the leader's barrier)
       tc_fence_before();
-      mbar_arrive(&tempty[a]);
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (CL == 1) mbar_arrive(&tempty[a]);
+        else mbar_arrive_cluster_relaxed(cluster_addr(&tempty[a], 0));
+      }
     }
     if (pending_store && lane == 0) bulk_wait0();   // stores complete before the CTA exits
     __syncwarp();
@@ -533,10 +647,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
   tc_fence_before();
   __syncthreads();
+  // a pair frees its tensor memory together, once both CTAs' epilogues are done and
+  // no copy or arrival of either CTA is still aimed at the other
+  if constexpr (CL > 1) cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_cg<CL>(tmem_base, TMEM_COLS);
   }
 }
 
@@ -585,12 +702,12 @@ template <> struct MapType<__nv_bfloat16> { static constexpr CUtensorMapDataType
 template <> struct MapType<float> { static constexpr CUtensorMapDataType v = CU_TENSOR_MAP_DATA_TYPE_FLOAT32; };
 template <> struct MapType<int32_t> { static constexpr CUtensorMapDataType v = CU_TENSOR_MAP_DATA_TYPE_INT32; };
 
-template <typename TIn, typename TOut, typename TRes, int BN, int EPI, int NCH>
+template <typename TIn, typename TOut, typename TRes, int BN, int EPI, int NCH, int CL>
 cudaError_t gemm_tc_launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int grid_rows,
                            cudaStream_t stream) {
-  constexpr int STAGES = stages_for<TOut, BN, EPI>();
+  constexpr int STAGES = stages_for<TOut, BN, EPI, CL>();
   static_assert(STAGES >= 2, "pipeline depth");
-  constexpr size_t SMEM = smem_bytes(BN, STAGES, epi_stage_total<TOut, EPI>());
+  constexpr size_t SMEM = smem_bytes(BN, CL, STAGES, epi_stage_total<TOut, EPI>());
   static_assert(SMEM <= kSmemLimit, "shared memory per CTA");
   CUtensorMap tc;
   std::memset(&tc, 0, sizeof(tc));
@@ -601,18 +718,51 @@ cudaError_t gemm_tc_launch(const CUtensorMap& ta, const CUtensorMap& tb, const G
                       32, 32, swz))
       return cudaErrorInvalidValue;
   }
-  auto kern = gemm_tc_kernel<TIn, TOut, TRes, BN, STAGES, EPI, NCH>;
+  auto kern = gemm_tc_kernel<TIn, TOut, TRes, BN, STAGES, EPI, NCH, CL>;
   static bool attr_set = false;
+  static int max_clusters = 0;   // clusters of CL CTAs that fit on the GPU at once
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM));
     if (e != cudaSuccess) return e;
+    if constexpr (CL > 1) {
+      cudaLaunchConfig_t oc{};
+      oc.gridDim = dim3(static_cast<unsigned>(num_sms() / CL * CL));
+      oc.blockDim = dim3(gemm_threads<EPI>());
+      oc.dynamicSmemBytes = SMEM;
+      cudaLaunchAttribute oa[1];
+      oa[0].id = cudaLaunchAttributeClusterDimension;
+      oa[0].val.clusterDim.x = CL;
+      oa[0].val.clusterDim.y = 1;
+      oa[0].val.clusterDim.z = 1;
+      oc.attrs = oa;
+      oc.numAttrs = 1;
+      e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &oc);
+      if (e != cudaSuccess) return e;
+    } else {
+      max_clusters = num_sms();
+    }
     attr_set = true;
   }
+  if (max_clusters < 1) return cudaErrorNotSupported;
   const int num_m = (grid_rows + kBM - 1) / kBM;
-  const long long units = static_cast<long long>(num_m) * (p.N / BN) * p.splits;
-  int grid = units < num_sms() ? static_cast<int>(units) : num_sms();
-  if (grid < 1) grid = 1;
-  return launch_pdl(kern, dim3(grid), dim3(kThreads), SMEM, stream, ta, tb, tc, p);
+  const long long units = static_cast<long long>((num_m + CL - 1) / CL) * (p.N / BN) * p.splits;
+  int clusters = units < max_clusters ? static_cast<int>(units) : max_clusters;
+  if (clusters < 1) clusters = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL));
+  cfg.blockDim = dim3(gemm_threads<EPI>());
+  cfg.dynamicSmemBytes = SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CL;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = CL > 1 ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p);
 }
 
 // Tile shape choice (the per-shape GEMM configuration of the Kuaishou article's
@@ -624,10 +774,10 @@ struct TileChoice {
   int splits = 1;
 };
 
-TileChoice choose_tiles(int M, int N, int K, int max_bn, int max_splits) {
+TileChoice choose_tiles(int M, int N, int K, int max_bn, int max_splits, int cl = 1) {
   static const int cands[] = {256, 192, 144, 128, 96, 64, 48, 32, 16};
-  const int sms = num_sms();
-  const int num_m = (M + kBM - 1) / kBM;
+  const int sms = num_sms() / cl;                       // concurrent work units (clusters)
+  const int num_m = (M + kBM * cl - 1) / (kBM * cl);    // row-tile groups
   const int num_k = (K + kBK - 1) / kBK;
   TileChoice best;
   double best_cost = 1e30;
@@ -648,47 +798,49 @@ TileChoice choose_tiles(int M, int N, int K, int max_bn, int max_splits) {
   return best;
 }
 
-template <typename TIn, typename TOut, typename TRes, int EPI, int NCH>
+template <typename TIn, typename TOut, typename TRes, int EPI, int NCH, int CL = 1>
 cudaError_t dispatch_bn(int bn, const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, int gr,
                         cudaStream_t stream) {
   if constexpr (NCH == 1) {
     switch (bn) {
-      case 256: return gemm_tc_launch<TIn, TOut, TRes, 256, EPI, 1>(ta, tb, p, gr, stream);
-      case 192: return gemm_tc_launch<TIn, TOut, TRes, 192, EPI, 1>(ta, tb, p, gr, stream);
-      case 144: return gemm_tc_launch<TIn, TOut, TRes, 144, EPI, 1>(ta, tb, p, gr, stream);
-      case 128: return gemm_tc_launch<TIn, TOut, TRes, 128, EPI, 1>(ta, tb, p, gr, stream);
-      case 96: return gemm_tc_launch<TIn, TOut, TRes, 96, EPI, 1>(ta, tb, p, gr, stream);
-      case 64: return gemm_tc_launch<TIn, TOut, TRes, 64, EPI, 1>(ta, tb, p, gr, stream);
-      case 48: return gemm_tc_launch<TIn, TOut, TRes, 48, EPI, 1>(ta, tb, p, gr, stream);
-      case 32: return gemm_tc_launch<TIn, TOut, TRes, 32, EPI, 1>(ta, tb, p, gr, stream);
-      case 16: return gemm_tc_launch<TIn, TOut, TRes, 16, EPI, 1>(ta, tb, p, gr, stream);
+      case 256: return gemm_tc_launch<TIn, TOut, TRes, 256, EPI, 1, CL>(ta, tb, p, gr, stream);
+      case 192: return gemm_tc_launch<TIn, TOut, TRes, 192, EPI, 1, CL>(ta, tb, p, gr, stream);
+      case 144: return gemm_tc_launch<TIn, TOut, TRes, 144, EPI, 1, CL>(ta, tb, p, gr, stream);
+      case 128: return gemm_tc_launch<TIn, TOut, TRes, 128, EPI, 1, CL>(ta, tb, p, gr, stream);
+      case 96: return gemm_tc_launch<TIn, TOut, TRes, 96, EPI, 1, CL>(ta, tb, p, gr, stream);
+      case 64: return gemm_tc_launch<TIn, TOut, TRes, 64, EPI, 1, CL>(ta, tb, p, gr, stream);
+      case 48: return gemm_tc_launch<TIn, TOut, TRes, 48, EPI, 1, CL>(ta, tb, p, gr, stream);
+      case 32: return gemm_tc_launch<TIn, TOut, TRes, 32, EPI, 1, CL>(ta, tb, p, gr, stream);
+      case 16: return gemm_tc_launch<TIn, TOut, TRes, 16, EPI, 1, CL>(ta, tb, p, gr, stream);
       default: return cudaErrorNotSupported;
     }
   } else {
+    static_assert(CL == 1, "the chunked integer GEMM runs unclustered");
     switch (bn) {   // NCH x BN <= 512 tensor-memory columns
-      case 128: return gemm_tc_launch<TIn, TOut, TRes, 128, EPI, NCH>(ta, tb, p, gr, stream);
-      case 96: return gemm_tc_launch<TIn, TOut, TRes, 96, EPI, NCH>(ta, tb, p, gr, stream);
-      case 64: return gemm_tc_launch<TIn, TOut, TRes, 64, EPI, NCH>(ta, tb, p, gr, stream);
-      case 48: return gemm_tc_launch<TIn, TOut, TRes, 48, EPI, NCH>(ta, tb, p, gr, stream);
-      case 32: return gemm_tc_launch<TIn, TOut, TRes, 32, EPI, NCH>(ta, tb, p, gr, stream);
-      case 16: return gemm_tc_launch<TIn, TOut, TRes, 16, EPI, NCH>(ta, tb, p, gr, stream);
+      case 128: return gemm_tc_launch<TIn, TOut, TRes, 128, EPI, NCH, 1>(ta, tb, p, gr, stream);
+      case 96: return gemm_tc_launch<TIn, TOut, TRes, 96, EPI, NCH, 1>(ta, tb, p, gr, stream);
+      case 64: return gemm_tc_launch<TIn, TOut, TRes, 64, EPI, NCH, 1>(ta, tb, p, gr, stream);
+      case 48: return gemm_tc_launch<TIn, TOut, TRes, 48, EPI, NCH, 1>(ta, tb, p, gr, stream);
+      case 32: return gemm_tc_launch<TIn, TOut, TRes, 32, EPI, NCH, 1>(ta, tb, p, gr, stream);
+      case 16: return gemm_tc_launch<TIn, TOut, TRes, 16, EPI, NCH, 1>(ta, tb, p, gr, stream);
       default: return cudaErrorNotSupported;
     }
   }
 }
 
-template <typename T>
+template <typename T, int CL>
 cudaError_t dispatch_float(int bn, int epi, rpp_dtype out_dtype, rpp_dtype res_dtype, const CUtensorMap& ta,
                            const CUtensorMap& tb, const GemmParams& p, int gr, cudaStream_t stream) {
   switch (epi) {
-    case RPP_EPI_BIAS: return dispatch_bn<T, T, T, RPP_EPI_BIAS, 1>(bn, ta, tb, p, gr, stream);
-    case RPP_EPI_BIAS_GELU: return dispatch_bn<T, T, T, RPP_EPI_BIAS_GELU, 1>(bn, ta, tb, p, gr, stream);
+    case RPP_EPI_BIAS: return dispatch_bn<T, T, T, RPP_EPI_BIAS, 1, CL>(bn, ta, tb, p, gr, stream);
+    case RPP_EPI_BIAS_GELU: return dispatch_bn<T, T, T, RPP_EPI_BIAS_GELU, 1, CL>(bn, ta, tb, p, gr, stream);
     case RPP_EPI_BIAS_RESIDUAL:
       if (out_dtype == RPP_F32 && res_dtype == RPP_F32)
-        return dispatch_bn<T, float, float, RPP_EPI_BIAS_RESIDUAL, 1>(bn, ta, tb, p, gr, stream);
-      if (out_dtype == RPP_F32) return dispatch_bn<T, float, T, RPP_EPI_BIAS_RESIDUAL, 1>(bn, ta, tb, p, gr, stream);
-      return dispatch_bn<T, T, T, RPP_EPI_BIAS_RESIDUAL, 1>(bn, ta, tb, p, gr, stream);
-    case EPI_ACC: return dispatch_bn<T, float, T, EPI_ACC, 1>(bn, ta, tb, p, gr, stream);
+        return dispatch_bn<T, float, float, RPP_EPI_BIAS_RESIDUAL, 1, CL>(bn, ta, tb, p, gr, stream);
+      if (out_dtype == RPP_F32)
+        return dispatch_bn<T, float, T, RPP_EPI_BIAS_RESIDUAL, 1, CL>(bn, ta, tb, p, gr, stream);
+      return dispatch_bn<T, T, T, RPP_EPI_BIAS_RESIDUAL, 1, CL>(bn, ta, tb, p, gr, stream);
+    case EPI_ACC: return dispatch_bn<T, float, T, EPI_ACC, 1, CL>(bn, ta, tb, p, gr, stream);
     default: return cudaErrorNotSupported;
   }
 }
@@ -712,6 +864,12 @@ bool gemm_tc_supported(int N, int K) {
   return K % 8 == 0 && K > 0 && N % 16 == 0 && choose_tiles(1, N, K, 256, 1).bn != 0;
 }
 
+namespace {
+int g_cluster_mode = 0;   // 0 automatic, 1 never, 2 always (where the GEMM has two row tiles)
+}
+
+void set_gemm_cluster_mode(int mode) { g_cluster_mode = mode; }
+
 cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t stream) {
   const bool is_int = g.epi >= EPI_I32 && g.epi <= EPI_DQ_BIAS_GELU_Q;
   const int num_k = (g.K + kBK - 1) / kBK;
@@ -721,7 +879,13 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t stream) {
   // splitting K is only possible for the raw fp32 accumulator output
   const bool can_split = g.max_splits > 1 && g.epi == EPI_ACC;
   const int rows_hint = (g.rows_hint > 0 && g.rows_hint < g.M_max) ? g.rows_hint : g.M_max;
-  TileChoice tc = choose_tiles(rows_hint, g.N, g.K, max_bn, can_split ? g.max_splits : 1);
+  // A CTA pair (a two-CTA thread-block cluster) computes a 256-row tile with
+  // cta_group::2 MMAs issued by the even CTA: each CTA holds its 128 rows of A and
+  // half of the W tile, halving the shared-memory traffic per MMA.
+  // Pairs pay off when the MMAs dominate (long K, many row tiles); short-K or
+  // few-tile GEMMs are epilogue- or latency-bound and run unpaired.
+  int cl = (!is_int && (g_cluster_mode == 2 || (g_cluster_mode == 0 && rows_hint >= 8192 && g.K >= 1024))) ? 2 : 1;
+  TileChoice tc = choose_tiles(rows_hint, g.N, g.K, max_bn, can_split ? g.max_splits : 1, cl);
   if (g.force_bn) tc.bn = g.force_bn;
   const int bn = tc.bn;
   if (!bn || g.N % bn || bn > max_bn) return cudaErrorNotSupported;
@@ -730,18 +894,31 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t stream) {
       (is_int || g.in_dtype == RPP_BF16) ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   CUtensorMap ta, tb;
   if (!make_tmap_2d(&ta, g.a, dt, 2, g.M_max, g.K, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
-  if (!make_tmap_2d(&tb, g.w_t, dt, 2, g.N, g.K, bn, kBK, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
   GemmParams p{g.M_max, g.rows, g.N, g.K, g.bias, g.residual, g.out, g.a_scale, g.w_scale, g.q_scale, g.err,
                tc.splits, static_cast<long long>(g.M_max) * g.N};
   if (is_int) {
+    if (!make_tmap_2d(&tb, g.w_t, dt, 2, g.N, g.K, bn, kBK, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     if (nch == 1) return dispatch_int<1>(bn, g.epi, ta, tb, p, rows_hint, stream);
     return dispatch_int<4>(bn, g.epi, ta, tb, p, rows_hint, stream);
   }
-  if (g.in_dtype == RPP_BF16)
-    return dispatch_float<__nv_bfloat16>(bn, g.epi, g.out_dtype, g.res_dtype, ta, tb, p, rows_hint, stream);
-  if (g.in_dtype == RPP_F16)
-    return dispatch_float<__half>(bn, g.epi, g.out_dtype, g.res_dtype, ta, tb, p, rows_hint, stream);
-  return cudaErrorNotSupported;
+  if (g.in_dtype != RPP_BF16 && g.in_dtype != RPP_F16) return cudaErrorNotSupported;
+  for (;;) {
+    // each CTA of a cluster loads bn / cl rows of the W tile
+    if (!make_tmap_2d(&tb, g.w_t, dt, 2, g.N, g.K, bn / cl, kBK, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    cudaError_t e;
+    if (g.in_dtype == RPP_BF16)
+      e = cl == 2 ? dispatch_float<__nv_bfloat16, 2>(bn, g.epi, g.out_dtype, g.res_dtype, ta, tb, p, rows_hint, stream)
+                  : dispatch_float<__nv_bfloat16, 1>(bn, g.epi, g.out_dtype, g.res_dtype, ta, tb, p, rows_hint, stream);
+    else
+      e = cl == 2 ? dispatch_float<__half, 2>(bn, g.epi, g.out_dtype, g.res_dtype, ta, tb, p, rows_hint, stream)
+                  : dispatch_float<__half, 1>(bn, g.epi, g.out_dtype, g.res_dtype, ta, tb, p, rows_hint, stream);
+    if (e == cudaErrorNotSupported && cl == 2) {   // no pair of SMs available: run unclustered
+      cl = 1;
+      continue;
+    }
+    return e;
+  }
 }
 
 }  // namespace rpp

@@ -100,6 +100,8 @@ struct TcGemmArgs {
 };
 bool gemm_tc_supported(int N, int K);
 cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t stream);
+// 0 automatic, 1 never cluster, 2 cluster whenever the GEMM is fp16/bf16
+void set_gemm_cluster_mode(int mode);
 
 cudaError_t launch_gemm_f32(const float* a, const float* w_t, const float* bias, const float* residual, float* out,
                             int M_max, const int32_t* rows, int N, int K, int epi, int32_t* err, cudaStream_t stream);

@@ -84,3 +84,15 @@ def test_size_queries(lib):
     # workspace too small is reported before any launch
     assert lib.rpp_encoder_layer_forward(C.byref(cfg), 256, None, 256, 256, 4, 512, 128, 256, 256, 16, None,
                                          None) == -4
+
+
+def test_tuning_and_profiling_knobs_validate_on_the_host(lib):
+    assert lib.rpp_set_gemm_cluster_mode(3) == -1
+    assert lib.rpp_set_gemm_cluster_mode(-1) == -1
+    for m in (1, 2, 0):
+        assert lib.rpp_set_gemm_cluster_mode(m) == 0
+    assert lib.rpp_set_launch_event_filter(b"") == -1
+    assert lib.rpp_set_launch_event_filter(b"x" * 64) == -1
+    assert lib.rpp_set_launch_event_filter(b"gemm_fc1") == 0
+    assert lib.rpp_set_launch_event_filter(None) == 0
+    assert lib.rpp_launch_event_count() == 0

@@ -52,6 +52,31 @@ def test_tc_gemm_shapes(M, N, K):
     _gemm_case("fp16", M, N, K, rpp.RPP_EPI_BIAS, seed=M)
 
 
+@pytest.fixture
+def cluster_mode():
+    """Set the GEMM's CTA-pair mode for one test, back to automatic afterwards."""
+    def set_mode(m):
+        assert rpp.lib().rpp_set_gemm_cluster_mode(m) == 0
+    yield set_mode
+    set_mode(0)
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("M,N,K,epi,rows", [
+    (1, 16, 8, 0, None),          # one row tile: with pairs forced, the partner tile is empty
+    (300, 256, 192, 1, None),     # three row tiles: the last pair is half empty
+    (517, 3072, 1024, 0, None),
+    (2304, 768, 3072, 2, None),
+    (1000, 768, 256, 2, 613),     # device row count, odd number of live tiles
+    (384, 144, 64, 0, 129),
+])
+def test_tc_gemm_cluster_modes(cluster_mode, mode, M, N, K, epi, rows):
+    """Unpaired and paired (thread-block cluster, W tile multicast) GEMMs, each against
+    the oracle, on shapes with an odd number of row tiles."""
+    cluster_mode(mode)
+    _gemm_case("bf16" if epi == 2 else "fp16", M, N, K, epi, seed=M + mode, rows=rows)
+
+
 def test_tc_gemm_device_row_count():
     _gemm_case("bf16", 1000, 768, 256, rpp.RPP_EPI_BIAS_RESIDUAL, rows=613)
     _gemm_case("fp16", 512, 128, 64, rpp.RPP_EPI_BIAS, rows=0)

@@ -52,6 +52,21 @@ def test_layer_small(idx, B, L, lens, hint):
     assert_close(got, ref, cfg.dtype, cfg.name)
 
 
+@pytest.mark.parametrize("mode", [1, 2])
+def test_layer_gemm_cluster_modes(mode):
+    """The BERT-base layer with its GEMMs unpaired and always paired into clusters."""
+    cfg = CONFIGS[1]
+    wl = make_bert_workload(cfg, B=6, L=128, layers=1, lengths=np.array([128, 1, 17, 64, 65, 100], np.int32),
+                            affine=True)
+    assert rpp.lib().rpp_set_gemm_cluster_mode(mode) == 0
+    try:
+        got, _ = _run_path(wl, cfg.dtype, hint=True)
+    finally:
+        rpp.lib().rpp_set_gemm_cluster_mode(0)
+    ref, _, _ = oracle.bert_forward(wl["x_padded"], wl["lengths"], wl["layers"], cfg.nh, cfg.eps)
+    assert_close(got, ref, cfg.dtype, f"{cfg.name} cluster mode {mode}")
+
+
 def test_layer_all_lengths_zero_gives_zero_output():
     cfg = CONFIGS[1]
     wl = make_bert_workload(cfg, B=3, L=16, layers=1, lengths=np.zeros(3, np.int32))
