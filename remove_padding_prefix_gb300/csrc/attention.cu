@@ -92,12 +92,13 @@ __global__ void __launch_bounds__(128) attention_varlen_kernel(const T* __restri
                                                                float scale_log2, int32_t* err) {
   pdl_wait();
   pdl_trigger();
-  if (device_error_set(err)) return;
   const int b = blockIdx.z;
   const int h = blockIdx.y;
   const int q0 = blockIdx.x * kBMq;
+  // the error word and the sequence bounds are read together (one round trip)
   const int c0 = cu[b];
   const int c1 = cu[b + 1];
+  if (device_error_set(err)) return;
   const int len = c1 - c0;
   if (c0 < 0 || len < 0 || c1 > T_max || len > max_len) {
     if (threadIdx.x == 0) set_device_error(err, len > max_len ? RPP_DERR_LENGTH : RPP_DERR_ROWS);

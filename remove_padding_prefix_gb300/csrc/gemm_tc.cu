@@ -774,7 +774,7 @@ struct TileChoice {
   int splits = 1;
 };
 
-TileChoice choose_tiles(int M, int N, int K, int max_bn, int max_splits, int cl = 1) {
+TileChoice choose_tiles(int M, int N, int K, int max_bn, int max_splits, int cl = 1, int wpq = 2) {
   static const int cands[] = {256, 192, 144, 128, 96, 64, 48, 32, 16};
   const int sms = num_sms() / cl;                       // concurrent work units (clusters)
   const int num_m = (M + kBM * cl - 1) / (kBM * cl);    // row-tile groups
@@ -787,7 +787,12 @@ TileChoice choose_tiles(int M, int N, int K, int max_bn, int max_splits, int cl 
       const int kps = (num_k + sp - 1) / sp;
       const long long units = static_cast<long long>(num_m) * (N / bn) * sp;
       const long long waves = (units + sms - 1) / sms;
-      const double cost = static_cast<double>(waves) * (kps * (bn + 32.0) + 6.0 * bn) + (sp - 1) * 64.0;
+      // With a few K blocks per unit the epilogue is the bottleneck, and a tile's
+      // epilogue takes as long as its busiest warp (each of the wpq warps of a lane
+      // quadrant takes every wpq-th 32-column slice); with more, it overlaps the next
+      // unit's MMAs and only its size counts.
+      const double epi = kps <= 4 ? 6.0 * 32.0 * wpq * ((bn + 32 * wpq - 1) / (32 * wpq)) : 6.0 * bn;
+      const double cost = static_cast<double>(waves) * (kps * (bn + 32.0) + epi) + (sp - 1) * 64.0;
       if (cost < best_cost - 1e-9) {
         best_cost = cost;
         best.bn = bn;
@@ -885,7 +890,8 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t stream) {
   // Pairs pay off when the MMAs dominate (long K, many row tiles); short-K or
   // few-tile GEMMs are epilogue- or latency-bound and run unpaired.
   int cl = (!is_int && (g_cluster_mode == 2 || (g_cluster_mode == 0 && rows_hint >= 8192 && g.K >= 1024))) ? 2 : 1;
-  TileChoice tc = choose_tiles(rows_hint, g.N, g.K, max_bn, can_split ? g.max_splits : 1, cl);
+  const int wpq = g.epi == RPP_EPI_BIAS_GELU ? epi_warps<RPP_EPI_BIAS_GELU>() / 4 : 2;
+  TileChoice tc = choose_tiles(rows_hint, g.N, g.K, max_bn, can_split ? g.max_splits : 1, cl, wpq);
   if (g.force_bn) tc.bn = g.force_bn;
   const int bn = tc.bn;
   if (!bn || g.N % bn || bn > max_bn) return cudaErrorNotSupported;

@@ -15,6 +15,8 @@ namespace rpp {
 
 namespace {
 
+constexpr int kMaxSlices = 4;   // split-K partial sums a LayerNorm input may consist of
+
 __device__ __forceinline__ int8_t quantize_one(float v, float inv_s) {
   const float t = __fmul_rn(v, inv_s);          // one IEEE fp32 multiply
   int q = __float2int_rn(t);                    // round half to even
@@ -54,25 +56,48 @@ __device__ __forceinline__ void store_vec(TOut* p, const float* o) {
 // memory, loaded once per CTA.  In padded-output mode the grid walks the padded
 // [B, L] slots: a valid slot normalises its packed row and writes it in place, a pad
 // slot is written as zeros (the padding rebuild of the last layer, fused).
-template <typename T, typename TOut, int G, int VPL>
+template <typename T, typename TOut, int G, int VPL, int NS>
 __global__ void __launch_bounds__(128) layernorm_kernel(LnArgs a) {
   pdl_wait();
   pdl_trigger();
-  if (device_error_set(a.err)) return;
   const int H = a.H;
-  int M = a.rows ? *a.rows : a.M_max;
-  if (M > a.M_max || M < 0) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) set_device_error(a.err, RPP_DERR_ROWS);
-    return;
+  // The prologue's global reads (error word, device row count, gamma / beta / bias)
+  // are independent: all are issued before any is used, one round trip in all.
+  constexpr int kPre = 8;   // values of each parameter vector a thread stages (H <= 1024)
+  float pg[kPre], pb[kPre], pc[kPre];
+#pragma unroll
+  for (int k = 0; k < kPre; ++k) {
+    const int i = threadIdx.x + k * 128;
+    if (i < H) {
+      pg[k] = __ldg(a.gamma + i);
+      pb[k] = __ldg(a.beta + i);
+      pc[k] = a.add_bias ? __ldg(a.add_bias + i) : 0.f;
+    }
   }
+  const bool err_set = device_error_set(a.err);
+  int M = a.rows ? *a.rows : a.M_max;
   extern __shared__ float ln_smem[];
   float* s_gamma = ln_smem;
   float* s_beta = ln_smem + H;
   float* s_bias = ln_smem + 2 * H;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) {
+#pragma unroll
+  for (int k = 0; k < kPre; ++k) {
+    const int i = threadIdx.x + k * 128;
+    if (i < H) {
+      s_gamma[i] = pg[k];
+      s_beta[i] = pb[k];
+      s_bias[i] = pc[k];
+    }
+  }
+  for (int i = threadIdx.x + kPre * 128; i < H; i += blockDim.x) {
     s_gamma[i] = a.gamma[i];
     s_beta[i] = a.beta[i];
-    if (a.add_bias) s_bias[i] = a.add_bias[i];
+    s_bias[i] = a.add_bias ? a.add_bias[i] : 0.f;
+  }
+  if (err_set) return;
+  if (M > a.M_max || M < 0) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) set_device_error(a.err, RPP_DERR_ROWS);
+    return;
   }
   __syncthreads();
 
@@ -109,12 +134,18 @@ __global__ void __launch_bounds__(128) layernorm_kernel(LnArgs a) {
       }
     }
     const bool valid = src >= 0;
-    // ---- loads: input, residual (issued together)
-    uint4 rx[VPL];
+    // ---- loads: input and its split-K slices (NS > 1), residual -- all issued together
+    uint4 rx[NS][VPL];
     uint4 rr[VPL][EPV / 4];
-    const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<long long>(valid ? src : 0) * H);
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) rx[i] = valid ? xr[i * G + gl] : make_uint4(0u, 0u, 0u, 0u);
+    for (int sl = 0; sl < NS; ++sl) {
+      if (sl == 0 || sl < a.n_in) {
+        const uint4* xr =
+            reinterpret_cast<const uint4*>(x + sl * a.in_stride + static_cast<long long>(valid ? src : 0) * H);
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) rx[sl][i] = valid ? xr[i * G + gl] : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
     const bool has_res = a.residual != nullptr && valid;
     if (has_res) {
 #pragma unroll
@@ -133,9 +164,22 @@ __global__ void __launch_bounds__(128) layernorm_kernel(LnArgs a) {
     }
     float v[VPL][EPV];
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) unpack16<T>(rx[i], v[i]);
-    // split-K partial sums of the preceding GEMM: the other slices of this row
-    for (int sl = 1; sl < a.n_in; ++sl) {
+    for (int i = 0; i < VPL; ++i) unpack16<T>(rx[0][i], v[i]);
+    // split-K partial sums of the preceding GEMM: the other slices of this row (those
+    // beyond the NS loaded up front, one round trip each)
+#pragma unroll
+    for (int sl = 1; sl < NS; ++sl) {
+      if (sl < a.n_in) {
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+          float f[EPV];
+          unpack16<T>(rx[sl][i], f);
+#pragma unroll
+          for (int j = 0; j < EPV; ++j) v[i][j] += f[j];
+        }
+      }
+    }
+    for (int sl = NS; sl < a.n_in; ++sl) {
       const uint4* xs =
           reinterpret_cast<const uint4*>(x + sl * a.in_stride + static_cast<long long>(valid ? src : 0) * H);
 #pragma unroll
@@ -296,7 +340,7 @@ __global__ void amax_kernel(const T* __restrict__ x, int M_max, const int32_t* r
   if (lane_id() == 0) atomic_max_nonneg(amax, m);
 }
 
-template <typename T, typename TOut, int G, int VPL>
+template <typename T, typename TOut, int G, int VPL, int NS>
 cudaError_t ln_launch(const LnArgs& a, cudaStream_t stream) {
   const int threads = 128;
   const int rows_per_block = (threads / 32) * (32 / G);
@@ -306,15 +350,23 @@ cudaError_t ln_launch(const LnArgs& a, cudaStream_t stream) {
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   const size_t smem = 3 * static_cast<size_t>(a.H) * sizeof(float);
-  return launch_pdl(layernorm_kernel<T, TOut, G, VPL>, dim3(static_cast<unsigned>(blocks)), dim3(threads), smem,
+  return launch_pdl(layernorm_kernel<T, TOut, G, VPL, NS>, dim3(static_cast<unsigned>(blocks)), dim3(threads), smem,
                     stream, a);
 }
 
 template <typename T, typename TOut>
 cudaError_t ln_dispatch(const LnArgs& a, cudaStream_t stream) {
   const int V = a.H / Vec<T>::N;   // 16-byte vectors per row
-#define RPP_LN_CASE(G_, VPL_) \
-  if (V == (G_) * (VPL_)) return ln_launch<T, TOut, G_, VPL_>(a, stream);
+  // split-K slices (fp32 input only) take the variant that loads all of them at once,
+  // where the registers allow (up to 8 vectors per lane)
+#define RPP_LN_CASE(G_, VPL_)                                                              \
+  if (V == (G_) * (VPL_)) {                                                                \
+    if constexpr (std::is_same<T, float>::value && (VPL_) <= 8) {                          \
+      if (a.n_in > 2) return ln_launch<T, TOut, G_, VPL_, kMaxSlices>(a, stream);         \
+      if (a.n_in == 2) return ln_launch<T, TOut, G_, VPL_, 2>(a, stream);                 \
+    }                                                                                      \
+    return ln_launch<T, TOut, G_, VPL_, 1>(a, stream);                                     \
+  }
   RPP_LN_CASE(32, 1) RPP_LN_CASE(32, 2) RPP_LN_CASE(32, 3) RPP_LN_CASE(32, 4)
   RPP_LN_CASE(32, 5) RPP_LN_CASE(32, 6) RPP_LN_CASE(32, 8) RPP_LN_CASE(32, 12) RPP_LN_CASE(32, 16)
   RPP_LN_CASE(16, 1) RPP_LN_CASE(16, 3) RPP_LN_CASE(8, 1) RPP_LN_CASE(8, 3) RPP_LN_CASE(8, 5)
@@ -341,6 +393,7 @@ bool layernorm_supported(int H, rpp_dtype dtype) {
 cudaError_t launch_layernorm(const LnArgs& args, cudaStream_t stream) {
   LnArgs a = args;
   if (a.n_in > 1 && a.in_dtype != RPP_F32) return cudaErrorNotSupported;
+  if (a.n_in < 1) return cudaErrorInvalidValue;
   a.res_kind = !a.residual ? 0 : (a.res_dtype == RPP_F32 ? 1 : (a.res_dtype == RPP_F16 ? 2 : 3));
   if (a.residual && a.in_dtype != RPP_F32) return cudaErrorNotSupported;   // residual adds use 4-element groups
   if (a.pad_cu && (a.pad_B <= 0 || a.pad_L <= 0)) return cudaErrorInvalidValue;

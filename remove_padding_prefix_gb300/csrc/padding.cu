@@ -138,6 +138,7 @@ __global__ void __launch_bounds__(kFusedThreads) offsets_remove_kernel(const int
   __shared__ int32_t s_cu[kFusedMaxB + 1];
   __shared__ int32_t s_warp[kFusedThreads / 32];
   const int tid = threadIdx.x;
+  const bool err_before = device_error_set(err);   // read with the lengths, checked after the scan
   constexpr int PER = kFusedMaxB / kFusedThreads;   // lengths per thread
   int32_t v[PER];
   int32_t run = 0;
@@ -184,22 +185,32 @@ __global__ void __launch_bounds__(kFusedThreads) offsets_remove_kernel(const int
   __syncthreads();
   if (blockIdx.x == 0)
     for (int b = tid; b <= B; b += kFusedThreads) cu[b] = s_cu[b];
-  pdl_wait();
-  pdl_trigger();
-  if (device_error_set(err)) return;
-  // copy the valid rows; padded row r = b*L + p goes to packed row cu[b] + p
-  const long long total = static_cast<long long>(B) * L * vpr;
-  for (long long i = blockIdx.x * static_cast<long long>(kFusedThreads) + tid; i < total;
-       i += static_cast<long long>(gridDim.x) * kFusedThreads) {
-    const long long r = i / vpr;
-    const int c = static_cast<int>(i - r * vpr);
-    const int b = static_cast<int>(r / L);
-    const int p = static_cast<int>(r - static_cast<long long>(b) * L);
-    const int32_t c0 = s_cu[b];
-    if (p < s_cu[b + 1] - c0) {
-      packed[(static_cast<long long>(c0) + p) * vpr + c] = __ldg(padded + i);
-      if (c == 0) po[c0 + p] = b * L - c0;
+  if (err_before) return;
+  // one warp per packed row j: its sequence b is found by binary search in the scan,
+  // the row's 16-byte vectors are read (up to 8 per lane in flight) and written
+  const int T = s_cu[B];
+  const int lane = tid & 31;
+  const int warps = gridDim.x * (kFusedThreads / 32);
+  for (int j = blockIdx.x * (kFusedThreads / 32) + (tid >> 5); j < T; j += warps) {
+    int lo = 0, hi = B;   // largest b with s_cu[b] <= j (and s_cu[b + 1] > j)
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_cu[mid] <= j) lo = mid; else hi = mid;
     }
+    const int b = lo;
+    const int c0 = s_cu[b];
+    const uint4* src = padded + (static_cast<long long>(b) * L + (j - c0)) * vpr;
+    uint4* dst = packed + static_cast<long long>(j) * vpr;
+    for (int c = lane; c < vpr; c += 32 * 8) {
+      uint4 t[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (c + 32 * u < vpr) t[u] = __ldg(src + c + 32 * u);
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (c + 32 * u < vpr) dst[c + 32 * u] = t[u];
+    }
+    if (lane == 0) po[j] = b * L - c0;
   }
 }
 
@@ -211,8 +222,8 @@ cudaError_t launch_offsets_remove(const int32_t* lengths, int B, int L, int row_
                                   int32_t* cu, int32_t* po, void* packed, int32_t* err, cudaStream_t stream) {
   if (!offsets_remove_fusable(B)) return cudaErrorNotSupported;
   const int vpr = row_bytes / 16;
-  const long long total = static_cast<long long>(B) * L * vpr;
-  long long blocks = (total + kFusedThreads - 1) / kFusedThreads;
+  // a warp per packed row, at most B * L rows
+  long long blocks = (static_cast<long long>(B) * L + kFusedThreads / 32 - 1) / (kFusedThreads / 32);
   const long long cap = static_cast<long long>(num_sms()) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
