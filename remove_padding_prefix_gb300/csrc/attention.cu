@@ -343,6 +343,8 @@ cudaError_t launch_attention_varlen(const void* qkv, const int32_t* cu, int B, i
     return launch_pdl(attention_varlen_f32_kernel, grid, dim3(kF32Rows), 0, stream, static_cast<const float*>(qkv), cu,
                       T_max, max_len, nh, static_cast<float*>(out), scale, err);
   }
+  if (dtype == RPP_F16 || dtype == RPP_BF16)
+    return launch_attention_tc(qkv, cu, B, T_max, max_len, nh, dtype, out, err, stream);
   dim3 grid((max_len + kBMq - 1) / kBMq, nh, B);
   const float scale_log2 = scale * 1.4426950408889634f;
   if (dtype == RPP_F16) {

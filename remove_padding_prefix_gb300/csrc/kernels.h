@@ -106,6 +106,12 @@ void set_gemm_cluster_mode(int mode);
 cudaError_t launch_gemm_f32(const float* a, const float* w_t, const float* bias, const float* residual, float* out,
                             int M_max, const int32_t* rows, int N, int K, int epi, int32_t* err, cudaStream_t stream);
 
+// 2D row-major [rows, cols] tensor map, box = box_cols x box_rows (defined with the GEMM)
+bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, long long rows,
+                  int cols, int box_rows, int box_cols, CUtensorMapSwizzle swz);
+// tcgen05 varlen attention, head size 64, fp16 / bf16
+cudaError_t launch_attention_tc(const void* qkv, const int32_t* cu, int B, int T_max, int max_len, int nh,
+                                rpp_dtype dtype, void* out, int32_t* err, cudaStream_t stream);
 cudaError_t launch_attention_varlen(const void* qkv, const int32_t* cu, int B, int T_max, int max_len, int nh, int d,
                                     rpp_dtype dtype, void* out, int32_t* err, cudaStream_t stream);
 

@@ -71,165 +71,206 @@ __device__ __forceinline__ uint32_t pack2w(float lo, float hi) {
 
 __device__ __forceinline__ int region(int c, int I, int w, int s) { return c < I - w ? 0 : (c < I - s ? 1 : 2); }
 
-// One CTA (4 warps) per (window, head): 12 KB of shared memory, so many CTAs share an
-// SM and one CTA's gather latency hides behind another's arithmetic.  The bias of the
-// head (fp32, preprocessed) is read through the L1 cache; every window reuses it.
+// One CTA (4 warps) per head and a strided set of windows (persistent over windows):
+// each thread builds, once, its 32 scores' bias (from the preprocessed fp32 table, in
+// log2 units; -inf for padding keys) and, for shifted blocks, the region-mask bits of
+// the four window kinds (interior, last window row, last window column, corner: only
+// windows touching the wrap seam mix regions).  Per window the score epilogue is then
+// one FMA and a select per element.  The next window's rows are gathered (cp.async)
+// into the second of two shared-memory buffers while the current one is computed.
 template <typename T>
-__global__ void __launch_bounds__(128) window_attention_kernel(const T* __restrict__ qkv,
-                                                               const float* __restrict__ bias, T* __restrict__ out,
-                                                               int I, int w, int s, int nh, long long n_win,
-                                                               float scale_log2, int32_t* err) {
+__global__ void __launch_bounds__(128, 4) window_attention_kernel(const T* __restrict__ qkv,
+                                                                  const float* __restrict__ bias,
+                                                                  T* __restrict__ out, int I, int w, int s, int nh,
+                                                                  long long n_win, float scale_log2, int32_t* err) {
   pdl_wait();
   pdl_trigger();
-  if (device_error_set(err)) return;
-  const long long wid = blockIdx.y + static_cast<long long>(gridDim.y) * blockIdx.z;
-  if (wid >= n_win) return;
   constexpr int TILE = kWRows * kWD * 2;   // bytes of one 64 x 32 tile
-  __shared__ __align__(128) uint8_t sQKV[3 * TILE];
-  __shared__ int sRow[kWRows];   // raster rows of the window's tokens
-  __shared__ int sLab[kWRows];   // region labels in the shifted frame
+  __shared__ __align__(128) uint8_t sQKV[2][3 * TILE];
+  __shared__ int sRow[2][kWRows];          // raster rows of the window's tokens
   const int C = nh * kWD;
   const int N = w * w;
-  // the heads of one window are neighbouring CTAs (x fastest), so the rows they each
-  // read a 64-byte piece of are still in L2 for the others
   const int h = blockIdx.x;
   const int nWs = I / w;
   const int nW = nWs * nWs;
-  const int img = static_cast<int>(wid / nW);
-  const int wr = static_cast<int>(wid - static_cast<long long>(img) * nW);
-  const int wy = wr / nWs, wx = wr - (wr / nWs) * nWs;
   const int tid = threadIdx.x;
   const int warp = warp_id();
   const int lane = lane_id();
-
-  // padding rows (N..63) of Q, K and V are zero (V's must be: P = 0 there, and 0 * junk
-  // could be NaN)
-  for (int i = tid; i < 3 * (kWRows - N) * 4; i += blockDim.x) {
-    const int tile = i / ((kWRows - N) * 4);
-    const int r = N + (i / 4) % (kWRows - N);
-    *reinterpret_cast<uint4*>(sQKV + tile * TILE + swz64(r, i & 3)) = make_uint4(0u, 0u, 0u, 0u);
-  }
-  if (tid < N) {
-    const int y = wy * w + tid / w, x = wx * w + tid % w;
-    int ys = y + s, xs = x + s;
-    if (ys >= I) ys -= I;
-    if (xs >= I) xs -= I;
-    sRow[tid] = img * I * I + ys * I + xs;
-    sLab[tid] = s > 0 ? 3 * region(y, I, w, s) + region(x, I, w, s) : 0;
-  }
-  __syncthreads();
-  // gather this head's Q, K and V rows: N rows x 3 parts x 4 chunks of 16 bytes
-  for (int i = tid; i < N * 12; i += blockDim.x) {
-    const int r = i / 12;
-    const int cc = i - r * 12;
-    const int part = cc >> 2;
-    const T* src = qkv + static_cast<long long>(sRow[r]) * (3 * C) + part * C + h * kWD + (cc & 3) * 8;
-    cp_async_16(sQKV + part * TILE + swz64(r, cc & 3), src, true);
-  }
-  cp_async_commit();
-  cp_async_wait<0>();
-  __syncthreads();
-
-  const uint32_t sQa = smem_u32(sQKV);
-  const uint32_t sKa = smem_u32(sQKV + TILE);
-  const uint32_t sVa = smem_u32(sQKV + 2 * TILE);
   const int rA = warp * 16 + (lane >> 2);   // this thread's two query rows: rA, rA + 8
-  uint32_t qf[2][4];
-#pragma unroll
-  for (int kk = 0; kk < 2; ++kk) {
-    const int r = warp * 16 + (lane & 15);
-    ldsm_x4w(sQa + swz64(r, kk * 2 + (lane >> 4)), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
-  }
-  float sc[8][4];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
-#pragma unroll
-  for (int kk = 0; kk < 2; ++kk) {
-#pragma unroll
-    for (int np = 0; np < 4; ++np) {
-      uint32_t b0, b1, b2, b3;
-      const int r = np * 16 + (lane & 7) + ((lane >> 4) << 3);
-      ldsm_x4w(sKa + swz64(r, kk * 2 + ((lane >> 3) & 1)), b0, b1, b2, b3);
-      mma_w<T>(sc[2 * np], qf[kk], b0, b1);
-      mma_w<T>(sc[2 * np + 1], qf[kk], b2, b3);
-    }
-  }
-  // scores -> log2 domain with bias and region mask; softmax over the N keys
   const float log2e = 1.4426950408889634f;
+
+  // ---- per-thread constants: bias of its 32 scores and the mask bits of the four kinds
   const float* bh = bias + static_cast<long long>(h) * N * N;
-  const int labA = rA < N ? sLab[rA] : -1;
-  const int labB = rA + 8 < N ? sLab[rA + 8] : -1;
-  float mx[2] = {-INFINITY, -INFINITY};
+  float bv[8][4];
+  uint32_t mask[4] = {0u, 0u, 0u, 0u};   // bit 4j+e: pair excluded in window kind k
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int t = rA + ((e >> 1) << 3);
       const int u = j * 8 + 2 * (lane & 3) + (e & 1);
-      const int lt = (e >> 1) ? labB : labA;
-      float v = -INFINITY;
-      if (u < N && t < N && lt == sLab[u]) v = sc[j][e] * scale_log2 + __ldg(bh + t * N + u) * log2e;
-      sc[j][e] = v;
-    }
-    mx[0] = fmaxf(mx[0], fmaxf(sc[j][0], sc[j][1]));
-    mx[1] = fmaxf(mx[1], fmaxf(sc[j][2], sc[j][3]));
-  }
-  float sum[2] = {0.f, 0.f};
+      bv[j][e] = u >= N ? -INFINITY : (t < N ? __ldg(bh + t * N + u) * log2e : 0.f);
+      if (s > 0 && t < N && u < N) {
+        // region labels in the shifted frame for a window in the last row (ky = 1) or
+        // column (kx = 1) of windows; elsewhere every token is in region 0
+        const int tyy = I - w + t / w, txx = I - w + t % w;
+        const int uyy = I - w + u / w, uxx = I - w + u % w;
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
-    mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
-    if (mx[i] == -INFINITY) mx[i] = 0.f;   // padding query rows
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    sc[j][0] = exp2f(sc[j][0] - mx[0]);
-    sc[j][1] = exp2f(sc[j][1] - mx[0]);
-    sc[j][2] = exp2f(sc[j][2] - mx[1]);
-    sc[j][3] = exp2f(sc[j][3] - mx[1]);
-    sum[0] += sc[j][0] + sc[j][1];
-    sum[1] += sc[j][2] + sc[j][3];
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], 1);
-    sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], 2);
-    sum[i] = sum[i] > 0.f ? 1.f / sum[i] : 0.f;
-  }
-  float o[4][4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
-    uint32_t pa[4];
-    pa[0] = pack2w<T>(sc[2 * kk][0], sc[2 * kk][1]);
-    pa[1] = pack2w<T>(sc[2 * kk][2], sc[2 * kk][3]);
-    pa[2] = pack2w<T>(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-    pa[3] = pack2w<T>(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
-#pragma unroll
-    for (int dp = 0; dp < 2; ++dp) {
-      uint32_t b0, b1, b2, b3;
-      const int r = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
-      ldsm_x4w_t(sVa + swz64(r, dp * 2 + (lane >> 4)), b0, b1, b2, b3);
-      mma_w<T>(o[2 * dp], pa, b0, b1);
-      mma_w<T>(o[2 * dp + 1], pa, b2, b3);
+        for (int k = 1; k < 4; ++k) {
+          const bool ky = k & 2, kx = k & 1;
+          const int lt = 3 * (ky ? region(tyy, I, w, s) : 0) + (kx ? region(txx, I, w, s) : 0);
+          const int lu = 3 * (ky ? region(uyy, I, w, s) : 0) + (kx ? region(uxx, I, w, s) : 0);
+          if (lt != lu) mask[k] |= 1u << (4 * j + e);
+        }
+      }
     }
   }
-  // normalised output over this warp's own Q rows, then scattered back to the raster rows
-  __syncwarp();
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t lo = pack2w<T>(o[j][0] * sum[0], o[j][1] * sum[0]);
-    const uint32_t hi = pack2w<T>(o[j][2] * sum[1], o[j][3] * sum[1]);
-    *reinterpret_cast<uint32_t*>(sQKV + swz64(rA, j) + (lane & 3) * 4) = lo;
-    *reinterpret_cast<uint32_t*>(sQKV + swz64(rA + 8, j) + (lane & 3) * 4) = hi;
+  if (device_error_set(err)) return;
+
+  // padding rows (N..63) of Q, K and V are zero in both buffers (V's must be: P = 0
+  // there, and 0 * junk could be NaN); the gathers never write them
+  for (int i = tid; i < 2 * 3 * (kWRows - N) * 4; i += blockDim.x) {
+    const int bt = i / ((kWRows - N) * 4);   // buffer * 3 + tile
+    const int r = N + (i / 4) % (kWRows - N);
+    *reinterpret_cast<uint4*>(sQKV[bt / 3] + (bt % 3) * TILE + swz64(r, i & 3)) = make_uint4(0u, 0u, 0u, 0u);
   }
-  __syncthreads();
-  for (int i = tid; i < N * 4; i += blockDim.x) {
-    const int r = i >> 2;
-    const int cc = i & 3;
-    const uint4 v = *reinterpret_cast<const uint4*>(sQKV + swz64(r, cc));
-    *reinterpret_cast<uint4*>(out + static_cast<long long>(sRow[r]) * C + h * kWD + cc * 8) = v;
+
+  auto window_rows = [&](int buf, long long wid) {   // threads tid < N
+    if (tid < N) {
+      const int img = static_cast<int>(wid / nW);
+      const int wr = static_cast<int>(wid - static_cast<long long>(img) * nW);
+      const int wy = wr / nWs, wx = wr - (wr / nWs) * nWs;
+      int ys = wy * w + tid / w + s, xs = wx * w + tid % w + s;
+      if (ys >= I) ys -= I;
+      if (xs >= I) xs -= I;
+      sRow[buf][tid] = img * I * I + ys * I + xs;
+    }
+  };
+  auto gather = [&](int buf) {   // this head's Q, K, V rows: N rows x 3 parts x 4 chunks
+    for (int i = tid; i < N * 12; i += blockDim.x) {
+      const int r = i / 12;
+      const int cc = i - r * 12;
+      const int part = cc >> 2;
+      const T* src = qkv + static_cast<long long>(sRow[buf][r]) * (3 * C) + part * C + h * kWD + (cc & 3) * 8;
+      cp_async_16(sQKV[buf] + part * TILE + swz64(r, cc & 3), src, true);
+    }
+    cp_async_commit();
+  };
+
+  long long wid = blockIdx.y;
+  if (wid < n_win) {
+    window_rows(0, wid);
+    __syncthreads();
+    gather(0);
+  }
+  for (int it = 0; wid < n_win; ++it, wid += gridDim.y) {
+    const int buf = it & 1;
+    const long long nxt = wid + gridDim.y;
+    if (nxt < n_win) {   // prefetch the next window into the other buffer
+      window_rows(buf ^ 1, nxt);
+      __syncthreads();
+      gather(buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const int wr = static_cast<int>(wid % nW);
+    const int kind = s > 0 ? 2 * (wr / nWs == nWs - 1) + (wr % nWs == nWs - 1) : 0;
+    const uint32_t mk = mask[0] | (kind == 1 ? mask[1] : 0u) | (kind == 2 ? mask[2] : 0u) | (kind == 3 ? mask[3] : 0u);
+
+    const uint32_t sQa = smem_u32(sQKV[buf]);
+    const uint32_t sKa = sQa + TILE;
+    const uint32_t sVa = sQa + 2 * TILE;
+    uint32_t qf[2][4];
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const int r = warp * 16 + (lane & 15);
+      ldsm_x4w(sQa + swz64(r, kk * 2 + (lane >> 4)), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
+    }
+    float sc[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        uint32_t b0, b1, b2, b3;
+        const int r = np * 16 + (lane & 7) + ((lane >> 4) << 3);
+        ldsm_x4w(sKa + swz64(r, kk * 2 + ((lane >> 3) & 1)), b0, b1, b2, b3);
+        mma_w<T>(sc[2 * np], qf[kk], b0, b1);
+        mma_w<T>(sc[2 * np + 1], qf[kk], b2, b3);
+      }
+    }
+    // scores -> log2 domain with bias and region mask; softmax over the N keys
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float v = fmaf(sc[j][e], scale_log2, bv[j][e]);
+        sc[j][e] = (mk >> (4 * j + e)) & 1u ? -INFINITY : v;
+      }
+      mx[0] = fmaxf(mx[0], fmaxf(sc[j][0], sc[j][1]));
+      mx[1] = fmaxf(mx[1], fmaxf(sc[j][2], sc[j][3]));
+    }
+    float sum[2] = {0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 1));
+      mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], 2));
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      sc[j][0] = ex2_approx(sc[j][0] - mx[0]);
+      sc[j][1] = ex2_approx(sc[j][1] - mx[0]);
+      sc[j][2] = ex2_approx(sc[j][2] - mx[1]);
+      sc[j][3] = ex2_approx(sc[j][3] - mx[1]);
+      sum[0] += sc[j][0] + sc[j][1];
+      sum[1] += sc[j][2] + sc[j][3];
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], 1);
+      sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], 2);
+      sum[i] = 1.f / sum[i];   // >= 1: the row's maximum contributes 2^0
+    }
+    float o[4][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      uint32_t pa[4];
+      pa[0] = pack2w<T>(sc[2 * kk][0], sc[2 * kk][1]);
+      pa[1] = pack2w<T>(sc[2 * kk][2], sc[2 * kk][3]);
+      pa[2] = pack2w<T>(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+      pa[3] = pack2w<T>(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+#pragma unroll
+      for (int dp = 0; dp < 2; ++dp) {
+        uint32_t b0, b1, b2, b3;
+        const int r = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+        ldsm_x4w_t(sVa + swz64(r, dp * 2 + (lane >> 4)), b0, b1, b2, b3);
+        mma_w<T>(o[2 * dp], pa, b0, b1);
+        mma_w<T>(o[2 * dp + 1], pa, b2, b3);
+      }
+    }
+    // normalised output over this warp's own Q rows, then scattered back to the raster rows
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t lo = pack2w<T>(o[j][0] * sum[0], o[j][1] * sum[0]);
+      const uint32_t hi = pack2w<T>(o[j][2] * sum[1], o[j][3] * sum[1]);
+      *reinterpret_cast<uint32_t*>(sQKV[buf] + swz64(rA, j) + (lane & 3) * 4) = lo;
+      *reinterpret_cast<uint32_t*>(sQKV[buf] + swz64(rA + 8, j) + (lane & 3) * 4) = hi;
+    }
+    __syncthreads();
+    for (int i = tid; i < N * 4; i += blockDim.x) {
+      const int r = i >> 2;
+      const int cc = i & 3;
+      const uint4 v = *reinterpret_cast<const uint4*>(sQKV[buf] + swz64(r, cc));
+      *reinterpret_cast<uint4*>(out + static_cast<long long>(sRow[buf][r]) * C + h * kWD + cc * 8) = v;
+    }
+    __syncthreads();   // this buffer (and its rows) may be refilled next
   }
 }
 
@@ -254,11 +295,21 @@ template <typename T>
 cudaError_t wa_launch(int B, const void* qkv, const float* bias, void* out, int nh, int I, int w, int s, int32_t* err,
                       cudaStream_t stream) {
   const long long windows = static_cast<long long>(B) * (I / w) * (I / w);
-  if (windows > 65535LL * 65535LL || nh > 1024) return cudaErrorNotSupported;
-  const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kWD));
+  if (windows > 0x7fffffffLL || nh > 1024) return cudaErrorNotSupported;
   if (windows == 0) return cudaSuccess;
-  const long long gy = windows < 65535 ? windows : 65535;
-  dim3 grid(nh, static_cast<unsigned>(gy), static_cast<unsigned>((windows + gy - 1) / gy));
+  const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kWD));
+  // persistent over windows: exactly as many CTAs as fit on the GPU at once (a CTA
+  // more would run alone after the others), split across the heads
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, window_attention_kernel<T>, 128, 0);
+    if (e != cudaSuccess || per_sm < 1) per_sm = 1;
+  }
+  long long per_head = static_cast<long long>(num_sms()) * per_sm / nh;
+  if (per_head < 1) per_head = 1;
+  if (per_head > windows) per_head = windows;
+  if (per_head > 65535) per_head = 65535;
+  dim3 grid(nh, static_cast<unsigned>(per_head));
   return launch_pdl(window_attention_kernel<T>, grid, dim3(128), 0, stream, static_cast<const T*>(qkv), bias,
                     static_cast<T*>(out), I, w, s, nh, windows, scale_log2, err);
 }

@@ -101,7 +101,7 @@ def test_layernorm(dtype, H):
     assert_close(down(y), oracle.layernorm(x, g, b, eps), dtype, f"layernorm {dtype} H={H}")
 
 
-def _attention_case(dtype, lengths, nh, seed=0, max_len=None):
+def _attention_case(dtype, lengths, nh, seed=0, max_len=None, poison=False):
     rng = np.random.default_rng(seed)
     lengths = np.asarray(lengths, np.int32)
     L = int(max_len or max(1, lengths.max()))
@@ -113,7 +113,10 @@ def _attention_case(dtype, lengths, nh, seed=0, max_len=None):
     err = rpp.new_error_word()
     cu, _ = rpp.build_offsets(lt, L, err=err)
     out = torch.full((T_max, nh * d), float("nan"), dtype=TDT[dtype], device=dev())
-    rpp.attention_varlen(up(qkv, dtype), cu, len(lengths), L, nh, out=out, err=err)
+    qkv_d = up(qkv, dtype)
+    if poison:   # capacity rows past T hold NaN: a kernel must never let them reach a valid output
+        qkv_d[T:] = float("nan")
+    rpp.attention_varlen(qkv_d, cu, len(lengths), L, nh, out=out, err=err)
     check_err(err)
     cu_ref, _, _ = oracle.build_offsets(lengths, L)
     H = nh * d
@@ -126,6 +129,13 @@ def _attention_case(dtype, lengths, nh, seed=0, max_len=None):
 @pytest.mark.parametrize("dtype", ["fp16", "bf16", "fp32"])
 def test_attention_ragged(dtype):
     _attention_case(dtype, [1, 63, 64, 65, 128, 129, 200, 7], nh=4, seed=1)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16", "fp32"])
+def test_attention_ignores_non_finite_capacity_rows(dtype):
+    # the last sequence ends inside a key tile, so its last tile spans rows past T
+    _attention_case(dtype, [130, 57, 201], nh=2, seed=5, poison=True)
+    _attention_case(dtype, [3], nh=1, seed=6, poison=True)
 
 
 def test_attention_bert_large_lengths():

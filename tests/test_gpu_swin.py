@@ -26,10 +26,13 @@ def test_relative_position_bias_exact():
     assert np.array_equal(bias.cpu().numpy(), oracle.relative_position_bias(table, 7).astype(np.float32))
 
 
-@pytest.mark.parametrize("I,s,dtype", [(14, 3, "fp16"), (14, 0, "fp16"), (56, 3, "bf16"), (21, 2, "fp16")])
-def test_window_attention(I, s, dtype):
+@pytest.mark.parametrize("I,s,dtype,B", [(14, 3, "fp16", 2), (14, 0, "fp16", 2), (56, 3, "bf16", 2), (21, 2, "fp16", 2),
+                                         (56, 3, "fp16", 9)])
+def test_window_attention(I, s, dtype, B):
+    """B = 9 at 56 x 56 gives more windows than the kernel's CTAs per head, so each CTA
+    walks several windows (with the next one's rows prefetched)."""
     rng = np.random.default_rng(I + s)
-    B, C = 2, 96
+    C = 96
     qkv = round_to_dtype(rng.standard_normal((B, I * I, 3 * C), dtype=np.float32), dtype)
     table = round_to_dtype(0.5 * rng.standard_normal((169, 3), dtype=np.float32), dtype)
     cfg = _cfg(I, s, dtype)
