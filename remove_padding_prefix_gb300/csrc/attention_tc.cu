@@ -78,7 +78,12 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attention_tc_kernel(const __g
   const int q0 = blockIdx.x * kQT;
   const int c0 = cu[b];
   const int c1 = cu[b + 1];
-  if (device_error_set(err)) return;
+  // other CTAs of this launch may set the error word at any time: one thread reads it
+  // and the whole CTA follows that one reading (all threads return here, or none)
+  __shared__ int s_quit;
+  if (threadIdx.x == 0) s_quit = device_error_set(err) ? 1 : 0;
+  __syncthreads();
+  if (s_quit) return;
   const int len = c1 - c0;
   if (c0 < 0 || len < 0 || c1 > T_max || len > max_len) {
     if (threadIdx.x == 0) set_device_error(err, len > max_len ? RPP_DERR_LENGTH : RPP_DERR_ROWS);
@@ -104,7 +109,9 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attention_tc_kernel(const __g
   uint64_t* p_full = bars + 6;
   uint64_t* o_full = bars + 7;
   uint64_t* drain = bars + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  uint64_t* ex_tile = bars + 9;     // [4] per lane quadrant: the row-max exchange of a tile
+  uint64_t* ex_end = bars + 13;     // [4] per lane quadrant: the row-sum exchange at the end
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id();
@@ -119,6 +126,10 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attention_tc_kernel(const __g
     mbar_init(p_full, 256);
     mbar_init(o_full, 1);
     mbar_init(drain, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&ex_tile[i], 64);
+      mbar_init(&ex_end[i], 64);
+    }
     *abort_flag = 0;
     fence_mbarrier_init();
     tma_prefetch_desc(&tm);
@@ -221,7 +232,6 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attention_tc_kernel(const __g
     const int hf = (warp - 2) >> 2;
     const int r = q * 32 + lane;                  // query row of the tile
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    const int bar_id = 1 + q;                      // named barrier of the quadrant's two warps
     float m = neg_inf(), l = 0.f;                  // reference maximum (log2 units) and row sum
     bool ok = true;
     for (int j = 0; j < nkb; ++j) {
@@ -253,8 +263,14 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attention_tc_kernel(const __g
         for (int e = 8; e < 64; ++e) pm[e & 7] = fmaxf(pm[e & 7], __uint_as_float(v[e]));
         mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
       }
+      // exchange with the other half of the row (bounded wait on the pair's barrier)
       s_red[(j & 1) * 256 + hf * 128 + r] = mx;
-      named_bar_sync(bar_id, 64);
+      mbar_arrive(&ex_tile[q]);
+      w = mbar_wait_bounded(&ex_tile[q], j & 1, abort_flag) ? 1 : 0;
+      if (!__all_sync(0xffffffffu, w)) {
+        ok = false;
+        break;
+      }
       mx = fmaxf(mx, s_red[(j & 1) * 256 + (hf ^ 1) * 128 + r]) * scale_log2;   // the row's tile maximum
       // Lazy rescaling: the reference maximum moves only when the tile's exceeds it by
       // more than 8 (P stays below 2^8); then O (in tensor memory) and the row sum are
@@ -312,9 +328,13 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attention_tc_kernel(const __g
       mbar_arrive(p_full);
     }
     // the pair's two halves of the row sum
-    s_red[512 + hf * 128 + r] = l;
-    named_bar_sync(bar_id, 64);
-    l += s_red[512 + (hf ^ 1) * 128 + r];
+    if (ok) {
+      s_red[512 + hf * 128 + r] = l;
+      mbar_arrive(&ex_end[q]);
+      const int w = mbar_wait_bounded(&ex_end[q], 0, abort_flag) ? 1 : 0;
+      ok = __all_sync(0xffffffffu, w) != 0;
+      l += s_red[512 + (hf ^ 1) * 128 + r];
+    }
     if (ok) {
       const int w = mbar_wait_bounded(o_full, (nkb - 1) & 1, abort_flag) ? 1 : 0;
       ok = __all_sync(0xffffffffu, w) != 0;
