@@ -88,10 +88,11 @@ RPP_API rpp_status rpp_get_device_error(const int32_t* err, int32_t* host_code, 
  * a host array of cudaEvent_t owned by the caller; capacity 0 disables the hook.
  * Not thread-safe: one profiling caller at a time. */
 RPP_API rpp_status rpp_set_launch_events(void* const* events, int capacity);
-/* Tuning knob of the fp16/bf16 tensor-core GEMMs (no counterpart in the pages):
- * 0 (default) pairs CTAs on neighbouring 128-row tiles into a thread-block cluster
- * whenever the expected row count exceeds one tile -- each CTA of the pair loads half
- * of the shared weight tile and multicasts it to both; 1 never pairs; 2 always pairs.
+/* Tuning knob of the fp16 / bf16 tensor-core GEMMs (no counterpart in the pages):
+ * 0 (default) pairs CTAs into two-CTA clusters running cta_group::2 MMAs on 256-row
+ * tiles (each CTA holds its 128 A rows and half of the weight tile) when K >= 1024 and
+ * the expected row count is >= 8192; 1 never pairs; 2 always pairs.  The exact int8
+ * GEMM always runs unpaired (pairs measured no faster there).
  * The arithmetic per output element is the same in every mode, except that the
  * tile shape and K split are chosen per mode, and a different K split changes the
  * fp32 summation order.  Process-wide, not thread-safe; RPP_EINVAL outside 0..2. */

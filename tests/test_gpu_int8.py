@@ -47,6 +47,23 @@ def test_int8_gemm_int32_accumulators_bit_exact(M, N, K):
     assert np.array_equal(acc.cpu().numpy().astype(np.int64), oracle.int8_gemm(a, w.T))
 
 
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("M,N,K", [(300, 256, 1024), (385, 128, 4096), (8300, 1024, 1024)])
+def test_int8_gemm_cluster_modes_bit_exact(mode, M, N, K):
+    """The integer GEMM under every CTA-pair mode setting (it runs unpaired in all of
+    them), one and four exact K chunks, odd numbers of row tiles: int32 accumulators
+    bit-exact."""
+    rng = np.random.default_rng(M + K + mode)
+    a = rng.integers(-127, 128, size=(M, K), dtype=np.int64).astype(np.int8)
+    w = rng.integers(-127, 128, size=(N, K), dtype=np.int64).astype(np.int8)
+    assert rpp.lib().rpp_set_gemm_cluster_mode(mode) == 0
+    try:
+        acc = rpp.gemm_i8_i32(torch.as_tensor(a, device=dev()), torch.as_tensor(w, device=dev()))
+    finally:
+        rpp.lib().rpp_set_gemm_cluster_mode(0)
+    assert np.array_equal(acc.cpu().numpy().astype(np.int64), oracle.int8_gemm(a, w.T))
+
+
 def test_int8_gemm_adversarial_extremes():
     """All-+-127 operands: every chunk partial reaches +-(1024 * 127^2) = +-16 516 096, just
     under 2^24, and the full sum reaches +-66 064 384 for K = 4096."""
