@@ -31,7 +31,7 @@ from .encoder import (linear, gelu, layernorm, attention_varlen, bert_layer,
                       bert_forward, bert_stack_packed)
 from .swin import (shift, unshift, window_partition, window_reverse, window_coords,
                    relative_position_bias, shift_attend_mask, window_attention,
-                   swin_block)
+                   swin_block, patch_merge)
 from .int8 import (quantize_weight_per_channel, quantize_activation, int8_gemm,
                    int8_linear, bert_layer_int8, calibrate_int8, prepare_int8_layer)
 
@@ -40,7 +40,7 @@ __all__ = [
     "linear", "gelu", "layernorm", "attention_varlen", "bert_layer", "bert_forward",
     "bert_stack_packed",
     "shift", "unshift", "window_partition", "window_reverse", "window_coords",
-    "relative_position_bias", "shift_attend_mask", "window_attention", "swin_block",
+    "relative_position_bias", "shift_attend_mask", "window_attention", "swin_block", "patch_merge",
     "quantize_weight_per_channel", "quantize_activation", "int8_gemm", "int8_linear",
     "bert_layer_int8", "calibrate_int8", "prepare_int8_layer",
 ]

@@ -21,6 +21,11 @@ definitions are taken):
   only when 3 r(y) + r(x) agrees.  Excluded pairs are dropped from the softmax (the
   usual additive -100 differs from exclusion by e^-100).
 * Attention scale 1 / sqrt(d); LayerNorm eps 1e-5.
+* Downsampling between stages (the talk shows stages at falling resolution with a
+  downsampling step between them, without its formula): the standard patch merging is
+  taken.  Output token (py, px) concatenates the four input tokens (2py, 2px),
+  (2py+1, 2px), (2py, 2px+1), (2py+1, 2px+1) in that order (4C channels), applies
+  LayerNorm over the 4C channels and a bias-free linear map 4C -> 2C.
 """
 import numpy as np
 
@@ -163,4 +168,24 @@ def swin_block(x, wt, I, w, s, nh, eps):
         m = linear(gelu(linear(layernorm(xa, wt["gamma2"], wt["beta2"], eps), wt["W1"], wt["b1"])),
                    wt["W2"], wt["b2"])
         out[b] = xa + m
+    return out
+
+
+def patch_merge(x, I, gamma, beta, W, eps):
+    """Stage downsampling of x [B, I*I, C] (raster) into [B, (I/2)^2, 2C]: the 2 x 2
+    neighbourhood of each output token concatenated in the order (0,0), (1,0), (0,1),
+    (1,1) of (row offset, column offset), LayerNorm over 4C, then x @ W with W [4C, 2C]
+    and no bias."""
+    x = np.asarray(x, np.float64)
+    B, T_img, C = x.shape
+    assert T_img == I * I and I % 2 == 0
+    Ih = I // 2
+    out = np.empty((B, Ih * Ih, W.shape[1]), np.float64)
+    for b in range(B):
+        img = x[b].reshape(I, I, C)
+        cat = np.empty((Ih, Ih, 4 * C), np.float64)
+        for k, (dy, dx) in enumerate(((0, 0), (1, 0), (0, 1), (1, 1))):
+            cat[:, :, k * C:(k + 1) * C] = img[dy::2, dx::2, :]
+        h = layernorm(cat.reshape(Ih * Ih, 4 * C), gamma, beta, eps)
+        out[b] = linear(h, W)
     return out

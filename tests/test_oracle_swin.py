@@ -166,3 +166,42 @@ def test_swin_block_images_independent():
     x[1] += 1.0
     y2 = oracle.swin_block(x, wl["weights"], cfg.I, cfg.w, cfg.s, cfg.nh, cfg.eps)
     assert np.array_equal(y1[0], y2[0]) and np.array_equal(y1[2], y2[2])
+
+
+def _patch_merge_torch(x, I, gamma, beta, W, eps):
+    """Library route: the 2 x 2 neighbourhoods by view/permute (channel block k = 2 dx + dy),
+    torch layer_norm and matmul in fp64."""
+    B, _, C = x.shape
+    t = torch.as_tensor(x, dtype=torch.float64).view(B, I // 2, 2, I // 2, 2, C)   # [B, py, dy, px, dx, C]
+    t = t.permute(0, 1, 3, 4, 2, 5).reshape(B, (I // 2) ** 2, 4 * C)               # [B, py, px, dx, dy, C]
+    t = torch.nn.functional.layer_norm(t, (4 * C,), torch.as_tensor(gamma, dtype=torch.float64),
+                                       torch.as_tensor(beta, dtype=torch.float64), eps)
+    return (t @ torch.as_tensor(W, dtype=torch.float64)).numpy()
+
+
+@pytest.mark.parametrize("I,C", [(4, 8), (8, 96), (14, 24)])
+def test_patch_merge_matches_library_route(I, C):
+    rng = np.random.default_rng(I * C)
+    B = 2
+    x = rng.standard_normal((B, I * I, C))
+    gamma = 1 + 0.1 * rng.standard_normal(4 * C)
+    beta = 0.1 * rng.standard_normal(4 * C)
+    W = 0.05 * rng.standard_normal((4 * C, 2 * C))
+    got = oracle.patch_merge(x, I, gamma, beta, W, 1e-5)
+    assert got.shape == (B, (I // 2) ** 2, 2 * C)
+    assert np.allclose(got, _patch_merge_torch(x, I, gamma, beta, W, 1e-5), rtol=1e-12, atol=1e-12)
+
+
+def test_patch_merge_gathers_each_token_once():
+    """Tokens carrying their own raster index: every input token lands in exactly one output
+    token, in the slot its (row, column) parity names."""
+    I, C = 6, 1
+    x = np.arange(I * I, dtype=np.float64).reshape(1, I * I, 1)
+    # W = identity (4C -> 4C here) exposes the normalised concatenation itself
+    got = oracle.patch_merge(x, I, np.ones(4), np.zeros(4), np.eye(4), 0.0)[0]   # [9, 4]
+    for py in range(I // 2):
+        for px in range(I // 2):
+            src = [(2 * py + dy) * I + (2 * px + dx) for dy, dx in ((0, 0), (1, 0), (0, 1), (1, 1))]
+            v = np.array(src, np.float64)
+            ref = (v - v.mean()) / np.sqrt(v.var())
+            assert np.allclose(got[py * (I // 2) + px], ref, atol=1e-12)
