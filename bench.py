@@ -307,8 +307,74 @@ class SwinWorkload:
         return imgs * c.I * c.I / dt, f"{imgs} images ({imgs * c.I * c.I} tokens) of the seeded batch, fp64 numpy", dt
 
 
+class MergeWorkload:
+    """Swin stage downsampling (patch merge: 2x2 gather + LayerNorm over 4C, then the
+    4C -> 2C GEMM) on the stage-1 output shape."""
+
+    NAME = "swin_t_patch_merge_fp16"
+
+    def __init__(self, cfg, rank):
+        from workloads import make_patch_merge_workload
+        self.cfg = cfg
+        self.wl = make_patch_merge_workload(cfg, seed=cfg.seed + 300 + 7919 * rank)
+        self.T = cfg.T                        # input tokens
+        self.R = cfg.B * (cfg.I // 2) ** 2    # output tokens
+        self.tokens_per_step = self.T
+        self.dtype = {"fp16": "f16", "bf16": "bf16"}[cfg.dtype]
+
+    def config(self):
+        c = self.cfg
+        return {"workload": f"{self.NAME}: B={c.B} images {c.I}x{c.I} C={c.C} -> {c.I // 2}x{c.I // 2} C={2 * c.C} "
+                            f"(2x2 gather + LayerNorm(4C) + bias-free 4C->2C map); value counts input tokens",
+                "global_batch": c.B, "seq_len": c.I * c.I, "valid_tokens": self.T}
+
+    def setup(self, rpp, torch, dev):
+        c, wl = self.cfg, self.wl
+        self.tdt = rpp.torch_dtype(c.dtype)
+        self.pm = rpp.PatchMerge(rpp.merge_cfg(c.I, c.C, c.eps, c.dtype), wl["gamma"], wl["beta"], wl["W"], dev)
+        self.x = torch.as_tensor(wl["x"].reshape(-1, c.C)).to(dev, self.tdt)
+        self.y = torch.empty(self.R, 2 * c.C, dtype=self.tdt, device=dev)
+        self.ws = self.pm.workspace(c.B, dev)
+        self.err = rpp.new_error_word(dev)
+        self.rpp = rpp
+
+    def step(self, x=None):
+        self.rpp.patch_merge_forward(self.pm, self.x if x is None else x, self.cfg.B, y=self.y, workspace=self.ws,
+                                     err=self.err)
+
+    def host_io(self, torch):
+        xh = torch.empty(self.x.shape, dtype=self.tdt, pin_memory=True)
+        xh.copy_(self.x.cpu())
+        yh = torch.empty(self.y.shape, dtype=self.tdt, pin_memory=True)
+        xd = torch.empty_like(self.x)
+        return [(xh, xd)], (self.y, yh), lambda: self.step(xd)
+
+    def work(self, label):
+        C_, R, e = self.cfg.C, self.R, 2
+        if label == "patch_merge_ln":      # every input token read once, the 4C rows written once
+            return 0.0, e * (self.T * C_ + R * 4 * C_)
+        if label == "gemm_reduction":
+            return 2.0 * R * 4 * C_ * 2 * C_, e * (R * 4 * C_ + 8 * C_ * C_ + R * 2 * C_)
+        return 0.0, 0.0
+
+    def oracle_rate(self, budget_s):
+        import oracle
+        c, wl = self.cfg, self.wl
+        imgs = 0
+        t0 = time.perf_counter()
+        for b in range(c.B):
+            oracle.patch_merge(wl["x"][b:b + 1], c.I, wl["gamma"], wl["beta"], wl["W"], c.eps)
+            imgs += 1
+            if time.perf_counter() - t0 > budget_s:
+                break
+        dt = time.perf_counter() - t0
+        return imgs * c.I * c.I / dt, f"{imgs} images ({imgs * c.I * c.I} input tokens) of the seeded batch, fp64 numpy", dt
+
+
 def make_workload(name, rank):
     from workloads import config_by_name
+    if name == MergeWorkload.NAME:
+        return MergeWorkload(config_by_name("swin_t_stage1_fp16"), rank)
     cfg = config_by_name(name)
     return (SwinWorkload if cfg.kind == "swin" else BertWorkload)(cfg, rank)
 

@@ -381,6 +381,33 @@ RPP_API rpp_status rpp_swin_block_forward(const rpp_swin_cfg* cfg, const void* b
                                   void* y, void* workspace, size_t workspace_bytes, int32_t* err,
                                   rpp_stream stream);
 
+/* ------------------------------------------------------------------------------
+ * Swin stage downsampling (the talk's downsampling between stages; standard patch
+ * merging): output token (py, px) = LayerNorm over the 4C concatenation of input tokens
+ * (2py, 2px), (2py+1, 2px), (2py, 2px+1), (2py+1, 2px+1), then a bias-free 4C -> 2C map.
+ * ------------------------------------------------------------------------------ */
+typedef struct rpp_merge_cfg {
+  int img;       /* I: input image side in tokens, even */
+  int channels;  /* C: input channels (multiple of 8, <= 768); the output has 2C */
+  float eps;     /* LayerNorm eps */
+  int dtype;     /* RPP_F16 or RPP_BF16 */
+} rpp_merge_cfg;
+
+/* Bytes of the prepared weights, and the preparation: W [4C, 2C] of cfg dtype ([in, out],
+ * input blocks in the concatenation order above) stored K-major; gamma, beta [4C] of cfg
+ * dtype stored fp32.  dst: device, 16-byte aligned, rpp_patch_merge_bytes bytes. */
+RPP_API size_t rpp_patch_merge_bytes(const rpp_merge_cfg* cfg);
+RPP_API rpp_status rpp_patch_merge_prepare(const rpp_merge_cfg* cfg, const void* gamma, const void* beta,
+                                           const void* W, void* dst, rpp_stream stream);
+/* Workspace bytes for B images (the normalised 4C rows). */
+RPP_API size_t rpp_patch_merge_workspace_bytes(const rpp_merge_cfg* cfg, int B);
+/* x: device [B*I*I, C] raster order; y: device [B*(I/2)^2, 2C] raster order of the halved
+ * image.  RPP_EUNSUPPORTED for odd I or C outside the supported set; RPP_EWORKSPACE if
+ * workspace_bytes is too small. */
+RPP_API rpp_status rpp_patch_merge_forward(const rpp_merge_cfg* cfg, const void* prepared, int B, const void* x,
+                                           void* y, void* workspace, size_t workspace_bytes, int32_t* err,
+                                           rpp_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

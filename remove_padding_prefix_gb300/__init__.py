@@ -18,13 +18,14 @@ import torch
 from . import _abi
 from ._abi import (RPP_F32, RPP_F16, RPP_BF16, RPP_I8, RPP_EPI_BIAS, RPP_EPI_BIAS_GELU,  # noqa: F401
                    RPP_EPI_BIAS_RESIDUAL, RPP_DERR_LENGTH, RPP_DERR_TIMEOUT, RPP_DERR_ROWS, RPP_DERR_TMEM, EncoderCfg, LayerSrc,
-                   SwinCfg, SwinSrc)
+                   SwinCfg, SwinSrc, MergeCfg)
 
 __all__ = [
     "RppError", "lib", "torch_dtype", "dtype_code", "build_offsets", "remove_padding", "rebuild_padding", "linear",
     "layernorm", "attention_varlen", "encoder_cfg", "EncoderLayer", "encoder_layer_forward",
     "encoder_layer_calibrate", "encoder_forward", "quantize_weight", "quantize_activation", "gemm_i8_i32",
     "swin_cfg", "SwinBlock", "swin_prepare_bias", "window_attention_forward", "swin_block_forward",
+    "merge_cfg", "PatchMerge", "patch_merge_forward",
     "get_device_error", "new_error_word",
 ]
 
@@ -313,4 +314,41 @@ def swin_block_forward(block: SwinBlock, x, B: int, y=None, workspace=None, err=
     _check("rpp_swin_block_forward",
            lib().rpp_swin_block_forward(C.byref(block.cfg), _p(block.block), B, _p(x), _p(out), _p(ws), ws.numel(),
                                         _p(err), _stream(stream)))
+    return out
+
+
+# ---------------------------------------------------------------- Swin patch merging
+def merge_cfg(I, C_, eps, dtype) -> MergeCfg:
+    code = dtype_code(dtype) if not isinstance(dtype, int) else dtype
+    return MergeCfg(I, C_, float(eps), code)
+
+
+class PatchMerge:
+    """Prepared patch-merging weights (K-major reduction map, fp32 LayerNorm parameters)."""
+
+    def __init__(self, cfg: MergeCfg, gamma, beta, W, device="cuda", stream=None):
+        self.cfg = cfg
+        nbytes = lib().rpp_patch_merge_bytes(C.byref(cfg))
+        if nbytes == 0:
+            raise RppError("rpp_patch_merge_bytes", _abi.RPP_EUNSUPPORTED)
+        self.block = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        tdt = _TORCH[cfg.dtype]
+        up = lambda a: torch.as_tensor(np.ascontiguousarray(a)).to(device=device, dtype=tdt).contiguous()
+        g, b, w = up(gamma), up(beta), up(W)
+        _check("rpp_patch_merge_prepare", lib().rpp_patch_merge_prepare(C.byref(cfg), _p(g), _p(b), _p(w),
+                                                                        _p(self.block), _stream(stream)))
+        (stream or torch.cuda.current_stream()).synchronize()
+
+    def workspace(self, B: int, device="cuda") -> torch.Tensor:
+        return torch.empty(lib().rpp_patch_merge_workspace_bytes(C.byref(self.cfg), B), dtype=torch.uint8,
+                           device=device)
+
+
+def patch_merge_forward(pm: PatchMerge, x, B: int, y=None, workspace=None, err=None, stream=None):
+    I, C_ = pm.cfg.img, pm.cfg.channels
+    out = y if y is not None else torch.empty(B * (I // 2) * (I // 2), 2 * C_, dtype=x.dtype, device=x.device)
+    ws = workspace if workspace is not None else pm.workspace(B, x.device)
+    _check("rpp_patch_merge_forward",
+           lib().rpp_patch_merge_forward(C.byref(pm.cfg), _p(pm.block), B, _p(x), _p(out), _p(ws), ws.numel(),
+                                         _p(err), _stream(stream)))
     return out

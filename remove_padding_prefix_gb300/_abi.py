@@ -36,6 +36,10 @@ class SwinCfg(C.Structure):
                 ("mlp", i32), ("eps", f32), ("dtype", i32)]
 
 
+class MergeCfg(C.Structure):
+    _fields_ = [("img", i32), ("channels", i32), ("eps", f32), ("dtype", i32)]
+
+
 class SwinSrc(C.Structure):
     _fields_ = [(n, vp) for n in ("gamma1", "beta1", "Wqkv", "bqkv", "table", "Wo", "bo", "gamma2", "beta2",
                                   "W1", "b1", "W2", "b2")]
@@ -75,6 +79,10 @@ SIGNATURES = {
     "rpp_swin_prepare_block": (i32, [C.POINTER(SwinCfg), C.POINTER(SwinSrc), vp, vp]),
     "rpp_swin_workspace_bytes": (sz, [C.POINTER(SwinCfg), i32]),
     "rpp_swin_block_forward": (i32, [C.POINTER(SwinCfg), vp, i32, vp, vp, vp, sz, vp, vp]),
+    "rpp_patch_merge_bytes": (sz, [C.POINTER(MergeCfg)]),
+    "rpp_patch_merge_prepare": (i32, [C.POINTER(MergeCfg), vp, vp, vp, vp, vp]),
+    "rpp_patch_merge_workspace_bytes": (sz, [C.POINTER(MergeCfg), i32]),
+    "rpp_patch_merge_forward": (i32, [C.POINTER(MergeCfg), vp, i32, vp, vp, vp, sz, vp, vp]),
 }
 
 _lib = None

@@ -847,3 +847,81 @@ rpp_status rpp_swin_block_forward(const rpp_swin_cfg* cfg, const void* block, in
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- Swin patch merging
+namespace rpp {
+namespace {
+struct MergeLayout {
+  size_t w, gamma, beta, zero_bias, total;
+};
+MergeLayout merge_layout(const rpp_merge_cfg* c) {
+  MergeLayout L{};
+  const size_t C = static_cast<size_t>(c->channels);
+  size_t o = 0;
+  L.w = o;         o = align_up(o + 8 * C * C * 2);   // K-major [2C, 4C]
+  L.gamma = o;     o = align_up(o + 4 * C * 4);
+  L.beta = o;      o = align_up(o + 4 * C * 4);
+  L.zero_bias = o; o = align_up(o + 2 * C * 4);
+  L.total = o;
+  return L;
+}
+rpp_status merge_cfg_supported(const rpp_merge_cfg* c) {
+  if (!c) return RPP_EINVAL;
+  if (c->dtype != RPP_F16 && c->dtype != RPP_BF16) return RPP_EUNSUPPORTED;
+  if (!patch_merge_supported(c->channels, c->img) || !gemm_tc_supported(2 * c->channels, 4 * c->channels))
+    return RPP_EUNSUPPORTED;
+  if (!(c->eps > 0.f)) return RPP_EINVAL;
+  return RPP_OK;
+}
+}  // namespace
+}  // namespace rpp
+
+using namespace rpp;
+
+size_t rpp_patch_merge_bytes(const rpp_merge_cfg* cfg) {
+  if (merge_cfg_supported(cfg) != RPP_OK) return 0;
+  return merge_layout(cfg).total;
+}
+
+rpp_status rpp_patch_merge_prepare(const rpp_merge_cfg* cfg, const void* gamma, const void* beta, const void* W,
+                                   void* dst, rpp_stream stream) {
+  const rpp_status st = merge_cfg_supported(cfg);
+  if (st != RPP_OK) return st;
+  if (!gamma || !beta || !W || !dst || !aligned16(dst)) return RPP_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const MergeLayout P = merge_layout(cfg);
+  const rpp_dtype dt = static_cast<rpp_dtype>(cfg->dtype);
+  const int C = cfg->channels;
+  RPP_TRY(launch_transpose_to_kmajor(W, 4 * C, 2 * C, 2, at<void>(dst, P.w), 4 * C, s));
+  RPP_TRY(launch_to_f32(gamma, dt, 4 * C, at<float>(dst, P.gamma), s));
+  RPP_TRY(launch_to_f32(beta, dt, 4 * C, at<float>(dst, P.beta), s));
+  RPP_TRY(cudaMemsetAsync(at<float>(dst, P.zero_bias), 0, 2 * static_cast<size_t>(C) * 4, s));
+  return RPP_OK;
+}
+
+size_t rpp_patch_merge_workspace_bytes(const rpp_merge_cfg* cfg, int B) {
+  if (merge_cfg_supported(cfg) != RPP_OK || B <= 0) return 0;
+  const size_t rows = static_cast<size_t>(B) * (cfg->img / 2) * (cfg->img / 2);
+  return align_up(rows * 4 * cfg->channels * 2);
+}
+
+rpp_status rpp_patch_merge_forward(const rpp_merge_cfg* cfg, const void* prepared, int B, const void* x, void* y,
+                                   void* workspace, size_t workspace_bytes, int32_t* err, rpp_stream stream) {
+  const rpp_status st = merge_cfg_supported(cfg);
+  if (st != RPP_OK) return st;
+  if (!prepared || !x || !y || !workspace || B <= 0) return RPP_EINVAL;
+  if (!aligned16(prepared) || !aligned16(x) || !aligned16(y) || !aligned16(workspace)) return RPP_EINVAL;
+  if (workspace_bytes < rpp_patch_merge_workspace_bytes(cfg, B)) return RPP_EWORKSPACE;
+  const long long rows_l = static_cast<long long>(B) * (cfg->img / 2) * (cfg->img / 2);
+  if (rows_l * 4 > 0x7fffffffLL) return RPP_EUNSUPPORTED;
+  const int rows = static_cast<int>(rows_l);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const MergeLayout P = merge_layout(cfg);
+  const rpp_dtype dt = static_cast<rpp_dtype>(cfg->dtype);
+  const int C = cfg->channels;
+  RPP_LAUNCH("patch_merge_ln", s, launch_patch_merge_ln(x, B, cfg->img, C, dt, at<float>(prepared, P.gamma),
+                                                        at<float>(prepared, P.beta), cfg->eps, workspace, err, s));
+  RPP_LAUNCH("gemm_reduction", s, linear(dt, workspace, at<void>(prepared, P.w), at<float>(prepared, P.zero_bias),
+                                         nullptr, y, rows, nullptr, 2 * C, 4 * C, RPP_EPI_BIAS, err, s));
+  return RPP_OK;
+}

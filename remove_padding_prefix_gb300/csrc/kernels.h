@@ -112,6 +112,10 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, in
 // tcgen05 varlen attention, head size 64, fp16 / bf16
 cudaError_t launch_attention_tc(const void* qkv, const int32_t* cu, int B, int T_max, int max_len, int nh,
                                 rpp_dtype dtype, void* out, int32_t* err, cudaStream_t stream);
+// Swin patch merging: the 2 x 2 gather fused into the LayerNorm over 4C channels
+bool patch_merge_supported(int C, int I);
+cudaError_t launch_patch_merge_ln(const void* x, int B, int I, int C, rpp_dtype dtype, const float* gamma,
+                                  const float* beta, float eps, void* out, int32_t* err, cudaStream_t stream);
 cudaError_t launch_attention_varlen(const void* qkv, const int32_t* cu, int B, int T_max, int max_len, int nh, int d,
                                     rpp_dtype dtype, void* out, int32_t* err, cudaStream_t stream);
 

@@ -96,3 +96,14 @@ def test_tuning_and_profiling_knobs_validate_on_the_host(lib):
     assert lib.rpp_set_launch_event_filter(b"gemm_fc1") == 0
     assert lib.rpp_set_launch_event_filter(None) == 0
     assert lib.rpp_launch_event_count() == 0
+
+
+def test_patch_merge_size_queries_and_validation(lib):
+    from remove_padding_prefix_gb300 import _abi
+    ok = _abi.MergeCfg(56, 96, 1e-5, _abi.RPP_F16)
+    assert lib.rpp_patch_merge_bytes(C.byref(ok)) >= 8 * 96 * 96 * 2 + 10 * 96 * 4
+    assert lib.rpp_patch_merge_workspace_bytes(C.byref(ok), 2) >= 2 * 28 * 28 * 4 * 96 * 2
+    assert lib.rpp_patch_merge_bytes(C.byref(_abi.MergeCfg(7, 96, 1e-5, _abi.RPP_F16))) == 0     # odd side
+    assert lib.rpp_patch_merge_bytes(C.byref(_abi.MergeCfg(56, 100, 1e-5, _abi.RPP_F16))) == 0   # C % 8
+    assert lib.rpp_patch_merge_bytes(C.byref(_abi.MergeCfg(56, 96, 1e-5, _abi.RPP_F32))) == 0    # 16-bit only
+    assert lib.rpp_patch_merge_forward(C.byref(ok), None, 1, None, None, None, 0, None, None) == -1

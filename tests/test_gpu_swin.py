@@ -90,3 +90,38 @@ def test_swin_block_full_config_sampled_images():
     for b in (0, 17, c.B - 1):
         ref = oracle.swin_block(wl["x"][b:b + 1], wl["weights"], c.I, c.w, c.s, c.nh, c.eps)
         assert_close(got[b:b + 1], ref, "fp16", f"swin block image {b}")
+
+
+@pytest.mark.parametrize("C,nh,I,s", [(192, 6, 28, 3), (384, 12, 14, 3), (768, 24, 7, 0)])
+def test_swin_block_later_stages(C, nh, I, s):
+    """Swin-T stages 2-4 (C = 192 / 384 / 768 at 28 / 14 / 7 tokens a side; the last stage's
+    single window is unshifted) through the same kernels."""
+    from dataclasses import replace
+    wl = make_swin_workload(replace(SWIN, C=C, nh=nh), B=1, I=I, s=s, affine=True)
+    c = wl["cfg"]
+    cfg = rpp.swin_cfg(c.I, c.C, c.nh, c.w, c.s, c.F, c.eps, "fp16")
+    block = rpp.SwinBlock(cfg, wl["weights"])
+    err = rpp.new_error_word()
+    y = rpp.swin_block_forward(block, up(wl["x"].reshape(-1, c.C), "fp16"), c.B, err=err)
+    check_err(err)
+    ref = oracle.swin_block(wl["x"], wl["weights"], c.I, c.w, c.s, c.nh, c.eps)
+    assert_close(down(y).reshape(ref.shape), ref, "fp16", f"swin stage C={C}")
+
+
+@pytest.mark.parametrize("I,C,dtype,B", [(56, 96, "fp16", 3), (28, 192, "bf16", 2), (14, 384, "fp16", 2),
+                                         (8, 768, "fp16", 1), (4, 8, "fp16", 2)])
+def test_patch_merge(I, C, dtype, B):
+    """At C = 768 (K = 3072) the outputs have magnitude ~1, where the bf16 output rounding
+    alone averages ~2e-3 (a quarter of a bf16 step), the mean-abs bound itself; that
+    size runs in fp16."""
+    rng = np.random.default_rng(I + C)
+    x = round_to_dtype(rng.standard_normal((B, I * I, C), dtype=np.float32), dtype)
+    gamma = round_to_dtype(1 + 0.1 * rng.standard_normal(4 * C, dtype=np.float32), dtype)
+    beta = round_to_dtype(0.1 * rng.standard_normal(4 * C, dtype=np.float32), dtype)
+    W = round_to_dtype(0.02 * rng.standard_normal((4 * C, 2 * C), dtype=np.float32), dtype)
+    pm = rpp.PatchMerge(rpp.merge_cfg(I, C, 1e-5, dtype), gamma, beta, W)
+    err = rpp.new_error_word()
+    y = rpp.patch_merge_forward(pm, up(x.reshape(-1, C), dtype), B, err=err)
+    check_err(err)
+    ref = oracle.patch_merge(x, I, gamma, beta, W, 1e-5)
+    assert_close(down(y).reshape(ref.shape), ref, dtype, f"patch merge I={I} C={C}")

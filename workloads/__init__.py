@@ -29,7 +29,7 @@ import numpy as np
 __all__ = [
     "EncoderConfig", "SwinConfig", "CONFIGS", "config_by_name",
     "round_to_dtype", "draw_lengths", "make_bert_workload", "make_swin_workload",
-    "make_calibration_batch",
+    "make_calibration_batch", "make_patch_merge_workload",
 ]
 
 
@@ -243,3 +243,20 @@ def make_swin_workload(cfg: SwinConfig, *, seed: Optional[int] = None, B: Option
             wt["gamma" + k] = np.ones(C, np.float32)
             wt["beta" + k] = np.zeros(C, np.float32)
     return {"cfg": cfg, "x": x, "weights": wt}
+
+
+def make_patch_merge_workload(cfg: SwinConfig, *, seed: Optional[int] = None, B: Optional[int] = None,
+                              I: Optional[int] = None) -> dict:
+    """Seeded input and weights of the stage downsampling after a Swin stage of `cfg`'s
+    shape (seed + 300 unless given): dict(cfg, x [B, I*I, C], gamma [4C], beta [4C],
+    W [4C, 2C]).  Draw order: x, gamma, beta, W."""
+    if B is not None or I is not None:
+        cfg = replace(cfg, B=B or cfg.B, I=I or cfg.I)
+    rng = np.random.default_rng(np.random.PCG64(cfg.seed + 300 if seed is None else seed))
+    dt = cfg.storage_dtype
+    C = cfg.C
+    x = _normal(rng, (cfg.B, cfg.I * cfg.I, C), 1.0, dt)
+    gamma = round_to_dtype(1.0 + 0.1 * rng.standard_normal(4 * C, dtype=np.float32), dt)
+    beta = _normal(rng, (4 * C,), 0.1, dt)
+    W = _normal(rng, (4 * C, 2 * C), cfg.weight_std, dt)
+    return {"cfg": cfg, "x": x, "gamma": gamma, "beta": beta, "W": W}
