@@ -676,6 +676,8 @@ rpp_status rpp_encoder_forward(const rpp_encoder_cfg* cfg, const void* const* la
   if (st != RPP_OK) return st;
   if (!layers || num_layers <= 0 || !lengths || !x_padded || !y_padded || !cu_seqlens || !padding_offset || !packed)
     return RPP_EINVAL;
+  for (int i = 0; i < num_layers; ++i)   // every layer is checked before any kernel is launched
+    if (!layers[i] || !aligned16(layers[i])) return RPP_EINVAL;
   if (cfg->int8 && !act_scales) return RPP_EINVAL;
   const rpp_dtype dt = static_cast<rpp_dtype>(cfg->dtype);
   const int H = cfg->hidden;
