@@ -63,7 +63,9 @@ __global__ void __launch_bounds__(128) layernorm_kernel(LnArgs a) {
   const int H = a.H;
   // The prologue's global reads (error word, device row count, gamma / beta / bias)
   // are independent: all are issued before any is used, one round trip in all.
-  constexpr int kPre = 8;   // values of each parameter vector a thread stages (H <= 1024)
+  // values of each parameter vector a thread stages: this instantiation's row width
+  // (G lanes x VPL vectors x EPV elements) over the 128 threads
+  constexpr int kPre = (G * VPL * Vec<T>::N + 127) / 128;
   float pg[kPre], pb[kPre], pc[kPre];
 #pragma unroll
   for (int k = 0; k < kPre; ++k) {
@@ -123,8 +125,9 @@ __global__ void __launch_bounds__(128) layernorm_kernel(LnArgs a) {
     long long dst = -1;        // output row
     if (it < n_iter) {
       if (padded) {
-        const int b = static_cast<int>(it / a.pad_L);
-        const int p = static_cast<int>(it - static_cast<long long>(b) * a.pad_L);
+        // 32-bit division: the host keeps pad_B * pad_L below 2^31
+        const unsigned b = static_cast<unsigned>(it) / static_cast<unsigned>(a.pad_L);
+        const int p = static_cast<int>(static_cast<unsigned>(it) - b * static_cast<unsigned>(a.pad_L));
         const int c0 = a.pad_cu[b];
         if (p < a.pad_cu[b + 1] - c0) src = c0 + p;
         dst = it;
@@ -136,7 +139,10 @@ __global__ void __launch_bounds__(128) layernorm_kernel(LnArgs a) {
     const bool valid = src >= 0;
     // ---- loads: input and its split-K slices (NS > 1), residual -- all issued together
     uint4 rx[NS][VPL];
-    uint4 rr[VPL][EPV / 4];
+    // residual adds are taken only with fp32 input (the host rejects the rest): 16-bit
+    // instantiations carry no residual registers
+    constexpr bool kRes = std::is_same<T, float>::value;
+    uint4 rr[kRes ? VPL : 1][kRes ? EPV / 4 : 1];
 #pragma unroll
     for (int sl = 0; sl < NS; ++sl) {
       if (sl == 0 || sl < a.n_in) {
@@ -146,7 +152,8 @@ __global__ void __launch_bounds__(128) layernorm_kernel(LnArgs a) {
         for (int i = 0; i < VPL; ++i) rx[sl][i] = valid ? xr[i * G + gl] : make_uint4(0u, 0u, 0u, 0u);
       }
     }
-    const bool has_res = a.residual != nullptr && valid;
+    const bool has_res = kRes && a.residual != nullptr && valid;
+    if constexpr (kRes) {
     if (has_res) {
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
@@ -161,6 +168,7 @@ __global__ void __launch_bounds__(128) layernorm_kernel(LnArgs a) {
           }
         }
       }
+    }
     }
     float v[VPL][EPV];
 #pragma unroll
@@ -199,6 +207,7 @@ __global__ void __launch_bounds__(128) layernorm_kernel(LnArgs a) {
         for (int j = 0; j < EPV; ++j) v[i][j] += s_bias[col0 + j];
       }
     }
+    if constexpr (kRes) {
     if (has_res) {
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
@@ -221,6 +230,7 @@ __global__ void __launch_bounds__(128) layernorm_kernel(LnArgs a) {
           v[i][4 * j + 0] += f[0]; v[i][4 * j + 1] += f[1]; v[i][4 * j + 2] += f[2]; v[i][4 * j + 3] += f[3];
         }
       }
+    }
     }
     // ---- statistics (biased variance, two passes over the registers)
     float sum = 0.f;
@@ -346,7 +356,18 @@ cudaError_t ln_launch(const LnArgs& a, cudaStream_t stream) {
   const int rows_per_block = (threads / 32) * (32 / G);
   const long long n_iter = a.pad_cu ? static_cast<long long>(a.pad_B) * a.pad_L : a.M_max;
   long long blocks = (n_iter + rows_per_block - 1) / rows_per_block;
-  const long long cap = static_cast<long long>(num_sms()) * 16;
+  // the row loop is grid-strided: one wave of resident blocks covers any row count
+  // without a partial last wave
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int n = 0;
+    const size_t smem_row = 3 * static_cast<size_t>(G) * VPL * Vec<T>::N * sizeof(float);   // = smem below
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, layernorm_kernel<T, TOut, G, VPL, NS>, threads, smem_row) !=
+            cudaSuccess || n < 1)
+      n = 4;
+    per_sm = n;
+  }
+  const long long cap = static_cast<long long>(num_sms()) * per_sm;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   const size_t smem = 3 * static_cast<size_t>(a.H) * sizeof(float);
@@ -397,6 +418,7 @@ cudaError_t launch_layernorm(const LnArgs& args, cudaStream_t stream) {
   a.res_kind = !a.residual ? 0 : (a.res_dtype == RPP_F32 ? 1 : (a.res_dtype == RPP_F16 ? 2 : 3));
   if (a.residual && a.in_dtype != RPP_F32) return cudaErrorNotSupported;   // residual adds use 4-element groups
   if (a.pad_cu && (a.pad_B <= 0 || a.pad_L <= 0)) return cudaErrorInvalidValue;
+  if (a.pad_cu && static_cast<long long>(a.pad_B) * a.pad_L > 0x7fffffffLL) return cudaErrorNotSupported;
   using BF = __nv_bfloat16;
   if (a.in_dtype == a.out_dtype) {
     switch (a.in_dtype) {
