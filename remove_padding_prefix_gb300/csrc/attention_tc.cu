@@ -274,23 +274,32 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attention_tc_kernel(const __g
       mx = fmaxf(mx, s_red[(j & 1) * 256 + (hf ^ 1) * 128 + r]) * scale_log2;   // the row's tile maximum
       // Lazy rescaling: the reference maximum moves only when the tile's exceeds it by
       // more than 8 (P stays below 2^8); then O (in tensor memory) and the row sum are
-      // rescaled.  Both threads of a row see the same values and decide alike.
+      // rescaled.  Both threads of a row see the same values and decide alike.  The
+      // decision is per row, but the tensor-memory loads and stores are warp-collective:
+      // when any row of the warp rescales, the whole warp runs them (scale 1 for rows
+      // that keep their maximum -- exact), so no lane skips a collective instruction
+      // whatever the rows hold (query rows past the sequence end hold arbitrary data).
       if (j == 0) {
         m = mx;
-      } else if (mx > m + 8.0f) {
-        const float alpha = ex2_approx(m - mx);
+      } else {
+        const bool move = mx > m + 8.0f;
+        if (__any_sync(0xffffffffu, move)) {
+          const float alpha = move ? ex2_approx(m - mx) : 1.0f;
 #pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          uint32_t ov[16];
-          tmem_ld_32x32b_x16(t_lane + kKT + hf * 32 + c * 16, ov);
-          tmem_ld_wait();
+          for (int c = 0; c < 2; ++c) {
+            uint32_t ov[16];
+            tmem_ld_32x32b_x16(t_lane + kKT + hf * 32 + c * 16, ov);
+            tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-          tmem_st_32x32b_x16(t_lane + kKT + hf * 32 + c * 16, ov);
+            for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st_32x32b_x16(t_lane + kKT + hf * 32 + c * 16, ov);
+          }
+          tmem_st_wait();
+          if (move) {
+            l *= alpha;
+            m = mx;
+          }
         }
-        tmem_st_wait();
-        l *= alpha;
-        m = mx;
       }
       // P = 2^(s - m) for this half's 64 keys (one 64-key column block of P)
       float ps[4] = {0.f, 0.f, 0.f, 0.f};   // independent partial sums

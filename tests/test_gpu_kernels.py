@@ -114,8 +114,14 @@ def _attention_case(dtype, lengths, nh, seed=0, max_len=None, poison=False):
     cu, _ = rpp.build_offsets(lt, L, err=err)
     out = torch.full((T_max, nh * d), float("nan"), dtype=TDT[dtype], device=dev())
     qkv_d = up(qkv, dtype)
-    if poison:   # capacity rows past T hold NaN: a kernel must never let them reach a valid output
+    if poison == "nan":   # capacity rows past T hold NaN: a kernel must never let them reach a valid output
         qkv_d[T:] = float("nan")
+    elif poison == "large":
+        # capacity rows past T hold large finite values of both signs: the query rows past
+        # the last sequence's end (computed, never stored) then see row maxima that jump
+        # between key tiles in some rows of a warp and not in others
+        big = 300.0 * np.sign(rng.standard_normal((T_max - T, 3 * nh * d))) * rng.uniform(0.5, 1.0, (T_max - T, 1))
+        qkv_d[T:] = torch.as_tensor(big, dtype=torch.float32, device=dev()).to(qkv_d.dtype)
     rpp.attention_varlen(qkv_d, cu, len(lengths), L, nh, out=out, err=err)
     check_err(err)
     cu_ref, _, _ = oracle.build_offsets(lengths, L)
@@ -134,8 +140,17 @@ def test_attention_ragged(dtype):
 @pytest.mark.parametrize("dtype", ["fp16", "bf16", "fp32"])
 def test_attention_ignores_non_finite_capacity_rows(dtype):
     # the last sequence ends inside a key tile, so its last tile spans rows past T
-    _attention_case(dtype, [130, 57, 201], nh=2, seed=5, poison=True)
-    _attention_case(dtype, [3], nh=1, seed=6, poison=True)
+    _attention_case(dtype, [130, 57, 201], nh=2, seed=5, poison="nan")
+    _attention_case(dtype, [3], nh=1, seed=6, poison="nan")
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16", "fp32"])
+def test_attention_rows_past_sequence_end_with_large_values(dtype):
+    """Rows past T hold large values: the out-of-sequence query rows of the last query
+    tile rescale their running maximum while the valid rows of the same warp do not.
+    The valid outputs must not change and the kernel must run to completion."""
+    _attention_case(dtype, [130, 57, 201], nh=2, seed=8, poison="large")
+    _attention_case(dtype, [64, 300], nh=3, seed=9, poison="large")
 
 
 def test_attention_bert_large_lengths():

@@ -17,9 +17,11 @@ from gpu_util import dev, up, down, assert_close, check_err, TOL
 pytestmark = pytest.mark.gpu
 
 
-def _run_path(wl, dtype, layers=None, hint=False):
+def _run_path(wl, dtype, layers=None, hint=False, poison=None):
     """hint=True passes the true token count as the tile-shape hint (the bench's launch
-    configuration: exact-size tiles and split-K with LayerNorm-side reduction)."""
+    configuration: exact-size tiles and split-K with LayerNorm-side reduction).
+    poison: a byte every workspace byte is set to before the call (the capacity past the
+    token count is never written and must never reach a valid output)."""
     cfg = wl["cfg"]
     layers = layers if layers is not None else wl["layers"]
     T = int(wl["lengths"].sum())
@@ -28,7 +30,11 @@ def _run_path(wl, dtype, layers=None, hint=False):
     lengths = torch.as_tensor(wl["lengths"], device=dev())
     x = up(wl["x_padded"].reshape(-1, cfg.H), dtype)
     err = rpp.new_error_word()
-    y, cu, po = rpp.encoder_forward(prepared, lengths, x, cfg.L, err=err)
+    ws = None
+    if poison is not None:
+        ws = prepared[0].workspace(cfg.B * cfg.L, dev())
+        ws.view(torch.uint8).fill_(poison)
+    y, cu, po = rpp.encoder_forward(prepared, lengths, x, cfg.L, workspace=ws, err=err)
     check_err(err)
     # the fused offsets + removal of the whole-path call: offsets bit-exact
     cu_ref, po_ref, T = oracle.build_offsets(wl["lengths"], cfg.L)
@@ -50,6 +56,20 @@ def test_layer_small(idx, B, L, lens, hint):
     got, _ = _run_path(wl, cfg.dtype, hint=hint)
     ref, _, _ = oracle.bert_forward(wl["x_padded"], wl["lengths"], wl["layers"], cfg.nh, cfg.eps)
     assert_close(got, ref, cfg.dtype, cfg.name)
+
+
+@pytest.mark.parametrize("hint", [False, True])
+@pytest.mark.parametrize("idx,lens", [(1, [128, 1, 17, 64, 65, 100]), (2, [384, 129, 33])])
+def test_layer_poisoned_workspace(idx, lens, hint):
+    """Workspace bytes 0x47 (7.3 in fp16, 5.1e4 in bf16 and fp32) before the call: the
+    unwritten capacity rows past the token count feed the attention's out-of-sequence
+    query rows large values; the valid outputs match the oracle all the same."""
+    cfg = CONFIGS[idx]
+    wl = make_bert_workload(cfg, B=len(lens), L=max(lens) if idx == 1 else 384, layers=1,
+                            lengths=np.array(lens, np.int32), affine=True)
+    got, _ = _run_path(wl, cfg.dtype, hint=hint, poison=0x47)
+    ref, _, _ = oracle.bert_forward(wl["x_padded"], wl["lengths"], wl["layers"], cfg.nh, cfg.eps)
+    assert_close(got, ref, cfg.dtype, f"{cfg.name} poisoned workspace")
 
 
 @pytest.mark.parametrize("mode", [1, 2])
