@@ -71,33 +71,48 @@ template <> __device__ __forceinline__ uint4 pack16<__nv_bfloat16>(const float* 
 }
 
 // Exact-form GELU, x * Phi(x), evaluated through the complementary error function:
-// with t = |x| / sqrt(2), Phi(x) = 1 - erfc(t) / 2 for x >= 0 and erfc(t) / 2 for x < 0,
-// so x Phi(x) = x / 2 + |x| (1/2 - e) with e = erfc(t) / 2 for either sign.  And
-// erfc(t) = exp(P(t) - t^2), P a degree-7 least-squares Chebyshev fit of
-// log(erfcx(t)) = log(exp(t^2) erfc(t)) on [0, 3.9]; the base-2 change, the -t^2 and
-// the halving are folded into the coefficients (Q = log2(e) (P - t^2) - 1, from
-// fit_gelu.py next to this file), so e = 2^Q(t).  Beyond t = 3.9, erfc < 3.5e-8 and t
-// is clamped.  One exp2, eight FMAs and three other operations per element; against
-// the fp64 definition the error is at most 6.8e-7 absolute on [-8, 8], far below
-// fp16/bf16 output rounding.
+// with e = erfc(|x| / sqrt(2)) / 2, Phi(x) = 1 - e for x >= 0 and e for x < 0, so
+// x Phi(x) = relu(x) - |x| e for either sign.  And erfc(t) = exp(P(t) - t^2), P a
+// least-squares Chebyshev fit of log(erfcx(t)) = log(exp(t^2) erfc(t)); the base-2
+// change, the -t^2, the halving and t = |x| / sqrt(2) are folded into the coefficients
+// (fit_gelu.py next to this file derives them), so e = 2^Q(a) with a = min(|x|, A).
+// Beyond A, |x| e < 1e-7 and a is clamped.  Two fits:
+//   DEG 7 (fp32 outputs, int8 codes): at most 6.4e-7 absolute error on [-10, 10];
+//   DEG 5 (fp16 / bf16 outputs): at most 3.8e-5 (near |x| = 0.4 to 1.2, a third of
+//     half an fp16 ulp there), 4.3e-6 on average over [-10, 10] against 4.6e-4 for the
+//     fp16 rounding of the output itself.
+// One exp2, DEG + 1 FMAs and two other operations per element.
 __device__ __forceinline__ float ex2_approx(float v) {
   float r;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
   return r;
 }
+template <int DEG = 7>
 __device__ __forceinline__ float gelu_erf(float x) {
+  static_assert(DEG == 7 || DEG == 5, "fitted degrees: 7 and 5");
   const float ax = fabsf(x);
-  const float t = fminf(ax * 0.70710678118654752f, 3.9f);
-  float q = -2.174795191e-05f;
-  q = fmaf(q, t, 5.064556026e-04f);
-  q = fmaf(q, t, -5.337523762e-03f);
-  q = fmaf(q, t, 3.422686458e-02f);
-  q = fmaf(q, t, -1.528851390e-01f);
-  q = fmaf(q, t, -9.167622924e-01f);
-  q = fmaf(q, t, -1.628153682e+00f);
-  q = fmaf(q, t, -9.999938607e-01f);
-  const float e = ex2_approx(q);   // erfc(t) / 2
-  return fmaf(ax, 0.5f - e, 0.5f * x);
+  float q;
+  if constexpr (DEG == 7) {
+    const float a = fminf(ax, 5.939696789e+00f);
+    q = -1.899352810e-06f;
+    q = fmaf(q, a, 6.287013821e-05f);
+    q = fmaf(q, a, -9.402981959e-04f);
+    q = fmaf(q, a, 8.544798940e-03f);
+    q = fmaf(q, a, -5.403082818e-02f);
+    q = fmaf(q, a, -4.584006965e-01f);
+    q = fmaf(q, a, -1.151272178e+00f);
+    q = fmaf(q, a, -9.999941587e-01f);
+  } else {
+    const float a = fminf(ax, 5.515432835e+00f);
+    q = -2.286325034e-04f;
+    q = fmaf(q, a, 4.808620550e-03f);
+    q = fmaf(q, a, -4.431765527e-02f);
+    q = fmaf(q, a, -4.702030122e-01f);
+    q = fmaf(q, a, -1.145930171e+00f);
+    q = fmaf(q, a, -1.000390410e+00f);
+  }
+  const float e = ex2_approx(q);   // erfc(|x| / sqrt(2)) / 2
+  return fmaf(-ax, e, fmaxf(x, 0.f));
 }
 
 // ---------------------------------------------------------------- shared memory / mbarrier

@@ -179,7 +179,7 @@ __device__ __forceinline__ void epi_math(const GemmParams& p, float* v, int row,
   }
   if constexpr (EPI == RPP_EPI_BIAS_GELU || EPI == EPI_DQ_BIAS_GELU_Q) {
 #pragma unroll
-    for (int j = 0; j < NV; ++j) v[j] = gelu_erf(v[j]);
+    for (int j = 0; j < NV; ++j) v[j] = gelu_erf<(EPI == RPP_EPI_BIAS_GELU && sizeof(TOut) == 2) ? 5 : 7>(v[j]);
   }
   if constexpr (EPI == EPI_DQ_BIAS_GELU_Q) {
 #pragma unroll
