@@ -186,3 +186,22 @@ def test_device_gelu_against_exact_definition():
     ref = oracle.gelu(x.astype(np.float64))
     err = np.abs(got - ref)
     assert np.all(err <= 5e-7 * (1.0 + np.abs(x))), (err.max(), x[np.argmax(err)])
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_device_gelu_16bit_outputs(dtype):
+    """16-bit outputs take the degree-5 fit (at most 3.8e-5 from x * Phi(x)): with identity
+    weights the accumulator is exactly x, and each output is within half a step of its
+    dtype plus that fit error of the fp64 definition."""
+    rng = np.random.default_rng(11)
+    x = round_to_dtype(np.concatenate([np.linspace(-8, 8, 64 * 500), rng.standard_normal(64 * 500) * 2]
+                                      ).astype(np.float32), dtype)
+    a = x.reshape(-1, 64)
+    eye = np.eye(64, dtype=np.float32)
+    out = rpp.linear(up(a, dtype), up(eye, dtype), torch.zeros(64, device=dev()), epilogue=rpp.RPP_EPI_BIAS_GELU)
+    got = down(out).reshape(-1).astype(np.float64)
+    ref = oracle.gelu(x.astype(np.float64))
+    mant = 10 if dtype == "fp16" else 7
+    half_step = np.ldexp(1.0, np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -14))).astype(int) - mant - 1)
+    err = np.abs(got - ref)
+    assert np.all(err <= half_step + 4e-5), (err.max(), x[np.argmax(err - half_step)])
