@@ -291,6 +291,8 @@ class SwinWorkload:
             return 2.0 * T * C_ * F, e * (T * C_ + F * C_ + T * F)
         if label == "gemm_fc2":
             return 2.0 * T * F * C_, e * (T * F + F * C_ + 2 * T * C_)
+        if label == "swin_mlp":   # FC1 + GELU + FC2 + residual, hidden layer on chip: h, y in, out
+            return 4.0 * T * C_ * F, e * (3 * T * C_ + 2 * F * C_)
         return 0.0, 0.0
 
     def oracle_rate(self, budget_s):

@@ -386,7 +386,7 @@ rpp_status encoder_layer_run(const rpp_encoder_cfg* c, const void* layer, const 
 
 // ---------------------------------------------------------------- prepared Swin block
 struct SwinLayout {
-  size_t wqkv, wo, w1, w2, bqkv, bo, b1, b2, g1, be1, g2, be2, bias, total;
+  size_t wqkv, wo, w1, w2, w1kn, bqkv, bo, b1, b2, g1, be1, g2, be2, bias, total;
 };
 
 rpp_status swin_cfg_supported(const rpp_swin_cfg* c) {
@@ -411,6 +411,7 @@ SwinLayout swin_layout(const rpp_swin_cfg* c) {
   L.wo = o;   o = align_up(o + C * C * e);
   L.w1 = o;   o = align_up(o + F * C * e);
   L.w2 = o;   o = align_up(o + C * F * e);
+  L.w1kn = o; o = align_up(o + (swin_mlp_supported(c->channels, c->mlp) ? C * F * e : 0));   // fused MLP's W1
   L.bqkv = o; o = align_up(o + 3 * C * 4);
   L.bo = o;   o = align_up(o + C * 4);
   L.b1 = o;   o = align_up(o + F * 4);
@@ -781,6 +782,8 @@ rpp_status rpp_swin_prepare_block(const rpp_swin_cfg* cfg, const rpp_swin_src* s
   RPP_TRY(launch_transpose_to_kmajor(src->Wo, C, C, 2, at<void>(dst, P.wo), C, s));
   RPP_TRY(launch_transpose_to_kmajor(src->W1, C, F, 2, at<void>(dst, P.w1), C, s));
   RPP_TRY(launch_transpose_to_kmajor(src->W2, F, C, 2, at<void>(dst, P.w2), F, s));
+  if (swin_mlp_supported(C, F))   // W1 as given ([C, F]: the fused MLP reads it N-major)
+    RPP_TRY(cudaMemcpyAsync(at<void>(dst, P.w1kn), src->W1, static_cast<size_t>(C) * F * 2, cudaMemcpyDeviceToDevice, s));
   RPP_TRY(launch_to_f32(src->bqkv, dt, 3 * C, at<float>(dst, P.bqkv), s));
   RPP_TRY(launch_to_f32(src->bo, dt, C, at<float>(dst, P.bo), s));
   RPP_TRY(launch_to_f32(src->b1, dt, F, at<float>(dst, P.b1), s));
@@ -841,6 +844,11 @@ rpp_status rpp_swin_block_forward(const rpp_swin_cfg* cfg, const void* block, in
   l2.gamma = at<float>(block, P.g2);
   l2.beta = at<float>(block, P.be2);
   RPP_LAUNCH("layernorm2", s, launch_layernorm(l2, s));
+  if (swin_mlp_supported(C, F)) {   // FC1 + GELU + FC2 + residual in one kernel, hidden layer on chip
+    RPP_LAUNCH("swin_mlp", s, launch_swin_mlp(h, at<void>(block, P.w1kn), at<float>(block, P.b1), at<void>(block, P.w2),
+                                             at<float>(block, P.b2), xa, y, T, C, F, dt, err, s));
+    return RPP_OK;
+  }
   RPP_LAUNCH("gemm_fc1", s, linear(dt, h, at<void>(block, P.w1), at<float>(block, P.b1), nullptr, g, T, nullptr, F, C, RPP_EPI_BIAS_GELU,
                  err, s));
   RPP_LAUNCH("gemm_fc2", s, linear(dt, g, at<void>(block, P.w2), at<float>(block, P.b2), xa, y, T, nullptr, C, F, RPP_EPI_BIAS_RESIDUAL,

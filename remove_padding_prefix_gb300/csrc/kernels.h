@@ -112,6 +112,12 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, in
 // tcgen05 varlen attention, head size 64, fp16 / bf16
 cudaError_t launch_attention_tc(const void* qkv, const int32_t* cu, int B, int T_max, int max_len, int nh,
                                 rpp_dtype dtype, void* out, int32_t* err, cudaStream_t stream);
+// Swin MLP fused on the tensor cores (C = 96, F = 384): out = resid + FC2(GELU(FC1(h) + b1)) + b2;
+// w1_kn is W1 as [C, F] (K rows, N columns), w2_nk is W2 as [C, F] (N rows, K columns)
+bool swin_mlp_supported(int C, int F);
+cudaError_t launch_swin_mlp(const void* h, const void* w1_kn, const float* b1, const void* w2_nk, const float* b2,
+                            const void* resid, void* out, int M, int C, int F, rpp_dtype dtype, int32_t* err,
+                            cudaStream_t stream);
 // Swin patch merging: the 2 x 2 gather fused into the LayerNorm over 4C channels
 bool patch_merge_supported(int C, int I);
 cudaError_t launch_patch_merge_ln(const void* x, int B, int I, int C, rpp_dtype dtype, const float* gamma,
