@@ -9,13 +9,14 @@
 // and y once and writes out once (6 C bytes in 16-bit types), against 6 C + 4 F for the
 // two separate GEMMs.
 //
-// Persistent, one CTA per SM, 18 warps:
+// Persistent, one CTA per SM, 2 + EW warps (EW = 16 epilogue warps; 8 warps of twice
+// the columns measured 8% slower on the Swin-T stage-1 block):
 //   warp 0      TMA: W1 once (before the programmatic-launch wait -- the weights are
 //               not written by the preceding kernel), each tile's h rows, and W2 one
 //               64-wide K panel at a time through a two-slot ring (from L2);
 //   warp 1      MMA issue (one thread): FC1 of a tile in two halves of 192 hidden
 //               columns, FC2 in six 64-wide K blocks;
-//   warps 2-17  epilogue: per 64-column block of the hidden activation, tensor memory
+//   warps 2..   epilogue: per 64-column block of the hidden activation, tensor memory
 //               -> registers, + b1, GELU, fp16/bf16 -> a 128-byte-swizzled K-major block
 //               in shared memory; per tile, the FC2 accumulator + b2 + y -> out.
 // Shared memory (bytes): W1 as six MN-major panels [96 K rows x 64 N] (73 728), two
@@ -42,7 +43,7 @@ namespace {
 constexpr int kMC = 96;                        // C
 constexpr int kMF = 384;                       // F = 4C
 constexpr int kMBM = 128;                      // tokens per tile
-constexpr int kMThreads = 576;                 // 18 warps
+constexpr int kMlpEW = 16;                     // epilogue warps (8 or 16)
 constexpr uint32_t kPanel = kMC * 128;         // 96 rows x 128 bytes
 constexpr uint32_t kW1Bytes = 6 * kPanel;
 constexpr int kW2Slots = 2;
@@ -58,14 +59,20 @@ template <typename T> struct MlpFmt;
 template <> struct MlpFmt<__half> { static constexpr int v = 0; };
 template <> struct MlpFmt<__nv_bfloat16> { static constexpr int v = 1; };
 
-template <typename T>
-__global__ void __launch_bounds__(kMThreads, 1)
+template <int EW>
+constexpr int mlp_threads() { return 64 + 32 * EW; }
+
+template <typename T, int EW>
+__global__ void __launch_bounds__(mlp_threads<EW>(), 1)
 swin_mlp_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmW1,
                 const __grid_constant__ CUtensorMap tmW2, const float* __restrict__ b1, const float* __restrict__ b2,
                 const T* __restrict__ resid, T* __restrict__ out, int M, int32_t* err) {
   constexpr int fmt = MlpFmt<T>::v;
   constexpr uint32_t IDESC_FC1 = idesc_f16(fmt, kMBM, 64) | (1u << 16);   // B (W1 panel) MN-major
   constexpr uint32_t IDESC_FC2 = idesc_f16(fmt, kMBM, kMC);
+  static_assert(EW == 8 || EW == 16, "two or four epilogue warps per lane quadrant");
+  constexpr int WPQ = EW / 4;    // epilogue warps per tensor-memory lane quadrant
+  constexpr int CW = 64 / WPQ;   // hidden columns of a 64-wide block per warp
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -98,14 +105,14 @@ swin_mlp_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__
     mbar_init(a_empty, 1);
     for (int h = 0; h < 2; ++h) {
       mbar_init(&s_full[h], 1);
-      mbar_init(&s_empty[h], 16);
+      mbar_init(&s_empty[h], EW);
     }
     for (int b = 0; b < kHBufs; ++b) {
-      mbar_init(&h_full[b], 16);
+      mbar_init(&h_full[b], EW);
       mbar_init(&h_empty[b], 1);
     }
     mbar_init(o_full, 1);
-    mbar_init(o_empty, 16);
+    mbar_init(o_empty, EW);
     mbar_init(drain, 1);
     for (int k = 0; k < kW2Slots; ++k) {
       mbar_init(&p_full[k], 1);
@@ -243,7 +250,7 @@ swin_mlp_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__
   } else {
     // ------------------------------------------------------------ epilogue warps
     const int q = warp & 3;                  // tensor-memory lane quadrant
-    const int part = (warp - 2) >> 2;        // 0..3
+    const int part = (warp - 2) >> 2;        // 0 .. WPQ - 1
     const int r = q * 32 + lane;             // row of the tile
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     bool ok = true;
@@ -253,82 +260,99 @@ swin_mlp_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__
       if (lane == 0) w = mbar_wait_bounded(bar, parity, abort_flag) ? 1 : 0;
       return __shfl_sync(0xffffffffu, w, 0) != 0;
     };
-    // G(i, b): GELU of hidden block b (this warp: its 16 columns of the block)
+    // G(i, b): GELU of hidden block b (this warp: its CW columns of the block)
     auto gelu_block = [&](int i, int b) -> bool {
       const int buf = b;   // block b of every tile: FC2(i - 1, b) has released it
       if ((b == 0 || b == 3) && !wait_all(&s_full[b / 3], i & 1)) return false;
       if (!wait_all(&h_empty[buf], (i & 1) ^ 1)) return false;
-      const int col = 64 * b + 16 * part;
+      const int col = 64 * b + CW * part;
       const float4* bb = reinterpret_cast<const float4*>(b1 + col);
-      const float4 c0 = __ldg(bb), c1 = __ldg(bb + 1), c2 = __ldg(bb + 2), c3 = __ldg(bb + 3);
+      float4 bq[CW / 4];
+#pragma unroll
+      for (int k = 0; k < CW / 4; ++k) bq[k] = __ldg(bb + k);
       tc_fence_after();
-      uint32_t v[16];
+      uint32_t v[CW];
       tmem_ld_32x32b_x16(t_lane + col, v);
+      if constexpr (CW == 32) tmem_ld_32x32b_x16(t_lane + col + 16, v + 16);
       tmem_ld_wait();
       if (b == 2 || b == 5) {   // this warp has read its share of the FC1 half
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_empty[b / 3]);
       }
-      const float bias[16] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w,
-                              c2.x, c2.y, c2.z, c2.w, c3.x, c3.y, c3.z, c3.w};
-      float f[16];
+      float f[CW];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) f[e] = gelu_erf<5>(__uint_as_float(v[e]) + bias[e]);
-      // 16 columns = 32 bytes = 16-byte chunks 2 part and 2 part + 1 of the 128-byte
-      // row, at chunk ^ (r & 7) (the 128-byte swizzle)
+      for (int k = 0; k < CW / 4; ++k) {
+        f[4 * k + 0] = gelu_erf<5>(__uint_as_float(v[4 * k + 0]) + bq[k].x);
+        f[4 * k + 1] = gelu_erf<5>(__uint_as_float(v[4 * k + 1]) + bq[k].y);
+        f[4 * k + 2] = gelu_erf<5>(__uint_as_float(v[4 * k + 2]) + bq[k].z);
+        f[4 * k + 3] = gelu_erf<5>(__uint_as_float(v[4 * k + 3]) + bq[k].w);
+      }
+      // CW columns = CW / 8 16-byte chunks of the 128-byte row, starting at chunk
+      // (CW / 8) part, each at chunk ^ (r & 7) (the 128-byte swizzle)
       uint8_t* row = sH + buf * kHBytes + r * 128;
-      *reinterpret_cast<uint4*>(row + (((2 * part) ^ (r & 7)) << 4)) = pack16<T>(f);
-      *reinterpret_cast<uint4*>(row + (((2 * part + 1) ^ (r & 7)) << 4)) = pack16<T>(f + 8);
+#pragma unroll
+      for (int c = 0; c < CW / 8; ++c)
+        *reinterpret_cast<uint4*>(row + ((((CW / 8) * part + c) ^ (r & 7)) << 4)) = pack16<T>(f + 8 * c);
       fence_proxy_async_smem();   // visible to the tensor core
       __syncwarp();
       if (lane == 0) mbar_arrive(&h_full[buf]);
       return true;
     };
-    // the residual rows of tile i (parts 0..2: 32 columns, 64 bytes of the row each),
-    // requested a few hidden blocks before F(i) needs them
+    // The final epilogue works in 16-column chunks of the C = 96 outputs: chunk c of a
+    // row belongs to part c % WPQ of its lane quadrant (at most NC chunks a warp).
+    constexpr int NC = (kMC / 16 + WPQ - 1) / WPQ;
+    // the residual rows of tile i (32 bytes a chunk), requested a few hidden blocks
+    // before F(i) needs them
     auto load_resid = [&](int i, uint4* rv) {
       const long long grow = static_cast<long long>(kMBM) * tile_of(i) + r;
-      if (part < 3 && grow < M) {
-        const uint4* rr = reinterpret_cast<const uint4*>(resid + grow * kMC + 32 * part);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) rv[c] = rr[c];
+      for (int k = 0; k < NC; ++k) {
+        const int c = part + WPQ * k;
+        if (c < kMC / 16 && grow < M) {
+          const uint4* rr = reinterpret_cast<const uint4*>(resid + grow * kMC + 16 * c);
+          rv[2 * k] = rr[0];
+          rv[2 * k + 1] = rr[1];
+        }
       }
     };
-    // F(i): FC2 accumulator + b2 + residual -> out (parts 0..2: 32 columns each)
+    // F(i): FC2 accumulator + b2 + residual -> out
     auto final_epi = [&](int i, const uint4* rv) -> bool {
       if (!wait_all(o_full, i & 1)) return false;
       tc_fence_after();
-      uint32_t v[32];
-      if (part < 3) {
-        tmem_ld_32x32b_x32(t_lane + kFc2Col + 32 * part, v);
-        tmem_ld_wait();
-      }
+      uint32_t v[NC][16];
+#pragma unroll
+      for (int k = 0; k < NC; ++k)
+        if (part + WPQ * k < kMC / 16) tmem_ld_32x32b_x16(t_lane + kFc2Col + 16 * (part + WPQ * k), v[k]);
+      tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(o_empty);
       const long long grow = static_cast<long long>(kMBM) * tile_of(i) + r;
-      if (part < 3 && grow < M) {
-        const int col = 32 * part;
-        uint4* oo = reinterpret_cast<uint4*>(out + grow * kMC + col);
-        const float4* bb = reinterpret_cast<const float4*>(b2 + col);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float rf[8];
-          unpack16<T>(rv[c], rf);
-          const float4 x0 = __ldg(bb + 2 * c), x1 = __ldg(bb + 2 * c + 1);
-          const float bias[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-          float o8[8];
+      for (int k = 0; k < NC; ++k) {
+        const int c = part + WPQ * k;
+        if (c < kMC / 16 && grow < M) {
+          uint4* oo = reinterpret_cast<uint4*>(out + grow * kMC + 16 * c);
+          const float4* bb = reinterpret_cast<const float4*>(b2 + 16 * c);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) o8[e] = __uint_as_float(v[8 * c + e]) + bias[e] + rf[e];
-          oo[c] = pack16<T>(o8);
+          for (int h = 0; h < 2; ++h) {
+            float rf[8];
+            unpack16<T>(rv[2 * k + h], rf);
+            const float4 x0 = __ldg(bb + 2 * h), x1 = __ldg(bb + 2 * h + 1);
+            const float bias[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            float o8[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o8[e] = __uint_as_float(v[k][8 * h + e]) + bias[e] + rf[e];
+            oo[h] = pack16<T>(o8);
+          }
         }
       }
       return true;
     };
     for (int b = 0; b < 6 && ok && n > 0; ++b) ok = gelu_block(0, b);
     for (int i = 0; i < n && ok; ++i) {
-      uint4 rv[4];
+      uint4 rv[2 * NC];
       load_resid(i, rv);
       if (i + 1 < n) ok = gelu_block(i + 1, 0) && gelu_block(i + 1, 1);
       if (ok) ok = final_epi(i, rv);
@@ -350,19 +374,19 @@ swin_mlp_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__
   }
 }
 
-template <typename T>
+template <typename T, int EW = kMlpEW>
 cudaError_t mlp_launch(const CUtensorMap& th, const CUtensorMap& t1, const CUtensorMap& t2, const float* b1,
                        const float* b2, const void* resid, void* out, int M, int32_t* err, cudaStream_t stream) {
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(swin_mlp_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(swin_mlp_kernel<T, EW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kMlpSmem));
     if (e != cudaSuccess) return e;
     attr = true;
   }
   const int tiles = (M + kMBM - 1) / kMBM;
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  return launch_pdl(swin_mlp_kernel<T>, dim3(static_cast<unsigned>(grid)), dim3(kMThreads), kMlpSmem, stream, th, t1,
+  return launch_pdl(swin_mlp_kernel<T, EW>, dim3(static_cast<unsigned>(grid)), dim3(mlp_threads<EW>()), kMlpSmem, stream, th, t1,
                     t2, b1, b2, static_cast<const T*>(resid), static_cast<T*>(out), M, err);
 }
 
