@@ -341,6 +341,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int ncl = gridDim.x / CL;          // pairs in the grid
   const bool leader = rank == 0;           // issues the MMAs of the pair
 
+  // Stages whose W part was issued before the programmatic-launch wait (unpaired
+  // GEMMs): the weights are never written by a kernel that lets its dependents start
+  // early, so this CTA's first unit's first W boxes can be in flight while the
+  // preceding kernel drains; its A boxes follow after the wait.
+  int npre = 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);     // in a pair only the leader's is used
@@ -357,12 +362,26 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if constexpr (kTma) tma_prefetch_desc(&tmC);
+    if constexpr (CL == 1) {
+      // unit cid: column block (cid / S) % num_n, K blocks [kb0, kb1) (independent of M)
+      const int nk = (p.K + kBK - 1) / kBK;
+      const int kps0 = (nk + p.splits - 1) / p.splits;
+      const int t0 = cid / p.splits;
+      const int kb0 = (cid - t0 * p.splits) * kps0;
+      const int kb1 = min(nk, kb0 + kps0);
+      const int n0 = (t0 % (p.N / BN)) * BN;
+      npre = kb1 > kb0 ? min(kb1 - kb0, STAGES) : 0;
+      for (int s = 0; s < npre; ++s) {
+        mbar_expect_tx(&full[s], B_PART);
+        tma_load_2d(sB + s * B_BYTES_AL, &tmB, &full[s], (kb0 + s) * kBK, n0);
+      }
+    }
   }
   if (warp == 1) {
     tmem_alloc_cg<CL>(tmem_slot, TMEM_COLS);
     tmem_relinquish_cg<CL>();
   }
-  if (threadIdx.x == 32) {
+  if (CL > 1 && threadIdx.x == 32) {
     // The weights are never written by the preceding kernel: warm L2 with this CTA's
     // first weight boxes while that kernel drains.  The (tile, split) order puts the
     // column block of unit `cid` at (unit / S) % num_n regardless of M.
@@ -444,6 +463,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const uint32_t s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
+          if (static_cast<int>(it) < npre) {   // first pass, W part already in flight
+            mbar_arrive_expect_tx(&full[s], A_BYTES);
+            tma_load_2d(sA + s * A_BYTES, &tmA, &full[s], kb * kBK, m0);
+            continue;
+          }
           if (!mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag)) {
             ok = false;
             break;
@@ -466,6 +490,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         set_device_error(p.err, RPP_DERR_TIMEOUT);
         *abort_flag = 1;
       }
+      // early W boxes of a unit this CTA does not have (fewer rows than the grid was
+      // sized for, or an error raised upstream): complete those phases without A
+      for (; static_cast<int>(it) < npre; ++it) mbar_arrive(&full[it % STAGES]);
       // wait (bounded) for the copies still in flight: the last min(it, STAGES) loads
       // (a pair's partner: the leader waits for them, and the pair meets at the end)
       if (leader) {
