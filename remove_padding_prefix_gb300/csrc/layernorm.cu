@@ -118,38 +118,55 @@ __global__ void __launch_bounds__(128) layernorm_kernel(LnArgs a) {
   if (a.q_codes) inv_s = __fdiv_rn(1.0f, *a.q_scale);
   float local_amax = 0.f;
 
-  for (long long it0 = static_cast<long long>(wglob) * GPW; it0 < n_iter;
-       it0 += static_cast<long long>(warps_total) * GPW) {
+  // packed row normalised for loop position itx (-1: none)
+  auto src_of = [&](long long itx) -> int {
+    if (itx >= n_iter) return -1;
+    if (!padded) return static_cast<int>(itx);
+    // 32-bit division: the host keeps pad_B * pad_L below 2^31
+    const unsigned b = static_cast<unsigned>(itx) / static_cast<unsigned>(a.pad_L);
+    const int p = static_cast<int>(static_cast<unsigned>(itx) - b * static_cast<unsigned>(a.pad_L));
+    const int c0 = a.pad_cu[b];
+    return p < a.pad_cu[b + 1] - c0 ? c0 + p : -1;
+  };
+  // residual adds are taken only with fp32 input (the host rejects the rest): 16-bit
+  // instantiations carry no residual registers
+  constexpr bool kRes = std::is_same<T, float>::value;
+  // 16-bit input (one slice, no residual): the next row's vectors are requested before
+  // this row's arithmetic, two rows in flight per group
+  constexpr bool kPf = !kRes && NS == 1;
+  const long long stride_it = static_cast<long long>(warps_total) * GPW;
+  uint4 nx[kPf ? VPL : 1];
+  if constexpr (kPf) {
+    const int s0 = src_of(static_cast<long long>(wglob) * GPW + gw);
+    const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<long long>(s0 >= 0 ? s0 : 0) * H);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) nx[i] = s0 >= 0 ? xr[i * G + gl] : make_uint4(0u, 0u, 0u, 0u);
+  }
+
+  for (long long it0 = static_cast<long long>(wglob) * GPW; it0 < n_iter; it0 += stride_it) {
     const long long it = it0 + gw;
-    int src = -1;              // packed row normalised by this group (-1: none)
-    long long dst = -1;        // output row
-    if (it < n_iter) {
-      if (padded) {
-        // 32-bit division: the host keeps pad_B * pad_L below 2^31
-        const unsigned b = static_cast<unsigned>(it) / static_cast<unsigned>(a.pad_L);
-        const int p = static_cast<int>(static_cast<unsigned>(it) - b * static_cast<unsigned>(a.pad_L));
-        const int c0 = a.pad_cu[b];
-        if (p < a.pad_cu[b + 1] - c0) src = c0 + p;
-        dst = it;
-      } else {
-        src = static_cast<int>(it);
-        dst = it;
-      }
-    }
+    const int src = src_of(it);                        // packed row normalised by this group
+    const long long dst = it < n_iter ? it : -1;       // output row
     const bool valid = src >= 0;
     // ---- loads: input and its split-K slices (NS > 1), residual -- all issued together
     uint4 rx[NS][VPL];
-    // residual adds are taken only with fp32 input (the host rejects the rest): 16-bit
-    // instantiations carry no residual registers
-    constexpr bool kRes = std::is_same<T, float>::value;
     uint4 rr[kRes ? VPL : 1][kRes ? EPV / 4 : 1];
+    if constexpr (kPf) {
 #pragma unroll
-    for (int sl = 0; sl < NS; ++sl) {
-      if (sl == 0 || sl < a.n_in) {
-        const uint4* xr =
-            reinterpret_cast<const uint4*>(x + sl * a.in_stride + static_cast<long long>(valid ? src : 0) * H);
+      for (int i = 0; i < VPL; ++i) rx[0][i] = nx[i];
+      const int sn = src_of(it + stride_it);
+      const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<long long>(sn >= 0 ? sn : 0) * H);
 #pragma unroll
-        for (int i = 0; i < VPL; ++i) rx[sl][i] = valid ? xr[i * G + gl] : make_uint4(0u, 0u, 0u, 0u);
+      for (int i = 0; i < VPL; ++i) nx[i] = sn >= 0 ? xr[i * G + gl] : make_uint4(0u, 0u, 0u, 0u);
+    } else {
+#pragma unroll
+      for (int sl = 0; sl < NS; ++sl) {
+        if (sl == 0 || sl < a.n_in) {
+          const uint4* xr =
+              reinterpret_cast<const uint4*>(x + sl * a.in_stride + static_cast<long long>(valid ? src : 0) * H);
+#pragma unroll
+          for (int i = 0; i < VPL; ++i) rx[sl][i] = valid ? xr[i * G + gl] : make_uint4(0u, 0u, 0u, 0u);
+        }
       }
     }
     const bool has_res = kRes && a.residual != nullptr && valid;
