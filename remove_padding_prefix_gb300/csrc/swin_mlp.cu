@@ -52,7 +52,8 @@ constexpr uint32_t kAtom = kMBM * 128;         // 128 rows x 128 bytes
 constexpr uint32_t kABytes = 2 * kAtom;
 constexpr int kHBufs = 6;
 constexpr uint32_t kHBytes = kAtom;
-constexpr size_t kMlpSmem = 1024 + kW1Bytes + kW2Bytes + kABytes + kHBufs * kHBytes + 256;
+constexpr uint32_t kB1Bytes = kMF * 4;          // b1 staged once (fp32)
+constexpr size_t kMlpSmem = 1024 + kW1Bytes + kW2Bytes + kABytes + kHBufs * kHBytes + kB1Bytes + 256;
 constexpr uint32_t kFc2Col = kMF;              // FC2 accumulator columns [384, 480)
 
 template <typename T> struct MlpFmt;
@@ -80,7 +81,8 @@ swin_mlp_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__
   uint8_t* sW2 = sW1 + kW1Bytes;
   uint8_t* sA = sW2 + kW2Bytes;
   uint8_t* sH = sA + kABytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sH + kHBufs * kHBytes);
+  float* sB1 = reinterpret_cast<float*>(sH + kHBufs * kHBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sH + kHBufs * kHBytes + kB1Bytes);
   uint64_t* w_full = bars;        // W1 landed
   uint64_t* a_full = bars + 1;
   uint64_t* a_empty = bars + 2;
@@ -131,6 +133,7 @@ swin_mlp_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
+  for (int j = threadIdx.x; j < kMF; j += blockDim.x) sB1[j] = b1[j];   // prepared data
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -254,11 +257,9 @@ swin_mlp_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__
     const int r = q * 32 + lane;             // row of the tile
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     bool ok = true;
-    // lane 0 waits, the warp follows its verdict
+    // the whole warp polls (one barrier word, one answer for all lanes)
     auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
-      int w = 1;
-      if (lane == 0) w = mbar_wait_bounded(bar, parity, abort_flag) ? 1 : 0;
-      return __shfl_sync(0xffffffffu, w, 0) != 0;
+      return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort_flag) ? 1 : 0) != 0;
     };
     // G(i, b): GELU of hidden block b (this warp: its CW columns of the block)
     auto gelu_block = [&](int i, int b) -> bool {
@@ -266,10 +267,10 @@ swin_mlp_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__
       if ((b == 0 || b == 3) && !wait_all(&s_full[b / 3], i & 1)) return false;
       if (!wait_all(&h_empty[buf], (i & 1) ^ 1)) return false;
       const int col = 64 * b + CW * part;
-      const float4* bb = reinterpret_cast<const float4*>(b1 + col);
+      const float4* bb = reinterpret_cast<const float4*>(sB1 + col);
       float4 bq[CW / 4];
 #pragma unroll
-      for (int k = 0; k < CW / 4; ++k) bq[k] = __ldg(bb + k);
+      for (int k = 0; k < CW / 4; ++k) bq[k] = bb[k];
       tc_fence_after();
       uint32_t v[CW];
       tmem_ld_32x32b_x16(t_lane + col, v);
