@@ -261,44 +261,42 @@ swin_mlp_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__
     auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abort_flag) ? 1 : 0) != 0;
     };
-    // G(i, b): GELU of hidden block b (this warp: its CW columns of the block)
-    auto gelu_block = [&](int i, int b) -> bool {
-      const int buf = b;   // block b of every tile: FC2(i - 1, b) has released it
-      if ((b == 0 || b == 3) && !wait_all(&s_full[b / 3], i & 1)) return false;
-      if (!wait_all(&h_empty[buf], (i & 1) ^ 1)) return false;
+    // tensor memory -> registers for hidden block b (this warp: its CW columns), not waited
+    auto ld_block = [&](int b, uint32_t* v) {
       const int col = 64 * b + CW * part;
-      const float4* bb = reinterpret_cast<const float4*>(sB1 + col);
-      float4 bq[CW / 4];
-#pragma unroll
-      for (int k = 0; k < CW / 4; ++k) bq[k] = bb[k];
-      tc_fence_after();
-      uint32_t v[CW];
       tmem_ld_32x32b_x16(t_lane + col, v);
       if constexpr (CW == 32) tmem_ld_32x32b_x16(t_lane + col + 16, v + 16);
-      tmem_ld_wait();
-      if (b == 2 || b == 5) {   // this warp has read its share of the FC1 half
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_empty[b / 3]);
-      }
+    };
+    // G(i, b) once its accumulator values are in registers: + b1, GELU, into hidden
+    // buffer b (after FC2(i - 1, b) has released it)
+    auto store_block = [&](int i, int b, const uint32_t* v) -> bool {
+      if (!wait_all(&h_empty[b], (i & 1) ^ 1)) return false;
+      const float4* bb = reinterpret_cast<const float4*>(sB1 + 64 * b + CW * part);
       float f[CW];
 #pragma unroll
       for (int k = 0; k < CW / 4; ++k) {
-        f[4 * k + 0] = gelu_erf<5>(__uint_as_float(v[4 * k + 0]) + bq[k].x);
-        f[4 * k + 1] = gelu_erf<5>(__uint_as_float(v[4 * k + 1]) + bq[k].y);
-        f[4 * k + 2] = gelu_erf<5>(__uint_as_float(v[4 * k + 2]) + bq[k].z);
-        f[4 * k + 3] = gelu_erf<5>(__uint_as_float(v[4 * k + 3]) + bq[k].w);
+        const float4 bq = bb[k];
+        f[4 * k + 0] = gelu_erf<5>(__uint_as_float(v[4 * k + 0]) + bq.x);
+        f[4 * k + 1] = gelu_erf<5>(__uint_as_float(v[4 * k + 1]) + bq.y);
+        f[4 * k + 2] = gelu_erf<5>(__uint_as_float(v[4 * k + 2]) + bq.z);
+        f[4 * k + 3] = gelu_erf<5>(__uint_as_float(v[4 * k + 3]) + bq.w);
       }
       // CW columns = CW / 8 16-byte chunks of the 128-byte row, starting at chunk
       // (CW / 8) part, each at chunk ^ (r & 7) (the 128-byte swizzle)
-      uint8_t* row = sH + buf * kHBytes + r * 128;
+      uint8_t* row = sH + b * kHBytes + r * 128;
 #pragma unroll
       for (int c = 0; c < CW / 8; ++c)
         *reinterpret_cast<uint4*>(row + ((((CW / 8) * part + c) ^ (r & 7)) << 4)) = pack16<T>(f + 8 * c);
       fence_proxy_async_smem();   // visible to the tensor core
       __syncwarp();
-      if (lane == 0) mbar_arrive(&h_full[buf]);
+      if (lane == 0) mbar_arrive(&h_full[b]);
       return true;
+    };
+    // this warp has read its share of FC1 half hf (its loads have completed)
+    auto half_read = [&](int hf) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[hf]);
     };
     // The final epilogue works in 16-column chunks of the C = 96 outputs: chunk c of a
     // row belongs to part c % WPQ of its lane quadrant (at most NC chunks a warp).
@@ -321,19 +319,20 @@ swin_mlp_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__
     auto final_epi = [&](int i, const uint4* rv) -> bool {
       if (!wait_all(o_full, i & 1)) return false;
       tc_fence_after();
-      uint32_t v[NC][16];
-#pragma unroll
-      for (int k = 0; k < NC; ++k)
-        if (part + WPQ * k < kMC / 16) tmem_ld_32x32b_x16(t_lane + kFc2Col + 16 * (part + WPQ * k), v[k]);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(o_empty);
       const long long grow = static_cast<long long>(kMBM) * tile_of(i) + r;
 #pragma unroll
       for (int k = 0; k < NC; ++k) {
         const int c = part + WPQ * k;
-        if (c < kMC / 16 && grow < M) {
+        if (c >= kMC / 16) continue;   // uniform per warp
+        uint32_t v[1][16];
+        tmem_ld_32x32b_x16(t_lane + kFc2Col + 16 * c, v[0]);
+        tmem_ld_wait();
+        if (k + 1 >= NC || part + WPQ * (k + 1) >= kMC / 16) {   // this warp's last chunk read
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(o_empty);
+        }
+        if (grow < M) {
           uint4* oo = reinterpret_cast<uint4*>(out + grow * kMC + 16 * c);
           const float4* bb = reinterpret_cast<const float4*>(b2 + 16 * c);
 #pragma unroll
@@ -344,20 +343,41 @@ swin_mlp_kernel(const __grid_constant__ CUtensorMap tmH, const __grid_constant__
             const float bias[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
             float o8[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o8[e] = __uint_as_float(v[k][8 * h + e]) + bias[e] + rf[e];
+            for (int e = 0; e < 8; ++e) o8[e] = __uint_as_float(v[0][8 * h + e]) + bias[e] + rf[e];
             oo[h] = pack16<T>(o8);
           }
         }
       }
       return true;
     };
-    for (int b = 0; b < 6 && ok && n > 0; ++b) ok = gelu_block(0, b);
+    // the six hidden blocks of tile i, each block's tensor-memory load issued before the
+    // previous block's arithmetic (within a half, whose accumulator is complete); F(fi)
+    // (when asked) between the halves
+    uint32_t va[CW], vb[CW];
+    auto tile_blocks = [&](int i, bool with_f, int fi, const uint4* rv) -> bool {
+      for (int hf = 0; hf < 2; ++hf) {
+        const int b0 = 3 * hf;
+        if (!wait_all(&s_full[hf], i & 1)) return false;
+        tc_fence_after();
+        ld_block(b0, va);
+        tmem_ld_wait();
+        ld_block(b0 + 1, vb);
+        if (!store_block(i, b0, va)) return false;
+        tmem_ld_wait();
+        ld_block(b0 + 2, va);
+        if (!store_block(i, b0 + 1, vb)) return false;
+        tmem_ld_wait();
+        half_read(hf);
+        if (!store_block(i, b0 + 2, va)) return false;
+        if (hf == 0 && with_f && !final_epi(fi, rv)) return false;
+      }
+      return true;
+    };
+    if (n > 0) ok = tile_blocks(0, false, 0, nullptr);
     for (int i = 0; i < n && ok; ++i) {
       uint4 rv[2 * NC];
       load_resid(i, rv);
-      if (i + 1 < n) ok = gelu_block(i + 1, 0) && gelu_block(i + 1, 1);
-      if (ok) ok = final_epi(i, rv);
-      for (int b = 2; b < 6 && ok && i + 1 < n; ++b) ok = gelu_block(i + 1, b);
+      ok = i + 1 < n ? tile_blocks(i + 1, true, i, rv) : final_epi(i, rv);
     }
     if (!ok && lane == 0) {
       set_device_error(err, RPP_DERR_TIMEOUT);
