@@ -17,8 +17,10 @@
 //   warp 1      MMA issue (one thread): FC1 of a tile in two halves of 192 hidden
 //               columns, FC2 in six 64-wide K blocks;
 //   warps 2..   epilogue: per 64-column block of the hidden activation, tensor memory
-//               -> registers, + b1, GELU, fp16/bf16 -> a 128-byte-swizzled K-major block
-//               in shared memory; per tile, the FC2 accumulator + b2 + y -> out.
+//               -> registers (the next block's load issued before this block's
+//               arithmetic), + b1 (staged in shared memory), GELU, fp16/bf16 -> a
+//               128-byte-swizzled K-major block in shared memory; per tile, the FC2
+//               accumulator + b2 + y -> out, y's rows requested a half tile ahead.
 // Shared memory (bytes): W1 as six MN-major panels [96 K rows x 64 N] (73 728), two
 // W2 slots, each a K-major panel [96 N rows x 64 K] (24 576), the h tile as two K-major
 // atoms (the TMA zero-fills columns 96..127, 32 768), and the whole tile's hidden
@@ -29,10 +31,11 @@
 // Order of work (i = this CTA's tile counter), chosen so that every hand-off overlaps
 // other work:
 //   MMA:      FC2(i, 0..2) | FC1(i+1, half 0) | FC2(i, 3..5) | FC1(i+1, half 1)
-//   epilogue: G(i+1, 0), G(i+1, 1) | F(i) | G(i+1, 2..5)
+//   epilogue: G(i+1, 0..2) | F(i) | G(i+1, 3..5)
 //   TMA:      W2 panels of FC2(i, 0..2) | h of tile i + 1 | W2 panels of FC2(i, 3..5)
 // where G(i, b) is the GELU of hidden block b of tile i and F(i) the final epilogue.
-// FC1(i+1, half 0) overwrites columns the epilogue finished reading with G(i, 2);
+// FC1(i+1, half h) overwrites columns the epilogue finished reading in G(i, 3h..3h+2);
+// F(i) needs FC2(i, 5), issued after G(i, 5) with three blocks of work in between;
 // FC2(i+1, 0) waits until F(i) has read the FC2 accumulator.  Every wait is bounded.
 #include "kernels.h"
 
