@@ -365,7 +365,8 @@ RPP_API rpp_status rpp_window_attention_forward(const rpp_swin_cfg* cfg, int B, 
                                         rpp_stream stream);
 
 /* Bytes of the prepared Swin block weights, and the preparation itself (K-major
- * weights, fp32 biases / LayerNorm parameters, the relative-position bias). */
+ * weights, fp32 biases / LayerNorm parameters, the relative-position bias; at C = 96
+ * with mlp = 384 also W1 as given, [C, mlp], read N-major by the fused MLP). */
 RPP_API size_t rpp_swin_block_bytes(const rpp_swin_cfg* cfg);
 RPP_API rpp_status rpp_swin_prepare_block(const rpp_swin_cfg* cfg, const rpp_swin_src* src, void* dst,
                                   rpp_stream stream);
@@ -376,7 +377,9 @@ RPP_API size_t rpp_swin_workspace_bytes(const rpp_swin_cfg* cfg, int B);
 /* Pre-LN Swin block on x [B*I*I, C] (raster order), y may alias x:
  *   x' = x + proj(WindowAttention(LN1 x)),  y = x' + W2 GELU(W1 LN2(x') + b1) + b2,
  * with the QKV projection run on raster-order tokens (a row-wise GEMM commutes with
- * the window permutation) and the permutation applied inside the attention kernel. */
+ * the window permutation) and the permutation applied inside the attention kernel.
+ * At C = 96 with mlp = 384 (Swin-T stage 1) the MLP line is one kernel whose hidden
+ * activation [B*I*I, mlp] stays on chip; the other widths run it as two GEMMs. */
 RPP_API rpp_status rpp_swin_block_forward(const rpp_swin_cfg* cfg, const void* block, int B, const void* x,
                                   void* y, void* workspace, size_t workspace_bytes, int32_t* err,
                                   rpp_stream stream);
