@@ -80,6 +80,14 @@ def test_size_queries(lib):
     assert lib.rpp_gemm_i8_workspace_bytes(128, 64, 256) >= (128 + 64) * 256 * 2
     sw = _abi.SwinCfg(56, 96, 3, 7, 3, 384, 1e-5, _abi.RPP_F16)
     assert lib.rpp_swin_block_bytes(C.byref(sw)) > 0
+    # C = 96 with MLP 384 runs the fused MLP, which keeps a second copy of W1 ([C, mlp], read
+    # N-major); other widths hold the K-major copy only
+    Cs, F = 96, 384
+    kmajor = (3 * Cs * Cs + Cs * Cs + 2 * F * Cs) * 2
+    assert lib.rpp_swin_block_bytes(C.byref(sw)) >= kmajor + F * Cs * 2
+    sw192 = _abi.SwinCfg(28, 192, 6, 7, 3, 768, 1e-5, _abi.RPP_F16)
+    b192 = lib.rpp_swin_block_bytes(C.byref(sw192))
+    assert (3 * 192 * 192 + 192 * 192 + 2 * 768 * 192) * 2 <= b192 < (3 * 192 * 192 + 192 * 192 + 3 * 768 * 192) * 2
     assert lib.rpp_swin_workspace_bytes(C.byref(sw), 2) >= 2 * 56 * 56 * (96 * 5 + 384) * 2
     # workspace too small is reported before any launch
     assert lib.rpp_encoder_layer_forward(C.byref(cfg), 256, None, 256, 256, 4, 512, 128, 256, 256, 16, None,
