@@ -107,8 +107,9 @@ def test_int8_layer_small():
 
 
 def test_int8_layer_full_config_sampled():
-    """configs[3] at full size; sequences sampled (per-sequence independence), scales
-    from the oracle's calibration on the seeded calibration batch."""
+    """The BERT-large-shaped int8 layer (B=64, L=256) at full size; sequences sampled
+    (per-sequence independence), scales from the oracle's calibration on the seeded
+    calibration batch."""
     cfg = INT8
     wl = make_bert_workload(cfg)
     cal = make_calibration_batch(cfg)

@@ -95,7 +95,8 @@ def test_layer_all_lengths_zero_gives_zero_output():
 
 
 def test_bert_base_full_config():
-    """configs[1] at full size (the bench workload), every output against the oracle."""
+    """The BERT-base-shaped fp16 layer (B=32, L=128) at full size (the bench workload), every
+    output against the oracle."""
     cfg = CONFIGS[1]
     wl = make_bert_workload(cfg)
     ref, _, _ = oracle.bert_forward(wl["x_padded"], wl["lengths"], wl["layers"], cfg.nh, cfg.eps)
@@ -142,8 +143,8 @@ def _teacher_forced_stack(wl, dtype, n_layers, sample):
 
 
 def test_bert_large_stack_sampled_sequences():
-    """configs[2]: 24 bf16 layers at full size; each layer checked (teacher-forced) on
-    four sequences, longest and shortest included."""
+    """The BERT-large-shaped bf16 stack (B=64, L=384): 24 layers at full size; each layer
+    checked (teacher-forced) on four sequences, longest and shortest included."""
     cfg = CONFIGS[2]
     wl = make_bert_workload(cfg)
     lens = wl["lengths"]

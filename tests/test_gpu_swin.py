@@ -101,7 +101,7 @@ def test_swin_block_multi_tile_ragged():
 
 
 def test_swin_block_full_config_sampled_images():
-    """configs[4] (B=64, 56x56, C=96) at full size; images are independent, so the oracle
+    """The Swin-T stage-1 block (B=64, 56x56, C=96) at full size; images are independent, so the oracle
     checks three of them, the first and the last included."""
     wl = make_swin_workload(SWIN)
     c = wl["cfg"]
