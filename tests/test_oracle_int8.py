@@ -93,3 +93,207 @@ def test_int8_layer_close_to_float_layer():
     assert err.mean() < 0.05 and err.max() < 0.5
     # a structural mistake (say, a dropped residual) would move outputs by O(1)
     assert not np.allclose(yq, oracle.layernorm(x, np.ones(cfg.H), np.zeros(cfg.H), cfg.eps), atol=0.3)
+
+
+# ---------------------------------------------------------------- exact pins of the int8 flow
+# A small layer (H = 8, two heads of 4, F = 8) built so that every GEMM input of the
+# float layer lies exactly on the grid of its activation scale, with odd codes and codes
+# above 63 in each.  Then quantisation is lossless with the right scale and lossy with
+# any other power-of-two scale (a coarser one cannot hold the odd codes, a finer one
+# clamps the large codes), so the int8 layer must equal the float layer to rounding,
+# and a scale taken for the wrong tensor or a residual taken from the wrong place must
+# show up in the output.
+#
+# Construction (sigma = [1, -1, 1, -1, ...], P = projection onto span{sigma, 1},
+# Pp = I - P; scales s0 = 2^-4 (QKV input), s1 = 2^-2 (attention output), s2 = 2^-5
+# (FC1 input), s3 = 2^-3 (FC2 input)):
+#   Q weights 0 -> every score is 0 -> attention is the plain mean of V over the
+#     sequence (lengths 1 and 2, pairs differing by an even-coded multiple of
+#     sigma and 1);
+#   V weights 4 I -> attention output 4 * mean(x) on the s1 grid;
+#   Wo = -Pp / 4 -> x + proj = x P, a row a sigma + b 1: LayerNorm with eps = 0 maps it
+#     to sign(a) sigma exactly, so LN1's output is +-gamma1 sigma + beta1 (dyadic);
+#   W1 = 8 I, b1 chosen so each column's pre-GELU value is >= 9 (GELU(h) = h in fp64)
+#     or <= -9 (GELU(h) = 0), the positive ones on the s3 grid.
+_SIG = np.array([1.0, -1.0] * 4)
+_S = (2.0 ** -4, 2.0 ** -2, 2.0 ** -5, 2.0 ** -3)   # s0, s1, s2, s3: four distinct scales
+
+
+def _grid_case():
+    H, F, nh = 8, 8, 2
+    s0, s1, s2, s3 = _S
+    rng = np.random.default_rng(77)
+    # x codes: three single-token sequences and two pairs; pair rows differ by
+    # 2 * (p sigma + q 1) codes, so the pair mean has integer codes
+    rows, lengths = [], []
+    for _ in range(3):
+        c = rng.integers(-120, 121, size=H)
+        c[0] = 125 if c[0] >= 0 else -125    # a large code: a 2x finer scale clamps it
+        c[1] |= 1                             # an odd code: a 2x coarser scale loses it
+        rows.append(c)
+        lengths.append(1)
+    for p, q in ((3, -5), (-7, 2)):
+        a = rng.integers(-90, 91, size=H)
+        a[2] = 97
+        a[3] |= 1
+        rows += [a, a + 2 * (p * _SIG + q).astype(np.int64)]
+        lengths.append(2)
+    xcodes = np.array(rows, np.int64)
+    assert np.abs(xcodes).max() <= 127
+    x = xcodes * s0
+    cu = np.concatenate([[0], np.cumsum(lengths)])
+
+    P = (np.outer(_SIG, _SIG) + np.ones((H, H))) / H
+    Pp = np.eye(H) - P
+    # weights as codes x per-column power-of-two scales (the float layer is codes * scale)
+    wqkv_codes = np.zeros((H, 3 * H), np.int64)
+    wqkv_s = np.ones(3 * H)
+    wqkv_codes[:, H:2 * H] = rng.integers(-127, 128, size=(H, H))   # K: anything (Q = 0)
+    wqkv_s[H:2 * H] = 2.0 ** -7
+    wqkv_codes[:, 2 * H:] = 64 * np.eye(H, dtype=np.int64)          # V = 4 x
+    wqkv_s[2 * H:] = 2.0 ** -4
+    wo_codes = np.rint(-Pp * 4).astype(np.int64)                     # -Pp / 4 = codes / 16
+    assert np.array_equal(wo_codes / 16.0, -Pp / 4)
+    wo_s = np.full(H, 2.0 ** -4)
+    gamma1 = np.array([2.5, 1.75, 3.0, 1.78125, 1.75, 2.0, 1.96875, 2.25])
+    beta1 = np.array([0.9375, -0.5, 0.25, 0.03125, -1.0, 0.5, 0.0, -1.71875])
+    w1_codes = 32 * np.eye(H, dtype=np.int64)                        # W1 = 8 I
+    w1_s = np.full(F, 2.0 ** -2)
+    targets = np.array([9.25, 10.125, 11.0, 12.375, 13.5, 14.625, 15.0, 15.875])
+    b1 = np.zeros(F)
+    for f in range(F):   # the larger of the two possible LN1 outputs of column f maps to its target
+        hi = max(gamma1[f] + beta1[f], -gamma1[f] + beta1[f])
+        b1[f] = targets[f] - 8 * hi
+    w2_codes = rng.integers(-127, 128, size=(F, H))
+    w2_s = 2.0 ** -rng.integers(6, 9, size=H).astype(np.float64)
+    b2 = rng.integers(-64, 65, size=H) * 2.0 ** -8
+
+    f32 = lambda a: np.asarray(a, np.float32)
+    layer = {"Wqkv": wqkv_codes * wqkv_s, "bqkv": np.zeros(3 * H), "Wo": wo_codes * wo_s, "bo": np.zeros(H),
+             "W1": w1_codes * w1_s, "b1": b1, "W2": w2_codes * w2_s, "b2": b2,
+             "gamma1": gamma1, "beta1": beta1, "gamma2": np.ones(H), "beta2": np.zeros(H)}
+    qlayer = {"Wqkv_q": wqkv_codes.astype(np.int8), "Wqkv_s": f32(wqkv_s), "Wo_q": wo_codes.astype(np.int8),
+              "Wo_s": f32(wo_s), "W1_q": w1_codes.astype(np.int8), "W1_s": f32(w1_s),
+              "W2_q": w2_codes.astype(np.int8), "W2_s": f32(w2_s)}
+    for k in ("bqkv", "bo", "b1", "b2", "gamma1", "beta1", "gamma2", "beta2"):
+        qlayer[k] = layer[k]
+    return x, cu, layer, qlayer, nh
+
+
+def _on_grid(t, s, what):
+    codes = np.asarray(t, np.float64) / s
+    assert np.array_equal(codes, np.rint(codes)), f"{what} off the grid"
+    assert np.abs(codes).max() <= 127, f"{what} beyond 127 codes"
+    c = np.rint(codes).astype(np.int64)
+    assert (c % 2 != 0).any() and np.abs(c).max() > 63, f"{what} must hold odd and large codes"
+
+
+def test_grid_case_construction_is_exact():
+    """The construction above really puts each GEMM input of the float layer on its grid
+    (checked with the oracle's float pieces, which have their own pins)."""
+    x, cu, layer, _, nh = _grid_case()
+    s0, s1, s2, s3 = _S
+    H = x.shape[1]
+    _on_grid(x, s0, "QKV input")
+    qkv = oracle.linear(x, layer["Wqkv"], layer["bqkv"])
+    assert np.all(qkv[:, :H] == 0)
+    attn = oracle.attention_varlen(qkv[:, :H], qkv[:, H:2 * H], qkv[:, 2 * H:], cu, nh)
+    _on_grid(attn, s1, "attention output")
+    y = x + oracle.linear(attn, layer["Wo"], layer["bo"])
+    x1 = oracle.layernorm(y, layer["gamma1"], layer["beta1"], 0.0)
+    _on_grid(x1, s2, "LN1 output")
+    h = oracle.linear(x1, layer["W1"], layer["b1"])
+    assert np.all((h >= 9) | (h <= -9))
+    g = oracle.gelu(h)
+    assert np.array_equal(g, np.where(h > 0, h, 0.0))
+    _on_grid(g, s3, "GELU output")
+
+
+def test_int8_layer_equals_float_layer_on_grid():
+    """With every GEMM input on its scale's grid the int8 layer is the float layer."""
+    x, cu, layer, qlayer, nh = _grid_case()
+    yq = oracle.bert_layer_int8(x, cu, qlayer, np.array(_S, np.float32), nh, 0.0)
+    yf = oracle.bert_layer(x, cu, layer, nh, 0.0)
+    assert np.abs(yq - yf).max() < 1e-12
+
+
+@pytest.mark.parametrize("i,j", [(0, 1), (0, 2), (0, 3), (1, 2), (1, 3), (2, 3)])
+def test_int8_layer_grid_case_sees_every_scale_swap(i, j):
+    """The pin above is sensitive: exchanging any two of the four scales moves the
+    output far beyond rounding (so a scale wired to the wrong tensor cannot pass it)."""
+    x, cu, layer, qlayer, nh = _grid_case()
+    s = list(_S)
+    s[i], s[j] = s[j], s[i]
+    yq = oracle.bert_layer_int8(x, cu, qlayer, np.array(s, np.float32), nh, 0.0)
+    yf = oracle.bert_layer(x, cu, layer, nh, 0.0)
+    assert np.abs(yq - yf).max() > 1e-3
+
+
+def test_int8_layer_grid_case_sees_the_residual_source():
+    """The FC2 residual is LN1's output, not the layer input: the two differ here by
+    O(1), so a layer that took the wrong one could not match the float layer."""
+    x, cu, layer, _, nh = _grid_case()
+    x1 = oracle.layernorm(x + oracle.linear(oracle.attention_varlen(
+        *np.split(oracle.linear(x, layer["Wqkv"], layer["bqkv"]), 3, axis=1), cu, nh), layer["Wo"], layer["bo"]),
+        layer["gamma1"], layer["beta1"], 0.0)
+    assert np.abs(x1 - x).max() > 1.0
+
+
+def test_calibration_scales_hand_checked():
+    """calibrate_int8 on the grid case: the four max-abs values written out by hand from
+    the construction (mean of V, +-gamma1 + beta1, the GELU targets)."""
+    x, cu, layer, _, nh = _grid_case()
+    lengths = np.diff(cu)
+    L = int(lengths.max())
+    B = len(lengths)
+    xp = np.zeros((B, L, x.shape[1]))
+    for b in range(B):
+        xp[b, :lengths[b]] = x[cu[b]:cu[b + 1]]
+    s = oracle.calibrate_int8(xp, lengths, layer, nh, 0.0)
+    # QKV input: the largest |x|
+    assert s[0] == np.float32(np.abs(x).max() / 127)
+    # attention output: 4 x the per-sequence mean of x (Q = 0: uniform weights)
+    means = np.concatenate([np.repeat(x[cu[b]:cu[b + 1]].mean(axis=0, keepdims=True), lengths[b], axis=0)
+                            for b in range(B)])
+    assert s[1] == np.float32(np.abs(4 * means).max() / 127)
+    # LN1 output: +-gamma1 sigma + beta1 with the sign of the row's sigma component
+    sign = np.sign(x @ _SIG)   # x + proj = x P, whose sigma component has the sign of x . sigma
+    x1 = sign[:, None] * _SIG[None, :] * layer["gamma1"][None, :] + layer["beta1"][None, :]
+    assert s[2] == np.float32(np.abs(x1).max() / 127)
+    # FC2 input: GELU(8 x1 + b1) = the positive targets, 0 for the negative side
+    h = 8 * x1 + layer["b1"]
+    assert s[3] == np.float32(np.where(h > 0, h, 0).max() / 127)
+    # the four tensors have different maxima, so a scale taken from a neighbouring
+    # tensor (say the pre-LN sum for the FC1 input, the pre-GELU value for the FC2
+    # input) cannot pass
+    assert len(set(np.float32(v) for v in s)) == 4
+
+
+def test_calibration_scales_match_library_route():
+    """calibrate_int8 on the int8 configuration's shapes (small batch) against torch's own
+    scaled_dot_product_attention (padded batch, key mask), layer_norm and exact gelu in
+    fp64: all four scales, within fp32 rounding of the max-abs / 127."""
+    import torch
+    torch.set_grad_enabled(False)
+    cfg = INT8
+    wl = make_bert_workload(cfg, B=3, L=24, lengths=np.array([24, 7, 13]))
+    layer, lens = wl["layers"][0], wl["lengths"]
+    B, L, H, nh, d = 3, 24, cfg.H, cfg.nh, cfg.d
+    s = oracle.calibrate_int8(wl["x_padded"], lens, layer, nh, cfg.eps)
+    t = lambda a: torch.from_numpy(np.asarray(a, np.float64))
+    xp = t(wl["x_padded"])
+    valid = torch.from_numpy(np.arange(L)[None, :] < lens[:, None])
+    qkv = xp @ t(layer["Wqkv"]) + t(layer["bqkv"])
+    q, k, v = [qkv[..., i * H:(i + 1) * H].reshape(B, L, nh, d).transpose(1, 2) for i in range(3)]
+    attn = torch.nn.functional.scaled_dot_product_attention(q, k, v, attn_mask=valid[:, None, None, :])
+    attn = attn.transpose(1, 2).reshape(B, L, H)
+    x1 = torch.nn.functional.layer_norm(xp + attn @ t(layer["Wo"]) + t(layer["bo"]), (H,), t(layer["gamma1"]),
+                                        t(layer["beta1"]), eps=cfg.eps)
+    g = torch.nn.functional.gelu(x1 @ t(layer["W1"]) + t(layer["b1"]), approximate="none")
+    want = [float(a[valid].abs().max()) / 127 for a in (xp, attn, x1, g)]
+    assert np.allclose(s.astype(np.float64), want, rtol=2e-7, atol=0)
+    # neighbouring tensors are far apart: pre-LN sum vs LN output, pre-GELU vs GELU
+    pre_ln = xp + attn @ t(layer["Wo"]) + t(layer["bo"])
+    pre_gelu = x1 @ t(layer["W1"]) + t(layer["b1"])
+    assert abs(float(pre_ln[valid].abs().max()) / 127 - s[2]) > 1e-3 * s[2]
+    assert abs(float(pre_gelu[valid].abs().max()) / 127 - s[3]) > 1e-3 * s[3]
