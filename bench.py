@@ -1,11 +1,12 @@
 """Benchmark: valid tokens/s per encoder layer on one GB300, with roofline fractions.
 
 One step = one pass of the whole hot path over one batch of synthetic input.  The
-default workload is the BERT-base-shaped fp16 layer (B=32, L=128, lengths U[16,128],
-H=768, 12 heads, FFN 3072): offsets + padding removal -> encoder layer -> LayerNorm
-with the padding rebuild, one C-ABI call (rpp_encoder_forward).  --workload picks
-another configuration: bert_large_bf16_x24 (24 layers), bert_large_int8, tiny_fp32,
-swin_t_stage1_fp16 (one shifted-window block, rpp_swin_block_forward).
+default workload is the largest single-GPU configuration, the BERT-large-shaped bf16
+stack (B=64, L=384, half the lengths U[32,128] and half U[256,384], H=1024, 16 heads,
+FFN 4096, 24 layers): offsets + padding removal -> 24 encoder layers -> LayerNorm with
+the padding rebuild, one C-ABI call (rpp_encoder_forward).  --workload picks another
+configuration: bert_base_fp16, bert_large_int8, tiny_fp32, swin_t_stage1_fp16 (one
+shifted-window block, rpp_swin_block_forward), swin_t_patch_merge_fp16.
 
 Timing: W warm-up steps, then K steps, each bracketed by its own CUDA events on the
 launch stream, with a 512 MiB write between timed steps to flush the 129 MB L2 (the
@@ -15,7 +16,10 @@ replays one captured CUDA graph of the step; the eager (direct C-ABI call) numbe
 reported next to it.  value = valid tokens per step x layers x ranks / time.
 
 Extra keys: roofline (dominant kernel, timed live inside the step with the library's
-launch-event hook), cpu_baseline (the CPU oracle on a bounded sample, host cores),
+launch-event hook; algorithmic bytes and flops per launch as the method steps define
+them, never the design's own intermediates), layer_roofline (the step against the sum
+of the method steps' ideal times), cpu_baseline (the CPU oracle on a bounded sample,
+all host cores, with a single-thread run of the same oracle beside it),
 e2e (the same metric through host buffers: pinned H2D of the step's inputs and D2H of
 its output inside the timed region), gpu_launches, clocks (nvidia-smi sampled during
 the timed region), kernels (per-kernel breakdown).  --impl reference times the CPU
@@ -48,7 +52,8 @@ def parse():
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--workload", default="bert_base_fp16")
+    p.add_argument("--workload", default="bert_large_bf16_x24")
+    p.add_argument("--oracle-rate", type=float, default=0.0, help=argparse.SUPPRESS)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-graph", action="store_true")
@@ -100,6 +105,56 @@ def reduce_max(value, world, device):
     t = torch.tensor([value], dtype=torch.float64, device=device)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
+
+
+def oracle_single_thread(args, budget_s):
+    """The oracle timed on ONE host thread: a child process of this script with every
+    BLAS / OpenMP pool capped at one thread before numpy loads.  Returns the child's
+    {value, sample, dt} or None if it could not run."""
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS",
+              "VECLIB_MAXIMUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[k] = "1"
+    cmd = [sys.executable, os.path.abspath(__file__), "--workload", args.workload, "--oracle-rate", str(budget_s)]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=budget_s * 10 + 120)
+    except (OSError, subprocess.TimeoutExpired):
+        return None
+    for line in reversed(r.stdout.strip().splitlines()):
+        try:
+            return json.loads(line)
+        except ValueError:
+            continue
+    return None
+
+
+def measure_int8_peak(torch, dev):
+    """Dense int8 GEMM rate of this GPU: torch._int_mm (cuBLASLt) on 8192^3, best of 10
+    (CUDA events), in TOP/s.  None if the library call is not available here."""
+    n = 8192
+    try:
+        a = torch.randint(-127, 128, (n, n), dtype=torch.int8, device=dev)
+        b = torch.randint(-127, 128, (n, n), dtype=torch.int8, device=dev)
+        for mat2 in (b, b.t().contiguous().t()):
+            try:
+                torch._int_mm(a, mat2)
+            except RuntimeError:
+                continue
+            torch.cuda.synchronize()
+            best = None
+            for _ in range(10):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                torch._int_mm(a, mat2)
+                e1.record()
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1)
+                best = ms if best is None else min(best, ms)
+            return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    except (RuntimeError, AttributeError):
+        return None
+    return None
 
 
 # ---------------------------------------------------------------- workloads
@@ -168,33 +223,33 @@ class BertWorkload:
         return [(xh, xd), (lh, ld)], (self.y, yh), lambda: self.step(xd, ld)
 
     def work(self, label):
-        """(flops, bytes) per launch: algorithmic work of the packed batch (T valid tokens);
-        the dense padded work that removal avoids is not counted."""
+        """(flops, bytes) per launch: the algorithmic work of the method step(s) the kernel
+        computes, over the packed batch (T valid tokens), with each operand read once and
+        each result written once in the storage type e.  Intermediates of this design
+        (fp32 split-K slices, the fp32 residual copy) are not counted: they are traffic,
+        not work.  The dense padded work that removal avoids is not counted either."""
         c, T = self.cfg, self.T
         H, F, B, L = c.H, c.F, c.B, c.L
         e = 4 if c.storage_dtype == "fp32" else 2
-        r1 = 4 if c.storage_dtype == "bf16" else e   # FC2 residual: fp32 copy of LN1 output for bf16
         lab = label.replace("_i8", "")
-        if lab == "gemm_qkv":
+        if lab == "gemm_qkv":      # X and Wqkv in, Q|K|V out
             return 2.0 * T * H * 3 * H, e * (T * H + 3 * H * H + 3 * T * H)
-        if lab == "gemm_proj":   # reads attn and Wo; writes the fp32 accumulator
-            return 2.0 * T * H * H, e * (T * H + H * H) + 4 * T * H
+        if lab == "gemm_proj":     # A and Wo in, C out, plus the residual read
+            return 2.0 * T * H * H, e * (T * H + H * H + T * H + T * H)
         if lab == "gemm_fc1":
             return 2.0 * T * H * F, e * (T * H + F * H + T * F)
-        if lab == "gemm_fc2":
-            return 2.0 * T * F * H, e * (T * F + F * H) + 4 * T * H
-        if lab == "attention":   # QK^T and PV over valid keys; Q, K, V read once, O written once
+        if lab == "gemm_fc2":      # A and W2 in, C out, plus the residual read
+            return 2.0 * T * F * H, e * (T * F + F * H + T * H + T * H)
+        if lab == "attention":     # QK^T and PV over valid keys; Q, K, V read once, O written once
             return 4.0 * H * self.sum_len2, e * 4 * T * H
-        if lab == "layernorm1":  # fp32 sum + residual in, activation out (+ fp32 copy for bf16)
-            return 0.0, 4 * T * H + 2 * e * T * H + (4 * T * H if c.storage_dtype == "bf16" else 0)
-        if lab == "layernorm2":
-            return 0.0, 4 * T * H + r1 * T * H + e * T * H
-        if lab == "layernorm2_rebuild":   # padded output with zero pads
-            return 0.0, 4 * T * H + r1 * T * H + e * B * L * H
-        if lab == "offsets_remove":
-            return 0.0, 4 * B + 2 * e * T * H + 4 * (T + B + 1)
+        if lab in ("layernorm1", "layernorm2"):   # row in, row out (+ the int8 code copy)
+            return 0.0, 2 * e * T * H + (T * H if c.dtype == "int8" and lab == "layernorm1" else 0)
+        if lab == "layernorm2_rebuild":   # valid rows in, every padded slot out (pads are zeros)
+            return 0.0, e * T * H + e * B * L * H
+        if lab == "offsets_remove":       # lengths in; cu, offsets out; valid rows gathered
+            return 0.0, 4 * B + 4 * (B + 1) + 4 * T + 2 * e * T * H
         if lab in ("quantize_x", "quantize_attn"):
-            return 0.0, e * T * H + 2 * T * H
+            return 0.0, e * T * H + T * H
         if lab == "build_offsets":
             return 0.0, 4 * (2 * B + 1 + T)
         if lab == "remove_padding":
@@ -202,6 +257,13 @@ class BertWorkload:
         if lab == "rebuild_padding":
             return 0.0, e * T * H + e * B * L * H
         return 0.0, 0.0
+
+    def method_steps(self):
+        """(flops, bytes) of every method step of one step of the path (offsets and
+        removal, each layer's seven steps, the rebuild), for the layer-level roofline."""
+        per_layer = [self.work(k) for k in ("gemm_qkv", "attention", "gemm_proj", "layernorm1", "gemm_fc1",
+                                            "gemm_fc2", "layernorm2")]
+        return [self.work("offsets_remove")] + per_layer * self.cfg.layers + [self.work("rebuild_padding")]
 
     def oracle_rate(self, budget_s):
         """The oracle, as it stands, over whole sequences of the batch for ~budget_s."""
@@ -295,6 +357,12 @@ class SwinWorkload:
             return 4.0 * T * C_ * F, e * (3 * T * C_ + 2 * F * C_)
         return 0.0, 0.0
 
+    def method_steps(self):
+        """S1-S7 of the block, each with its own operands (FC1's output written and read
+        once between the two MLP GEMMs, as the method states the step)."""
+        return [self.work(k) for k in ("layernorm1", "gemm_qkv", "window_attention", "gemm_proj", "layernorm2",
+                                       "gemm_fc1", "gemm_fc2")]
+
     def oracle_rate(self, budget_s):
         import oracle
         c, wl = self.cfg, self.wl
@@ -358,6 +426,9 @@ class MergeWorkload:
         if label == "gemm_reduction":
             return 2.0 * R * 4 * C_ * 2 * C_, e * (R * 4 * C_ + 8 * C_ * C_ + R * 2 * C_)
         return 0.0, 0.0
+
+    def method_steps(self):
+        return [self.work("patch_merge_ln"), self.work("gemm_reduction")]
 
     def oracle_rate(self, budget_s):
         import oracle
@@ -432,7 +503,7 @@ def run_reference(args, wk, rank):
     tot_tokens = tot_t = 0.0
     sample = ""
     for _ in range(args.steps):
-        v, sample, dt = wk.oracle_rate(5.0)
+        v, sample, dt = wk.oracle_rate(3.0)
         tot_tokens += v * dt
         tot_t += dt
     value = tot_tokens / tot_t
@@ -451,6 +522,10 @@ def main():
     args = parse()
     rank, world, local = dist_env()
     wk = make_workload(args.workload, rank)
+    if args.oracle_rate > 0:   # child mode of the single-thread oracle leg (no GPU, no torch)
+        v, sample, dt = wk.oracle_rate(args.oracle_rate)
+        print(json.dumps({"value": v, "sample": sample, "dt": dt}), flush=True)
+        return None
     if args.impl == "reference":
         return run_reference(args, wk, rank)
 
@@ -505,12 +580,17 @@ def main():
         for _ in range(3):
             graph.replay()
         torch.cuda.synchronize()
-    out_dir = os.path.join(ROOT, "gpurun_out")
-    clk_path = os.path.join(out_dir, f"clocks_rank{rank}.csv") if os.path.isdir(out_dir) else f"/tmp/rpp_clk{rank}.csv"
+    import tempfile
+    fd, clk_path = tempfile.mkstemp(prefix=f"rpp_clocks_rank{rank}_", suffix=".csv")
+    os.close(fd)
     proc, fh = clocks_sampler_start(clk_path)
     time.sleep(0.3)
     total_s = timed(graph.replay if graph is not None else wk.step)
     clocks = clocks_sampler_stop(proc, fh, clk_path, local)
+    try:
+        os.unlink(clk_path)
+    except OSError:
+        pass
     code = rpp.get_device_error(wk.err)
     if code:
         raise SystemExit(f"device error {code}")
@@ -578,6 +658,7 @@ def main():
             prev = evs[i]
     del hook_graph
     peaks, peak_kind = load_peaks()
+    int8_peak = measure_int8_peak(torch, dev) if getattr(wk.cfg, "dtype", "") == "int8" else None
     per_launch = {}
     for lab, vals in kernels.items():
         cnt = len(vals) / reps
@@ -593,6 +674,8 @@ def main():
             ach = b_ / (ms * 1e-3) / 1e9
             d = {"bound": "hbm", "achieved": ach, "unit": "GB/s", "frac": ach / peaks["hbm_gbs"] if b_ else None}
         d.update({"launches_per_step": cnt, "ms_per_launch": ms, "ms_per_step": ms * cnt, "flops": f_, "bytes": b_})
+        if lab.endswith("_i8") and f_ and int8_peak:   # the exact int8 GEMMs run on the bf16 pipe
+            d["frac_of_int8_peak"] = f_ / (ms * 1e-3) / 1e12 / int8_peak
         per_launch[lab] = d
     dom = max(per_launch, key=lambda k: per_launch[k]["ms_per_step"])
     # The dominant kernel alone: events just before and after each of its launches
@@ -647,6 +730,20 @@ def main():
                        "(other launches unmarked), graph replays with L2 flushed between them"
                        if dom_ms is not None else "CUDA events after every launch of an eager step")}
 
+    # ---- the whole step against the sum of its method steps' ideal times
+    ideal_s = 0.0
+    for f_, b_ in wk.method_steps():
+        ideal_s += max(f_ / (peaks["bf16_tflops"] * 1e12), b_ / (peaks["hbm_gbs"] * 1e9))
+    ideal_sus = 0.0
+    for f_, b_ in wk.method_steps():
+        ideal_sus += max(f_ / (peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * 1e12),
+                         b_ / (peaks["hbm_gbs"] * 1e9))
+    step_s = total_s / args.steps
+    layer_roof = {"ideal_ms_per_step": ideal_s * 1e3, "ms_per_step": step_s * 1e3, "frac": ideal_s / step_s,
+                  "frac_vs_sustained_bf16": ideal_sus / step_s,
+                  "how": ("sum over the method steps of max(flops / bf16 dense peak, algorithmic bytes / HBM copy "
+                          "bandwidth), measured peaks; divided by the graph-replayed step time")}
+
     # ---- end to end through host buffers (eager calls of the public API)
     e2e = None
     if not args.no_e2e:
@@ -671,6 +768,9 @@ def main():
     if rank == 0 and not args.no_cpu_baseline:
         v, sample, _ = wk.oracle_rate(12.0)
         cpu = {"value": v, "unit": "tokens/s", "cores": threads_used(), "kind": "oracle", "sample": sample}
+        one = oracle_single_thread(args, 12.0)
+        if one is not None:
+            cpu["single_thread"] = {"value": one["value"], "unit": "tokens/s", "cores": 1, "sample": one["sample"]}
 
     if world > 1:
         torch.distributed.barrier()
@@ -682,10 +782,11 @@ def main():
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": wk.dtype, "data": "synthetic", "config": cfgd,
-                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "roofline": roof, "layer_roofline": layer_roof, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": int(n_launch_step * args.steps) if n_launch_step else None, "clocks": clocks,
                 "value_eager": value_eager, "ms_per_step_eager": 1e3 * eager_s / args.steps,
                 "kernels": per_launch,
+                "int8_peak_tops": int8_peak,
                 "kernel_timing": ("CUDA events recorded as graph nodes after every launch, replayed after the timed "
                                   "region with the same L2 flush" if graph is not None else
                                   "CUDA events recorded after every launch of an eager step")}

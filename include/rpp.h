@@ -88,7 +88,8 @@ RPP_API rpp_status rpp_get_device_error(const int32_t* err, int32_t* host_code, 
  * a host array of cudaEvent_t owned by the caller; capacity 0 disables the hook.
  * Not thread-safe: one profiling caller at a time. */
 RPP_API rpp_status rpp_set_launch_events(void* const* events, int capacity);
-/* Tuning knob of the fp16 / bf16 tensor-core GEMMs (no counterpart in the pages):
+/* TEST / TUNING ONLY -- not part of the method's calls.  Process-wide knob of the
+ * fp16 / bf16 tensor-core GEMMs (no counterpart in the pages):
  * 0 (default) pairs CTAs into two-CTA clusters running cta_group::2 MMAs on 256-row
  * tiles (each CTA holds its 128 A rows and half of the weight tile) when K >= 1024 and
  * the expected row count is >= 8192; 1 never pairs; 2 always pairs.  The exact int8
@@ -97,6 +98,15 @@ RPP_API rpp_status rpp_set_launch_events(void* const* events, int capacity);
  * tile shape and K split are chosen per mode, and a different K split changes the
  * fp32 summation order.  Process-wide, not thread-safe; RPP_EINVAL outside 0..2. */
 RPP_API rpp_status rpp_set_gemm_cluster_mode(int mode);
+
+/* TEST ONLY -- exercises the failure detection of the bounded waits (no counterpart in
+ * the pages).  The next fp16 / bf16 / int8 tensor-core GEMM launch of this process issues
+ * no operand loads, and its pipeline waits give up after `limit_us` microseconds instead
+ * of the normal 4 s: the launch records RPP_DERR_TIMEOUT in the error word, drains,
+ * frees its tensor memory and exits, and the context stays usable.  The setting is
+ * consumed by that one launch.  Process-wide, not thread-safe; RPP_EINVAL unless
+ * 1 <= limit_us <= 1000000. */
+RPP_API rpp_status rpp_test_stall_next_gemm(unsigned int limit_us);
 
 /* Restrict the hook to launches labelled `label` (NULL: every launch, the default).
  * With a filter, an event is recorded just BEFORE and just after each matching
@@ -313,9 +323,11 @@ RPP_API rpp_status rpp_gemm_i8_i32(const int8_t* aq, const int8_t* wq_t, int32_t
  *  - All calls share the one scratch array, which keeps the previous call's contents;
  *    each call writes every byte it reads, so nothing needs clearing, but calls whose
  *    kernels overlap on the GPU (unordered streams) race on it.
- *  - The first call on each device looks up the scratch array's device address
- *    (cudaGetSymbolAddress, with that device current); make that first call before
- *    any stream capture. */
+ *  - Every call looks up the scratch array's device address on the current device
+ *    (cudaGetSymbolAddress), so it stays valid across cudaDeviceReset; the first call
+ *    on a device also loads the library's device code there, so make that first call
+ *    before any stream capture.
+ *  - Errors map to the same statuses as rpp_gemm_i8_i32. */
 #define RPP_GEMM_I8_NOALLOC_SCRATCH_BYTES (8u << 20) /* 8 MiB */
 RPP_API rpp_status rpp_gemm_i8_i32_noalloc(const int8_t* aq, const int8_t* wq_t, int32_t* acc, int M,
                                            int N, int K, int32_t* err, rpp_stream stream);

@@ -28,13 +28,7 @@ inline size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 inline int esize(rpp_dtype dt) { return dt == RPP_F32 ? 4 : (dt == RPP_I8 ? 1 : 2); }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-inline rpp_status from_cuda(cudaError_t e) {
-  if (e == cudaSuccess) return RPP_OK;
-  cudaGetLastError();   // clear a sticky launch-configuration error
-  if (e == cudaErrorNotSupported) return RPP_EUNSUPPORTED;
-  if (e == cudaErrorInvalidValue) return RPP_EINVAL;
-  return RPP_ECUDA;
-}
+inline rpp_status from_cuda(cudaError_t e) { return status_from_cuda(e); }
 
 // ---------------------------------------------------------------- launch-event hook
 // While enabled (rpp_set_launch_events), every kernel launch of the path is followed
@@ -473,6 +467,12 @@ rpp_status rpp_set_launch_events(void* const* events, int capacity) {
 rpp_status rpp_set_gemm_cluster_mode(int mode) {
   if (mode < 0 || mode > 2) return RPP_EINVAL;
   set_gemm_cluster_mode(mode);
+  return RPP_OK;
+}
+
+rpp_status rpp_test_stall_next_gemm(unsigned int limit_us) {
+  if (limit_us == 0 || limit_us > 1000000u) return RPP_EINVAL;
+  set_gemm_stall_next(static_cast<unsigned long long>(limit_us) * 1000ull);
   return RPP_OK;
 }
 

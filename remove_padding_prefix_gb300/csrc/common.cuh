@@ -161,14 +161,15 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // wait) or once another role of the CTA has raised the abort flag, it gives up and
 // returns false; the caller records an error and unwinds.
 constexpr uint64_t kWaitLimitNs = 4000000000ull;   // 4 s
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 31u) == 0) {
       if (abort_flag && *abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+      if (global_timer_ns() - t0 > limit_ns) return false;
     }
   }
 }

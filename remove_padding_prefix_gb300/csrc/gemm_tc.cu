@@ -95,6 +95,8 @@ struct GemmParams {
   int32_t* err;
   int splits;               // K splits per tile (1 = none)
   long long split_stride;   // elements between the fp32 partial slices
+  unsigned long long wait_ns;   // limit of the pipeline's bounded waits (the drains keep the default)
+  int stall;                // test hook: the producer issues no loads, so the waits run out
 };
 
 constexpr uint32_t pow2_cols(uint32_t c) {
@@ -362,7 +364,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if constexpr (kTma) tma_prefetch_desc(&tmC);
-    if constexpr (CL == 1) {
+    if (CL == 1 && !p.stall) {
       // unit cid: column block (cid / S) % num_n, K blocks [kb0, kb1) (independent of M)
       const int nk = (p.K + kBK - 1) / kBK;
       const int kps0 = (nk + p.splits - 1) / p.splits;
@@ -454,7 +456,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int unit = cid; unit < total && ok; unit += ncl) {
+      // (test hook) no loads at all: the consumers' bounded waits run out
+      for (int unit = p.stall ? total : cid; unit < total && ok; unit += ncl) {
         const int tile = unit / S;
         const int kb0 = (unit - tile * S) * kps;
         const int kb1 = min(num_k, kb0 + kps);
@@ -468,7 +471,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             tma_load_2d(sA + s * A_BYTES, &tmA, &full[s], kb * kBK, m0);
             continue;
           }
-          if (!mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag)) {
+          if (!mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -511,7 +514,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int kb1 = min(num_k, kb0 + kps);
         const uint32_t a = NBUF == 2 ? (acc_it & 1u) : 0u;
         const uint32_t aph = NBUF == 2 ? ((acc_it >> 1) & 1u) : (acc_it & 1u);
-        if (!mbar_wait_bounded(&tempty[a], aph ^ 1u, abort_flag)) {
+        if (!mbar_wait_bounded(&tempty[a], aph ^ 1u, abort_flag, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -522,7 +525,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           const uint32_t d_tmem = tmem_base + (a * NCH + chunk) * ACC;
           const uint32_t s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
-          if (!mbar_wait_bounded(&full[s], ph, abort_flag)) {
+          if (!mbar_wait_bounded(&full[s], ph, abort_flag, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -582,7 +585,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
       }
       int ok = 1;
-      if (lane == 0) ok = mbar_wait_bounded(&tfull[a], aph, abort_flag) ? 1 : 0;
+      if (lane == 0) ok = mbar_wait_bounded(&tfull[a], aph, abort_flag, p.wait_ns) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
         if (lane == 0) {
@@ -898,9 +901,11 @@ bool gemm_tc_supported(int N, int K) {
 
 namespace {
 int g_cluster_mode = 0;   // 0 automatic, 1 never, 2 always (where the GEMM has two row tiles)
+unsigned long long g_stall_next_ns = 0;   // test hook: nonzero = the next launch stalls, waits give up after this
 }
 
 void set_gemm_cluster_mode(int mode) { g_cluster_mode = mode; }
+void set_gemm_stall_next(unsigned long long limit_ns) { g_stall_next_ns = limit_ns; }
 
 cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t stream) {
   const bool is_int = g.epi >= EPI_I32 && g.epi <= EPI_DQ_BIAS_GELU_Q;
@@ -928,7 +933,12 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t stream) {
   CUtensorMap ta, tb;
   if (!make_tmap_2d(&ta, g.a, dt, 2, g.M_max, g.K, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
   GemmParams p{g.M_max, g.rows, g.N, g.K, g.bias, g.residual, g.out, g.a_scale, g.w_scale, g.q_scale, g.err,
-               tc.splits, static_cast<long long>(g.M_max) * g.N};
+               tc.splits, static_cast<long long>(g.M_max) * g.N, kWaitLimitNs, 0};
+  if (g_stall_next_ns) {   // consumed by this one launch
+    p.stall = 1;
+    p.wait_ns = g_stall_next_ns;
+    g_stall_next_ns = 0;
+  }
   if (is_int) {
     if (!make_tmap_2d(&tb, g.w_t, dt, 2, g.N, g.K, bn, kBK, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     if (nch == 1) return dispatch_int<1>(bn, g.epi, ta, tb, p, rows_hint, stream);

@@ -8,6 +8,16 @@ namespace rpp {
 
 int num_sms();   // SM count of the current device (cached per device)
 
+// Status of the C ABI for a CUDA runtime result; clears a sticky launch error.  Shared
+// by every entry point so that the same failure maps to the same status everywhere.
+inline rpp_status status_from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return RPP_OK;
+  cudaGetLastError();
+  if (e == cudaErrorNotSupported) return RPP_EUNSUPPORTED;
+  if (e == cudaErrorInvalidValue) return RPP_EINVAL;
+  return RPP_ECUDA;
+}
+
 // epilogue codes beyond the public rpp_epilogue (int8 layer)
 enum InternalEpilogue {
   EPI_I32 = 3,               // raw int32 accumulators
@@ -102,6 +112,9 @@ bool gemm_tc_supported(int N, int K);
 cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t stream);
 // 0 automatic, 1 never cluster, 2 cluster whenever the GEMM is fp16/bf16
 void set_gemm_cluster_mode(int mode);
+// test hook: the next tensor-core GEMM launch issues no operand loads and its pipeline
+// waits give up after limit_ns (it records RPP_DERR_TIMEOUT and exits cleanly)
+void set_gemm_stall_next(unsigned long long limit_ns);
 
 cudaError_t launch_gemm_f32(const float* a, const float* w_t, const float* bias, const float* residual, float* out,
                             int M_max, const int32_t* rows, int N, int K, int epi, int32_t* err, cudaStream_t stream);

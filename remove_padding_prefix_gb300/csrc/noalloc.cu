@@ -17,11 +17,10 @@
 //    byte a call reads is written earlier by the same call, so nothing needs clearing,
 //    but two calls whose kernels overlap on the GPU (different streams, no ordering
 //    between them) race on the array and give wrong results;
-//  * the first call on a device looks up the array's device address with
-//    cudaGetSymbolAddress (once per device, with that device current); make that first
-//    call outside any stream capture.
-#include <mutex>
-
+//  * every call looks up the array's device address on the current device with
+//    cudaGetSymbolAddress (cheap, no stream work), so the address stays right after a
+//    cudaDeviceReset or a context change; the first call on a device also loads the
+//    library's device code there, so make that first call outside any stream capture.
 #include "kernels.h"
 
 namespace rpp {
@@ -33,25 +32,15 @@ constexpr size_t kNoAllocScratchBytes = RPP_GEMM_I8_NOALLOC_SCRATCH_BYTES;
 // address: only the address returned by cudaGetSymbolAddress may be handed to kernels.
 static __device__ __align__(256) uint8_t g_i8_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-void* g_scratch_dev_ptr[kMaxDevices] = {};
-std::mutex g_scratch_mu;
-
-// Device address of the scratch array on the current device (looked up once per device).
+// Device address of the scratch array in the current device's context.  Looked up on
+// every call rather than cached: after a cudaDeviceReset the module is loaded again and
+// the array may sit at another address.
 cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_i8_noalloc_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_dev_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_i8_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    if (!p) return cudaErrorInvalidSymbol;
-    g_scratch_dev_ptr[dev] = p;
-  }
-  *out = g_scratch_dev_ptr[dev];
+  if (!p) return cudaErrorInvalidSymbol;
+  *out = p;
   return cudaSuccess;
 }
 
@@ -70,10 +59,8 @@ extern "C" rpp_status rpp_gemm_i8_i32_noalloc(const int8_t* aq, const int8_t* wq
   const size_t w_bytes = round256(static_cast<size_t>(N) * K * 2);
   if (a_bytes + w_bytes > kNoAllocScratchBytes) return RPP_EWORKSPACE;
   void* base = nullptr;
-  if (scratch_address(&base) != cudaSuccess) {
-    cudaGetLastError();
-    return RPP_ECUDA;
-  }
+  const cudaError_t ea = scratch_address(&base);
+  if (ea != cudaSuccess) return status_from_cuda(ea);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void* a_codes = base;
   void* w_codes = static_cast<uint8_t*>(base) + a_bytes;
@@ -93,7 +80,5 @@ extern "C" rpp_status rpp_gemm_i8_i32_noalloc(const int8_t* aq, const int8_t* wq
     g.err = err;
     e = launch_gemm_tc(g, s);
   }
-  if (e == cudaSuccess) return RPP_OK;
-  cudaGetLastError();
-  return e == cudaErrorNotSupported ? RPP_EUNSUPPORTED : RPP_ECUDA;
+  return status_from_cuda(e);   // the same mapping as rpp_gemm_i8_i32
 }

@@ -115,3 +115,9 @@ def test_patch_merge_size_queries_and_validation(lib):
     assert lib.rpp_patch_merge_bytes(C.byref(_abi.MergeCfg(56, 100, 1e-5, _abi.RPP_F16))) == 0   # C % 8
     assert lib.rpp_patch_merge_bytes(C.byref(_abi.MergeCfg(56, 96, 1e-5, _abi.RPP_F32))) == 0    # 16-bit only
     assert lib.rpp_patch_merge_forward(C.byref(ok), None, 1, None, None, None, 0, None, None) == -1
+
+
+def test_stall_hook_rejects_out_of_range_limits(lib):
+    """The test-only stall hook takes 1 us .. 1 s and nothing else (no launch here)."""
+    assert lib.rpp_test_stall_next_gemm(0) == -1
+    assert lib.rpp_test_stall_next_gemm(1000001) == -1

@@ -71,7 +71,8 @@ def cluster_mode():
     (384, 144, 64, 0, 129),
 ])
 def test_tc_gemm_cluster_modes(cluster_mode, mode, M, N, K, epi, rows):
-    """Unpaired and paired (thread-block cluster, W tile multicast) GEMMs, each against
+    """Unpaired and paired GEMMs (a two-CTA cluster, each CTA loading its own A rows and half
+    of the W tile for cta_group::2 MMAs), each against
     the oracle, on shapes with an odd number of row tiles."""
     cluster_mode(mode)
     _gemm_case("bf16" if epi == 2 else "fp16", M, N, K, epi, seed=M + mode, rows=rows)
