@@ -101,8 +101,11 @@ cudaError_t launch_attention_varlen(const void* qkv, const int32_t* cu, int B, i
     return launch_pdl(attention_varlen_f32_kernel, grid, dim3(kF32Rows), 0, stream, static_cast<const float*>(qkv), cu,
                       T_max, max_len, nh, static_cast<float*>(out), scale, err);
   }
-  if (dtype == RPP_F16 || dtype == RPP_BF16)
+  if (dtype == RPP_F16 || dtype == RPP_BF16) {
+    if (attention_sched_supported(B, max_len))
+      return launch_attention_sched(qkv, cu, B, T_max, max_len, nh, dtype, out, err, stream);
     return launch_attention_tc(qkv, cu, B, T_max, max_len, nh, dtype, out, err, stream);
+  }
   return cudaErrorNotSupported;
 }
 

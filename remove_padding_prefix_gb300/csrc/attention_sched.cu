@@ -1,0 +1,541 @@
+// Persistent variable-length multi-head attention on the 5th-generation tensor cores
+// (head size 64, fp16 or bf16): the encoder layer's fMHA.
+//
+// The Swin talk (§3) runs fMHA as batch GEMM + softmax + batch GEMM in one kernel with
+// the head transposes folded into its I/O; the Kuaishou article (Fig. 10) runs the
+// attention on the padding-free packed batch, where it is the one kernel that needs
+// the sequence bounds.  This kernel takes the sequence bounds from cu_seqlens and:
+//
+//  * Schedules work longest-first.  A work item is (sequence, head, 128-query tile);
+//    its cost is the sequence's number of 128-key tiles.  Every CTA builds the same
+//    item list from cu_seqlens in its prologue -- sequences grouped by tile count,
+//    largest first, stable within a group -- and a persistent grid of two CTAs per SM
+//    walks it round-robin.  The q-tiles of one (sequence, head) are neighbours in the
+//    list, so the CTAs that share its K and V tiles run at the same time and read them
+//    from L2.
+//  * Keeps S, P and O in tensor memory: S = Q K^T (columns [0, 128)), P (the 16-bit
+//    softmax numerators, columns [128, 192): 128 keys, two per 32-bit column) and O
+//    (columns [192, 256)).  O += P V reads P straight from tensor memory (the A operand
+//    of tcgen05.mma may live there), so P never goes through shared memory.
+//  * Runs the softmax with one thread per query row (four warps): the thread loads its
+//    row of S (tcgen05.ld), masks keys past the sequence, takes the row maximum,
+//    writes 2^(s - m) rounded to the input type into P and keeps the fp32 row sum.
+//    The reference maximum m moves only when a tile's maximum exceeds it by more than
+//    8 (log2 units), so P stays below 2^8; O and the sum are then rescaled in tensor
+//    memory.  Tensor-memory loads and stores are warp-collective, so that decision is
+//    taken per warp (scale 1 for rows that keep their maximum).
+//  * Overlaps: S_{j+1} is issued as soon as the softmax has read S_j, before P_j V_j;
+//    K and V tiles are double-buffered and the next item's Q tile loads while the
+//    current item finishes.  Partial tiles shrink the MMAs to whole 16-key steps; warps
+//    whose 32 query rows all lie past the sequence skip the softmax arithmetic.
+//
+// Keys past the sequence end get -inf before the maximum (P = 0 there); the V rows of
+// the last 16-key step that lie past the end are zeroed in shared memory, so nothing
+// beyond the sequence (another sequence, or unwritten capacity holding NaN) reaches a
+// valid output.  Query rows past the end are computed and never stored.  Every
+// mbarrier wait is bounded; a wait that gives up records RPP_DERR_TIMEOUT, raises the
+// CTA's abort flag, and the CTA drains its copies and MMAs, frees tensor memory and
+// exits.
+#include "kernels.h"
+
+namespace rpp {
+
+namespace {
+
+constexpr int kT = 128;                        // queries per item, keys per tile
+constexpr int kDh = 64;                        // head size
+constexpr int kThreads = 192;                  // warp 0 TMA, warp 1 MMA, warps 2..5 softmax
+constexpr uint32_t kTile = kT * kDh * 2;       // one 128 x 64 tile of Q, K or V (16 KB)
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColS = 0, kColP = 128, kColO = 192;
+constexpr int kMaxCls = 64;                    // tiles per sequence: max_len <= 8192
+constexpr int kMaxB = 4096;                    // sequences per batch
+
+// shared-memory layout (bytes from the 1024-aligned base)
+constexpr uint32_t kOffQ = 0;                  // [2] tiles
+constexpr uint32_t kOffK = 2 * kTile;          // [2]
+constexpr uint32_t kOffV = 4 * kTile;          // [2]
+constexpr uint32_t kOffBar = 6 * kTile;        // 16 mbarriers
+constexpr uint32_t kOffMisc = kOffBar + 16 * 8;   // tmem slot, abort flag, counts
+constexpr uint32_t kOffCls = kOffMisc + 64;    // 4 int arrays of kMaxCls + 2
+constexpr uint32_t kOffPerm = kOffCls + 4 * (kMaxCls + 2) * 4;   // int16 [B]
+
+size_t smem_bytes(int B) { return 1024 + kOffPerm + ((static_cast<size_t>(B) * 2 + 15) & ~static_cast<size_t>(15)); }
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+template <typename T> struct Fmt;
+template <> struct Fmt<__half> { static constexpr int v = 0; };
+template <> struct Fmt<__nv_bfloat16> { static constexpr int v = 1; };
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float a, float b);   // a -> low half (the even key)
+template <>
+__device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16: A (M x K, one row per lane, two 16-bit
+// elements per 32-bit column) from tensor memory
+__device__ __forceinline__ void tc_mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The CTA-wide item list: sequences grouped by tile count (largest first), items of a
+// sequence in (head, q-tile) order.
+struct Sched {
+  const int* item_off;   // [c]: first item of tile count c (c = n_cls .. 1), item_off[0] = total
+  const int* seq_off;    // [c]: first position in perm of the sequences with c tiles
+  const int16_t* perm;   // sequence indices, grouped
+  int n_cls, nh;
+};
+struct Item {
+  int b, h, q0, c0, len, ntiles;
+};
+__device__ __forceinline__ Item decode(const Sched& s, const int32_t* cu, int g) {
+  int c = s.n_cls;
+  while (c > 1 && g >= s.item_off[c - 1]) --c;   // classes laid out n_cls, n_cls - 1, ...: item_off decreasing in c
+  // g lies in class c: [item_off[c], item_off[c - 1])
+  const int idx = g - s.item_off[c];
+  const int per_seq = s.nh * c;
+  const int sq = idx / per_seq;
+  const int rem = idx - sq * per_seq;
+  Item it;
+  it.b = s.perm[s.seq_off[c] + sq];
+  it.h = rem / c;
+  it.q0 = (rem - it.h * c) * kT;
+  it.c0 = __ldg(cu + it.b);
+  it.len = __ldg(cu + it.b + 1) - it.c0;
+  it.ntiles = c;
+  return it;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 2)
+attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __restrict__ cu, int B, int T_max,
+                       int max_len, int nh, int n_cls, T* __restrict__ out, float scale_log2, int32_t* err) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* q_full = bars + 0;    // [2]
+  uint64_t* q_empty = bars + 2;   // [2]
+  uint64_t* k_full = bars + 4;    // [2]
+  uint64_t* k_empty = bars + 6;   // [2]
+  uint64_t* v_full = bars + 8;    // [2]
+  uint64_t* v_empty = bars + 10;  // [2]
+  uint64_t* s_full = bars + 12;   // S computed (commit)
+  uint64_t* s_free = bars + 13;   // S read by the four softmax warps
+  uint64_t* p_full = bars + 14;   // P written by the four softmax warps
+  uint64_t* pv_done = bars + 15;  // O += P V completed (commit)
+  uint64_t* o_free = reinterpret_cast<uint64_t*>(smem + kOffMisc + 32);   // O read out (four warps)
+  uint64_t* drain = reinterpret_cast<uint64_t*>(smem + kOffMisc + 40);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  int* s_status = reinterpret_cast<int*>(smem + kOffMisc + 8);   // 0 ok, else the device error to record / quit
+  int* cls_cnt = reinterpret_cast<int*>(smem + kOffCls);
+  int* seq_off = cls_cnt + (kMaxCls + 2);
+  int* item_off = seq_off + (kMaxCls + 2);
+  int* cursor = item_off + (kMaxCls + 2);
+  int16_t* perm = reinterpret_cast<int16_t*>(smem + kOffPerm);
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+
+  // everything below reads what the preceding kernels wrote (the QKV rows, cu_seqlens)
+  pdl_wait();
+  pdl_trigger();
+
+  if (threadIdx.x == 0) {
+    *s_status = device_error_set(err) ? -1 : 0;   // -1: quit without recording
+    *abort_flag = 0;
+  }
+  for (int c = threadIdx.x; c < kMaxCls + 2; c += kThreads) cls_cnt[c] = 0;
+  __syncthreads();
+  if (*s_status) return;
+
+  // ---- item list: tile counts per sequence (all threads), then a stable grouping (warp 0)
+  for (int b = threadIdx.x; b < B; b += kThreads) {
+    const int c0 = __ldg(cu + b), c1 = __ldg(cu + b + 1), len = c1 - c0;
+    if (c0 < 0 || len < 0 || c1 > T_max || len > max_len) {
+      atomicCAS(s_status, 0, len > max_len ? RPP_DERR_LENGTH : RPP_DERR_ROWS);
+    } else {
+      atomicAdd(&cls_cnt[(len + kT - 1) / kT], 1);
+    }
+  }
+  __syncthreads();
+  if (*s_status) {
+    if (threadIdx.x == 0 && *s_status > 0) set_device_error(err, *s_status);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    int so = 0, io = 0;
+    for (int c = n_cls; c >= 1; --c) {   // largest tile count first
+      seq_off[c] = so;
+      item_off[c] = io;
+      cursor[c] = so;
+      so += cls_cnt[c];
+      io += cls_cnt[c] * nh * c;
+    }
+    item_off[0] = io;   // the total, which is also where class 1 ends
+  }
+  __syncthreads();
+  if (warp == 0) {
+    for (int b0 = 0; b0 < B; b0 += 32) {
+      const int b = b0 + lane;
+      int c = -1;
+      if (b < B) c = (__ldg(cu + b + 1) - __ldg(cu + b) + kT - 1) / kT;
+      const unsigned peers = __match_any_sync(0xffffffffu, c);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      if (c > 0) perm[cursor[c] + rank] = static_cast<int16_t>(b);
+      __syncwarp();
+      if (c > 0 && rank == 0) cursor[c] += __popc(peers);
+      __syncwarp();
+    }
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 4);
+    mbar_init(p_full, 4);
+    mbar_init(pv_done, 1);
+    mbar_init(o_free, 4);
+    mbar_init(drain, 1);
+    fence_mbarrier_init();
+    tma_prefetch_desc(&tm);
+  }
+  const int n_items = item_off[0];
+  if (static_cast<int>(blockIdx.x) >= n_items) return;   // uniform: nothing allocated yet
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int H = nh * kDh;
+  const Sched sch{item_off, seq_off, perm, n_cls, nh};
+  uint8_t* sQ = smem + kOffQ;
+  uint8_t* sK = smem + kOffK;
+  uint8_t* sV = smem + kOffV;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t nq = 0, nk = 0, nv = 0;
+      bool ok = true;
+      for (int g = blockIdx.x; g < n_items && ok; g += gridDim.x) {
+        const Item it = decode(sch, cu, g);
+        {
+          const uint32_t qb = nq & 1u;
+          if (!mbar_wait_bounded(&q_empty[qb], ((nq >> 1) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(&q_full[qb], kTile);
+          tma_load_2d(sQ + qb * kTile, &tm, &q_full[qb], it.h * kDh, it.c0 + it.q0);
+          ++nq;
+        }
+        for (int j = 0; j < it.ntiles; ++j) {
+          const uint32_t kb = nk & 1u;
+          if (!mbar_wait_bounded(&k_empty[kb], ((nk >> 1) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(&k_full[kb], kTile);
+          tma_load_2d(sK + kb * kTile, &tm, &k_full[kb], H + it.h * kDh, it.c0 + j * kT);
+          ++nk;
+          const uint32_t vb = nv & 1u;
+          if (!mbar_wait_bounded(&v_empty[vb], ((nv >> 1) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(&v_full[vb], kTile);
+          tma_load_2d(sV + vb * kTile, &tm, &v_full[vb], 2 * H + it.h * kDh, it.c0 + j * kT);
+          ++nv;
+        }
+      }
+      if (!ok) {
+        set_device_error(err, RPP_DERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // the copies still in flight land before the CTA can exit: the last load into
+      // each buffer (at most one outstanding phase per buffer)
+      for (uint32_t i = nq > 2 ? nq - 2 : 0; i < nq; ++i) mbar_wait_bounded(&q_full[i & 1u], (i >> 1) & 1u, nullptr);
+      for (uint32_t i = nk > 2 ? nk - 2 : 0; i < nk; ++i) mbar_wait_bounded(&k_full[i & 1u], (i >> 1) & 1u, nullptr);
+      for (uint32_t i = nv > 2 ? nv - 2 : 0; i < nv; ++i) mbar_wait_bounded(&v_full[i & 1u], (i >> 1) & 1u, nullptr);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr int fmt = Fmt<T>::v;
+      constexpr uint32_t IDESC_O = idesc_f16(fmt, kT, kDh) | (1u << 16);   // B (= V) MN-major
+      const uint32_t d_s = tmem_base + kColS;
+      const uint32_t d_o = tmem_base + kColO;
+      const uint32_t a_p = tmem_base + kColP;
+      uint32_t nq = 0, nk = 0, nv = 0, ns = 0, npv = 0, nit = 0;
+      bool ok = true;
+      // O += P_j V_j for tile j of the current item
+      auto issue_pv = [&](const Item& it, int j) -> bool {
+        if (!mbar_wait_bounded(p_full, npv & 1u, abort_flag)) return false;
+        const uint32_t vb = nv & 1u;
+        if (!mbar_wait_bounded(&v_full[vb], (nv >> 1) & 1u, abort_flag)) return false;
+        if (j == 0 && nit > 0 && !mbar_wait_bounded(o_free, (nit - 1) & 1u, abort_flag)) return false;
+        tc_fence_after();
+        const int kvalid = min(kT, it.len - j * kT);
+        const int ksteps = (kvalid + 15) >> 4;
+        const uint64_t vdesc = sw128_kmajor_desc(smem_u32(sV + vb * kTile));
+        for (int k = 0; k < ksteps; ++k)   // 16 keys: P columns +8, V rows +16 (two 8-row atoms, 2048 bytes)
+          tc_mma_f16_tmem_a(d_o, a_p + 8u * k, vdesc + 128u * k, IDESC_O, (j | k) ? 1u : 0u);
+        tc_commit(&v_empty[vb]);
+        tc_commit(pv_done);
+        ++nv;
+        ++npv;
+        return true;
+      };
+      for (int g = blockIdx.x; g < n_items && ok; g += gridDim.x) {
+        const Item it = decode(sch, cu, g);
+        const uint32_t qb = nq & 1u;
+        if (!mbar_wait_bounded(&q_full[qb], (nq >> 1) & 1u, abort_flag)) { ok = false; break; }
+        const uint64_t qdesc = sw128_kmajor_desc(smem_u32(sQ + qb * kTile));
+        for (int j = 0; j < it.ntiles && ok; ++j) {
+          const int nvalid = min(kT, it.len - j * kT);
+          const uint32_t idesc_s = idesc_f16(fmt, kT, (nvalid + 15) & ~15);
+          const uint32_t kb = nk & 1u;
+          if (!mbar_wait_bounded(&k_full[kb], (nk >> 1) & 1u, abort_flag)) { ok = false; break; }
+          if (ns > 0 && !mbar_wait_bounded(s_free, (ns - 1) & 1u, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t kdesc = sw128_kmajor_desc(smem_u32(sK + kb * kTile));
+#pragma unroll
+          for (int k = 0; k < kDh / 16; ++k) tc_mma_f16(d_s, qdesc + 2u * k, kdesc + 2u * k, idesc_s, k ? 1u : 0u);
+          tc_commit(s_full);
+          tc_commit(&k_empty[kb]);
+          ++nk;
+          ++ns;
+          if (j == it.ntiles - 1) {
+            tc_commit(&q_empty[qb]);
+            ++nq;
+          }
+          if (j > 0 && !issue_pv(it, j - 1)) { ok = false; break; }
+        }
+        if (ok && !issue_pv(it, it.ntiles - 1)) ok = false;
+        ++nit;
+      }
+      if (!ok) {
+        set_device_error(err, RPP_DERR_TIMEOUT);
+        *abort_flag = 1;
+      }
+      // every MMA issued by this thread completes before tensor memory is released
+      tc_commit(drain);
+      mbar_wait_bounded(drain, 0, nullptr);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax, one thread per query row
+    const int quad = warp & 3;                       // tensor-memory lane quadrant of this warp
+    const int r = quad * 32 + lane;                  // query row of the item
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
+    uint32_t ns = 0, npv = 0, nit = 0;
+    bool ok = true;
+    for (int g = blockIdx.x; g < n_items && ok; g += gridDim.x) {
+      const Item it = decode(sch, cu, g);
+      const bool active = it.q0 + quad * 32 < it.len;   // warp-uniform: some row of this warp is a query
+      float m = neg_inf(), l = 0.f;
+      for (int j = 0; j < it.ntiles; ++j) {
+        const int nvalid = min(kT, it.len - j * kT);
+        const int nch = (nvalid + 31) >> 5;          // 32-key chunks holding keys of the sequence
+        int w = mbar_wait_bounded(s_full, ns & 1u, abort_flag) ? 1 : 0;
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        tc_fence_after();
+        // pass 1: the row maximum over this tile's keys (keys past the sequence: -inf),
+        // two 32-key chunks per tensor-memory round trip
+        float mx = neg_inf();
+        if (active) {
+          float pm[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2) {
+            if (64 * c2 < nvalid) {
+              uint32_t v[64];
+              tmem_ld_32x32b_x32(t_lane + kColS + 64 * c2, v);
+              if (64 * c2 + 32 < nvalid) tmem_ld_32x32b_x32(t_lane + kColS + 64 * c2 + 32, v + 32);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 64; ++e)
+                if (64 * c2 + e < nvalid) pm[e & 3] = fmaxf(pm[e & 3], __uint_as_float(v[e]));
+            }
+          }
+          mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])) * scale_log2;
+        }
+        // P_{j-1} and O: the previous P V must be done before P is rewritten or O rescaled
+        if (j > 0) {
+          w = mbar_wait_bounded(pv_done, (npv - 1) & 1u, abort_flag) ? 1 : 0;
+          if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+          tc_fence_after();
+        }
+        if (active) {
+          if (j == 0) {
+            m = mx;
+          } else {
+            const bool move = mx > m + 8.0f;
+            if (__any_sync(0xffffffffu, move)) {
+              const float alpha = move ? ex2_approx(m - mx) : 1.0f;
+#pragma unroll 1
+              for (int c = 0; c < 4; ++c) {
+                uint32_t ov[16];
+                tmem_ld_32x32b_x16(t_lane + kColO + 16 * c, ov);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                tmem_st_32x32b_x16(t_lane + kColO + 16 * c, ov);
+              }
+              if (move) {
+                l *= alpha;
+                m = mx;
+              }
+            }
+          }
+          // pass 2: P = 2^(s - m), 32 keys (16 columns of P) per chunk, packed in place over
+          // the chunk's first 16 registers (pair e is written after keys 2e, 2e + 1 are read)
+          float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            if (c < nch) {
+              uint32_t v[32];
+              tmem_ld_32x32b_x32(t_lane + kColS + 32 * c, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e2 = 0; e2 < 16; ++e2) {
+                const int e = 32 * c + 2 * e2;
+                const float s0 = e < nvalid ? __uint_as_float(v[2 * e2]) : neg_inf();
+                const float s1 = e + 1 < nvalid ? __uint_as_float(v[2 * e2 + 1]) : neg_inf();
+                const float p0 = ex2_approx(fmaf(s0, scale_log2, -m));
+                const float p1 = ex2_approx(fmaf(s1, scale_log2, -m));
+                ps[e2 & 3] += p0 + p1;
+                v[e2] = pack2<T>(p0, p1);
+              }
+              tmem_st_32x32b_x16(t_lane + kColP + 16 * c, v);
+            }
+          }
+          l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+          tmem_st_wait();
+        }
+        // S has been read: the next S may be computed
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free);
+        ++ns;
+        // the last 16-key step of a partial tile: zero the V rows past the sequence
+        // (P is 0 there, but 0 * NaN would not be)
+        const int kpad = ((nvalid + 15) & ~15);
+        if (nvalid < kpad && r >= nvalid && r < kpad) {
+          const uint32_t vb = npv & 1u;   // V tile j is the npv-th V load of this CTA
+          if (mbar_wait_bounded(&v_full[vb], (npv >> 1) & 1u, abort_flag)) {
+            uint8_t* vrow = sV + vb * kTile + r * 128;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(vrow + (((u + r) & 7) << 4)) = make_uint4(0u, 0u, 0u, 0u);
+            fence_proxy_async_smem();
+          } else {
+            ok = false;
+          }
+        }
+        if (!__all_sync(0xffffffffu, ok ? 1 : 0)) { ok = false; break; }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
+        ++npv;
+      }
+      if (!ok) break;
+      // the item's O: wait for its last P V, scale by 1 / sum, store the valid rows
+      int w = mbar_wait_bounded(pv_done, (npv - 1) & 1u, abort_flag) ? 1 : 0;
+      if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+      tc_fence_after();
+      if (active) {
+        uint32_t ov[64];
+        tmem_ld_32x32b_x32(t_lane + kColO, ov);
+        tmem_ld_32x32b_x32(t_lane + kColO + 32, ov + 32);
+        tmem_ld_wait();
+        if (it.q0 + r < it.len) {
+          const float inv = 1.0f / l;
+          uint4* orow = reinterpret_cast<uint4*>(out + static_cast<long long>(it.c0 + it.q0 + r) * H + it.h * kDh);
+#pragma unroll
+          for (int u = 0; u < kDh / 8; ++u) {
+            const float* f = reinterpret_cast<const float*>(ov + 8 * u);
+            orow[u] = make_uint4(pack2<T>(f[0] * inv, f[1] * inv), pack2<T>(f[2] * inv, f[3] * inv),
+                                 pack2<T>(f[4] * inv, f[5] * inv), pack2<T>(f[6] * inv, f[7] * inv));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free);
+      ++nit;
+    }
+    if (!ok && lane == 0) {
+      set_device_error(err, RPP_DERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace
+
+bool attention_sched_supported(int B, int max_len) {
+  return B >= 1 && B <= kMaxB && max_len >= 1 && (max_len + kT - 1) / kT <= kMaxCls;
+}
+
+cudaError_t launch_attention_sched(const void* qkv, const int32_t* cu, int B, int T_max, int max_len, int nh,
+                                   rpp_dtype dtype, void* out, int32_t* err, cudaStream_t stream) {
+  if (B <= 0 || max_len <= 0 || T_max <= 0) return cudaSuccess;
+  if (dtype != RPP_F16 && dtype != RPP_BF16) return cudaErrorNotSupported;
+  if (!attention_sched_supported(B, max_len)) return cudaErrorNotSupported;
+  const int H = nh * kDh;
+  CUtensorMap tm;
+  const CUtensorMapDataType dt = dtype == RPP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if (!make_tmap_2d(&tm, qkv, dt, 2, T_max, 3 * H, kT, kDh, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+  const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kDh));
+  const int n_cls = (max_len + kT - 1) / kT;
+  // persistent: two CTAs per SM, never more CTAs than the largest possible item count
+  const long long max_items = static_cast<long long>(B) * nh * n_cls;
+  const int grid = static_cast<int>(max_items < 2LL * num_sms() ? max_items : 2LL * num_sms());
+  const size_t smem = smem_bytes(B);
+  if (dtype == RPP_F16) {
+    static size_t attr = 0;
+    if (attr < smem) {
+      cudaError_t e = cudaFuncSetAttribute(attention_sched_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem_bytes(kMaxB)));
+      if (e != cudaSuccess) return e;
+      attr = smem_bytes(kMaxB);
+    }
+    return launch_pdl(attention_sched_kernel<__half>, dim3(grid), dim3(kThreads), smem, stream, tm, cu, B, T_max,
+                      max_len, nh, n_cls, static_cast<__half*>(out), scale_log2, err);
+  }
+  static size_t attr_bf = 0;
+  if (attr_bf < smem) {
+    cudaError_t e = cudaFuncSetAttribute(attention_sched_kernel<__nv_bfloat16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem_bytes(kMaxB)));
+    if (e != cudaSuccess) return e;
+    attr_bf = smem_bytes(kMaxB);
+  }
+  return launch_pdl(attention_sched_kernel<__nv_bfloat16>, dim3(grid), dim3(kThreads), smem, stream, tm, cu, B,
+                    T_max, max_len, nh, n_cls, static_cast<__nv_bfloat16*>(out), scale_log2, err);
+}
+
+}  // namespace rpp

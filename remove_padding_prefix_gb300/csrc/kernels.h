@@ -122,7 +122,12 @@ cudaError_t launch_gemm_f32(const float* a, const float* w_t, const float* bias,
 // 2D row-major [rows, cols] tensor map, box = box_cols x box_rows (defined with the GEMM)
 bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, int elem_bytes, long long rows,
                   int cols, int box_rows, int box_cols, CUtensorMapSwizzle swz);
-// tcgen05 varlen attention, head size 64, fp16 / bf16
+// persistent longest-first tcgen05 varlen attention (S, P, O in tensor memory), head size 64
+bool attention_sched_supported(int B, int max_len);
+cudaError_t launch_attention_sched(const void* qkv, const int32_t* cu, int B, int T_max, int max_len, int nh,
+                                   rpp_dtype dtype, void* out, int32_t* err, cudaStream_t stream);
+// tcgen05 varlen attention, head size 64, fp16 / bf16 (one CTA per 128 queries; batches
+// beyond the persistent kernel's limits)
 cudaError_t launch_attention_tc(const void* qkv, const int32_t* cu, int B, int T_max, int max_len, int nh,
                                 rpp_dtype dtype, void* out, int32_t* err, cudaStream_t stream);
 // Swin MLP fused on the tensor cores (C = 96, F = 384): out = resid + FC2(GELU(FC1(h) + b1)) + b2;

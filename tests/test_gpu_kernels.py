@@ -160,6 +160,17 @@ def test_attention_bert_large_lengths():
     _attention_case("bf16", lens, nh=16, seed=2, max_len=384)
 
 
+def test_attention_many_sequences_and_long_tile_counts():
+    """Batches the persistent longest-first kernel takes (up to 4096 sequences, up to 64
+    key tiles) and beyond them (4100 sequences: the one-CTA-per-query-tile kernel), each
+    against the oracle; plus one sequence spanning many key tiles (lazy rescaling over
+    nine tiles)."""
+    rng = np.random.default_rng(21)
+    _attention_case("fp16", rng.integers(0, 4, 4096), nh=1, seed=22, max_len=3)
+    _attention_case("bf16", rng.integers(0, 4, 4100), nh=1, seed=23, max_len=3)
+    _attention_case("bf16", [1100, 5, 300], nh=2, seed=24, max_len=1100)
+
+
 def test_attention_empty_and_zero_length_sequences():
     _attention_case("fp16", [0, 5, 0, 0, 70], nh=2, seed=3)
     _attention_case("fp16", [0, 0], nh=2, seed=4, max_len=8)
