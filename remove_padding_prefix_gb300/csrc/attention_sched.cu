@@ -49,7 +49,7 @@ constexpr uint32_t kTile = kT * kDh * 2;       // one 128 x 64 tile of Q, K or V
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0, kColP = 128, kColO = 192;
 constexpr int kMaxCls = 64;                    // tiles per sequence: max_len <= 8192
-constexpr int kMaxB = 4096;                    // sequences per batch
+constexpr int kMaxB = 2048;                    // sequences per batch (two CTAs per SM still fit)
 
 // shared-memory layout (bytes from the 1024-aligned base)
 constexpr uint32_t kOffQ = 0;                  // [2] tiles
@@ -58,9 +58,10 @@ constexpr uint32_t kOffV = 4 * kTile;          // [2]
 constexpr uint32_t kOffBar = 6 * kTile;        // 16 mbarriers
 constexpr uint32_t kOffMisc = kOffBar + 16 * 8;   // tmem slot, abort flag, counts
 constexpr uint32_t kOffCls = kOffMisc + 64;    // 4 int arrays of kMaxCls + 2
-constexpr uint32_t kOffPerm = kOffCls + 4 * (kMaxCls + 2) * 4;   // int16 [B]
+constexpr uint32_t kOffPerm = kOffCls + 4 * (kMaxCls + 2) * 4;   // int16 [B], then cu_seqlens int32 [B + 1]
 
-size_t smem_bytes(int B) { return 1024 + kOffPerm + ((static_cast<size_t>(B) * 2 + 15) & ~static_cast<size_t>(15)); }
+__host__ __device__ constexpr uint32_t perm_bytes(int B) { return (static_cast<uint32_t>(B) * 2u + 15u) & ~15u; }
+size_t smem_bytes(int B) { return 1024 + kOffPerm + perm_bytes(B) + ((static_cast<size_t>(B + 1) * 4 + 15) & ~15ull); }
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
@@ -81,6 +82,39 @@ __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+template <typename T>
+__device__ __forceinline__ float2 unpack2(uint32_t v);
+template <>
+__device__ __forceinline__ float2 unpack2<__half>(uint32_t v) {
+  return __half22float2(*reinterpret_cast<__half2*>(&v));
+}
+template <>
+__device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t v) {
+  return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&v));
+}
+
+// ---- packed fp32 pairs (f32x2: two lanes of one 64-bit register, one instruction)
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  return static_cast<uint64_t>(__float_as_uint(lo)) | (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
+}
+__device__ __forceinline__ float f2_lo(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float f2_hi(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // D[tmem] (+)= A[tmem] * B[smem], kind::f16: A (M x K, one row per lane, two 16-bit
 // elements per 32-bit column) from tensor memory
 __device__ __forceinline__ void tc_mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
@@ -99,12 +133,13 @@ struct Sched {
   const int* item_off;   // [c]: first item of tile count c (c = n_cls .. 1), item_off[0] = total
   const int* seq_off;    // [c]: first position in perm of the sequences with c tiles
   const int16_t* perm;   // sequence indices, grouped
+  const int* cu;         // cu_seqlens, copied into shared memory
   int n_cls, nh;
 };
 struct Item {
   int b, h, q0, c0, len, ntiles;
 };
-__device__ __forceinline__ Item decode(const Sched& s, const int32_t* cu, int g) {
+__device__ __forceinline__ Item decode(const Sched& s, int g) {
   int c = s.n_cls;
   while (c > 1 && g >= s.item_off[c - 1]) --c;   // classes laid out n_cls, n_cls - 1, ...: item_off decreasing in c
   // g lies in class c: [item_off[c], item_off[c - 1])
@@ -116,8 +151,8 @@ __device__ __forceinline__ Item decode(const Sched& s, const int32_t* cu, int g)
   it.b = s.perm[s.seq_off[c] + sq];
   it.h = rem / c;
   it.q0 = (rem - it.h * c) * kT;
-  it.c0 = __ldg(cu + it.b);
-  it.len = __ldg(cu + it.b + 1) - it.c0;
+  it.c0 = s.cu[it.b];
+  it.len = s.cu[it.b + 1] - it.c0;
   it.ntiles = c;
   return it;
 }
@@ -149,6 +184,7 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
   int* item_off = seq_off + (kMaxCls + 2);
   int* cursor = item_off + (kMaxCls + 2);
   int16_t* perm = reinterpret_cast<int16_t*>(smem + kOffPerm);
+  int* s_cu = reinterpret_cast<int*>(smem + kOffPerm + perm_bytes(B));
 
   const int warp = warp_id();
   const int lane = lane_id();
@@ -165,9 +201,12 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
   __syncthreads();
   if (*s_status) return;
 
-  // ---- item list: tile counts per sequence (all threads), then a stable grouping (warp 0)
+  // ---- item list: tile counts per sequence (all threads), then a stable grouping (warp 0);
+  // cu_seqlens is kept in shared memory for the item decoding of every role
+  for (int b = threadIdx.x; b <= B; b += kThreads) s_cu[b] = __ldg(cu + b);
+  __syncthreads();
   for (int b = threadIdx.x; b < B; b += kThreads) {
-    const int c0 = __ldg(cu + b), c1 = __ldg(cu + b + 1), len = c1 - c0;
+    const int c0 = s_cu[b], c1 = s_cu[b + 1], len = c1 - c0;
     if (c0 < 0 || len < 0 || c1 > T_max || len > max_len) {
       atomicCAS(s_status, 0, len > max_len ? RPP_DERR_LENGTH : RPP_DERR_ROWS);
     } else {
@@ -195,7 +234,7 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
     for (int b0 = 0; b0 < B; b0 += 32) {
       const int b = b0 + lane;
       int c = -1;
-      if (b < B) c = (__ldg(cu + b + 1) - __ldg(cu + b) + kT - 1) / kT;
+      if (b < B) c = (s_cu[b + 1] - s_cu[b] + kT - 1) / kT;
       const unsigned peers = __match_any_sync(0xffffffffu, c);
       const int rank = __popc(peers & ((1u << lane) - 1u));
       if (c > 0) perm[cursor[c] + rank] = static_cast<int16_t>(b);
@@ -233,7 +272,7 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int H = nh * kDh;
-  const Sched sch{item_off, seq_off, perm, n_cls, nh};
+  const Sched sch{item_off, seq_off, perm, s_cu, n_cls, nh};
   uint8_t* sQ = smem + kOffQ;
   uint8_t* sK = smem + kOffK;
   uint8_t* sV = smem + kOffV;
@@ -244,7 +283,7 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
       uint32_t nq = 0, nk = 0, nv = 0;
       bool ok = true;
       for (int g = blockIdx.x; g < n_items && ok; g += gridDim.x) {
-        const Item it = decode(sch, cu, g);
+        const Item it = decode(sch, g);
         {
           const uint32_t qb = nq & 1u;
           if (!mbar_wait_bounded(&q_empty[qb], ((nq >> 1) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
@@ -304,7 +343,7 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
         return true;
       };
       for (int g = blockIdx.x; g < n_items && ok; g += gridDim.x) {
-        const Item it = decode(sch, cu, g);
+        const Item it = decode(sch, g);
         const uint32_t qb = nq & 1u;
         if (!mbar_wait_bounded(&q_full[qb], (nq >> 1) & 1u, abort_flag)) { ok = false; break; }
         const uint64_t qdesc = sw128_kmajor_desc(smem_u32(sQ + qb * kTile));
@@ -347,7 +386,7 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
     uint32_t ns = 0, npv = 0, nit = 0;
     bool ok = true;
     for (int g = blockIdx.x; g < n_items && ok; g += gridDim.x) {
-      const Item it = decode(sch, cu, g);
+      const Item it = decode(sch, g);
       const bool active = it.q0 + quad * 32 < it.len;   // warp-uniform: some row of this warp is a query
       float m = neg_inf(), l = 0.f;
       for (int j = 0; j < it.ntiles; ++j) {
@@ -356,82 +395,136 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
         int w = mbar_wait_bounded(s_full, ns & 1u, abort_flag) ? 1 : 0;
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
         tc_fence_after();
-        // pass 1: the row maximum over this tile's keys (keys past the sequence: -inf),
-        // two 32-key chunks per tensor-memory round trip
-        float mx = neg_inf();
         if (active) {
-          float pm[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
-#pragma unroll
-          for (int c2 = 0; c2 < 2; ++c2) {
-            if (64 * c2 < nvalid) {
-              uint32_t v[64];
-              tmem_ld_32x32b_x32(t_lane + kColS + 64 * c2, v);
-              if (64 * c2 + 32 < nvalid) tmem_ld_32x32b_x32(t_lane + kColS + 64 * c2 + 32, v + 32);
-              tmem_ld_wait();
-#pragma unroll
-              for (int e = 0; e < 64; ++e)
-                if (64 * c2 + e < nvalid) pm[e & 3] = fmaxf(pm[e & 3], __uint_as_float(v[e]));
-            }
-          }
-          mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])) * scale_log2;
-        }
-        // P_{j-1} and O: the previous P V must be done before P is rewritten or O rescaled
-        if (j > 0) {
-          w = mbar_wait_bounded(pv_done, (npv - 1) & 1u, abort_flag) ? 1 : 0;
-          if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-          tc_fence_after();
-        }
-        if (active) {
-          if (j == 0) {
-            m = mx;
-          } else {
-            const bool move = mx > m + 8.0f;
-            if (__any_sync(0xffffffffu, move)) {
-              const float alpha = move ? ex2_approx(m - mx) : 1.0f;
-#pragma unroll 1
-              for (int c = 0; c < 4; ++c) {
-                uint32_t ov[16];
-                tmem_ld_32x32b_x16(t_lane + kColO + 16 * c, ov);
-                tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                tmem_st_32x32b_x16(t_lane + kColO + 16 * c, ov);
-              }
-              if (move) {
-                l *= alpha;
-                m = mx;
-              }
-            }
-          }
-          // pass 2: P = 2^(s - m), 32 keys (16 columns of P) per chunk, packed in place over
-          // the chunk's first 16 registers (pair e is written after keys 2e, 2e + 1 are read)
-          float ps[4] = {0.f, 0.f, 0.f, 0.f};
+          // One pass over the tile's S, 32 keys at a time, the next chunk's load in
+          // flight while this one is processed.  The reference maximum m is the first
+          // chunk's maximum for the first tile of an item and moves lazily after that:
+          // only when a chunk's maximum exceeds it by more than 8, in which case O, the
+          // running sum and the P chunks already written for this tile are rescaled.
+          uint32_t va[32], vb[32];
+          tmem_ld_32x32b_x32(t_lane + kColS, va);
+          tmem_ld_wait_tied32(va);
+          bool pv_ready = j == 0;   // P and O are free once the previous P V has completed
+          uint64_t psum2[2] = {0ull, 0ull};   // four partial row sums, as packed pairs
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             if (c < nch) {
-              uint32_t v[32];
-              tmem_ld_32x32b_x32(t_lane + kColS + 32 * c, v);
-              tmem_ld_wait();
+              uint32_t* cur = (c & 1) ? vb : va;
+              uint32_t* nxt = (c & 1) ? va : vb;
+              if (c + 1 < nch) {
+                // nxt[0..15] fed the previous chunk's P store: it must have completed
+                if (c >= 1) tmem_st_wait_tied16(nxt);
+                tmem_ld_32x32b_x32(t_lane + kColS + 32 * (c + 1), nxt);
+              } else {
+                // every column of S is in registers: the next S may be computed
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_free);
+              }
+              if (32 * c + 32 > nvalid) {   // keys past the sequence: -inf
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                  if (32 * c + e >= nvalid) cur[e] = 0xff800000u;
+              }
+              float pm[4] = {__uint_as_float(cur[0]), __uint_as_float(cur[1]), __uint_as_float(cur[2]),
+                             __uint_as_float(cur[3])};
+#pragma unroll
+              for (int e = 4; e < 32; ++e) pm[e & 3] = fmaxf(pm[e & 3], __uint_as_float(cur[e]));
+              const float cm = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])) * scale_log2;
+              if (j == 0 && c == 0) {
+                m = cm;
+              } else {
+                const bool move = cm > m + 8.0f;
+                if (__any_sync(0xffffffffu, move)) {
+                  if (!pv_ready) {
+                    const int w2 = mbar_wait_bounded(pv_done, (npv - 1) & 1u, abort_flag) ? 1 : 0;
+                    if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
+                    tc_fence_after();
+                    pv_ready = true;
+                  }
+                  const float alpha = move ? ex2_approx(m - cm) : 1.0f;
+                  if (j > 0) {   // O holds the earlier tiles
+#pragma unroll 1
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                      uint32_t ov[16];
+                      tmem_ld_32x32b_x16(t_lane + kColO + 16 * q4, ov);
+                      tmem_ld_wait_tied16(ov);
+#pragma unroll
+                      for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                      tmem_st_32x32b_x16(t_lane + kColO + 16 * q4, ov);
+                      tmem_st_wait_tied16(ov);
+                    }
+                  }
+                  tmem_st_wait();   // the P chunks stored so far have landed before they are read back
+#pragma unroll 1
+                  for (int c2 = 0; c2 < c; ++c2) {   // this tile's P chunks written so far
+                    uint32_t pv[16];
+                    tmem_ld_32x32b_x16(t_lane + kColP + 16 * c2, pv);
+                    tmem_ld_wait_tied16(pv);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                      const float2 f = unpack2<T>(pv[e]);
+                      pv[e] = pack2<T>(f.x * alpha, f.y * alpha);
+                    }
+                    tmem_st_32x32b_x16(t_lane + kColP + 16 * c2, pv);
+                    tmem_st_wait_tied16(pv);
+                  }
+#pragma unroll
+                  for (int t = 0; t < 2; ++t)
+                    psum2[t] = f2_pack(f2_lo(psum2[t]) * alpha, f2_hi(psum2[t]) * alpha);
+                  if (move) {
+                    l *= alpha;
+                    m = cm;
+                  }
+                }
+              }
+              // P = 2^(s - m), packed in place over the chunk's first 16 registers (pair e
+              // is written after keys 2e and 2e + 1 are read); the scale-and-subtract and
+              // the fp32 row sum run on packed pairs.
+              const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
+              const uint64_t nm2 = f2_pack(-m, -m);
 #pragma unroll
               for (int e2 = 0; e2 < 16; ++e2) {
-                const int e = 32 * c + 2 * e2;
-                const float s0 = e < nvalid ? __uint_as_float(v[2 * e2]) : neg_inf();
-                const float s1 = e + 1 < nvalid ? __uint_as_float(v[2 * e2 + 1]) : neg_inf();
-                const float p0 = ex2_approx(fmaf(s0, scale_log2, -m));
-                const float p1 = ex2_approx(fmaf(s1, scale_log2, -m));
-                ps[e2 & 3] += p0 + p1;
-                v[e2] = pack2<T>(p0, p1);
+                const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(cur[2 * e2]), __uint_as_float(cur[2 * e2 + 1])),
+                                           sc2, nm2);
+                const float p0 = ex2_approx(f2_lo(x2));
+                const float p1 = ex2_approx(f2_hi(x2));
+                psum2[e2 & 1] = f2_add(psum2[e2 & 1], f2_pack(p0, p1));
+                cur[e2] = pack2<T>(p0, p1);
               }
-              tmem_st_32x32b_x16(t_lane + kColP + 16 * c, v);
+              if (!pv_ready) {
+                const int w2 = mbar_wait_bounded(pv_done, (npv - 1) & 1u, abort_flag) ? 1 : 0;
+                if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
+                tc_fence_after();
+                pv_ready = true;
+              }
+              tmem_st_32x32b_x16(t_lane + kColP + 16 * c, cur);
+              if (c + 1 < nch) tmem_ld_wait_tied32(nxt);
             }
           }
-          l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-          tmem_st_wait();
+          if (!ok) {   // nothing of this thread may still be reading or writing tensor memory
+            tmem_ld_wait();
+            tmem_st_wait();
+            break;
+          }
+          l += (f2_lo(psum2[0]) + f2_hi(psum2[0])) + (f2_lo(psum2[1]) + f2_hi(psum2[1]));
+          // the last P stores read their source registers until they complete
+          tmem_st_wait_tied16(va);
+          tmem_st_wait_tied16(vb);
+        } else {
+          // no query row in this warp: nothing to read or write.  It still waits for the
+          // previous P V before its p_full arrival below, as the active warps do before
+          // their P stores: p_full counts one arrival per warp, and a warp that arrived
+          // for the next tile before an active warp arrived for this one would complete
+          // this tile's phase without that warp's P.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(s_free);
+          if (j > 0) {
+            w = mbar_wait_bounded(pv_done, (npv - 1) & 1u, abort_flag) ? 1 : 0;
+            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+          }
         }
-        // S has been read: the next S may be computed
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s_free);
         ++ns;
         // the last 16-key step of a partial tile: zero the V rows past the sequence
         // (P is 0 there, but 0 * NaN would not be)
@@ -462,7 +555,8 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
         uint32_t ov[64];
         tmem_ld_32x32b_x32(t_lane + kColO, ov);
         tmem_ld_32x32b_x32(t_lane + kColO + 32, ov + 32);
-        tmem_ld_wait();
+        tmem_ld_wait_tied32(ov);
+        tmem_ld_wait_tied32(ov + 32);
         if (it.q0 + r < it.len) {
           const float inv = 1.0f / l;
           uint4* orow = reinterpret_cast<uint4*>(out + static_cast<long long>(it.c0 + it.q0 + r) * H + it.h * kDh);

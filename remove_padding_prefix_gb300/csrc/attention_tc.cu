@@ -293,6 +293,7 @@ __global__ void __launch_bounds__(kAttnThreads, 2) attention_tc_kernel(const __g
 #pragma unroll
             for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
             tmem_st_32x32b_x16(t_lane + kKT + hf * 32 + c * 16, ov);
+            tmem_st_wait_tied16(ov);   // the store reads ov until it completes
           }
           tmem_st_wait();
           if (move) {
