@@ -17,17 +17,22 @@
 //    softmax numerators, columns [128, 192): 128 keys, two per 32-bit column) and O
 //    (columns [192, 256)).  O += P V reads P straight from tensor memory (the A operand
 //    of tcgen05.mma may live there), so P never goes through shared memory.
-//  * Runs the softmax with one thread per query row (four warps): the thread loads its
-//    row of S (tcgen05.ld), masks keys past the sequence, takes the row maximum,
-//    writes 2^(s - m) rounded to the input type into P and keeps the fp32 row sum.
-//    The reference maximum m moves only when a tile's maximum exceeds it by more than
-//    8 (log2 units), so P stays below 2^8; O and the sum are then rescaled in tensor
-//    memory.  Tensor-memory loads and stores are warp-collective, so that decision is
-//    taken per warp (scale 1 for rows that keep their maximum).
-//  * Overlaps: S_{j+1} is issued as soon as the softmax has read S_j, before P_j V_j;
-//    K and V tiles are double-buffered and the next item's Q tile loads while the
-//    current item finishes.  Partial tiles shrink the MMAs to whole 16-key steps; warps
-//    whose 32 query rows all lie past the sequence skip the softmax arithmetic.
+//  * Runs the softmax on eight warps, two per tensor-memory lane quadrant: each warp
+//    owns 32 query rows and half of a tile's 128 keys.  A warp takes its half's row
+//    maximum (tcgen05.ld, keys past the sequence masked), the two warps of a quadrant
+//    exchange maxima through shared memory (bounded mbarrier wait), then each writes
+//    2^(s - m) rounded to the input type into its half of P and keeps its half of the
+//    fp32 row sum; the halves of the sum are added once per item.  The reference
+//    maximum m moves only when a tile's maximum exceeds it by more than 8 (log2 units),
+//    so P stays below 2^8; O and the sums are then rescaled in tensor memory.  Tensor-
+//    memory loads and stores are warp-collective, so that decision is taken per warp
+//    (scale 1 for rows that keep their maximum); both warps of a quadrant see the same
+//    rows and maxima and decide alike.
+//  * Overlaps: the MMA thread walks the CTA's tiles as one stream and issues S_{t+1}
+//    before P_t V_t, also across items; K and V tiles are double-buffered and the next
+//    item's Q tile loads while the current item finishes.  Partial tiles shrink the MMAs
+//    to whole 16-key steps; warps whose 32 query rows all lie past the sequence skip the
+//    softmax arithmetic.
 //
 // Keys past the sequence end get -inf before the maximum (P = 0 there); the V rows of
 // the last 16-key step that lie past the end are zeroed in shared memory, so nothing
@@ -44,7 +49,7 @@ namespace {
 
 constexpr int kT = 128;                        // queries per item, keys per tile
 constexpr int kDh = 64;                        // head size
-constexpr int kThreads = 192;                  // warp 0 TMA, warp 1 MMA, warps 2..5 softmax
+constexpr int kThreads = 320;                  // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
 constexpr uint32_t kTile = kT * kDh * 2;       // one 128 x 64 tile of Q, K or V (16 KB)
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0, kColP = 128, kColO = 192;
@@ -56,8 +61,9 @@ constexpr uint32_t kOffQ = 0;                  // [2] tiles
 constexpr uint32_t kOffK = 2 * kTile;          // [2]
 constexpr uint32_t kOffV = 4 * kTile;          // [2]
 constexpr uint32_t kOffBar = 6 * kTile;        // 16 mbarriers
-constexpr uint32_t kOffMisc = kOffBar + 16 * 8;   // tmem slot, abort flag, counts
-constexpr uint32_t kOffCls = kOffMisc + 64;    // 4 int arrays of kMaxCls + 2
+constexpr uint32_t kOffMisc = kOffBar + 16 * 8;   // tmem slot, abort flag, counts, more barriers
+constexpr uint32_t kOffX = kOffMisc + 128;      // pair exchange: float [2 parities][2 halves][128 rows]
+constexpr uint32_t kOffCls = kOffX + 2 * 2 * 128 * 4;   // 4 int arrays of kMaxCls + 2
 constexpr uint32_t kOffPerm = kOffCls + 4 * (kMaxCls + 2) * 4;   // int16 [B], then cu_seqlens int32 [B + 1]
 
 __host__ __device__ constexpr uint32_t perm_bytes(int B) { return (static_cast<uint32_t>(B) * 2u + 15u) & ~15u; }
@@ -82,17 +88,6 @@ __device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <typename T>
-__device__ __forceinline__ float2 unpack2(uint32_t v);
-template <>
-__device__ __forceinline__ float2 unpack2<__half>(uint32_t v) {
-  return __half22float2(*reinterpret_cast<__half2*>(&v));
-}
-template <>
-__device__ __forceinline__ float2 unpack2<__nv_bfloat16>(uint32_t v) {
-  return __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&v));
-}
-
 // ---- packed fp32 pairs (f32x2: two lanes of one 64-bit register, one instruction)
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
   return static_cast<uint64_t>(__float_as_uint(lo)) | (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
@@ -107,11 +102,6 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
 __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
   uint64_t d;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 
@@ -171,11 +161,13 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
   uint64_t* v_full = bars + 8;    // [2]
   uint64_t* v_empty = bars + 10;  // [2]
   uint64_t* s_full = bars + 12;   // S computed (commit)
-  uint64_t* s_free = bars + 13;   // S read by the four softmax warps
-  uint64_t* p_full = bars + 14;   // P written by the four softmax warps
+  uint64_t* s_free = bars + 13;   // S read by the eight softmax warps
+  uint64_t* p_full = bars + 14;   // P written by the eight softmax warps
   uint64_t* pv_done = bars + 15;  // O += P V completed (commit)
-  uint64_t* o_free = reinterpret_cast<uint64_t*>(smem + kOffMisc + 32);   // O read out (four warps)
+  uint64_t* o_free = reinterpret_cast<uint64_t*>(smem + kOffMisc + 32);   // O read out (eight warps)
   uint64_t* drain = reinterpret_cast<uint64_t*>(smem + kOffMisc + 40);
+  uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + kOffMisc + 48);   // [4] pair exchanges, per quadrant
+  float* xval = reinterpret_cast<float*>(smem + kOffX);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int* s_status = reinterpret_cast<int*>(smem + kOffMisc + 8);   // 0 ok, else the device error to record / quit
@@ -253,10 +245,11 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
       mbar_init(&v_empty[i], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(s_free, 4);
-    mbar_init(p_full, 4);
+    mbar_init(s_free, 8);
+    mbar_init(p_full, 8);
     mbar_init(pv_done, 1);
-    mbar_init(o_free, 4);
+    mbar_init(o_free, 8);
+    for (int i = 0; i < 4; ++i) mbar_init(&xbar[i], 2);
     mbar_init(drain, 1);
     fence_mbarrier_init();
     tma_prefetch_desc(&tm);
@@ -342,13 +335,22 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
         ++npv;
         return true;
       };
-      for (int g = blockIdx.x; g < n_items && ok; g += gridDim.x) {
-        const Item it = decode(sch, g);
-        const uint32_t qb = nq & 1u;
-        if (!mbar_wait_bounded(&q_full[qb], (nq >> 1) & 1u, abort_flag)) { ok = false; break; }
-        const uint64_t qdesc = sw128_kmajor_desc(smem_u32(sQ + qb * kTile));
-        for (int j = 0; j < it.ntiles && ok; ++j) {
-          const int nvalid = min(kT, it.len - j * kT);
+      // One stream of tiles across this CTA's items: S_{t+1} is issued before P_t V_t, also
+      // when tile t + 1 belongs to the next item, so the next item's scores are ready by
+      // the time the softmax warps have finished the current item.
+      int gs = blockIdx.x, js = 0;                  // the S cursor: item index and tile
+      Item its = decode(sch, gs);                   // (blockIdx.x < n_items here)
+      bool has_s = true, pend = false;              // pend: a tile whose S is issued and P V is not
+      Item itp = its;
+      int jp = 0;
+      uint64_t qdesc = 0;
+      while (ok && (has_s || pend)) {
+        if (has_s) {
+          if (js == 0) {
+            if (!mbar_wait_bounded(&q_full[nq & 1u], (nq >> 1) & 1u, abort_flag)) { ok = false; break; }
+            qdesc = sw128_kmajor_desc(smem_u32(sQ + (nq & 1u) * kTile));
+          }
+          const int nvalid = min(kT, its.len - js * kT);
           const uint32_t idesc_s = idesc_f16(fmt, kT, (nvalid + 15) & ~15);
           const uint32_t kb = nk & 1u;
           if (!mbar_wait_bounded(&k_full[kb], (nk >> 1) & 1u, abort_flag)) { ok = false; break; }
@@ -361,14 +363,24 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
           tc_commit(&k_empty[kb]);
           ++nk;
           ++ns;
-          if (j == it.ntiles - 1) {
-            tc_commit(&q_empty[qb]);
+          if (js == its.ntiles - 1) {
+            tc_commit(&q_empty[nq & 1u]);
             ++nq;
           }
-          if (j > 0 && !issue_pv(it, j - 1)) { ok = false; break; }
         }
-        if (ok && !issue_pv(it, it.ntiles - 1)) ok = false;
-        ++nit;
+        if (pend && !issue_pv(itp, jp)) { ok = false; break; }
+        if (pend && jp == itp.ntiles - 1) ++nit;
+        pend = has_s;
+        if (has_s) {   // the tile just issued waits for its P V; advance the S cursor
+          itp = its;
+          jp = js;
+          if (++js == its.ntiles) {
+            js = 0;
+            gs += gridDim.x;
+            has_s = gs < n_items;
+            if (has_s) its = decode(sch, gs);
+          }
+        }
       }
       if (!ok) {
         set_device_error(err, RPP_DERR_TIMEOUT);
@@ -379,157 +391,143 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
       mbar_wait_bounded(drain, 0, nullptr);
     }
   } else {
-    // ------------------------------------------------------------ softmax, one thread per query row
-    const int quad = warp & 3;                       // tensor-memory lane quadrant of this warp
+    // ------------------------------------------------------------ softmax: two warps per row block
+    // Warps 2..9: lane quadrant q = warp & 3 holds query rows 32 q .. 32 q + 31 in tensor
+    // memory; half hf = 0 (warps 2..5) takes keys [0, 64) of each tile, hf = 1 (warps
+    // 6..9) keys [64, 128).  The two warps of a quadrant meet once per tile to agree on
+    // the row maximum, and once per item to add their row sums.
+    const int quad = warp & 3;
+    const int hf = (warp - 2) >> 2;
     const int r = quad * 32 + lane;                  // query row of the item
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(quad * 32) << 16);
-    uint32_t ns = 0, npv = 0, nit = 0;
+    const uint32_t col_s = kColS + 64 * hf, col_p = kColP + 32 * hf, col_o = kColO + 32 * hf;
+    uint32_t ns = 0, npv = 0, nit = 0, nx = 0;       // S tiles, P V products, items, pair exchanges
     bool ok = true;
+    // exchange with the other warp of this quadrant: value v of row r in, the partner's out
+    auto exchange = [&](float v, float& other) -> bool {
+      const uint32_t par = nx & 1u;
+      xval[(par * 2 + hf) * kT + r] = v;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&xbar[quad]);
+      const int w = mbar_wait_bounded(&xbar[quad], par, abort_flag) ? 1 : 0;
+      ++nx;
+      if (!__all_sync(0xffffffffu, w)) return false;
+      other = xval[(par * 2 + (hf ^ 1)) * kT + r];
+      return true;
+    };
     for (int g = blockIdx.x; g < n_items && ok; g += gridDim.x) {
       const Item it = decode(sch, g);
-      const bool active = it.q0 + quad * 32 < it.len;   // warp-uniform: some row of this warp is a query
-      float m = neg_inf(), l = 0.f;
+      const bool active = it.q0 + quad * 32 < it.len;   // the same for both warps of the quadrant
+      float m = neg_inf(), l = 0.f;                     // l: this warp's half of the row sum
       for (int j = 0; j < it.ntiles; ++j) {
         const int nvalid = min(kT, it.len - j * kT);
-        const int nch = (nvalid + 31) >> 5;          // 32-key chunks holding keys of the sequence
+        const int nv_h = min(64, max(0, nvalid - 64 * hf));   // keys of this half inside the sequence
         int w = mbar_wait_bounded(s_full, ns & 1u, abort_flag) ? 1 : 0;
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
         tc_fence_after();
+        float mx = neg_inf();
         if (active) {
-          // One pass over the tile's S, 32 keys at a time, the next chunk's load in
-          // flight while this one is processed.  The reference maximum m is the first
-          // chunk's maximum for the first tile of an item and moves lazily after that:
-          // only when a chunk's maximum exceeds it by more than 8, in which case O, the
-          // running sum and the P chunks already written for this tile are rescaled.
-          uint32_t va[32], vb[32];
-          tmem_ld_32x32b_x32(t_lane + kColS, va);
-          tmem_ld_wait_tied32(va);
-          bool pv_ready = j == 0;   // P and O are free once the previous P V has completed
-          uint64_t psum2[2] = {0ull, 0ull};   // four partial row sums, as packed pairs
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            if (c < nch) {
-              uint32_t* cur = (c & 1) ? vb : va;
-              uint32_t* nxt = (c & 1) ? va : vb;
-              if (c + 1 < nch) {
-                // nxt[0..15] fed the previous chunk's P store: it must have completed
-                if (c >= 1) tmem_st_wait_tied16(nxt);
-                tmem_ld_32x32b_x32(t_lane + kColS + 32 * (c + 1), nxt);
-              } else {
-                // every column of S is in registers: the next S may be computed
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(s_free);
-              }
-              if (32 * c + 32 > nvalid) {   // keys past the sequence: -inf
+          // pass 1: this half's row maximum, 32 keys per tensor-memory load (keys past the
+          // sequence: -inf)
+          float pm[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
+#pragma unroll 1
+          for (int c = 0; c < 2; ++c) {
+            if (32 * c < nv_h) {
+              uint32_t v[32];
+              tmem_ld_32x32b_x32(t_lane + col_s + 32 * c, v);
+              tmem_ld_wait_tied32(v);
+              if (32 * c + 32 > nv_h) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
-                  if (32 * c + e >= nvalid) cur[e] = 0xff800000u;
+                  if (32 * c + e >= nv_h) v[e] = 0xff800000u;
               }
-              float pm[4] = {__uint_as_float(cur[0]), __uint_as_float(cur[1]), __uint_as_float(cur[2]),
-                             __uint_as_float(cur[3])};
 #pragma unroll
-              for (int e = 4; e < 32; ++e) pm[e & 3] = fmaxf(pm[e & 3], __uint_as_float(cur[e]));
-              const float cm = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])) * scale_log2;
-              if (j == 0 && c == 0) {
-                m = cm;
-              } else {
-                const bool move = cm > m + 8.0f;
-                if (__any_sync(0xffffffffu, move)) {
-                  if (!pv_ready) {
-                    const int w2 = mbar_wait_bounded(pv_done, (npv - 1) & 1u, abort_flag) ? 1 : 0;
-                    if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
-                    tc_fence_after();
-                    pv_ready = true;
-                  }
-                  const float alpha = move ? ex2_approx(m - cm) : 1.0f;
-                  if (j > 0) {   // O holds the earlier tiles
+              for (int e = 0; e < 32; e += 8)
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+                  pm[t] = fmaxf(fmaxf(pm[t], __uint_as_float(v[e + t])), __uint_as_float(v[e + t + 4]));
+            }
+          }
+          mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
+          float other;
+          if (!exchange(mx, other)) { ok = false; break; }
+          mx = fmaxf(mx, other) * scale_log2;
+        }
+        // P and O: the previous P V must be done before P is rewritten or O rescaled (every
+        // warp waits, active or not: p_full counts one arrival per warp, and a warp that
+        // arrived for the next tile before another warp arrived for this one would
+        // complete this tile's phase early)
+        if (j > 0) {
+          w = mbar_wait_bounded(pv_done, (npv - 1) & 1u, abort_flag) ? 1 : 0;
+          if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+          tc_fence_after();
+        }
+        if (active) {
+          if (j == 0) {
+            m = mx;
+          } else {
+            // lazy rescaling, decided alike by both warps of the quadrant (same rows,
+            // same maxima); the tensor-memory accesses are warp-collective
+            const bool move = mx > m + 8.0f;
+            if (__any_sync(0xffffffffu, move)) {
+              const float alpha = move ? ex2_approx(m - mx) : 1.0f;
 #pragma unroll 1
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                      uint32_t ov[16];
-                      tmem_ld_32x32b_x16(t_lane + kColO + 16 * q4, ov);
-                      tmem_ld_wait_tied16(ov);
+              for (int q2 = 0; q2 < 2; ++q2) {   // this warp's 32 columns of O
+                uint32_t ov[16];
+                tmem_ld_32x32b_x16(t_lane + col_o + 16 * q2, ov);
+                tmem_ld_wait_tied16(ov);
 #pragma unroll
-                      for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                      tmem_st_32x32b_x16(t_lane + kColO + 16 * q4, ov);
-                      tmem_st_wait_tied16(ov);
-                    }
-                  }
-                  tmem_st_wait();   // the P chunks stored so far have landed before they are read back
-#pragma unroll 1
-                  for (int c2 = 0; c2 < c; ++c2) {   // this tile's P chunks written so far
-                    uint32_t pv[16];
-                    tmem_ld_32x32b_x16(t_lane + kColP + 16 * c2, pv);
-                    tmem_ld_wait_tied16(pv);
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                      const float2 f = unpack2<T>(pv[e]);
-                      pv[e] = pack2<T>(f.x * alpha, f.y * alpha);
-                    }
-                    tmem_st_32x32b_x16(t_lane + kColP + 16 * c2, pv);
-                    tmem_st_wait_tied16(pv);
-                  }
-#pragma unroll
-                  for (int t = 0; t < 2; ++t)
-                    psum2[t] = f2_pack(f2_lo(psum2[t]) * alpha, f2_hi(psum2[t]) * alpha);
-                  if (move) {
-                    l *= alpha;
-                    m = cm;
-                  }
-                }
+                for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                tmem_st_32x32b_x16(t_lane + col_o + 16 * q2, ov);
+                tmem_st_wait_tied16(ov);
               }
-              // P = 2^(s - m), packed in place over the chunk's first 16 registers (pair e
-              // is written after keys 2e and 2e + 1 are read); the scale-and-subtract and
-              // the fp32 row sum run on packed pairs.
-              const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
-              const uint64_t nm2 = f2_pack(-m, -m);
+              if (move) {
+                l *= alpha;
+                m = mx;
+              }
+            }
+          }
+          // pass 2: P = 2^(s - m) for this half's keys, 32 per chunk, packed in place
+          // (pair e written after keys 2e, 2e + 1 are read); packed fp32 pairs for the
+          // scale and the sum; keys past the sequence give 0
+          const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
+          const uint64_t nm2 = f2_pack(-m, -m);
+          uint64_t psum2[2] = {0ull, 0ull};
+#pragma unroll 1
+          for (int c = 0; c < 2; ++c) {
+            if (32 * c < nv_h) {
+              uint32_t v[32];
+              tmem_ld_32x32b_x32(t_lane + col_s + 32 * c, v);
+              tmem_ld_wait_tied32(v);
+              if (32 * c + 32 > nv_h) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                  if (32 * c + e >= nv_h) v[e] = 0xff800000u;
+              }
 #pragma unroll
               for (int e2 = 0; e2 < 16; ++e2) {
-                const uint64_t x2 = f2_fma(f2_pack(__uint_as_float(cur[2 * e2]), __uint_as_float(cur[2 * e2 + 1])),
-                                           sc2, nm2);
+                const uint64_t x2 =
+                    f2_fma(f2_pack(__uint_as_float(v[2 * e2]), __uint_as_float(v[2 * e2 + 1])), sc2, nm2);
                 const float p0 = ex2_approx(f2_lo(x2));
                 const float p1 = ex2_approx(f2_hi(x2));
                 psum2[e2 & 1] = f2_add(psum2[e2 & 1], f2_pack(p0, p1));
-                cur[e2] = pack2<T>(p0, p1);
+                v[e2] = pack2<T>(p0, p1);
               }
-              if (!pv_ready) {
-                const int w2 = mbar_wait_bounded(pv_done, (npv - 1) & 1u, abort_flag) ? 1 : 0;
-                if (!__all_sync(0xffffffffu, w2)) { ok = false; break; }
-                tc_fence_after();
-                pv_ready = true;
-              }
-              tmem_st_32x32b_x16(t_lane + kColP + 16 * c, cur);
-              if (c + 1 < nch) tmem_ld_wait_tied32(nxt);
+              tmem_st_32x32b_x16(t_lane + col_p + 16 * c, v);
+              tmem_st_wait_tied16(v);
             }
           }
-          if (!ok) {   // nothing of this thread may still be reading or writing tensor memory
-            tmem_ld_wait();
-            tmem_st_wait();
-            break;
-          }
           l += (f2_lo(psum2[0]) + f2_hi(psum2[0])) + (f2_lo(psum2[1]) + f2_hi(psum2[1]));
-          // the last P stores read their source registers until they complete
-          tmem_st_wait_tied16(va);
-          tmem_st_wait_tied16(vb);
-        } else {
-          // no query row in this warp: nothing to read or write.  It still waits for the
-          // previous P V before its p_full arrival below, as the active warps do before
-          // their P stores: p_full counts one arrival per warp, and a warp that arrived
-          // for the next tile before an active warp arrived for this one would complete
-          // this tile's phase without that warp's P.
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(s_free);
-          if (j > 0) {
-            w = mbar_wait_bounded(pv_done, (npv - 1) & 1u, abort_flag) ? 1 : 0;
-            if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
-          }
         }
+        // S has been read by this warp (both passes)
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_free);
         ++ns;
         // the last 16-key step of a partial tile: zero the V rows past the sequence
-        // (P is 0 there, but 0 * NaN would not be)
+        // (P is 0 there, but 0 * NaN would not be); one warp of each quadrant does it
         const int kpad = ((nvalid + 15) & ~15);
-        if (nvalid < kpad && r >= nvalid && r < kpad) {
+        if (hf == 0 && nvalid < kpad && r >= nvalid && r < kpad) {
           const uint32_t vb = npv & 1u;   // V tile j is the npv-th V load of this CTA
           if (mbar_wait_bounded(&v_full[vb], (npv >> 1) & 1u, abort_flag)) {
             uint8_t* vrow = sV + vb * kTile + r * 128;
@@ -547,21 +545,24 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
         ++npv;
       }
       if (!ok) break;
-      // the item's O: wait for its last P V, scale by 1 / sum, store the valid rows
+      // the item's O: wait for its last P V, add the two halves of the row sum, scale this
+      // warp's 32 columns by 1 / sum and store the valid rows
       int w = mbar_wait_bounded(pv_done, (npv - 1) & 1u, abort_flag) ? 1 : 0;
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc_fence_after();
       if (active) {
-        uint32_t ov[64];
-        tmem_ld_32x32b_x32(t_lane + kColO, ov);
-        tmem_ld_32x32b_x32(t_lane + kColO + 32, ov + 32);
+        float other;
+        if (!exchange(l, other)) { ok = false; break; }
+        l += other;
+        uint32_t ov[32];
+        tmem_ld_32x32b_x32(t_lane + col_o, ov);
         tmem_ld_wait_tied32(ov);
-        tmem_ld_wait_tied32(ov + 32);
         if (it.q0 + r < it.len) {
           const float inv = 1.0f / l;
-          uint4* orow = reinterpret_cast<uint4*>(out + static_cast<long long>(it.c0 + it.q0 + r) * H + it.h * kDh);
+          uint4* orow = reinterpret_cast<uint4*>(out + static_cast<long long>(it.c0 + it.q0 + r) * H + it.h * kDh +
+                                                 32 * hf);
 #pragma unroll
-          for (int u = 0; u < kDh / 8; ++u) {
+          for (int u = 0; u < 4; ++u) {
             const float* f = reinterpret_cast<const float*>(ov + 8 * u);
             orow[u] = make_uint4(pack2<T>(f[0] * inv, f[1] * inv), pack2<T>(f[2] * inv, f[3] * inv),
                                  pack2<T>(f[4] * inv, f[5] * inv), pack2<T>(f[6] * inv, f[7] * inv));
