@@ -58,6 +58,20 @@ def test_layer_small(idx, B, L, lens, hint):
     assert_close(got, ref, cfg.dtype, cfg.name)
 
 
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_layer_hidden_not_multiple_of_256(dtype):
+    """H = 384 (six heads of 64): the proj and FC2 GEMMs write split-K fp32 partial sums
+    and separate LayerNorm kernels add them, with the bias and the residual (the path of
+    hidden sizes the fused GEMM + LayerNorm kernel does not take)."""
+    from dataclasses import replace
+    cfg = replace(CONFIGS[2], H=384, nh=6, F=1536, dtype=dtype, layers=1)
+    wl = make_bert_workload(cfg, B=4, L=200, lengths=np.array([200, 3, 77, 130], np.int32), affine=True)
+    for hint in (False, True):
+        got, _ = _run_path(wl, dtype, hint=hint)
+        ref, _, _ = oracle.bert_forward(wl["x_padded"], wl["lengths"], wl["layers"], cfg.nh, cfg.eps)
+        assert_close(got, ref, dtype, f"H=384 {dtype} hint={hint}")
+
+
 @pytest.mark.parametrize("hint", [False, True])
 @pytest.mark.parametrize("idx,lens", [(1, [128, 1, 17, 64, 65, 100]), (2, [384, 129, 33])])
 def test_layer_poisoned_workspace(idx, lens, hint):
