@@ -226,7 +226,8 @@ class BertWorkload:
         """(flops, bytes) per launch: the algorithmic work of the method step(s) the kernel
         computes, over the packed batch (T valid tokens), with each operand read once and
         each result written once in the storage type e.  Intermediates of this design
-        (fp32 split-K slices, the fp32 residual copy) are not counted: they are traffic,
+        (the fp16 pre-LayerNorm sums, the fp16 residual copy, fp32 split-K slices) are not
+        counted: they are traffic,
         not work.  The dense padded work that removal avoids is not counted either."""
         c, T = self.cfg, self.T
         H, F, B, L = c.H, c.F, c.B, c.L

@@ -95,7 +95,6 @@ struct LayerLayout {
   size_t bqkv, bo, b1, b2;           // fp32
   size_t g1, be1, g2, be2;           // fp32
   size_t sqkv, so, s1, s2;           // fp32 per-channel weight scales (int8)
-  size_t id16, idbf;                 // 256 x 256 identities, fp16 and bf16 (the fused residual MMAs)
   size_t total;
 };
 
@@ -147,9 +146,6 @@ LayerLayout layer_layout(const rpp_encoder_cfg* c) {
     L.so = o;   o = align_up(o + H * 4);
     L.s1 = o;   o = align_up(o + F * 4);
     L.s2 = o;   o = align_up(o + H * 4);
-  } else if (c->dtype != RPP_F32) {
-    L.id16 = o; o = align_up(o + 256 * 256 * 2);
-    L.idbf = o; o = align_up(o + 256 * 256 * 2);
   }
   L.total = o;
   return L;
@@ -296,39 +292,44 @@ rpp_status encoder_layer_run(const rpp_encoder_cfg* c, const void* layer, const 
     }
     return a;
   };
-  if (!c->int8 && dt != RPP_F32 && !amax && gemm_ln_supported(H, H, dt) && gemm_ln_supported(H, F, dt)) {
-    // proj -> LN1 and FC2 -> LN2 each as one kernel: the bias, the residual and the
-    // LayerNorm run in the GEMM's epilogue and the pre-LayerNorm sum stays fp32 on chip
-    // ([SW] §3: bias split off the GEMM and fused into the op before LayerNorm, here the
-    // whole LayerNorm).  bf16 layers also keep LN1's output in fp16 as the FC2 residual:
-    // fp16's 11 significand bits keep that residual's rounding an eighth of a bf16 step.
+  if (!c->int8 && dt != RPP_F32 && !amax) {
+    // proj and FC2 add their bias and the residual in the GEMM epilogue and write the
+    // pre-LayerNorm sum once, in fp16 ([SW] §3: bias split off the GEMM and fused into
+    // the op before LayerNorm; [KS] Fig. 7: each kernel's precision chosen for its
+    // values).  fp16's 11 significand bits keep the sum's rounding an eighth of a bf16
+    // step, and the LayerNorm reads 2 bytes per element instead of fp32 split-K slices.
+    // bf16 layers also keep LN1's output in fp16, as the FC2 residual, for the same reason.
+    void* hsum = h;   // [T_max, H] fp16 inside the split-K slice region
     __half* x1h = dt == RPP_BF16 ? at<__half>(ws, W.x1f) : nullptr;
     RPP_LAUNCH("gemm_qkv", s, linear(dt, x, at<void>(layer, P.wqkv), bqkv, nullptr, qkv, T_max, rows, 3 * H, H,
                                      RPP_EPI_BIAS, err, s, RPP_I8, RPP_I8, hint));
     RPP_LAUNCH("attention", s, launch_attention_varlen(qkv, cu, B, T_max, max_len, nh, d, dt, attn, err, s));
-    GemmLnArgs l1{};
-    l1.a = attn; l1.w_t = at<void>(layer, P.wo); l1.bias = bo; l1.gamma = g1; l1.beta = be1; l1.eps = c->eps;
-    l1.residual = x; l1.res_f16 = 0; l1.out = x1; l1.out_f16 = x1h;
-    l1.ident = at<void>(layer, dt == RPP_BF16 ? P.idbf : P.id16);
-    l1.M_max = T_max; l1.rows = rows; l1.K = H; l1.H = H; l1.dtype = dt; l1.rows_hint = hint; l1.err = err;
-    RPP_LAUNCH("gemm_proj_ln1", s, launch_gemm_ln(l1, s));
+    RPP_LAUNCH("gemm_proj", s, linear(dt, attn, at<void>(layer, P.wo), bo, x, hsum, T_max, rows, H, H,
+                                      RPP_EPI_BIAS_RESIDUAL, err, s, RPP_F16, dt, hint));
+    LnArgs l1 = ln_args(g1, be1);
+    l1.x = hsum;
+    l1.in_dtype = RPP_F16;
+    l1.y = x1;
+    l1.y16 = x1h;
+    RPP_LAUNCH("layernorm1", s, launch_layernorm(l1, s));
     RPP_LAUNCH("gemm_fc1", s, linear(dt, x1, at<void>(layer, P.w1), b1, nullptr, g, T_max, rows, F, H,
                                      RPP_EPI_BIAS_GELU, err, s, RPP_I8, RPP_I8, hint));
-    GemmLnArgs l2 = l1;
-    l2.a = g; l2.w_t = at<void>(layer, P.w2); l2.bias = b2; l2.gamma = g2; l2.beta = be2;
-    l2.residual = x1h ? static_cast<const void*>(x1h) : x1; l2.res_f16 = x1h ? 1 : 0;
-    l2.ident = at<void>(layer, (x1h || dt == RPP_F16) ? P.id16 : P.idbf);
-    l2.out = y; l2.out_f16 = nullptr; l2.K = F;
-    RPP_LAUNCH("gemm_fc2_ln2", s, launch_gemm_ln(l2, s));
-    if (pad.y)   // the last layer: scatter into the padded output, pad slots zero
-      RPP_LAUNCH("rebuild_padding", s, launch_rebuild_padding(y, cu, B, pad.L, H * esize(dt), pad.y, err, s));
+    RPP_LAUNCH("gemm_fc2", s, linear(dt, g, at<void>(layer, P.w2), b2, x1h ? static_cast<const void*>(x1h) : x1, hsum,
+                                     T_max, rows, H, F, RPP_EPI_BIAS_RESIDUAL, err, s, RPP_F16,
+                                     x1h ? RPP_F16 : dt, hint));
+    LnArgs l2 = ln_args(g2, be2);
+    l2.x = hsum;
+    l2.in_dtype = RPP_F16;
+    l2.y = y;
+    RPP_LAUNCH(pad.y ? "layernorm2_rebuild" : "layernorm2", s, launch_layernorm(final_ln(l2), s));
     return RPP_OK;
   }
   if (!c->int8) {
-    // proj / FC2 write raw fp32 accumulators (split-K slices); the LayerNorm after each
-    // adds the slices, the GEMM's bias and the residual while it reads the row
-    // ([SW] §3: bias split off the GEMM and fused into the next op).  The fp32 layer
-    // runs its GEMMs on CUDA cores, with bias and residual in the GEMM epilogue.
+    // Calibration passes of 16-bit layers: proj / FC2 write raw fp32 accumulators
+    // (split-K slices); the LayerNorm after each adds the slices, the GEMM's bias and the
+    // residual while it reads the row ([SW] §3: bias split off the GEMM and fused into
+    // the next op), and records the max-abs of its output.  The fp32 layer runs its
+    // GEMMs on CUDA cores, with bias and residual in the GEMM epilogue.
     const bool tc = dt != RPP_F32;
     float* x1f = fp32_residual(c) ? at<float>(ws, W.x1f) : nullptr;
     if (amax) RPP_LAUNCH("amax", s, launch_amax(x, T_max, rows, H, dt, amax + 0, err, s));
@@ -647,10 +648,6 @@ rpp_status rpp_prepare_layer(const rpp_encoder_cfg* cfg, const rpp_layer_src* sr
     RPP_TRY(launch_transpose_to_kmajor(src->Wo, H, H, e, at<void>(dst, P.wo), H, s));
     RPP_TRY(launch_transpose_to_kmajor(src->W1, H, F, e, at<void>(dst, P.w1), H, s));
     RPP_TRY(launch_transpose_to_kmajor(src->W2, F, H, e, at<void>(dst, P.w2), F, s));
-    if (dt != RPP_F32) {
-      RPP_TRY(launch_identity16(at<void>(dst, P.id16), 256, RPP_F16, s));
-      RPP_TRY(launch_identity16(at<void>(dst, P.idbf), 256, RPP_BF16, s));
-    }
   } else {
     // int8: the per-channel scales of Wq, Wk, Wv are the per-column scales of the
     // concatenated [H, 3H] matrix, so each part is quantised on its own

@@ -32,9 +32,10 @@
 // barrier.  Shared-memory operand traffic per MMA drops from (128 + BN) to
 // (128 + BN / 2) rows per CTA.
 //
-// Epilogues: bias | bias + GELU | bias + residual | raw fp32 accumulator (the encoder
-// layer's proj / FC2: bias and residual are added by the LayerNorm that reads the
-// rows next) and the int8 variants below.
+// Epilogues: bias | bias + GELU | bias + residual (any of fp32, fp16 or the input type
+// out; the encoder layer's proj / FC2 write their pre-LayerNorm sums in fp16) | raw fp32
+// accumulator (calibration passes: bias and residual are added by the LayerNorm that
+// reads the rows next) and the int8 variants below.
 //
 // The accumulator is double-buffered in tensor memory, so the epilogue of tile i
 // overlaps the MMAs of tile i+1.  Work units are assigned round-robin over a
@@ -874,6 +875,10 @@ cudaError_t dispatch_float(int bn, int epi, rpp_dtype out_dtype, rpp_dtype res_d
         return dispatch_bn<T, float, float, RPP_EPI_BIAS_RESIDUAL, 1, CL>(bn, ta, tb, p, gr, stream);
       if (out_dtype == RPP_F32)
         return dispatch_bn<T, float, T, RPP_EPI_BIAS_RESIDUAL, 1, CL>(bn, ta, tb, p, gr, stream);
+      if (out_dtype == RPP_F16 && res_dtype == RPP_F16)
+        return dispatch_bn<T, __half, __half, RPP_EPI_BIAS_RESIDUAL, 1, CL>(bn, ta, tb, p, gr, stream);
+      if (out_dtype == RPP_F16)
+        return dispatch_bn<T, __half, T, RPP_EPI_BIAS_RESIDUAL, 1, CL>(bn, ta, tb, p, gr, stream);
       return dispatch_bn<T, T, T, RPP_EPI_BIAS_RESIDUAL, 1, CL>(bn, ta, tb, p, gr, stream);
     case EPI_ACC: return dispatch_bn<T, float, T, EPI_ACC, 1, CL>(bn, ta, tb, p, gr, stream);
     default: return cudaErrorNotSupported;

@@ -58,6 +58,7 @@ struct LnArgs {
   void* y = nullptr;
   rpp_dtype out_dtype = RPP_F32;
   float* y32 = nullptr;
+  __half* y16 = nullptr;       // optional fp16 copy of y
   void* q_codes = nullptr;
   const float* q_scale = nullptr;
   float* amax = nullptr;
@@ -85,8 +86,6 @@ cudaError_t launch_quantize_weight(const void* w, int K, int N, rpp_dtype dtype,
 cudaError_t launch_transpose_to_kmajor(const void* w, int K, int N, int elem_bytes, void* dst, int dst_ld,
                                        cudaStream_t stream);
 cudaError_t launch_to_f32(const void* src, rpp_dtype dtype, long long n, float* dst, cudaStream_t stream);
-// n x n identity matrix of bf16 or fp16 elements
-cudaError_t launch_identity16(void* dst, int n, rpp_dtype dtype, cudaStream_t stream);
 
 struct TcGemmArgs {
   const void* a;           // [M_max, K] operand (fp16 / bf16, or bf16-held int8 codes)
@@ -118,30 +117,6 @@ void set_gemm_cluster_mode(int mode);
 // waits give up after limit_ns (it records RPP_DERR_TIMEOUT and exits cleanly)
 void set_gemm_stall_next(unsigned long long limit_ns);
 
-// GEMM + bias + residual + LayerNorm (the proj -> LN1 and FC2 -> LN2 steps of a 16-bit
-// layer): out = LN(a[M, K] @ w_t[H, K]^T + bias + residual) * gamma + beta, H = 256, 512, 768
-// or 1024; a cluster of H / 256 CTAs per 128-row block exchanges the row statistics
-struct GemmLnArgs {
-  const void* a;            // [M_max, K] of dtype
-  const void* w_t;          // [H, K] of dtype
-  const float* bias;        // [H]
-  const float* gamma;       // [H]
-  const float* beta;        // [H]
-  float eps;
-  const void* residual;     // [M_max, H]: dtype, or fp16 when res_f16
-  int res_f16;
-  const void* ident;        // 256 x 256 identity of the residual's type (adds the residual in the MMAs)
-  void* out;                // [M_max, H] of dtype
-  __half* out_f16;          // optional fp16 copy of out (the next residual of a bf16 layer)
-  int M_max;
-  const int32_t* rows;
-  int K, H;
-  rpp_dtype dtype;          // RPP_F16 or RPP_BF16
-  int rows_hint;
-  int32_t* err;
-};
-bool gemm_ln_supported(int H, int K, rpp_dtype dtype);
-cudaError_t launch_gemm_ln(const GemmLnArgs& g, cudaStream_t stream);
 
 cudaError_t launch_gemm_f32(const float* a, const float* w_t, const float* bias, const float* residual, float* out,
                             int M_max, const int32_t* rows, int N, int K, int epi, int32_t* err, cudaStream_t stream);

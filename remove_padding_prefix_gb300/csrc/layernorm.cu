@@ -56,45 +56,54 @@ __device__ __forceinline__ void store_vec(TOut* p, const float* o) {
 // memory, loaded once per CTA.  In padded-output mode the grid walks the padded
 // [B, L] slots: a valid slot normalises its packed row and writes it in place, a pad
 // slot is written as zeros (the padding rebuild of the last layer, fused).
+// Shared-memory position (in float4 units) of the 4 parameters starting at column 4 q.
+// Lane gl of a group reads, for its vector i and quarter j4, the float4 at
+// (i EPV/4 + j4) G + gl: the lanes of a group read consecutive float4s, so one
+// 16-byte shared load per quarter is free of bank conflicts.
+template <int G, int EPV>
+__device__ __forceinline__ int param_slot(int q) {
+  constexpr int E4 = EPV / 4;
+  const int vec = q / E4;   // = i G + gl
+  return ((vec / G) * E4 + q % E4) * G + vec % G;
+}
+
 template <typename T, typename TOut, int G, int VPL, int NS>
 __global__ void __launch_bounds__(128) layernorm_kernel(LnArgs a) {
+  const int H = a.H;
+  constexpr int EPV = Vec<T>::N;
+  // gamma, beta and the bias are layer weights, never written by the launch just
+  // before this one: their reads are issued before the grid-dependency wait, so they
+  // overlap the tail of the preceding kernel.  H = G VPL EPV exactly (the host
+  // dispatch), so each thread stages kPre float4 quarters of each vector.
+  constexpr int kQ = G * VPL * EPV / 4;
+  constexpr int kPre = (kQ + 127) / 128;
+  float4 pg[kPre], pb[kPre], pc[kPre];
+#pragma unroll
+  for (int k = 0; k < kPre; ++k) {
+    const int q = threadIdx.x + k * 128;
+    if (q < kQ) {
+      pg[k] = __ldg(reinterpret_cast<const float4*>(a.gamma) + q);
+      pb[k] = __ldg(reinterpret_cast<const float4*>(a.beta) + q);
+      pc[k] = a.add_bias ? __ldg(reinterpret_cast<const float4*>(a.add_bias) + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
   pdl_wait();
   pdl_trigger();
-  const int H = a.H;
-  // The prologue's global reads (error word, device row count, gamma / beta / bias)
-  // are independent: all are issued before any is used, one round trip in all.
-  // values of each parameter vector a thread stages: this instantiation's row width
-  // (G lanes x VPL vectors x EPV elements) over the 128 threads
-  constexpr int kPre = (G * VPL * Vec<T>::N + 127) / 128;
-  float pg[kPre], pb[kPre], pc[kPre];
-#pragma unroll
-  for (int k = 0; k < kPre; ++k) {
-    const int i = threadIdx.x + k * 128;
-    if (i < H) {
-      pg[k] = __ldg(a.gamma + i);
-      pb[k] = __ldg(a.beta + i);
-      pc[k] = a.add_bias ? __ldg(a.add_bias + i) : 0.f;
-    }
-  }
   const bool err_set = device_error_set(a.err);
   int M = a.rows ? *a.rows : a.M_max;
-  extern __shared__ float ln_smem[];
-  float* s_gamma = ln_smem;
-  float* s_beta = ln_smem + H;
-  float* s_bias = ln_smem + 2 * H;
+  extern __shared__ float4 ln_smem4[];
+  float4* s_gamma = ln_smem4;
+  float4* s_beta = ln_smem4 + kQ;
+  float4* s_bias = ln_smem4 + 2 * kQ;
 #pragma unroll
   for (int k = 0; k < kPre; ++k) {
-    const int i = threadIdx.x + k * 128;
-    if (i < H) {
-      s_gamma[i] = pg[k];
-      s_beta[i] = pb[k];
-      s_bias[i] = pc[k];
+    const int q = threadIdx.x + k * 128;
+    if (q < kQ) {
+      const int slot = param_slot<G, EPV>(q);
+      s_gamma[slot] = pg[k];
+      s_beta[slot] = pb[k];
+      s_bias[slot] = pc[k];
     }
-  }
-  for (int i = threadIdx.x + kPre * 128; i < H; i += blockDim.x) {
-    s_gamma[i] = a.gamma[i];
-    s_beta[i] = a.beta[i];
-    s_bias[i] = a.add_bias ? a.add_bias[i] : 0.f;
   }
   if (err_set) return;
   if (M > a.M_max || M < 0) {
@@ -103,7 +112,6 @@ __global__ void __launch_bounds__(128) layernorm_kernel(LnArgs a) {
   }
   __syncthreads();
 
-  constexpr int EPV = Vec<T>::N;
   constexpr int GPW = 32 / G;   // groups (rows) per warp
   const T* x = static_cast<const T*>(a.x);
   TOut* y = static_cast<TOut*>(a.y);
@@ -219,9 +227,11 @@ __global__ void __launch_bounds__(128) layernorm_kernel(LnArgs a) {
     if (a.add_bias) {
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
-        const int col0 = (i * G + gl) * EPV;
 #pragma unroll
-        for (int j = 0; j < EPV; ++j) v[i][j] += s_bias[col0 + j];
+        for (int j4 = 0; j4 < EPV / 4; ++j4) {
+          const float4 b4 = s_bias[(i * (EPV / 4) + j4) * G + gl];
+          v[i][4 * j4 + 0] += b4.x; v[i][4 * j4 + 1] += b4.y; v[i][4 * j4 + 2] += b4.z; v[i][4 * j4 + 3] += b4.w;
+        }
       }
     }
     if constexpr (kRes) {
@@ -277,13 +287,21 @@ __global__ void __launch_bounds__(128) layernorm_kernel(LnArgs a) {
       float o[EPV];
       if (valid) {
 #pragma unroll
-        for (int j = 0; j < EPV; ++j) o[j] = (v[i][j] - mean) * rstd * s_gamma[col0 + j] + s_beta[col0 + j];
+        for (int j4 = 0; j4 < EPV / 4; ++j4) {
+          const float4 g4 = s_gamma[(i * (EPV / 4) + j4) * G + gl];
+          const float4 b4 = s_beta[(i * (EPV / 4) + j4) * G + gl];
+          o[4 * j4 + 0] = (v[i][4 * j4 + 0] - mean) * rstd * g4.x + b4.x;
+          o[4 * j4 + 1] = (v[i][4 * j4 + 1] - mean) * rstd * g4.y + b4.y;
+          o[4 * j4 + 2] = (v[i][4 * j4 + 2] - mean) * rstd * g4.z + b4.z;
+          o[4 * j4 + 3] = (v[i][4 * j4 + 3] - mean) * rstd * g4.w + b4.w;
+        }
       } else {
 #pragma unroll
         for (int j = 0; j < EPV; ++j) o[j] = 0.f;   // pad slot of the padded output
       }
       store_vec<TOut, EPV>(yr + col0, o);
       if (!valid) continue;
+      if (a.y16) store_vec<__half, EPV>(a.y16 + dst * H + col0, o);   // fp16 copy (the next residual)
       if (a.y32) {   // fp32 copy of the normalised row (the next residual add reads it)
         float* yf = a.y32 + dst * H + col0;
 #pragma unroll
@@ -445,6 +463,7 @@ cudaError_t launch_layernorm(const LnArgs& args, cudaStream_t stream) {
       default: return cudaErrorNotSupported;
     }
   }
+  if (a.in_dtype == RPP_F16 && a.out_dtype == RPP_BF16) return ln_dispatch<__half, BF>(a, stream);
   if (a.in_dtype == RPP_F32 && a.out_dtype == RPP_F16) return ln_dispatch<float, __half>(a, stream);
   if (a.in_dtype == RPP_F32 && a.out_dtype == RPP_BF16) return ln_dispatch<float, BF>(a, stream);
   return cudaErrorNotSupported;

@@ -158,19 +158,6 @@ cudaError_t launch_quantize_codes_bf16(const void* x, const float* scale, void* 
   }
 }
 
-// n x n identity of 16-bit elements (one = 0x3F80 for bf16, 0x3C00 for fp16)
-__global__ void identity_kernel(uint16_t* __restrict__ dst, int n, uint16_t one) {
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i < static_cast<long long>(n) * n) dst[i] = (i / n == i % n) ? one : static_cast<uint16_t>(0);
-}
-
-cudaError_t launch_identity16(void* dst, int n, rpp_dtype dtype, cudaStream_t stream) {
-  const long long total = static_cast<long long>(n) * n;
-  identity_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, stream>>>(
-      static_cast<uint16_t*>(dst), n, dtype == RPP_BF16 ? static_cast<uint16_t>(0x3F80) : static_cast<uint16_t>(0x3C00));
-  return cudaGetLastError();
-}
-
 cudaError_t launch_i8_to_bf16(const int8_t* src, void* dst, long long n, cudaStream_t stream) {
   i8_to_bf16_kernel<<<grid_for(n, 256, 8), 256, 0, stream>>>(src, static_cast<__nv_bfloat16*>(dst), n);
   return cudaGetLastError();

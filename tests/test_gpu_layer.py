@@ -60,9 +60,9 @@ def test_layer_small(idx, B, L, lens, hint):
 
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 def test_layer_hidden_not_multiple_of_256(dtype):
-    """H = 384 (six heads of 64): the proj and FC2 GEMMs write split-K fp32 partial sums
-    and separate LayerNorm kernels add them, with the bias and the residual (the path of
-    hidden sizes the fused GEMM + LayerNorm kernel does not take)."""
+    """H = 384 (six heads of 64): a hidden size that is not a multiple of the widest GEMM
+    tile, so proj and FC2 (bias + residual epilogue, fp16 pre-LayerNorm sums) take
+    narrower column tiles than the BERT shapes."""
     from dataclasses import replace
     cfg = replace(CONFIGS[2], H=384, nh=6, F=1536, dtype=dtype, layers=1)
     wl = make_bert_workload(cfg, B=4, L=200, lengths=np.array([200, 3, 77, 130], np.int32), affine=True)
