@@ -227,8 +227,7 @@ class BertWorkload:
         computes, over the packed batch (T valid tokens), with each operand read once and
         each result written once in the storage type e.  Intermediates of this design
         (the fp16 pre-LayerNorm sums, the fp16 residual copy, fp32 split-K slices) are not
-        counted: they are traffic,
-        not work.  The dense padded work that removal avoids is not counted either."""
+        counted: they are traffic, not work.  The dense padded work that removal avoids is not counted either."""
         c, T = self.cfg, self.T
         H, F, B, L = c.H, c.F, c.B, c.L
         e = 4 if c.storage_dtype == "fp32" else 2
