@@ -385,6 +385,184 @@ __global__ void amax_kernel(const T* __restrict__ x, int M_max, const int32_t* r
   if (lane_id() == 0) atomic_max_nonneg(amax, m);
 }
 
+// ---------------------------------------------------------------- streaming 16-bit rows
+// LayerNorm of rows that arrive complete in a 16-bit type (the fp16 pre-LayerNorm sums of
+// a 16-bit layer): no slices, bias or residual to add.  One warp per row with H = 256 VPL
+// (lane l holds the 16-byte vectors l, l + 32, ...), the next row's vectors in flight
+// while this one is normalised, and the arithmetic on packed fp32 pairs (one f32x2
+// instruction per two elements).  Statistics as in the general kernel: fp32, two passes
+// over the registers, biased variance.  Padded-output mode as in the general kernel.
+constexpr int kLn16Threads = 256;
+
+template <typename TIn, typename TOut, int VPL>
+__global__ void __launch_bounds__(kLn16Threads) ln16_kernel(LnArgs a) {
+  constexpr int H = 256 * VPL;
+  constexpr int kQ = H / 4;   // float4 quarters of a parameter vector
+  constexpr int kPre = (kQ + kLn16Threads - 1) / kLn16Threads;
+  constexpr int kWarps = kLn16Threads / 32;
+  // gamma and beta are layer weights, not written by the preceding launch: read before
+  // the grid-dependency wait
+  float4 pg[kPre], pb[kPre];
+#pragma unroll
+  for (int k = 0; k < kPre; ++k) {
+    const int qd = threadIdx.x + k * kLn16Threads;
+    if (qd < kQ) {
+      pg[k] = __ldg(reinterpret_cast<const float4*>(a.gamma) + qd);
+      pb[k] = __ldg(reinterpret_cast<const float4*>(a.beta) + qd);
+    }
+  }
+  pdl_wait();
+  pdl_trigger();
+  const bool err_set = device_error_set(a.err);
+  const int M = a.rows ? *a.rows : a.M_max;
+  __shared__ float4 s_g[kQ], s_b[kQ];
+#pragma unroll
+  for (int k = 0; k < kPre; ++k) {
+    const int qd = threadIdx.x + k * kLn16Threads;
+    if (qd < kQ) {
+      const int slot = param_slot<32, 8>(qd);
+      s_g[slot] = pg[k];
+      s_b[slot] = pb[k];
+    }
+  }
+  if (err_set) return;
+  if (M > a.M_max || M < 0) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) set_device_error(a.err, RPP_DERR_ROWS);
+    return;
+  }
+  __syncthreads();
+
+  const TIn* x = static_cast<const TIn*>(a.x);
+  TOut* y = static_cast<TOut*>(a.y);
+  const int lane = lane_id();
+  const bool padded = a.pad_cu != nullptr;
+  // the host keeps pad_B * pad_L below 2^31
+  const unsigned n_iter = padded ? static_cast<unsigned>(a.pad_B) * static_cast<unsigned>(a.pad_L)
+                                 : static_cast<unsigned>(M);
+  const unsigned stride = gridDim.x * kWarps;
+  auto src_of = [&](unsigned itx) -> int {   // packed row normalised for loop position itx (-1: none)
+    if (itx >= n_iter) return -1;
+    if (!padded) return static_cast<int>(itx);
+    const unsigned b = itx / static_cast<unsigned>(a.pad_L);
+    const int p = static_cast<int>(itx - b * static_cast<unsigned>(a.pad_L));
+    const int c0 = a.pad_cu[b];
+    return p < a.pad_cu[b + 1] - c0 ? c0 + p : -1;
+  };
+  auto load_row = [&](int src, uint4* r) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + static_cast<size_t>(src >= 0 ? src : 0) * H);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) r[i] = src >= 0 ? xr[i * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
+  };
+  unsigned it = blockIdx.x * kWarps + warp_id();
+  int src = src_of(it);
+  uint4 nx[VPL];
+  load_row(src, nx);
+  for (; it < n_iter; it += stride) {
+    uint4 cur[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) cur[i] = nx[i];
+    const int src_next = src_of(it + stride);
+    load_row(src_next, nx);
+    TOut* yr = y + static_cast<size_t>(it) * H;
+    if (src < 0) {   // pad slot of the padded output
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) *reinterpret_cast<uint4*>(yr + (i * 32 + lane) * 8) = make_uint4(0u, 0u, 0u, 0u);
+      src = src_next;
+      continue;
+    }
+    uint64_t v[4 * VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      float f[8];
+      unpack16<TIn>(cur[i], f);
+#pragma unroll
+      for (int h = 0; h < 4; ++h) v[4 * i + h] = f2_pack(f[2 * h], f[2 * h + 1]);
+    }
+    uint64_t s2a = v[0], s2b = v[1];
+#pragma unroll
+    for (int k = 2; k < 4 * VPL; k += 2) {
+      s2a = f2_add(s2a, v[k]);
+      s2b = f2_add(s2b, v[k + 1]);
+    }
+    s2a = f2_add(s2a, s2b);
+    float sum = f2_lo(s2a) + f2_hi(s2a);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float mean = sum * (1.0f / H);
+    const uint64_t nm = f2_pack(-mean, -mean);
+    uint64_t q2a = 0ull, q2b = 0ull;
+#pragma unroll
+    for (int k = 0; k < 4 * VPL; k += 2) {
+      v[k] = f2_add(v[k], nm);
+      v[k + 1] = f2_add(v[k + 1], nm);
+      q2a = f2_fma(v[k], v[k], q2a);
+      q2b = f2_fma(v[k + 1], v[k + 1], q2b);
+    }
+    q2a = f2_add(q2a, q2b);
+    float ss = f2_lo(q2a) + f2_hi(q2a);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float rstd = rsqrtf(ss * (1.0f / H) + a.eps);
+    const uint64_t r2 = f2_pack(rstd, rstd);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      float o[8];
+#pragma unroll
+      for (int j4 = 0; j4 < 2; ++j4) {
+        const float4 g4 = s_g[(i * 2 + j4) * 32 + lane];
+        const float4 b4 = s_b[(i * 2 + j4) * 32 + lane];
+        const uint64_t o0 = f2_fma(v[4 * i + 2 * j4], f2_mul(f2_pack(g4.x, g4.y), r2), f2_pack(b4.x, b4.y));
+        const uint64_t o1 = f2_fma(v[4 * i + 2 * j4 + 1], f2_mul(f2_pack(g4.z, g4.w), r2), f2_pack(b4.z, b4.w));
+        o[4 * j4 + 0] = f2_lo(o0); o[4 * j4 + 1] = f2_hi(o0);
+        o[4 * j4 + 2] = f2_lo(o1); o[4 * j4 + 3] = f2_hi(o1);
+      }
+      const int col0 = (i * 32 + lane) * 8;
+      store_vec<TOut, 8>(yr + col0, o);
+      if (a.y16) store_vec<__half, 8>(a.y16 + static_cast<size_t>(it) * H + col0, o);
+    }
+    src = src_next;
+  }
+}
+
+template <typename TIn, typename TOut, int VPL>
+cudaError_t ln16_launch(const LnArgs& a, cudaStream_t stream) {
+  constexpr int kWarps = kLn16Threads / 32;
+  const long long n_iter = a.pad_cu ? static_cast<long long>(a.pad_B) * a.pad_L : a.M_max;
+  long long blocks = (n_iter + kWarps - 1) / kWarps;
+  static int per_sm = 0;   // one wave of resident blocks: the row loop is grid-strided
+  if (per_sm == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ln16_kernel<TIn, TOut, VPL>, kLn16Threads, 0) !=
+            cudaSuccess || n < 1)
+      n = 2;
+    per_sm = n;
+  }
+  const long long cap = static_cast<long long>(num_sms()) * per_sm;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return launch_pdl(ln16_kernel<TIn, TOut, VPL>, dim3(static_cast<unsigned>(blocks)), dim3(kLn16Threads), 0,
+                    stream, a);
+}
+
+template <typename TIn, typename TOut>
+cudaError_t ln16_dispatch(const LnArgs& a, cudaStream_t stream) {
+  switch (a.H / 256) {
+    case 1: return ln16_launch<TIn, TOut, 1>(a, stream);
+    case 2: return ln16_launch<TIn, TOut, 2>(a, stream);
+    case 3: return ln16_launch<TIn, TOut, 3>(a, stream);
+    case 4: return ln16_launch<TIn, TOut, 4>(a, stream);
+    case 6: return ln16_launch<TIn, TOut, 6>(a, stream);
+    default: return cudaErrorNotSupported;
+  }
+}
+
+bool ln16_applies(const LnArgs& a) {
+  const int v = a.H / 256;
+  return (a.in_dtype == RPP_F16 || a.in_dtype == RPP_BF16) && a.out_dtype != RPP_F32 && a.n_in == 1 &&
+         !a.residual && !a.add_bias && !a.q_codes && !a.amax && !a.y32 && a.H % 256 == 0 &&
+         (v == 1 || v == 2 || v == 3 || v == 4 || v == 6);
+}
+
 template <typename T, typename TOut, int G, int VPL, int NS>
 cudaError_t ln_launch(const LnArgs& a, cudaStream_t stream) {
   const int threads = 128;
@@ -455,6 +633,11 @@ cudaError_t launch_layernorm(const LnArgs& args, cudaStream_t stream) {
   if (a.pad_cu && (a.pad_B <= 0 || a.pad_L <= 0)) return cudaErrorInvalidValue;
   if (a.pad_cu && static_cast<long long>(a.pad_B) * a.pad_L > 0x7fffffffLL) return cudaErrorNotSupported;
   using BF = __nv_bfloat16;
+  if (ln16_applies(a)) {
+    if (a.in_dtype == RPP_F16 && a.out_dtype == RPP_F16) return ln16_dispatch<__half, __half>(a, stream);
+    if (a.in_dtype == RPP_F16 && a.out_dtype == RPP_BF16) return ln16_dispatch<__half, BF>(a, stream);
+    if (a.in_dtype == RPP_BF16 && a.out_dtype == RPP_BF16) return ln16_dispatch<BF, BF>(a, stream);
+  }
   if (a.in_dtype == a.out_dtype) {
     switch (a.in_dtype) {
       case RPP_F32: return ln_dispatch<float, float>(a, stream);

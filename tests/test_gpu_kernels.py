@@ -88,7 +88,8 @@ def test_f32_gemm(epi):
     _gemm_case("fp32", 150, 256, 1024, epi, seed=10 + epi)
 
 
-@pytest.mark.parametrize("dtype,H", [("fp32", 256), ("fp16", 768), ("bf16", 1024), ("fp16", 96), ("bf16", 96)])
+@pytest.mark.parametrize("dtype,H", [("fp32", 256), ("fp16", 768), ("bf16", 1024), ("fp16", 96), ("bf16", 96),
+                                     ("fp16", 256), ("bf16", 512), ("fp16", 1536)])
 def test_layernorm(dtype, H):
     rng = np.random.default_rng(H)
     M = 333
@@ -100,6 +101,26 @@ def test_layernorm(dtype, H):
     y = rpp.layernorm(up(x, dtype), torch.as_tensor(g, device=dev()), torch.as_tensor(b, device=dev()), eps, err=err)
     check_err(err)
     assert_close(down(y), oracle.layernorm(x, g, b, eps), dtype, f"layernorm {dtype} H={H}")
+
+
+@pytest.mark.parametrize("dtype,H", [("fp16", 1024), ("bf16", 768)])
+def test_layernorm_device_rows_in_place(dtype, H):
+    """Rows past the device row count stay untouched; y may alias x (each row is read
+    before it is written)."""
+    rng = np.random.default_rng(H + 7)
+    M_max, M = 700, 611
+    x = round_to_dtype(rng.standard_normal((M_max, H), dtype=np.float32) * 3 - 1, dtype)
+    g = (1 + 0.1 * rng.standard_normal(H)).astype(np.float32)
+    b = (0.1 * rng.standard_normal(H)).astype(np.float32)
+    err = rpp.new_error_word()
+    xd = up(x, dtype)
+    rows = torch.tensor([M], dtype=torch.int32, device=dev())
+    rpp.layernorm(xd, torch.as_tensor(g, device=dev()), torch.as_tensor(b, device=dev()), 1e-12, out=xd, rows=rows,
+                  err=err)
+    check_err(err)
+    got = down(xd)
+    assert_close(got[:M], oracle.layernorm(x[:M], g, b, 1e-12), dtype, f"in-place layernorm {dtype} H={H}")
+    assert np.array_equal(got[M:], x[M:])
 
 
 def _attention_case(dtype, lengths, nh, seed=0, max_len=None, poison=False, qk_scale=1.0):
