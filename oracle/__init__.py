@@ -33,7 +33,8 @@ from .swin import (shift, unshift, window_partition, window_reverse, window_coor
                    relative_position_bias, shift_attend_mask, window_attention,
                    swin_block, patch_merge)
 from .int8 import (quantize_weight_per_channel, quantize_activation, int8_gemm,
-                   int8_linear, bert_layer_int8, calibrate_int8, prepare_int8_layer)
+                   int8_linear, bert_layer_int8, calibrate_int8, prepare_int8_layer,
+                   attention_varlen_int8, calibrate_int8_qkv)
 
 __all__ = [
     "build_offsets", "remove_padding", "rebuild_padding",
@@ -43,4 +44,5 @@ __all__ = [
     "relative_position_bias", "shift_attend_mask", "window_attention", "swin_block", "patch_merge",
     "quantize_weight_per_channel", "quantize_activation", "int8_gemm", "int8_linear",
     "bert_layer_int8", "calibrate_int8", "prepare_int8_layer",
+    "attention_varlen_int8", "calibrate_int8_qkv",
 ]

@@ -297,3 +297,139 @@ def test_calibration_scales_match_library_route():
     pre_gelu = x1 @ t(layer["W1"]) + t(layer["b1"])
     assert abs(float(pre_ln[valid].abs().max()) / 127 - s[2]) > 1e-3 * s[2]
     assert abs(float(pre_gelu[valid].abs().max()) / 127 - s[3]) > 1e-3 * s[3]
+
+
+# ---------------------------------------------------------------- int8 attention
+
+def _brute_int8_attention(qc, kc, vc, s_q, s_k, s_v, cu, nh):
+    """The all-int8 attention restated with scalar Python loops (math.exp, Python's
+    round-half-to-even `round`), for tiny shapes."""
+    import math
+    T, Hd = qc.shape
+    d = Hd // nh
+    out = np.zeros((T, Hd))
+    for b in range(len(cu) - 1):
+        lo, hi = int(cu[b]), int(cu[b + 1])
+        for h in range(nh):
+            for i in range(lo, hi):
+                sc = []
+                for j in range(lo, hi):
+                    acc = 0
+                    for c in range(h * d, (h + 1) * d):
+                        acc += int(qc[i, c]) * int(kc[j, c])
+                    sc.append(acc * float(s_q) * float(s_k) / math.sqrt(d))
+                m = max(sc)
+                e = [math.exp(v - m) for v in sc]
+                tot = sum(e)
+                codes = [min(127, max(0, round(127 * v / tot))) for v in e]
+                for c in range(h * d, (h + 1) * d):
+                    acc = 0
+                    for jj, j in enumerate(range(lo, hi)):
+                        acc += codes[jj] * int(vc[j, c])
+                    out[i, c] = acc * float(s_v) / 127
+    return out
+
+
+def _int8_attention_case(seed, lengths, nh=2, d=4):
+    rng = np.random.default_rng(seed)
+    T = int(np.sum(lengths))
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    qc, kc, vc = (rng.integers(-127, 128, size=(T, nh * d)).astype(np.int8) for _ in range(3))
+    return qc, kc, vc, cu
+
+
+def test_int8_attention_matches_brute_force():
+    qc, kc, vc, cu = _int8_attention_case(3, [3, 5, 1, 4])
+    s_q, s_k, s_v = np.float32(0.011), np.float32(0.0043), np.float32(0.021)
+    got = oracle.attention_varlen_int8(qc, kc, vc, s_q, s_k, s_v, cu, 2)
+    ref = _brute_int8_attention(qc, kc, vc, s_q, s_k, s_v, cu, 2)
+    assert np.abs(got - ref).max() < 1e-12
+
+
+@pytest.mark.parametrize("n,code", [(1, 127), (2, 64), (3, 42), (4, 32), (5, 25), (7, 18)])
+def test_int8_attention_uniform_scores_closed_form(n, code):
+    """Q = 0: every score is 0, P = 1/n, its code is rne(127/n) (n = 2: 63.5 -> 64, the
+    even neighbour), and O = code * sum_j v_j * s_v / 127."""
+    rng = np.random.default_rng(n)
+    nh, d = 1, 8
+    qc = np.zeros((n, d), np.int8)
+    kc = rng.integers(-127, 128, size=(n, d)).astype(np.int8)
+    vc = rng.integers(-127, 128, size=(n, d)).astype(np.int8)
+    s_v = np.float32(0.5)
+    got = oracle.attention_varlen_int8(qc, kc, vc, 1.0, 1.0, s_v, np.array([0, n]), nh)
+    expect = code * vc.astype(np.int64).sum(axis=0) * 0.5 / 127
+    assert np.abs(got - np.tile(expect, (n, 1))).max() < 1e-12
+
+
+def test_int8_attention_close_to_float_attention():
+    """Against the float attention of the dequantised Q, K, V: P's codes are within half
+    a step (1/254) of P, so each output is within sum_j |v_j| / 254 of the float one
+    (and strictly nearer than the bound for most rows)."""
+    qc, kc, vc, cu = _int8_attention_case(11, [17, 40, 2, 64], nh=2, d=16)
+    s_q, s_k, s_v = np.float32(0.02), np.float32(0.03), np.float32(0.01)
+    got = oracle.attention_varlen_int8(qc, kc, vc, s_q, s_k, s_v, cu, 2)
+    ref = oracle.attention_varlen(qc * np.float64(s_q), kc * np.float64(s_k), vc * np.float64(s_v), cu, 2)
+    d = 16
+    for b in range(len(cu) - 1):
+        lo, hi = cu[b], cu[b + 1]
+        for h in range(2):
+            cs = slice(h * d, (h + 1) * d)
+            bound = np.abs(vc[lo:hi, cs].astype(np.float64) * s_v).sum(axis=0) / 254 + 1e-12
+            assert np.all(np.abs(got[lo:hi, cs] - ref[lo:hi, cs]) <= bound[None, :])
+    assert np.abs(got - ref).max() > 0   # the quantisation of P is visible
+
+
+def test_int8_attention_sequences_are_isolated():
+    qc, kc, vc, cu = _int8_attention_case(5, [6, 9, 3])
+    a = oracle.attention_varlen_int8(qc, kc, vc, 0.01, 0.02, 0.03, cu, 2)
+    kc2, vc2 = kc.copy(), vc.copy()
+    kc2[6:15] = -kc2[6:15]
+    vc2[6:15] = 7
+    b = oracle.attention_varlen_int8(qc, kc2, vc2, 0.01, 0.02, 0.03, cu, 2)
+    assert np.array_equal(a[:6], b[:6]) and np.array_equal(a[15:], b[15:])
+    assert not np.array_equal(a[6:15], b[6:15])
+
+
+def test_int8_attention_layer_on_grid():
+    """The all-int8 layer on the grid case with s_v = the grid of V (4 s0): a one-token
+    sequence has P = 1, code 127, attention output V exactly, so its rows equal the float
+    layer; a two-token sequence has P = 1/2, code 64, attention output
+    64 (v_1 + v_2) s_v / 127 in place of the mean."""
+    x, cu, layer, qlayer, nh = _grid_case()
+    s_v = 4 * _S[0]
+    scales7 = np.array(list(_S) + [2.0 ** -3, 2.0 ** -6, s_v], np.float32)
+    y7 = oracle.bert_layer_int8(x, cu, qlayer, scales7, nh, 0.0)
+    yf = oracle.bert_layer(x, cu, layer, nh, 0.0)
+    assert np.abs(y7[:3] - yf[:3]).max() < 1e-12
+    assert np.abs(y7[3:] - yf[3:]).max() > 1e-3
+    # the pairs' attention output, from the same pieces the layer uses
+    H = x.shape[1]
+    qkv = oracle.int8_linear(x, _S[0], qlayer["Wqkv_q"], qlayer["Wqkv_s"], qlayer["bqkv"])
+    vc = oracle.quantize_activation(qkv[:, 2 * H:], s_v).astype(np.int64)
+    att = oracle.attention_varlen_int8(oracle.quantize_activation(qkv[:, :H], 2.0 ** -3),
+                                       oracle.quantize_activation(qkv[:, H:2 * H], 2.0 ** -6),
+                                       vc.astype(np.int8), 2.0 ** -3, 2.0 ** -6, s_v, cu, nh)
+    for lo in (3, 5):
+        expect = 64 * (vc[lo] + vc[lo + 1]) * s_v / 127
+        assert np.abs(att[lo] - expect).max() < 1e-12 and np.abs(att[lo + 1] - expect).max() < 1e-12
+    # a wrong V scale breaks the one-token rows
+    bad = scales7.copy()
+    bad[6] = 2 * s_v
+    yb = oracle.bert_layer_int8(x, cu, qlayer, bad, nh, 0.0)
+    assert np.abs(yb[:3] - yf[:3]).max() > 1e-3
+
+
+def test_calibrate_int8_qkv_hand_checked():
+    """Scales of Q, K and V: max |.| / 127 over valid tokens of x Wqkv + b, per part."""
+    rng = np.random.default_rng(4)
+    H = 8
+    lengths = np.array([2, 0, 3], np.int32)
+    x = rng.standard_normal((3, 4, H))
+    x[0, 2:] = 1e6   # padding: never counted
+    x[2, 3:] = 1e6
+    layer = {"Wqkv": rng.standard_normal((H, 3 * H)), "bqkv": rng.standard_normal(3 * H)}
+    s = oracle.calibrate_int8_qkv(x, lengths, layer, 2)
+    rows = np.concatenate([x[0, :2], x[2, :3]])
+    qkv = rows @ layer["Wqkv"] + layer["bqkv"]
+    for i in range(3):
+        assert s[i] == np.float32(np.abs(qkv[:, i * H:(i + 1) * H]).max() / 127)
