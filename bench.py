@@ -5,7 +5,8 @@ default workload is the largest single-GPU configuration, the BERT-large-shaped 
 stack (B=64, L=384, half the lengths U[32,128] and half U[256,384], H=1024, 16 heads,
 FFN 4096, 24 layers): offsets + padding removal -> 24 encoder layers -> LayerNorm with
 the padding rebuild, one C-ABI call (rpp_encoder_forward).  --workload picks another
-configuration: bert_base_fp16, bert_large_int8, tiny_fp32, swin_t_stage1_fp16 (one
+configuration: bert_base_fp16, bert_large_int8, bert_large_int8_attn (the int8 config with
+the attention's products on codes too), tiny_fp32, swin_t_stage1_fp16 (one
 shifted-window block, rpp_swin_block_forward), swin_t_patch_merge_fp16.
 
 Timing: W warm-up steps, then K steps, each bracketed by its own CUDA events on the
@@ -160,22 +161,28 @@ def measure_int8_peak(torch, dev):
 # ---------------------------------------------------------------- workloads
 class BertWorkload:
     """BERT-shaped path: offsets + removal -> layers -> LN2 with padding rebuild."""
+    ALL_INT8 = "bert_large_int8_attn"
 
-    def __init__(self, cfg, rank):
+    def __init__(self, cfg, rank, all_int8=False):
         from workloads import make_bert_workload
         self.cfg = cfg
+        self.all_int8 = all_int8
         self.wl = make_bert_workload(cfg, seed=cfg.seed + 7919 * rank)   # each replica its own batch
         self.T = int(self.wl["lengths"].sum())
         self.sum_len2 = float((self.wl["lengths"].astype(np.float64) ** 2).sum())
         self.tokens_per_step = self.T * cfg.layers
         self.dtype = {"fp32": "f32", "fp16": "f16", "bf16": "bf16", "int8": "i8 GEMMs (exact), f16"}[cfg.dtype]
+        if all_int8:
+            self.dtype = "i8 GEMMs and attention products (exact), f16"
 
     def config(self):
         c = self.cfg
         lens = (f"50% U{list(c.bimodal[0])} + 50% U{list(c.bimodal[1])}" if c.bimodal
                 else f"U[{c.len_lo},{c.len_hi or c.L}]")
-        return {"workload": f"{c.name}: B={c.B} L={c.L} H={c.H} heads={c.nh}x{c.d} FFN={c.F} layers={c.layers} "
-                            f"dtype={c.dtype}, lengths {lens}, padding removed via offset mask",
+        name = self.ALL_INT8 if self.all_int8 else c.name
+        return {"workload": f"{name}: B={c.B} L={c.L} H={c.H} heads={c.nh}x{c.d} FFN={c.F} layers={c.layers} "
+                            f"dtype={c.dtype}{' (attention on codes too)' if self.all_int8 else ''}, lengths {lens}, "
+                            f"padding removed via offset mask",
                 "global_batch": c.B, "seq_len": c.L, "valid_tokens": self.T}
 
     def setup(self, rpp, torch, dev):
@@ -183,7 +190,8 @@ class BertWorkload:
         B, L, H = c.B, c.L, c.H
         self.tdt = rpp.torch_dtype(c.storage_dtype)
         int8 = c.dtype == "int8"
-        ecfg = rpp.encoder_cfg(c.H, c.nh, c.F, c.eps, c.storage_dtype, int8=int8, tokens_hint=self.T)
+        ecfg = rpp.encoder_cfg(c.H, c.nh, c.F, c.eps, c.storage_dtype, int8=(2 if self.all_int8 else int(int8)),
+                               tokens_hint=self.T)
         self.layers = [rpp.EncoderLayer(ecfg, l, dev) for l in wl["layers"]]
         self.lengths = torch.as_tensor(wl["lengths"], device=dev)
         self.x = torch.as_tensor(wl["x_padded"].reshape(B * L, H)).to(dev, self.tdt)
@@ -275,6 +283,9 @@ class BertWorkload:
             from workloads import make_calibration_batch
             cal = make_calibration_batch(c)
             scales = oracle.calibrate_int8(cal["x_padded"], cal["lengths"], wl["layers"][0], c.nh, c.eps)
+            if self.all_int8:
+                scales = np.concatenate([scales, oracle.calibrate_int8_qkv(cal["x_padded"], cal["lengths"],
+                                                                           wl["layers"][0], c.nh)])
             qlayers = [oracle.prepare_int8_layer(l) for l in wl["layers"]]
         tokens = seqs = 0
         t0 = time.perf_counter()
@@ -448,6 +459,8 @@ def make_workload(name, rank):
     from workloads import config_by_name
     if name == MergeWorkload.NAME:
         return MergeWorkload(config_by_name("swin_t_stage1_fp16"), rank)
+    if name == BertWorkload.ALL_INT8:   # the int8 config with the attention on codes as well
+        return BertWorkload(config_by_name("bert_large_int8"), rank, all_int8=True)
     cfg = config_by_name(name)
     return (SwinWorkload if cfg.kind == "swin" else BertWorkload)(cfg, rank)
 

@@ -192,6 +192,21 @@ RPP_API rpp_status rpp_attention_varlen(const void* qkv, const int32_t* cu_seqle
                                 int max_len, int nh, int d, rpp_dtype dtype, void* out, int32_t* err,
                                 rpp_stream stream);
 
+/* The same attention on int8 codes ([SW] §3 INT8 flow: every matrix product int8, with
+ * quantise / dequantise around it):
+ *  qkv_codes   device [T_max, 3*nh*d] int8 codes held in bf16 (each value an integer in
+ *              [-127, 127], exact in bf16), laid out as for rpp_attention_varlen
+ *  qkv_scales  device float32[3] = (s_q, s_k, s_v), the per-tensor scales of Q, K, V
+ *  out         device [T_max, nh*d] fp16; rows >= T untouched
+ * Per sequence and head: S = Qc Kc^T (exact integers), P = softmax over the sequence's
+ * keys of S s_q s_k / sqrt(d) (fp32), P's codes clamp(rne(127 P), 0, 127) (P is
+ * normalised before it is coded: the kernel reads S twice, first for the row maxima and
+ * sums), O = (Pc Vc) s_v / 127 with Pc Vc exact.  d must be 64; B <= 2048 and
+ * max_len <= 8192 (RPP_EUNSUPPORTED otherwise). */
+RPP_API rpp_status rpp_attention_varlen_i8(const void* qkv_codes, const float* qkv_scales,
+                                   const int32_t* cu_seqlens, int B, int T_max, int max_len, int nh,
+                                   int d, void* out, int32_t* err, rpp_stream stream);
+
 /* ------------------------------------------------------------------------------
  * Encoder layer (BERT-shaped, post-LayerNorm)
  * ------------------------------------------------------------------------------ */
@@ -202,7 +217,9 @@ typedef struct rpp_encoder_cfg {
   int ffn;       /* F */
   float eps;     /* LayerNorm eps */
   int dtype;     /* rpp_dtype of activations and float weights: RPP_F32, RPP_F16, RPP_BF16 */
-  int int8;      /* 1: the four linear GEMMs run on int8 codes (dtype must be RPP_F16) */
+  int int8;      /* 1: the four linear GEMMs run on int8 codes (dtype must be RPP_F16);
+                    2: also the attention (the QKV GEMM writes Q, K, V codes and both
+                    attention products run on codes, as rpp_attention_varlen_i8) */
   int tokens_hint; /* expected valid tokens per forward call (0: unknown, the capacity T_max is
                       assumed); only tile shapes and K splits depend on it, never the result */
 } rpp_encoder_cfg;
@@ -238,7 +255,8 @@ RPP_API size_t rpp_encoder_workspace_bytes(const rpp_encoder_cfg* cfg, int T_max
  *   y = LN2(x1 + GELU(x1 W1 + b1) W2 + b2).
  *  layer       device prepared block from rpp_prepare_layer
  *  act_scales  device float32[4] for int8 layers (scales of the QKV input, attention
- *              output, FC1 input and FC2 input), NULL otherwise
+ *              output, FC1 input and FC2 input), float32[7] for int8 == 2 (those four,
+ *              then the scales of Q, K and V), NULL otherwise
  *  x, y        device [T_max, H] of dtype; may alias
  *  cu_seqlens  device int32[B+1]; max_len >= every len_b
  *  workspace   device, >= rpp_encoder_workspace_bytes(cfg, T_max) bytes, 256-aligned */
@@ -249,9 +267,9 @@ RPP_API rpp_status rpp_encoder_layer_forward(const rpp_encoder_cfg* cfg, const v
                                      rpp_stream stream);
 
 /* Post-training calibration for the int8 layer: runs the float layer (cfg.int8 must be
- * 0, `layer` a float prepared block) and writes amax_out[0..3] = max |.| over valid
- * rows of the QKV input, the attention output, the FC1 input and the FC2 input.
- * amax_out: device float32[4], overwritten.  Scales for the int8 layer are amax / 127. */
+ * 0, `layer` a float prepared block) and writes amax_out[0..6] = max |.| over valid
+ * rows of the QKV input, the attention output, the FC1 input, the FC2 input, Q, K and V.
+ * amax_out: device float32[7], overwritten.  Scales for the int8 layer are amax / 127. */
 RPP_API rpp_status rpp_encoder_layer_calibrate(const rpp_encoder_cfg* cfg, const void* layer, const void* x,
                                        const int32_t* cu_seqlens, int B, int T_max, int max_len,
                                        float* amax_out, void* workspace, size_t workspace_bytes,

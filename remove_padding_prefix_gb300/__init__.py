@@ -22,7 +22,7 @@ from ._abi import (RPP_F32, RPP_F16, RPP_BF16, RPP_I8, RPP_EPI_BIAS, RPP_EPI_BIA
 
 __all__ = [
     "RppError", "lib", "torch_dtype", "dtype_code", "build_offsets", "remove_padding", "rebuild_padding", "linear",
-    "layernorm", "attention_varlen", "encoder_cfg", "EncoderLayer", "encoder_layer_forward",
+    "layernorm", "attention_varlen", "attention_varlen_i8", "encoder_cfg", "EncoderLayer", "encoder_layer_forward",
     "encoder_layer_calibrate", "encoder_forward", "quantize_weight", "quantize_activation", "gemm_i8_i32",
     "swin_cfg", "SwinBlock", "swin_prepare_bias", "window_attention_forward", "swin_block_forward",
     "merge_cfg", "PatchMerge", "patch_merge_forward",
@@ -146,10 +146,22 @@ def attention_varlen(qkv, cu_seqlens, B: int, max_len: int, nh: int, d: int = 64
     return o
 
 
+def attention_varlen_i8(qkv_codes, qkv_scales, cu_seqlens, B: int, max_len: int, nh: int, d: int = 64, out=None,
+                        err=None, stream=None):
+    """Attention on int8 codes held in a bf16 [T_max, 3*nh*d] tensor; qkv_scales: device
+    float32[3] (s_q, s_k, s_v); returns the fp16 [T_max, nh*d] output."""
+    T_max = qkv_codes.shape[0]
+    o = out if out is not None else torch.empty(T_max, nh * d, dtype=torch.float16, device=qkv_codes.device)
+    _check("rpp_attention_varlen_i8", lib().rpp_attention_varlen_i8(_p(qkv_codes), _p(qkv_scales), _p(cu_seqlens), B,
+                                                                    T_max, max_len, nh, d, _p(o), _p(err),
+                                                                    _stream(stream)))
+    return o
+
+
 # ---------------------------------------------------------------- encoder layer
 def encoder_cfg(H, nh, F, eps, dtype, int8=False, tokens_hint=0) -> EncoderCfg:
     code = dtype_code(dtype) if not isinstance(dtype, int) else dtype
-    return EncoderCfg(H, nh, H // nh, F, float(eps), code, 1 if int8 else 0, int(tokens_hint))
+    return EncoderCfg(H, nh, H // nh, F, float(eps), code, int(int8), int(tokens_hint))
 
 
 class EncoderLayer:
@@ -202,7 +214,7 @@ def encoder_layer_forward(layer: EncoderLayer, x, cu_seqlens, B: int, max_len: i
 def encoder_layer_calibrate(layer: EncoderLayer, x, cu_seqlens, B: int, max_len: int, workspace=None, err=None,
                             stream=None):
     T_max = x.shape[0]
-    amax = torch.empty(4, dtype=torch.float32, device=x.device)
+    amax = torch.empty(7, dtype=torch.float32, device=x.device)
     ws = workspace if workspace is not None else layer.workspace(T_max, x.device)
     _check("rpp_encoder_layer_calibrate",
            lib().rpp_encoder_layer_calibrate(C.byref(layer.cfg), _p(layer.block), _p(x), _p(cu_seqlens), B, T_max,

@@ -62,6 +62,7 @@ SIGNATURES = {
     "rpp_linear": (i32, [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, vp, vp]),
     "rpp_layernorm": (i32, [vp, vp, vp, vp, i32, vp, i32, f32, i32, vp, vp]),
     "rpp_attention_varlen": (i32, [vp, vp, i32, i32, i32, i32, i32, i32, vp, vp, vp]),
+    "rpp_attention_varlen_i8": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp]),
     "rpp_layer_bytes": (sz, [C.POINTER(EncoderCfg)]),
     "rpp_prepare_layer": (i32, [C.POINTER(EncoderCfg), C.POINTER(LayerSrc), vp, vp]),
     "rpp_encoder_workspace_bytes": (sz, [C.POINTER(EncoderCfg), i32]),

@@ -103,6 +103,7 @@ bool encoder_cfg_ok(const rpp_encoder_cfg* c) {
   if (c->hidden <= 0 || c->heads <= 0 || c->ffn <= 0 || c->head_dim <= 0) return false;
   if (c->heads * c->head_dim != c->hidden) return false;
   if (c->dtype != RPP_F32 && c->dtype != RPP_F16 && c->dtype != RPP_BF16) return false;
+  if (c->int8 < 0 || c->int8 > 2) return false;
   if (c->int8 && c->dtype != RPP_F16) return false;
   return true;
 }
@@ -335,6 +336,7 @@ rpp_status encoder_layer_run(const rpp_encoder_cfg* c, const void* layer, const 
     if (amax) RPP_LAUNCH("amax", s, launch_amax(x, T_max, rows, H, dt, amax + 0, err, s));
     RPP_LAUNCH("gemm_qkv", s, linear(dt, x, at<void>(layer, P.wqkv), bqkv, nullptr, qkv, T_max, rows, 3 * H, H,
                                      RPP_EPI_BIAS, err, s, RPP_I8, RPP_I8, hint));
+    if (amax && tc) RPP_LAUNCH("amax_qkv", s, launch_amax_parts(qkv, T_max, rows, 3 * H, H, dt, amax + 4, err, s));
     RPP_LAUNCH("attention", s, launch_attention_varlen(qkv, cu, B, T_max, max_len, nh, d, dt, attn, err, s));
     if (amax) RPP_LAUNCH("amax", s, launch_amax(attn, T_max, rows, H, dt, amax + 1, err, s));
     LnArgs l1 = ln_args(g1, be1);
@@ -384,9 +386,19 @@ rpp_status encoder_layer_run(const rpp_encoder_cfg* c, const void* layer, const 
   const float* s2 = act_scales + 2;
   const float* s3 = act_scales + 3;
   RPP_LAUNCH("quantize_x", s, launch_quantize_codes_bf16(x, s0, cx, T_max, rows, H, dt, err, s));
-  RPP_LAUNCH("gemm_qkv_i8", s, linear_i8(cx, at<void>(layer, P.wqkv), bqkv, s0, at<float>(layer, P.sqkv), nullptr,
-                                          nullptr, qkv, dt, T_max, rows, 3 * H, H, EPI_DQ_BIAS, err, s, hint));
-  RPP_LAUNCH("attention", s, launch_attention_varlen(qkv, cu, B, T_max, max_len, nh, d, dt, attn, err, s));
+  if (c->int8 == 2) {
+    // all-int8 flow: the QKV GEMM writes the codes of Q, K and V (scales act_scales[4..6])
+    // and the attention runs both of its products on codes
+    const float* sqkv = act_scales + 4;
+    RPP_LAUNCH("gemm_qkv_i8", s, linear_i8(cx, at<void>(layer, P.wqkv), bqkv, s0, at<float>(layer, P.sqkv), sqkv,
+                                            nullptr, qkv, RPP_BF16, T_max, rows, 3 * H, H, EPI_DQ_BIAS_Q3, err, s,
+                                            hint));
+    RPP_LAUNCH("attention_i8", s, launch_attention_sched(qkv, cu, B, T_max, max_len, nh, RPP_BF16, attn, err, s, sqkv));
+  } else {
+    RPP_LAUNCH("gemm_qkv_i8", s, linear_i8(cx, at<void>(layer, P.wqkv), bqkv, s0, at<float>(layer, P.sqkv), nullptr,
+                                            nullptr, qkv, dt, T_max, rows, 3 * H, H, EPI_DQ_BIAS, err, s, hint));
+    RPP_LAUNCH("attention", s, launch_attention_varlen(qkv, cu, B, T_max, max_len, nh, d, dt, attn, err, s));
+  }
   RPP_LAUNCH("quantize_attn", s, launch_quantize_codes_bf16(attn, s1, ca, T_max, rows, H, dt, err, s));
   RPP_LAUNCH("gemm_proj_i8", s, linear_i8(ca, at<void>(layer, P.wo), nullptr, s1, at<float>(layer, P.so), nullptr,
                                            nullptr, h, RPP_F32, T_max, rows, H, H, EPI_DQ_ACC, err, s, hint));
@@ -622,6 +634,17 @@ rpp_status rpp_attention_varlen(const void* qkv, const int32_t* cu_seqlens, int 
                                            static_cast<cudaStream_t>(stream)));
 }
 
+rpp_status rpp_attention_varlen_i8(const void* qkv_codes, const float* qkv_scales, const int32_t* cu_seqlens, int B,
+                                   int T_max, int max_len, int nh, int d, void* out, int32_t* err,
+                                   rpp_stream stream) {
+  if (!qkv_codes || !qkv_scales || !cu_seqlens || !out || B <= 0 || T_max <= 0 || max_len <= 0 || nh <= 0 || d <= 0)
+    return RPP_EINVAL;
+  if (!aligned16(qkv_codes) || !aligned16(out)) return RPP_EINVAL;
+  if (d != 64 || !attention_sched_supported(B, max_len) || nh > 65535) return RPP_EUNSUPPORTED;
+  return from_cuda(launch_attention_sched(qkv_codes, cu_seqlens, B, T_max, max_len, nh, RPP_BF16, out, err,
+                                          static_cast<cudaStream_t>(stream), qkv_scales));
+}
+
 size_t rpp_layer_bytes(const rpp_encoder_cfg* cfg) {
   if (!encoder_cfg_ok(cfg)) return 0;
   return layer_layout(cfg).total;
@@ -692,7 +715,7 @@ rpp_status rpp_encoder_layer_calibrate(const rpp_encoder_cfg* cfg, const void* l
   if (!cfg || cfg->int8 || !amax_out) return RPP_EINVAL;
   if (cfg->dtype == RPP_F32) return RPP_EUNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(amax_out, 0, 4 * sizeof(float), s) != cudaSuccess) return RPP_ECUDA;
+  if (cudaMemsetAsync(amax_out, 0, 7 * sizeof(float), s) != cudaSuccess) return RPP_ECUDA;
   const size_t need = enc_ws_layout(cfg, T_max > 0 ? T_max : 1).total;
   if (workspace_bytes < need) return RPP_EWORKSPACE;
   // the output of the calibration pass is not needed: it goes to the QKV buffer, which

@@ -131,10 +131,18 @@ __device__ __forceinline__ Item decode(const Sched& s, int g) {
   return it;
 }
 
-template <typename T>
+// I8: Q, K and V are int8 codes held in bf16 (exact), i8_scales = (s_q, s_k, s_v) in
+// device memory, and every item takes two passes over its key tiles: the first computes
+// only the row maxima and sums, the second writes P's codes clamp(rne(127 P), 0, 127)
+// of the normalised softmax into tensor memory; S = Qc Kc^T and O = Pc Vc are then
+// exact integers in the fp32 accumulators, and O is written as fp16 O s_v / 127.
+template <typename T, bool I8>
 __global__ void __launch_bounds__(kThreads, 2)
 attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __restrict__ cu, int B, int T_max,
-                       int max_len, int nh, int n_cls, T* __restrict__ out, float scale_log2, int32_t* err) {
+                       int max_len, int nh, int n_cls, void* __restrict__ out_v, float scale_log2,
+                       const float* __restrict__ i8_scales, int32_t* err) {
+  using TOut = typename std::conditional<I8, __half, T>::type;
+  TOut* out = static_cast<TOut*>(out_v);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
@@ -268,12 +276,15 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
           tma_load_2d(sQ + qb * kTile, &tm, &q_full[qb], it.h * kDh, it.c0 + it.q0);
           ++nq;
         }
-        for (int j = 0; j < it.ntiles; ++j) {
+        const int nt = I8 ? 2 * it.ntiles : it.ntiles;   // int8: K for both passes, V for the second
+        for (int t = 0; t < nt; ++t) {
+          const int j = t < it.ntiles ? t : t - it.ntiles;
           const uint32_t kb = nk & 1u;
           if (!mbar_wait_bounded(&k_empty[kb], ((nk >> 1) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
           mbar_arrive_expect_tx(&k_full[kb], kTile);
           tma_load_2d(sK + kb * kTile, &tm, &k_full[kb], H + it.h * kDh, it.c0 + j * kT);
           ++nk;
+          if (I8 && t < it.ntiles) continue;
           const uint32_t vb = nv & 1u;
           if (!mbar_wait_bounded(&v_empty[vb], ((nv >> 1) & 1u) ^ 1u, abort_flag)) { ok = false; break; }
           mbar_arrive_expect_tx(&v_full[vb], kTile);
@@ -334,7 +345,8 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
             if (!mbar_wait_bounded(&q_full[nq & 1u], (nq >> 1) & 1u, abort_flag)) { ok = false; break; }
             qdesc = sw128_kmajor_desc(smem_u32(sQ + (nq & 1u) * kTile));
           }
-          const int nvalid = min(kT, its.len - js * kT);
+          const int jk = (I8 && js >= its.ntiles) ? js - its.ntiles : js;   // key tile of this S
+          const int nvalid = min(kT, its.len - jk * kT);
           const uint32_t idesc_s = idesc_f16(fmt, kT, (nvalid + 15) & ~15);
           const uint32_t kb = nk & 1u;
           if (!mbar_wait_bounded(&k_full[kb], (nk >> 1) & 1u, abort_flag)) { ok = false; break; }
@@ -347,18 +359,21 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
           tc_commit(&k_empty[kb]);
           ++nk;
           ++ns;
-          if (js == its.ntiles - 1) {
+          if (js == (I8 ? 2 * its.ntiles : its.ntiles) - 1) {
             tc_commit(&q_empty[nq & 1u]);
             ++nq;
           }
         }
         if (pend && !issue_pv(itp, jp)) { ok = false; break; }
         if (pend && jp == itp.ntiles - 1) ++nit;
-        pend = has_s;
-        if (has_s) {   // the tile just issued waits for its P V; advance the S cursor
-          itp = its;
-          jp = js;
-          if (++js == its.ntiles) {
+        // the tile just issued waits for its P V (int8: second-pass tiles only)
+        pend = has_s && (!I8 || js >= its.ntiles);
+        if (has_s) {   // advance the S cursor
+          if (pend) {
+            itp = its;
+            jp = js - (I8 ? its.ntiles : 0);
+          }
+          if (++js == (I8 ? 2 * its.ntiles : its.ntiles)) {
             js = 0;
             gs += gridDim.x;
             has_s = gs < n_items;
@@ -399,115 +414,159 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
       other = xval[(par * 2 + (hf ^ 1)) * kT + r];
       return true;
     };
+    // scores are scaled by `scale` in log2 units: log2(e) / sqrt(d), times s_q s_k for codes
+    float scale = scale_log2, o_scale = 0.f;
+    if constexpr (I8) {
+      scale = scale_log2 * __ldg(i8_scales) * __ldg(i8_scales + 1);
+      o_scale = __ldg(i8_scales + 2) / 127.0f;
+    }
+    // this half's row maximum of S (keys past the sequence: -inf), in raw score units
+    auto half_max = [&](int nv_h) -> float {
+      float pm[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        if (32 * c < nv_h) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(t_lane + col_s + 32 * c, v);
+          tmem_ld_wait_tied32(v);
+          if (32 * c + 32 > nv_h) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (32 * c + e >= nv_h) v[e] = 0xff800000u;
+          }
+#pragma unroll
+          for (int e = 0; e < 32; e += 8)
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+              pm[t] = fmaxf(fmaxf(pm[t], __uint_as_float(v[e + t])), __uint_as_float(v[e + t + 4]));
+        }
+      }
+      return fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
+    };
+    // Second read of this half of S: 2^(s scale - m) for its keys, 32 per chunk, with
+    // packed fp32 pairs for the scale and the sum (keys past the sequence give 0).
+    // MODE 0: P rounded to the input type, written to tensor memory; returns the sum.
+    // MODE 1: the sum only.  MODE 2: P's int8 codes clamp(rne(127 P inv_l), 0, 127).
+    auto half_exp = [&](int nv_h, float m, float inv_l, auto mode_tag) -> float {
+      constexpr int MODE = decltype(mode_tag)::value;
+      const uint64_t sc2 = f2_pack(scale, scale);
+      const uint64_t nm2 = f2_pack(-m, -m);
+      uint64_t psum2[2] = {0ull, 0ull};
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        if (32 * c < nv_h) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(t_lane + col_s + 32 * c, v);
+          tmem_ld_wait_tied32(v);
+          if (32 * c + 32 > nv_h) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (32 * c + e >= nv_h) v[e] = 0xff800000u;
+          }
+#pragma unroll
+          for (int e2 = 0; e2 < 16; ++e2) {   // pair e2 is written after keys 2 e2, 2 e2 + 1 are read
+            const uint64_t x2 =
+                f2_fma(f2_pack(__uint_as_float(v[2 * e2]), __uint_as_float(v[2 * e2 + 1])), sc2, nm2);
+            float p0 = ex2_approx(f2_lo(x2));
+            float p1 = ex2_approx(f2_hi(x2));
+            if constexpr (MODE == 2) {
+              p0 = fminf(rintf(p0 * inv_l * 127.0f), 127.0f);
+              p1 = fminf(rintf(p1 * inv_l * 127.0f), 127.0f);
+            } else {
+              psum2[e2 & 1] = f2_add(psum2[e2 & 1], f2_pack(p0, p1));
+            }
+            if constexpr (MODE != 1) v[e2] = pack2<T>(p0, p1);
+          }
+          if constexpr (MODE != 1) {
+            tmem_st_32x32b_x16(t_lane + col_p + 16 * c, v);
+            tmem_st_wait_tied16(v);
+          }
+        }
+      }
+      return (f2_lo(psum2[0]) + f2_hi(psum2[0])) + (f2_lo(psum2[1]) + f2_hi(psum2[1]));
+    };
     for (int g = blockIdx.x; g < n_items && ok; g += gridDim.x) {
       const Item it = decode(sch, g);
       const bool active = it.q0 + quad * 32 < it.len;   // the same for both warps of the quadrant
       float m = neg_inf(), l = 0.f;                     // l: this warp's half of the row sum
-      for (int j = 0; j < it.ntiles; ++j) {
+      float inv_l = 0.f;                                // int8: 1 / the whole row sum
+      const int nt = I8 ? 2 * it.ntiles : it.ntiles;
+      int jb = 0;                                       // P V products of this item so far
+      for (int t = 0; t < nt; ++t) {
+        const bool stats = I8 && t < it.ntiles;          // int8 first pass: maxima and sums only
+        const int j = t < it.ntiles ? t : t - it.ntiles; // key tile
         const int nvalid = min(kT, it.len - j * kT);
         const int nv_h = min(64, max(0, nvalid - 64 * hf));   // keys of this half inside the sequence
         int w = mbar_wait_bounded(s_full, ns & 1u, abort_flag) ? 1 : 0;
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
         tc_fence_after();
         float mx = neg_inf();
-        if (active) {
-          // pass 1: this half's row maximum, 32 keys per tensor-memory load (keys past the
-          // sequence: -inf)
-          float pm[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
-#pragma unroll 1
-          for (int c = 0; c < 2; ++c) {
-            if (32 * c < nv_h) {
-              uint32_t v[32];
-              tmem_ld_32x32b_x32(t_lane + col_s + 32 * c, v);
-              tmem_ld_wait_tied32(v);
-              if (32 * c + 32 > nv_h) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                  if (32 * c + e >= nv_h) v[e] = 0xff800000u;
-              }
-#pragma unroll
-              for (int e = 0; e < 32; e += 8)
-#pragma unroll
-                for (int t = 0; t < 4; ++t)
-                  pm[t] = fmaxf(fmaxf(pm[t], __uint_as_float(v[e + t])), __uint_as_float(v[e + t + 4]));
-            }
-          }
-          mx = fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3]));
+        if (active && (!I8 || stats)) {
+          mx = half_max(nv_h);
           float other;
           if (!exchange(mx, other)) { ok = false; break; }
-          mx = fmaxf(mx, other) * scale_log2;
+          mx = fmaxf(mx, other) * scale;
         }
         // P and O: the previous P V must be done before P is rewritten or O rescaled (every
         // warp waits, active or not: p_full counts one arrival per warp, and a warp that
         // arrived for the next tile before another warp arrived for this one would
         // complete this tile's phase early)
-        if (j > 0) {
+        if (!stats && jb > 0) {
           w = mbar_wait_bounded(pv_done, (npv - 1) & 1u, abort_flag) ? 1 : 0;
           if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
           tc_fence_after();
         }
         if (active) {
-          if (j == 0) {
-            m = mx;
+          if constexpr (!I8) {
+            if (j == 0) {
+              m = mx;
+            } else {
+              // lazy rescaling, decided alike by both warps of the quadrant (same rows,
+              // same maxima); the tensor-memory accesses are warp-collective
+              const bool move = mx > m + 8.0f;
+              if (__any_sync(0xffffffffu, move)) {
+                const float alpha = move ? ex2_approx(m - mx) : 1.0f;
+#pragma unroll 1
+                for (int q2 = 0; q2 < 2; ++q2) {   // this warp's 32 columns of O
+                  uint32_t ov[16];
+                  tmem_ld_32x32b_x16(t_lane + col_o + 16 * q2, ov);
+                  tmem_ld_wait_tied16(ov);
+#pragma unroll
+                  for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                  tmem_st_32x32b_x16(t_lane + col_o + 16 * q2, ov);
+                  tmem_st_wait_tied16(ov);
+                }
+                if (move) {
+                  l *= alpha;
+                  m = mx;
+                }
+              }
+            }
+            l += half_exp(nv_h, m, 0.f, std::integral_constant<int, 0>{});
+          } else if (stats) {
+            // the reference maximum moves lazily as above (no O yet: only the sum rescales)
+            if (j == 0) {
+              m = mx;
+            } else if (mx > m + 8.0f) {
+              l *= ex2_approx(m - mx);
+              m = mx;
+            }
+            l += half_exp(nv_h, m, 0.f, std::integral_constant<int, 1>{});
+            if (j == it.ntiles - 1) {   // end of the first pass: the whole row sum
+              float other;
+              if (!exchange(l, other)) { ok = false; break; }
+              inv_l = 1.0f / (l + other);
+            }
           } else {
-            // lazy rescaling, decided alike by both warps of the quadrant (same rows,
-            // same maxima); the tensor-memory accesses are warp-collective
-            const bool move = mx > m + 8.0f;
-            if (__any_sync(0xffffffffu, move)) {
-              const float alpha = move ? ex2_approx(m - mx) : 1.0f;
-#pragma unroll 1
-              for (int q2 = 0; q2 < 2; ++q2) {   // this warp's 32 columns of O
-                uint32_t ov[16];
-                tmem_ld_32x32b_x16(t_lane + col_o + 16 * q2, ov);
-                tmem_ld_wait_tied16(ov);
-#pragma unroll
-                for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-                tmem_st_32x32b_x16(t_lane + col_o + 16 * q2, ov);
-                tmem_st_wait_tied16(ov);
-              }
-              if (move) {
-                l *= alpha;
-                m = mx;
-              }
-            }
+            half_exp(nv_h, m, inv_l, std::integral_constant<int, 2>{});
           }
-          // pass 2: P = 2^(s - m) for this half's keys, 32 per chunk, packed in place
-          // (pair e written after keys 2e, 2e + 1 are read); packed fp32 pairs for the
-          // scale and the sum; keys past the sequence give 0
-          const uint64_t sc2 = f2_pack(scale_log2, scale_log2);
-          const uint64_t nm2 = f2_pack(-m, -m);
-          uint64_t psum2[2] = {0ull, 0ull};
-#pragma unroll 1
-          for (int c = 0; c < 2; ++c) {
-            if (32 * c < nv_h) {
-              uint32_t v[32];
-              tmem_ld_32x32b_x32(t_lane + col_s + 32 * c, v);
-              tmem_ld_wait_tied32(v);
-              if (32 * c + 32 > nv_h) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                  if (32 * c + e >= nv_h) v[e] = 0xff800000u;
-              }
-#pragma unroll
-              for (int e2 = 0; e2 < 16; ++e2) {
-                const uint64_t x2 =
-                    f2_fma(f2_pack(__uint_as_float(v[2 * e2]), __uint_as_float(v[2 * e2 + 1])), sc2, nm2);
-                const float p0 = ex2_approx(f2_lo(x2));
-                const float p1 = ex2_approx(f2_hi(x2));
-                psum2[e2 & 1] = f2_add(psum2[e2 & 1], f2_pack(p0, p1));
-                v[e2] = pack2<T>(p0, p1);
-              }
-              tmem_st_32x32b_x16(t_lane + col_p + 16 * c, v);
-              tmem_st_wait_tied16(v);
-            }
-          }
-          l += (f2_lo(psum2[0]) + f2_hi(psum2[0])) + (f2_lo(psum2[1]) + f2_hi(psum2[1]));
         }
-        // S has been read by this warp (both passes)
+        // S has been read by this warp
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(s_free);
         ++ns;
+        if (stats) continue;
         // the last 16-key step of a partial tile: zero the V rows past the sequence
         // (P is 0 there, but 0 * NaN would not be); one warp of each quadrant does it
         const int kpad = ((nvalid + 15) & ~15);
@@ -527,29 +586,32 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full);
         ++npv;
+        ++jb;
       }
       if (!ok) break;
-      // the item's O: wait for its last P V, add the two halves of the row sum, scale this
-      // warp's 32 columns by 1 / sum and store the valid rows
+      // the item's O: wait for its last P V; float: add the two halves of the row sum and
+      // scale by 1 / sum; int8: P was normalised, O scales by s_v / 127
       int w = mbar_wait_bounded(pv_done, (npv - 1) & 1u, abort_flag) ? 1 : 0;
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc_fence_after();
       if (active) {
-        float other;
-        if (!exchange(l, other)) { ok = false; break; }
-        l += other;
+        float inv = o_scale;
+        if constexpr (!I8) {
+          float other;
+          if (!exchange(l, other)) { ok = false; break; }
+          inv = 1.0f / (l + other);
+        }
         uint32_t ov[32];
         tmem_ld_32x32b_x32(t_lane + col_o, ov);
         tmem_ld_wait_tied32(ov);
         if (it.q0 + r < it.len) {
-          const float inv = 1.0f / l;
           uint4* orow = reinterpret_cast<uint4*>(out + static_cast<long long>(it.c0 + it.q0 + r) * H + it.h * kDh +
                                                  32 * hf);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const float* f = reinterpret_cast<const float*>(ov + 8 * u);
-            orow[u] = make_uint4(pack2<T>(f[0] * inv, f[1] * inv), pack2<T>(f[2] * inv, f[3] * inv),
-                                 pack2<T>(f[4] * inv, f[5] * inv), pack2<T>(f[6] * inv, f[7] * inv));
+            orow[u] = make_uint4(pack2<TOut>(f[0] * inv, f[1] * inv), pack2<TOut>(f[2] * inv, f[3] * inv),
+                                 pack2<TOut>(f[4] * inv, f[5] * inv), pack2<TOut>(f[6] * inv, f[7] * inv));
           }
         }
       }
@@ -579,42 +641,44 @@ bool attention_sched_supported(int B, int max_len) {
   return B >= 1 && B <= kMaxB && max_len >= 1 && (max_len + kT - 1) / kT <= kMaxCls;
 }
 
-cudaError_t launch_attention_sched(const void* qkv, const int32_t* cu, int B, int T_max, int max_len, int nh,
-                                   rpp_dtype dtype, void* out, int32_t* err, cudaStream_t stream) {
-  if (B <= 0 || max_len <= 0 || T_max <= 0) return cudaSuccess;
-  if (dtype != RPP_F16 && dtype != RPP_BF16) return cudaErrorNotSupported;
-  if (!attention_sched_supported(B, max_len)) return cudaErrorNotSupported;
-  const int H = nh * kDh;
-  CUtensorMap tm;
-  const CUtensorMapDataType dt = dtype == RPP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  if (!make_tmap_2d(&tm, qkv, dt, 2, T_max, 3 * H, kT, kDh, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+namespace {
+
+template <typename T, bool I8>
+cudaError_t launch_sched(const CUtensorMap& tm, const int32_t* cu, int B, int T_max, int max_len, int nh, void* out,
+                         const float* i8_scales, int32_t* err, cudaStream_t stream) {
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kDh));
   const int n_cls = (max_len + kT - 1) / kT;
   // persistent: two CTAs per SM, never more CTAs than the largest possible item count
   const long long max_items = static_cast<long long>(B) * nh * n_cls;
   const int grid = static_cast<int>(max_items < 2LL * num_sms() ? max_items : 2LL * num_sms());
   const size_t smem = smem_bytes(B);
-  if (dtype == RPP_F16) {
-    static size_t attr = 0;
-    if (attr < smem) {
-      cudaError_t e = cudaFuncSetAttribute(attention_sched_kernel<__half>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem_bytes(kMaxB)));
-      if (e != cudaSuccess) return e;
-      attr = smem_bytes(kMaxB);
-    }
-    return launch_pdl(attention_sched_kernel<__half>, dim3(grid), dim3(kThreads), smem, stream, tm, cu, B, T_max,
-                      max_len, nh, n_cls, static_cast<__half*>(out), scale_log2, err);
-  }
-  static size_t attr_bf = 0;
-  if (attr_bf < smem) {
-    cudaError_t e = cudaFuncSetAttribute(attention_sched_kernel<__nv_bfloat16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+  static size_t attr = 0;
+  if (attr < smem) {
+    cudaError_t e = cudaFuncSetAttribute(attention_sched_kernel<T, I8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem_bytes(kMaxB)));
     if (e != cudaSuccess) return e;
-    attr_bf = smem_bytes(kMaxB);
+    attr = smem_bytes(kMaxB);
   }
-  return launch_pdl(attention_sched_kernel<__nv_bfloat16>, dim3(grid), dim3(kThreads), smem, stream, tm, cu, B,
-                    T_max, max_len, nh, n_cls, static_cast<__nv_bfloat16*>(out), scale_log2, err);
+  return launch_pdl(attention_sched_kernel<T, I8>, dim3(grid), dim3(kThreads), smem, stream, tm, cu, B, T_max,
+                    max_len, nh, n_cls, out, scale_log2, i8_scales, err);
+}
+
+}  // namespace
+
+cudaError_t launch_attention_sched(const void* qkv, const int32_t* cu, int B, int T_max, int max_len, int nh,
+                                   rpp_dtype dtype, void* out, int32_t* err, cudaStream_t stream,
+                                   const float* i8_scales) {
+  if (B <= 0 || max_len <= 0 || T_max <= 0) return cudaSuccess;
+  if (dtype != RPP_F16 && dtype != RPP_BF16) return cudaErrorNotSupported;
+  if (i8_scales && dtype != RPP_BF16) return cudaErrorNotSupported;   // codes are held in bf16
+  if (!attention_sched_supported(B, max_len)) return cudaErrorNotSupported;
+  const int H = nh * kDh;
+  CUtensorMap tm;
+  const CUtensorMapDataType dt = dtype == RPP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if (!make_tmap_2d(&tm, qkv, dt, 2, T_max, 3 * H, kT, kDh, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+  if (i8_scales) return launch_sched<__nv_bfloat16, true>(tm, cu, B, T_max, max_len, nh, out, i8_scales, err, stream);
+  if (dtype == RPP_F16) return launch_sched<__half, false>(tm, cu, B, T_max, max_len, nh, out, nullptr, err, stream);
+  return launch_sched<__nv_bfloat16, false>(tm, cu, B, T_max, max_len, nh, out, nullptr, err, stream);
 }
 
 }  // namespace rpp

@@ -120,7 +120,7 @@ constexpr int res_vecs32() {
 }
 template <int EPI>
 constexpr bool is_int_epi() {
-  return EPI >= EPI_I32 && EPI <= EPI_DQ_BIAS_GELU_Q;
+  return (EPI >= EPI_I32 && EPI <= EPI_DQ_BIAS_GELU_Q) || EPI == EPI_DQ_BIAS_Q3;
 }
 
 __device__ __forceinline__ float code_of(float v, float inv_s) {
@@ -149,14 +149,14 @@ __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_
 template <int EPI>
 constexpr bool has_bias() {
   return EPI == RPP_EPI_BIAS || EPI == RPP_EPI_BIAS_GELU || EPI == RPP_EPI_BIAS_RESIDUAL || EPI == EPI_DQ_BIAS ||
-         EPI == EPI_DQ_BIAS_GELU_Q;
+         EPI == EPI_DQ_BIAS_GELU_Q || EPI == EPI_DQ_BIAS_Q3;
 }
 
 template <typename TOut, typename TRes, int EPI, int NV>
 __device__ __forceinline__ void epi_math(const GemmParams& p, float* v, int row, int n, bool first, float a_s,
                                          float inv_q, const uint4* rres = nullptr, const float4* bpre = nullptr) {
   if constexpr (EPI == EPI_I32 || EPI == EPI_ACC) return;
-  if constexpr (EPI == EPI_DQ_BIAS || EPI == EPI_DQ_ACC || EPI == EPI_DQ_BIAS_GELU_Q) {
+  if constexpr (EPI == EPI_DQ_BIAS || EPI == EPI_DQ_ACC || EPI == EPI_DQ_BIAS_GELU_Q || EPI == EPI_DQ_BIAS_Q3) {
     const float4* s4 = reinterpret_cast<const float4*>(p.w_scale + n);
 #pragma unroll
     for (int j = 0; j < NV / 4; ++j) {
@@ -187,6 +187,11 @@ __device__ __forceinline__ void epi_math(const GemmParams& p, float* v, int row,
   if constexpr (EPI == EPI_DQ_BIAS_GELU_Q) {
 #pragma unroll
     for (int j = 0; j < NV; ++j) v[j] = code_of(v[j], inv_q);
+  }
+  if constexpr (EPI == EPI_DQ_BIAS_Q3) {   // NV columns never straddle a third (N / 3 % 32 == 0)
+    const float iq = __fdiv_rn(1.0f, __ldg(p.q_scale + n / (p.N / 3)));
+#pragma unroll
+    for (int j = 0; j < NV; ++j) v[j] = code_of(v[j], iq);
   }
   if constexpr (EPI == RPP_EPI_BIAS_RESIDUAL) {
     if (first) {
@@ -559,7 +564,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint8_t* stage0 = sEpi + (warp - 2) * EPI_BUFS * EPI_STAGE;
     int sb = 0;   // staging block of the next store
     float a_s = 1.f, inv_q = 0.f;
-    if constexpr (EPI == EPI_DQ_BIAS || EPI == EPI_DQ_ACC || EPI == EPI_DQ_BIAS_GELU_Q) a_s = *p.a_scale;
+    if constexpr (EPI == EPI_DQ_BIAS || EPI == EPI_DQ_ACC || EPI == EPI_DQ_BIAS_GELU_Q || EPI == EPI_DQ_BIAS_Q3)
+      a_s = *p.a_scale;
     if constexpr (EPI == EPI_DQ_BIAS_GELU_Q) inv_q = __fdiv_rn(1.0f, *p.q_scale);
     uint32_t acc_it = 0;
     bool pending_store = false;
@@ -894,6 +900,7 @@ cudaError_t dispatch_int(int bn, int epi, const CUtensorMap& ta, const CUtensorM
     case EPI_DQ_BIAS: return dispatch_bn<BF, __half, __half, EPI_DQ_BIAS, NCH>(bn, ta, tb, p, gr, stream);
     case EPI_DQ_ACC: return dispatch_bn<BF, float, __half, EPI_DQ_ACC, NCH>(bn, ta, tb, p, gr, stream);
     case EPI_DQ_BIAS_GELU_Q: return dispatch_bn<BF, BF, BF, EPI_DQ_BIAS_GELU_Q, NCH>(bn, ta, tb, p, gr, stream);
+    case EPI_DQ_BIAS_Q3: return dispatch_bn<BF, BF, BF, EPI_DQ_BIAS_Q3, NCH>(bn, ta, tb, p, gr, stream);
     default: return cudaErrorNotSupported;
   }
 }
@@ -913,7 +920,8 @@ void set_gemm_cluster_mode(int mode) { g_cluster_mode = mode; }
 void set_gemm_stall_next(unsigned long long limit_ns) { g_stall_next_ns = limit_ns; }
 
 cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t stream) {
-  const bool is_int = g.epi >= EPI_I32 && g.epi <= EPI_DQ_BIAS_GELU_Q;
+  const bool is_int = (g.epi >= EPI_I32 && g.epi <= EPI_DQ_BIAS_GELU_Q) || g.epi == EPI_DQ_BIAS_Q3;
+  if (g.epi == EPI_DQ_BIAS_Q3 && (g.N % 3 || (g.N / 3) % 32)) return cudaErrorNotSupported;
   const int num_k = (g.K + kBK - 1) / kBK;
   const int nch = is_int ? (num_k + kChunkBlocks - 1) / kChunkBlocks : 1;
   if (nch > 4) return cudaErrorNotSupported;

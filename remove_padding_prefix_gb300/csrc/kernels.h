@@ -24,7 +24,9 @@ enum InternalEpilogue {
   EPI_DQ_BIAS = 4,           // acc * s_a * s_w[n] + b
   EPI_DQ_ACC = 5,            // acc * s_a * s_w[n] (fp32; bias and residual added by the next LayerNorm)
   EPI_DQ_BIAS_GELU_Q = 6,    // int8 code of GELU(acc * s_a * s_w[n] + b), held in a bf16 container
-  EPI_ACC = 7                // raw fp32 accumulator (split-K slices; bias and residual added by LayerNorm)
+  EPI_ACC = 7,               // raw fp32 accumulator (split-K slices; bias and residual added by LayerNorm)
+  EPI_DQ_BIAS_Q3 = 8         // int8 codes of acc * s_a * s_w[n] + b with one scale per third of the columns
+                             // (the Q, K and V parts of the QKV projection), held in a bf16 container
 };
 
 cudaError_t launch_build_offsets(const int32_t* lengths, int B, int L, int32_t* cu, int32_t* po, int32_t* err,
@@ -76,6 +78,9 @@ cudaError_t launch_quantize(const void* x, const float* scale, int8_t* q, int M_
                             rpp_dtype dtype, int32_t* err, cudaStream_t stream);
 cudaError_t launch_amax(const void* x, int M_max, const int32_t* rows, int H, rpp_dtype dtype, float* amax,
                         int32_t* err, cudaStream_t stream);
+// per-part max |x| of [M, W] rows split into W / part_w (<= 3) column parts -> amax[part]
+cudaError_t launch_amax_parts(const void* x, int M_max, const int32_t* rows, int W, int part_w, rpp_dtype dtype,
+                              float* amax, int32_t* err, cudaStream_t stream);
 
 // preprocessing and int8 code helpers (prep.cu)
 cudaError_t launch_quantize_codes_bf16(const void* x, const float* scale, void* codes, int M_max, const int32_t* rows,
@@ -102,7 +107,8 @@ struct TcGemmArgs {
   int epi;                 // rpp_epilogue or InternalEpilogue
   const float* a_scale;    // device scalar s_a (int8 epilogues)
   const float* w_scale;    // device [N] s_w (int8 epilogues)
-  const float* q_scale;    // device scalar for the requantised output (EPI_DQ_BIAS_GELU_Q)
+  const float* q_scale;    // device scalar for the requantised output (EPI_DQ_BIAS_GELU_Q), or three
+                           // (EPI_DQ_BIAS_Q3: the scales of the column thirds)
   int32_t* err;
   int force_bn;            // 0 = heuristic
   int rows_hint;           // expected rows (0 = M_max): tile shapes only, never correctness
@@ -126,8 +132,10 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, in
                   int cols, int box_rows, int box_cols, CUtensorMapSwizzle swz);
 // persistent longest-first tcgen05 varlen attention (S, P, O in tensor memory), head size 64
 bool attention_sched_supported(int B, int max_len);
+// i8_scales: device (s_q, s_k, s_v) for int8 codes held in bf16 (dtype RPP_BF16, fp16 out)
 cudaError_t launch_attention_sched(const void* qkv, const int32_t* cu, int B, int T_max, int max_len, int nh,
-                                   rpp_dtype dtype, void* out, int32_t* err, cudaStream_t stream);
+                                   rpp_dtype dtype, void* out, int32_t* err, cudaStream_t stream,
+                                   const float* i8_scales = nullptr);
 // tcgen05 varlen attention, head size 64, fp16 / bf16 (one CTA per 128 queries; batches
 // beyond the persistent kernel's limits)
 cudaError_t launch_attention_tc(const void* qkv, const int32_t* cu, int B, int T_max, int max_len, int nh,

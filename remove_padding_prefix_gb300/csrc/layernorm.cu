@@ -563,6 +563,50 @@ bool ln16_applies(const LnArgs& a) {
          (v == 1 || v == 2 || v == 3 || v == 4 || v == 6);
 }
 
+// max |x| of each part of [M, W] rows cut into column parts of width part_w (at most
+// three: the Q, K and V parts of the QKV projection), accumulated into amax[part]
+template <typename T>
+__global__ void amax_parts_kernel(const T* __restrict__ x, int M_max, const int32_t* rows, int W, int part_w,
+                                  float* amax, int32_t* err) {
+  pdl_wait();
+  pdl_trigger();
+  if (device_error_set(err)) return;
+  int M = rows ? *rows : M_max;
+  if (M > M_max || M < 0) M = 0;
+  const long long n8 = static_cast<long long>(M) * W / 8;
+  const int vpr = W / 8;   // vectors per row
+  float m0 = 0.f, m1 = 0.f, m2 = 0.f;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n8;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    float f[8];
+    if constexpr (sizeof(T) == 2) {
+      unpack16<T>(reinterpret_cast<const uint4*>(x)[i], f);
+    } else {
+      unpack16<T>(reinterpret_cast<const uint4*>(x)[2 * i], f);
+      unpack16<T>(reinterpret_cast<const uint4*>(x)[2 * i + 1], f + 4);
+    }
+    float m = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(f[j]));
+    const int part = static_cast<int>(i % vpr) * 8 / part_w;   // part_w % 8 == 0: a vector lies in one part
+    if (part == 0) m0 = fmaxf(m0, m);
+    else if (part == 1) m1 = fmaxf(m1, m);
+    else m2 = fmaxf(m2, m);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+    m2 = fmaxf(m2, __shfl_xor_sync(0xffffffffu, m2, o));
+  }
+  if (lane_id() == 0) {
+    const int np = W / part_w;
+    atomic_max_nonneg(amax, m0);
+    if (np > 1) atomic_max_nonneg(amax + 1, m1);
+    if (np > 2) atomic_max_nonneg(amax + 2, m2);
+  }
+}
+
 template <typename T, typename TOut, int G, int VPL, int NS>
 cudaError_t ln_launch(const LnArgs& a, cudaStream_t stream) {
   const int threads = 128;
@@ -688,6 +732,26 @@ cudaError_t launch_amax(const void* x, int M_max, const int32_t* rows, int H, rp
     case RPP_BF16:
       return launch_pdl(amax_kernel<__nv_bfloat16>, grid, dim3(256), 0, stream, static_cast<const __nv_bfloat16*>(x),
                         M_max, rows, H, amax, err);
+    default: return cudaErrorNotSupported;
+  }
+}
+
+cudaError_t launch_amax_parts(const void* x, int M_max, const int32_t* rows, int W, int part_w, rpp_dtype dtype,
+                              float* amax, int32_t* err, cudaStream_t stream) {
+  if (part_w <= 0 || part_w % 8 || W % part_w || W / part_w > 3) return cudaErrorInvalidValue;
+  const long long n8 = static_cast<long long>(M_max) * W / 8;
+  long long blocks = (n8 + 255) / 256;
+  const long long cap = static_cast<long long>(num_sms()) * 4;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  const dim3 grid(static_cast<unsigned>(blocks));
+  switch (dtype) {
+    case RPP_F16:
+      return launch_pdl(amax_parts_kernel<__half>, grid, dim3(256), 0, stream, static_cast<const __half*>(x), M_max,
+                        rows, W, part_w, amax, err);
+    case RPP_BF16:
+      return launch_pdl(amax_parts_kernel<__nv_bfloat16>, grid, dim3(256), 0, stream,
+                        static_cast<const __nv_bfloat16*>(x), M_max, rows, W, part_w, amax, err);
     default: return cudaErrorNotSupported;
   }
 }

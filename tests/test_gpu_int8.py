@@ -1,7 +1,9 @@
 """GPU parity of the INT8 path: weight and activation quantisation bit-exact, int32
 accumulators of the int8 GEMM bit-exact (including adversarial all-extreme inputs at
-the largest K), the calibration pass, and the int8 encoder layer within the int8
-tolerance (5e-2 on final outputs)."""
+the largest K), the calibration pass, the int8 encoder layer within the int8
+tolerance (5e-2 on final outputs), and the all-int8 flow: attention on codes (P's
+codes read back bit-exact where no code lies near a rounding tie, the output within
+the bound of a few flipped codes elsewhere) and the layer with int8 attention."""
 import numpy as np
 import pytest
 import torch
@@ -133,6 +135,124 @@ def test_calibration_matches_oracle():
     amax = rpp.encoder_layer_calibrate(prepared, x, cu, cfg.B, cfg.L, err=err)
     check_err(err)
     ref = oracle.calibrate_int8(wl["x_padded"], wl["lengths"], layer, cfg.nh, cfg.eps) * 127.0
+    ref_qkv = oracle.calibrate_int8_qkv(wl["x_padded"], wl["lengths"], layer, cfg.nh) * 127.0
     got = amax.cpu().numpy()
+    assert got.shape == (7,)
     assert got[0] == np.float32(np.abs(wl["x_padded"][np.arange(cfg.L)[None, :] < wl["lengths"][:, None]]).max())
-    assert np.allclose(got, ref, rtol=1e-2), (got, ref)
+    assert np.allclose(got[:4], ref, rtol=1e-2), (got, ref)
+    assert np.allclose(got[4:], ref_qkv, rtol=1e-2), (got, ref_qkv)
+
+
+# ---------------------------------------------------------------- int8 attention
+def _codes_case(seed, lengths, nh, spread=1.0):
+    rng = np.random.default_rng(seed)
+    lengths = np.asarray(lengths, np.int32)
+    T = int(lengths.sum())
+    T_max = max(T, 1) + 3
+    codes = rng.integers(-127, 128, size=(T_max, 3 * nh * 64)).astype(np.int64)
+    codes[:, :2 * nh * 64] = np.rint(codes[:, :2 * nh * 64] * spread).astype(np.int64)
+    codes = np.clip(codes, -127, 127)
+    err = rpp.new_error_word()
+    cu, _ = rpp.build_offsets(torch.as_tensor(lengths, device=dev()), int(max(1, lengths.max())), err=err)
+    return codes, cu, err, T
+
+
+def _run_i8_attention(codes, scales, cu, B, max_len, nh, err):
+    qkv = torch.as_tensor(codes.astype(np.float32), device=dev()).to(torch.bfloat16)
+    out = rpp.attention_varlen_i8(qkv, torch.as_tensor(np.asarray(scales, np.float32), device=dev()), cu, B, max_len,
+                                  nh, err=err)
+    torch.cuda.synchronize()
+    check_err(err)
+    return out.float().cpu().numpy().astype(np.float64)
+
+
+@pytest.mark.parametrize("lengths,nh", [([384, 1, 200, 129, 0, 64], 4), ([1000, 17], 2), ([128] * 40, 16)])
+def test_int8_attention_vs_oracle(lengths, nh):
+    """Random codes over ragged lengths (partial and whole tiles, one-token and empty
+    sequences, 1000 keys): the output within the effect of a few P codes flipped at a
+    rounding tie (each flip moves an output by at most s_v), nearly all outputs well inside."""
+    codes, cu, err, T = _codes_case(len(lengths) + nh, lengths, nh)
+    scales = (0.03, 0.025, 0.013)   # scores with a spread of several units: codes from 0 to 127
+    got = _run_i8_attention(codes, scales, cu, len(lengths), max(lengths), nh, err)
+    H = nh * 64
+    cc = codes[:T].astype(np.int8)
+    ref = oracle.attention_varlen_int8(cc[:, :H], cc[:, H:2 * H], cc[:, 2 * H:], *scales, cu.cpu().numpy(), nh)
+    d = np.abs(got[:T] - ref)
+    s_v = scales[2]
+    assert d.max() <= 3 * s_v, d.max()
+    assert (d > 2e-3 * s_v * 127).mean() < 0.02
+    assert d.mean() < s_v / 50
+
+
+def test_int8_attention_codes_read_back_exactly():
+    """V = 127 x one-hot rows (key j has code 127 in column j, head size 64, so up to 64
+    keys): O[q, j] = Pc[q, j] s_v, which reads P's codes back from the kernel.  Every code
+    whose 127 P (fp64) lies at least 1e-3 from a half-integer -- beyond the kernel's fp32
+    rounding of P -- must be reproduced bit-exactly (the integer scores Qc Kc^T, the
+    softmax and the coding are all checked); a code nearer a tie may be either neighbour."""
+    nh, lengths = 2, [64, 37, 5, 1, 50]
+    B, T = len(lengths), sum(lengths)
+    H = nh * 64
+    cu_np = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    scales = (0.02, 0.015, 0.5)
+    codes, cu, err, _ = _codes_case(1000, lengths, nh, spread=0.6)
+    codes[:, 2 * H:] = 0
+    for b in range(B):
+        for i in range(lengths[b]):
+            codes[cu_np[b] + i, 2 * H + i::64] = 127   # key i of its sequence: column i of every head
+    cc = codes[:T].astype(np.int8)
+    near_tie = np.zeros((T, H), bool)
+    for b in range(B):
+        lo, hi = cu_np[b], cu_np[b + 1]
+        for h in range(nh):
+            cs = slice(h * 64, (h + 1) * 64)
+            S = oracle.int8_gemm(cc[lo:hi, cs], cc[lo:hi, H:2 * H][:, cs].T).astype(np.float64)
+            z = S * scales[0] * scales[1] / 8.0
+            P = np.exp(z - z.max(axis=1, keepdims=True))
+            P /= P.sum(axis=1, keepdims=True)
+            frac = P * 127 - np.floor(P * 127)
+            near_tie[lo:hi, h * 64:h * 64 + (hi - lo)] = np.abs(frac - 0.5) < 1e-3
+    got = _run_i8_attention(codes, scales, cu, B, max(lengths), nh, err)
+    ref = oracle.attention_varlen_int8(cc[:, :H], cc[:, H:2 * H], cc[:, 2 * H:], *scales, cu_np, nh)
+    got_codes = np.rint(got[:T] / scales[2]).astype(np.int64)
+    ref_codes = np.rint(ref / scales[2]).astype(np.int64)
+    assert np.array_equal(got_codes[~near_tie], ref_codes[~near_tie])
+    assert np.abs(got_codes - ref_codes).max() <= 1
+    assert near_tie.mean() < 0.01
+    assert np.abs(got[:T] - got_codes * scales[2]).max() == 0   # outputs are exact multiples of s_v
+    assert ref_codes.max() > 60 and (ref_codes[:, :64] == 0).mean() > 0.1   # large and zero codes both occur
+
+
+def _int8_attn_case(wl, scales7):
+    cfg = wl["cfg"]
+    ecfg = rpp.encoder_cfg(cfg.H, cfg.nh, cfg.F, cfg.eps, "fp16", int8=2)
+    prepared = rpp.EncoderLayer(ecfg, wl["layers"][0])
+    lengths = torch.as_tensor(wl["lengths"], device=dev())
+    err = rpp.new_error_word()
+    cu, po = rpp.build_offsets(lengths, cfg.L, err=err)
+    x = rpp.remove_padding(up(wl["x_padded"].reshape(-1, cfg.H), "fp16"), po, cu, cfg.B, cfg.L, err=err)
+    y = rpp.encoder_layer_forward(prepared, x, cu, cfg.B, cfg.L, act_scales=torch.as_tensor(scales7, device=dev()),
+                                  err=err)
+    check_err(err)
+    return down(y), cu.cpu().numpy(), down(x)
+
+
+@pytest.mark.parametrize("full", [False, True])
+def test_int8_attention_layer(full):
+    """The all-int8 layer (QKV codes from the GEMM epilogue, attention on codes) against
+    the oracle's seven-scale layer: a small ragged batch, and the BERT-large-shaped int8
+    config with every sequence."""
+    cfg = INT8
+    if full:
+        wl = make_bert_workload(cfg)
+        cal = make_calibration_batch(cfg)
+    else:
+        wl = make_bert_workload(cfg, B=4, L=160, lengths=np.array([160, 1, 64, 129], np.int32), affine=True)
+        cal = wl
+    layer = wl["layers"][0]
+    s7 = np.concatenate([oracle.calibrate_int8(cal["x_padded"], cal["lengths"], layer, cfg.nh, cfg.eps),
+                         oracle.calibrate_int8_qkv(cal["x_padded"], cal["lengths"], layer, cfg.nh)])
+    got, cu, x = _int8_attn_case(wl, s7)
+    T = int(cu[-1])
+    ref = oracle.bert_layer_int8(x[:T], cu, oracle.prepare_int8_layer(layer), s7, cfg.nh, cfg.eps)
+    assert_close(got[:T], ref, "int8", f"all-int8 layer full={full}")
