@@ -295,32 +295,35 @@ rpp_status encoder_layer_run(const rpp_encoder_cfg* c, const void* layer, const 
   };
   if (!c->int8 && dt != RPP_F32 && !amax) {
     // proj and FC2 add their bias and the residual in the GEMM epilogue and write the
-    // pre-LayerNorm sum once, in fp16 ([SW] §3: bias split off the GEMM and fused into
-    // the op before LayerNorm; [KS] Fig. 7: each kernel's precision chosen for its
-    // values).  fp16's 11 significand bits keep the sum's rounding an eighth of a bf16
-    // step, and the LayerNorm reads 2 bytes per element instead of fp32 split-K slices.
-    // bf16 layers also keep LN1's output in fp16, as the FC2 residual, for the same reason.
-    void* hsum = h;   // [T_max, H] fp16 inside the split-K slice region
-    __half* x1h = dt == RPP_BF16 ? at<__half>(ws, W.x1f) : nullptr;
+    // pre-LayerNorm sum once ([SW] §3: bias split off the GEMM and fused into the op
+    // before LayerNorm; [KS] Fig. 7: each kernel's precision chosen for its values).
+    // fp16 layers keep the sum in fp16 (its rounding is that of the output).  bf16 layers
+    // keep it in fp32, and LN1 also writes x1 in fp32 as the FC2 residual: an fp16 sum and
+    // residual put the bf16 BERT-large layer above the 2e-2 bound (max-abs 2.09e-2, layer 8
+    // of 24), whose bf16 output rounding alone is 1.56e-2 for outputs in [4, 8).
+    const bool f32sum = dt == RPP_BF16;
+    const rpp_dtype sdt = f32sum ? RPP_F32 : RPP_F16;
+    void* hsum = h;   // [T_max, H] inside the split-K slice region
+    float* x1f = f32sum ? at<float>(ws, W.x1f) : nullptr;
     RPP_LAUNCH("gemm_qkv", s, linear(dt, x, at<void>(layer, P.wqkv), bqkv, nullptr, qkv, T_max, rows, 3 * H, H,
                                      RPP_EPI_BIAS, err, s, RPP_I8, RPP_I8, hint));
     RPP_LAUNCH("attention", s, launch_attention_varlen(qkv, cu, B, T_max, max_len, nh, d, dt, attn, err, s));
     RPP_LAUNCH("gemm_proj", s, linear(dt, attn, at<void>(layer, P.wo), bo, x, hsum, T_max, rows, H, H,
-                                      RPP_EPI_BIAS_RESIDUAL, err, s, RPP_F16, dt, hint));
+                                      RPP_EPI_BIAS_RESIDUAL, err, s, sdt, dt, hint));
     LnArgs l1 = ln_args(g1, be1);
     l1.x = hsum;
-    l1.in_dtype = RPP_F16;
+    l1.in_dtype = sdt;
     l1.y = x1;
-    l1.y16 = x1h;
+    l1.y32 = x1f;
     RPP_LAUNCH("layernorm1", s, launch_layernorm(l1, s));
     RPP_LAUNCH("gemm_fc1", s, linear(dt, x1, at<void>(layer, P.w1), b1, nullptr, g, T_max, rows, F, H,
                                      RPP_EPI_BIAS_GELU, err, s, RPP_I8, RPP_I8, hint));
-    RPP_LAUNCH("gemm_fc2", s, linear(dt, g, at<void>(layer, P.w2), b2, x1h ? static_cast<const void*>(x1h) : x1, hsum,
-                                     T_max, rows, H, F, RPP_EPI_BIAS_RESIDUAL, err, s, RPP_F16,
-                                     x1h ? RPP_F16 : dt, hint));
+    RPP_LAUNCH("gemm_fc2", s, linear(dt, g, at<void>(layer, P.w2), b2, x1f ? static_cast<const void*>(x1f) : x1, hsum,
+                                     T_max, rows, H, F, RPP_EPI_BIAS_RESIDUAL, err, s, sdt, x1f ? RPP_F32 : dt,
+                                     hint));
     LnArgs l2 = ln_args(g2, be2);
     l2.x = hsum;
-    l2.in_dtype = RPP_F16;
+    l2.in_dtype = sdt;
     l2.y = y;
     RPP_LAUNCH(pad.y ? "layernorm2_rebuild" : "layernorm2", s, launch_layernorm(final_ln(l2), s));
     return RPP_OK;

@@ -301,7 +301,6 @@ __global__ void __launch_bounds__(128) layernorm_kernel(LnArgs a) {
       }
       store_vec<TOut, EPV>(yr + col0, o);
       if (!valid) continue;
-      if (a.y16) store_vec<__half, EPV>(a.y16 + dst * H + col0, o);   // fp16 copy (the next residual)
       if (a.y32) {   // fp32 copy of the normalised row (the next residual add reads it)
         float* yf = a.y32 + dst * H + col0;
 #pragma unroll
@@ -385,27 +384,31 @@ __global__ void amax_kernel(const T* __restrict__ x, int M_max, const int32_t* r
   if (lane_id() == 0) atomic_max_nonneg(amax, m);
 }
 
-// ---------------------------------------------------------------- streaming 16-bit rows
-// LayerNorm of rows that arrive complete in a 16-bit type (the fp16 pre-LayerNorm sums of
-// a 16-bit layer): no slices, bias or residual to add.  One warp per row with H = 256 VPL
+// ---------------------------------------------------------------- streaming rows
+// LayerNorm of rows that arrive complete (the pre-LayerNorm sums that the proj and FC2
+// GEMMs write with bias and residual already added: fp16 in 16-bit layers, fp32 in bf16
+// layers): no slices, bias or residual to add.  One warp per row with H = 32 VPL EPV
 // (lane l holds the 16-byte vectors l, l + 32, ...), the next row's vectors in flight
 // while this one is normalised, and the arithmetic on packed fp32 pairs (one f32x2
 // instruction per two elements).  Statistics as in the general kernel: fp32, two passes
-// over the registers, biased variance.  Padded-output mode as in the general kernel.
-constexpr int kLn16Threads = 256;
+// over the registers, biased variance.  Optional fp32 copy of the output, and the
+// padded-output mode of the general kernel.
+constexpr int kLnsThreads = 256;
 
 template <typename TIn, typename TOut, int VPL>
-__global__ void __launch_bounds__(kLn16Threads) ln16_kernel(LnArgs a) {
-  constexpr int H = 256 * VPL;
-  constexpr int kQ = H / 4;   // float4 quarters of a parameter vector
-  constexpr int kPre = (kQ + kLn16Threads - 1) / kLn16Threads;
-  constexpr int kWarps = kLn16Threads / 32;
+__global__ void __launch_bounds__(kLnsThreads) ln_stream_kernel(LnArgs a) {
+  constexpr int EPV = Vec<TIn>::N;   // elements per 16-byte vector: 8 (16-bit) or 4 (fp32)
+  constexpr int E4 = EPV / 4;        // float4 quarters per vector
+  constexpr int H = 32 * VPL * EPV;
+  constexpr int kQ = H / 4;          // float4 quarters of a parameter vector
+  constexpr int kPre = (kQ + kLnsThreads - 1) / kLnsThreads;
+  constexpr int kWarps = kLnsThreads / 32;
   // gamma and beta are layer weights, not written by the preceding launch: read before
   // the grid-dependency wait
   float4 pg[kPre], pb[kPre];
 #pragma unroll
   for (int k = 0; k < kPre; ++k) {
-    const int qd = threadIdx.x + k * kLn16Threads;
+    const int qd = threadIdx.x + k * kLnsThreads;
     if (qd < kQ) {
       pg[k] = __ldg(reinterpret_cast<const float4*>(a.gamma) + qd);
       pb[k] = __ldg(reinterpret_cast<const float4*>(a.beta) + qd);
@@ -418,9 +421,9 @@ __global__ void __launch_bounds__(kLn16Threads) ln16_kernel(LnArgs a) {
   __shared__ float4 s_g[kQ], s_b[kQ];
 #pragma unroll
   for (int k = 0; k < kPre; ++k) {
-    const int qd = threadIdx.x + k * kLn16Threads;
+    const int qd = threadIdx.x + k * kLnsThreads;
     if (qd < kQ) {
-      const int slot = param_slot<32, 8>(qd);
+      const int slot = param_slot<32, EPV>(qd);
       s_g[slot] = pg[k];
       s_b[slot] = pb[k];
     }
@@ -453,34 +456,41 @@ __global__ void __launch_bounds__(kLn16Threads) ln16_kernel(LnArgs a) {
 #pragma unroll
     for (int i = 0; i < VPL; ++i) r[i] = src >= 0 ? xr[i * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
   };
+  constexpr int NP = VPL * EPV / 2;   // fp32 pairs per lane
   unsigned it = blockIdx.x * kWarps + warp_id();
   int src = src_of(it);
   uint4 nx[VPL];
   load_row(src, nx);
   for (; it < n_iter; it += stride) {
-    uint4 cur[VPL];
+    uint64_t v[NP];
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) cur[i] = nx[i];
+    for (int i = 0; i < VPL; ++i) {
+      float f[EPV];
+      unpack16<TIn>(nx[i], f);
+#pragma unroll
+      for (int h = 0; h < EPV / 2; ++h) v[i * (EPV / 2) + h] = f2_pack(f[2 * h], f[2 * h + 1]);
+    }
     const int src_next = src_of(it + stride);
     load_row(src_next, nx);
     TOut* yr = y + static_cast<size_t>(it) * H;
     if (src < 0) {   // pad slot of the padded output
+      constexpr int OV = sizeof(TOut) * EPV / 16 > 0 ? sizeof(TOut) * EPV / 16 : 1;   // 16-byte stores per vector
 #pragma unroll
-      for (int i = 0; i < VPL; ++i) *reinterpret_cast<uint4*>(yr + (i * 32 + lane) * 8) = make_uint4(0u, 0u, 0u, 0u);
+      for (int i = 0; i < VPL; ++i) {
+        if constexpr (sizeof(TOut) * EPV >= 16) {
+#pragma unroll
+          for (int u = 0; u < OV; ++u)
+            reinterpret_cast<uint4*>(yr + (i * 32 + lane) * EPV)[u] = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+          *reinterpret_cast<uint2*>(yr + (i * 32 + lane) * EPV) = make_uint2(0u, 0u);
+        }
+      }
       src = src_next;
       continue;
     }
-    uint64_t v[4 * VPL];
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      float f[8];
-      unpack16<TIn>(cur[i], f);
-#pragma unroll
-      for (int h = 0; h < 4; ++h) v[4 * i + h] = f2_pack(f[2 * h], f[2 * h + 1]);
-    }
     uint64_t s2a = v[0], s2b = v[1];
 #pragma unroll
-    for (int k = 2; k < 4 * VPL; k += 2) {
+    for (int k = 2; k < NP; k += 2) {
       s2a = f2_add(s2a, v[k]);
       s2b = f2_add(s2b, v[k + 1]);
     }
@@ -492,7 +502,7 @@ __global__ void __launch_bounds__(kLn16Threads) ln16_kernel(LnArgs a) {
     const uint64_t nm = f2_pack(-mean, -mean);
     uint64_t q2a = 0ull, q2b = 0ull;
 #pragma unroll
-    for (int k = 0; k < 4 * VPL; k += 2) {
+    for (int k = 0; k < NP; k += 2) {
       v[k] = f2_add(v[k], nm);
       v[k + 1] = f2_add(v[k + 1], nm);
       q2a = f2_fma(v[k], v[k], q2a);
@@ -506,33 +516,39 @@ __global__ void __launch_bounds__(kLn16Threads) ln16_kernel(LnArgs a) {
     const uint64_t r2 = f2_pack(rstd, rstd);
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
-      float o[8];
+      float o[EPV];
 #pragma unroll
-      for (int j4 = 0; j4 < 2; ++j4) {
-        const float4 g4 = s_g[(i * 2 + j4) * 32 + lane];
-        const float4 b4 = s_b[(i * 2 + j4) * 32 + lane];
-        const uint64_t o0 = f2_fma(v[4 * i + 2 * j4], f2_mul(f2_pack(g4.x, g4.y), r2), f2_pack(b4.x, b4.y));
-        const uint64_t o1 = f2_fma(v[4 * i + 2 * j4 + 1], f2_mul(f2_pack(g4.z, g4.w), r2), f2_pack(b4.z, b4.w));
+      for (int j4 = 0; j4 < E4; ++j4) {
+        const float4 g4 = s_g[(i * E4 + j4) * 32 + lane];
+        const float4 b4 = s_b[(i * E4 + j4) * 32 + lane];
+        const int k0 = i * (EPV / 2) + 2 * j4;
+        const uint64_t o0 = f2_fma(v[k0], f2_mul(f2_pack(g4.x, g4.y), r2), f2_pack(b4.x, b4.y));
+        const uint64_t o1 = f2_fma(v[k0 + 1], f2_mul(f2_pack(g4.z, g4.w), r2), f2_pack(b4.z, b4.w));
         o[4 * j4 + 0] = f2_lo(o0); o[4 * j4 + 1] = f2_hi(o0);
         o[4 * j4 + 2] = f2_lo(o1); o[4 * j4 + 3] = f2_hi(o1);
       }
-      const int col0 = (i * 32 + lane) * 8;
-      store_vec<TOut, 8>(yr + col0, o);
-      if (a.y16) store_vec<__half, 8>(a.y16 + static_cast<size_t>(it) * H + col0, o);
+      const int col0 = (i * 32 + lane) * EPV;
+      store_vec<TOut, EPV>(yr + col0, o);
+      if (a.y32) {
+        float* yf = a.y32 + static_cast<size_t>(it) * H + col0;
+#pragma unroll
+        for (int j = 0; j < EPV; j += 4)
+          *reinterpret_cast<float4*>(yf + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+      }
     }
     src = src_next;
   }
 }
 
 template <typename TIn, typename TOut, int VPL>
-cudaError_t ln16_launch(const LnArgs& a, cudaStream_t stream) {
-  constexpr int kWarps = kLn16Threads / 32;
+cudaError_t ln_stream_launch(const LnArgs& a, cudaStream_t stream) {
+  constexpr int kWarps = kLnsThreads / 32;
   const long long n_iter = a.pad_cu ? static_cast<long long>(a.pad_B) * a.pad_L : a.M_max;
   long long blocks = (n_iter + kWarps - 1) / kWarps;
   static int per_sm = 0;   // one wave of resident blocks: the row loop is grid-strided
   if (per_sm == 0) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ln16_kernel<TIn, TOut, VPL>, kLn16Threads, 0) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ln_stream_kernel<TIn, TOut, VPL>, kLnsThreads, 0) !=
             cudaSuccess || n < 1)
       n = 2;
     per_sm = n;
@@ -540,27 +556,34 @@ cudaError_t ln16_launch(const LnArgs& a, cudaStream_t stream) {
   const long long cap = static_cast<long long>(num_sms()) * per_sm;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  return launch_pdl(ln16_kernel<TIn, TOut, VPL>, dim3(static_cast<unsigned>(blocks)), dim3(kLn16Threads), 0,
+  return launch_pdl(ln_stream_kernel<TIn, TOut, VPL>, dim3(static_cast<unsigned>(blocks)), dim3(kLnsThreads), 0,
                     stream, a);
 }
 
+// vectors per lane of a supported row width (H = 32 VPL EPV), else 0
+int ln_stream_vpl(int H, rpp_dtype in) {
+  const int epv = in == RPP_F32 ? 4 : 8;
+  if (H % (32 * epv)) return 0;
+  const int v = H / (32 * epv);
+  return (v == 1 || v == 2 || v == 3 || v == 4 || v == 6 || v == 8) ? v : 0;
+}
+
 template <typename TIn, typename TOut>
-cudaError_t ln16_dispatch(const LnArgs& a, cudaStream_t stream) {
-  switch (a.H / 256) {
-    case 1: return ln16_launch<TIn, TOut, 1>(a, stream);
-    case 2: return ln16_launch<TIn, TOut, 2>(a, stream);
-    case 3: return ln16_launch<TIn, TOut, 3>(a, stream);
-    case 4: return ln16_launch<TIn, TOut, 4>(a, stream);
-    case 6: return ln16_launch<TIn, TOut, 6>(a, stream);
+cudaError_t ln_stream_dispatch(const LnArgs& a, cudaStream_t stream) {
+  switch (ln_stream_vpl(a.H, a.in_dtype)) {
+    case 1: return ln_stream_launch<TIn, TOut, 1>(a, stream);
+    case 2: return ln_stream_launch<TIn, TOut, 2>(a, stream);
+    case 3: return ln_stream_launch<TIn, TOut, 3>(a, stream);
+    case 4: return ln_stream_launch<TIn, TOut, 4>(a, stream);
+    case 6: return ln_stream_launch<TIn, TOut, 6>(a, stream);
+    case 8: return ln_stream_launch<TIn, TOut, 8>(a, stream);
     default: return cudaErrorNotSupported;
   }
 }
 
-bool ln16_applies(const LnArgs& a) {
-  const int v = a.H / 256;
-  return (a.in_dtype == RPP_F16 || a.in_dtype == RPP_BF16) && a.out_dtype != RPP_F32 && a.n_in == 1 &&
-         !a.residual && !a.add_bias && !a.q_codes && !a.amax && !a.y32 && a.H % 256 == 0 &&
-         (v == 1 || v == 2 || v == 3 || v == 4 || v == 6);
+bool ln_stream_applies(const LnArgs& a) {
+  return a.out_dtype != RPP_F32 && a.n_in == 1 && !a.residual && !a.add_bias && !a.q_codes && !a.amax &&
+         ln_stream_vpl(a.H, a.in_dtype) > 0;
 }
 
 // max |x| of each part of [M, W] rows cut into column parts of width part_w (at most
@@ -677,10 +700,12 @@ cudaError_t launch_layernorm(const LnArgs& args, cudaStream_t stream) {
   if (a.pad_cu && (a.pad_B <= 0 || a.pad_L <= 0)) return cudaErrorInvalidValue;
   if (a.pad_cu && static_cast<long long>(a.pad_B) * a.pad_L > 0x7fffffffLL) return cudaErrorNotSupported;
   using BF = __nv_bfloat16;
-  if (ln16_applies(a)) {
-    if (a.in_dtype == RPP_F16 && a.out_dtype == RPP_F16) return ln16_dispatch<__half, __half>(a, stream);
-    if (a.in_dtype == RPP_F16 && a.out_dtype == RPP_BF16) return ln16_dispatch<__half, BF>(a, stream);
-    if (a.in_dtype == RPP_BF16 && a.out_dtype == RPP_BF16) return ln16_dispatch<BF, BF>(a, stream);
+  if (ln_stream_applies(a)) {
+    if (a.in_dtype == RPP_F16 && a.out_dtype == RPP_F16) return ln_stream_dispatch<__half, __half>(a, stream);
+    if (a.in_dtype == RPP_F16 && a.out_dtype == RPP_BF16) return ln_stream_dispatch<__half, BF>(a, stream);
+    if (a.in_dtype == RPP_BF16 && a.out_dtype == RPP_BF16) return ln_stream_dispatch<BF, BF>(a, stream);
+    if (a.in_dtype == RPP_F32 && a.out_dtype == RPP_BF16) return ln_stream_dispatch<float, BF>(a, stream);
+    if (a.in_dtype == RPP_F32 && a.out_dtype == RPP_F16) return ln_stream_dispatch<float, __half>(a, stream);
   }
   if (a.in_dtype == a.out_dtype) {
     switch (a.in_dtype) {
