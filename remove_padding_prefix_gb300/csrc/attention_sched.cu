@@ -41,20 +41,17 @@
 // mbarrier wait is bounded; a wait that gives up records RPP_DERR_TIMEOUT, raises the
 // CTA's abort flag, and the CTA drains its copies and MMAs, frees tensor memory and
 // exits.
-#include "kernels.h"
+#include "attention_common.cuh"
 
 namespace rpp {
 
 namespace {
 
-constexpr int kT = 128;                        // queries per item, keys per tile
-constexpr int kDh = 64;                        // head size
+using namespace attn;
+
 constexpr int kThreads = 320;                  // warp 0 TMA, warp 1 MMA, warps 2..9 softmax
-constexpr uint32_t kTile = kT * kDh * 2;       // one 128 x 64 tile of Q, K or V (16 KB)
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0, kColP = 128, kColO = 192;
-constexpr int kMaxCls = 64;                    // tiles per sequence: max_len <= 8192
-constexpr int kMaxB = 2048;                    // sequences per batch (two CTAs per SM still fit)
 
 // shared-memory layout (bytes from the 1024-aligned base)
 constexpr uint32_t kOffQ = 0;                  // [2] tiles
@@ -63,73 +60,9 @@ constexpr uint32_t kOffV = 4 * kTile;          // [2]
 constexpr uint32_t kOffBar = 6 * kTile;        // 16 mbarriers
 constexpr uint32_t kOffMisc = kOffBar + 16 * 8;   // tmem slot, abort flag, counts, more barriers
 constexpr uint32_t kOffX = kOffMisc + 128;      // pair exchange: float [2 parities][2 halves][128 rows]
-constexpr uint32_t kOffCls = kOffX + 2 * 2 * 128 * 4;   // 4 int arrays of kMaxCls + 2
-constexpr uint32_t kOffPerm = kOffCls + 4 * (kMaxCls + 2) * 4;   // int16 [B], then cu_seqlens int32 [B + 1]
+constexpr uint32_t kOffSched = kOffX + 2 * 2 * 128 * 4;   // the item list (sched_bytes(B))
 
-__host__ __device__ constexpr uint32_t perm_bytes(int B) { return (static_cast<uint32_t>(B) * 2u + 15u) & ~15u; }
-size_t smem_bytes(int B) { return 1024 + kOffPerm + perm_bytes(B) + ((static_cast<size_t>(B + 1) * 4 + 15) & ~15ull); }
-
-__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
-
-template <typename T> struct Fmt;
-template <> struct Fmt<__half> { static constexpr int v = 0; };
-template <> struct Fmt<__nv_bfloat16> { static constexpr int v = 1; };
-
-template <typename T>
-__device__ __forceinline__ uint32_t pack2(float a, float b);   // a -> low half (the even key)
-template <>
-__device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
-  __half2 h = __floats2half2_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-template <>
-__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&h);
-}
-
-
-// D[tmem] (+)= A[tmem] * B[smem], kind::f16: A (M x K, one row per lane, two 16-bit
-// elements per 32-bit column) from tensor memory
-__device__ __forceinline__ void tc_mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                                  uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// The CTA-wide item list: sequences grouped by tile count (largest first), items of a
-// sequence in (head, q-tile) order.
-struct Sched {
-  const int* item_off;   // [c]: first item of tile count c (c = n_cls .. 1), item_off[0] = total
-  const int* seq_off;    // [c]: first position in perm of the sequences with c tiles
-  const int16_t* perm;   // sequence indices, grouped
-  const int* cu;         // cu_seqlens, copied into shared memory
-  int n_cls, nh;
-};
-struct Item {
-  int b, h, q0, c0, len, ntiles;
-};
-__device__ __forceinline__ Item decode(const Sched& s, int g) {
-  int c = s.n_cls;
-  while (c > 1 && g >= s.item_off[c - 1]) --c;   // classes laid out n_cls, n_cls - 1, ...: item_off decreasing in c
-  // g lies in class c: [item_off[c], item_off[c - 1])
-  const int idx = g - s.item_off[c];
-  const int per_seq = s.nh * c;
-  const int sq = idx / per_seq;
-  const int rem = idx - sq * per_seq;
-  Item it;
-  it.b = s.perm[s.seq_off[c] + sq];
-  it.h = rem / c;
-  it.q0 = (rem - it.h * c) * kT;
-  it.c0 = s.cu[it.b];
-  it.len = s.cu[it.b + 1] - it.c0;
-  it.ntiles = c;
-  return it;
-}
+size_t smem_bytes(int B) { return 1024 + kOffSched + sched_bytes(B); }
 
 // I8: Q, K and V are int8 codes held in bf16 (exact), i8_scales = (s_q, s_k, s_v) in
 // device memory, and every item takes two passes over its key tiles: the first computes
@@ -163,13 +96,6 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int* s_status = reinterpret_cast<int*>(smem + kOffMisc + 8);   // 0 ok, else the device error to record / quit
-  int* cls_cnt = reinterpret_cast<int*>(smem + kOffCls);
-  int* seq_off = cls_cnt + (kMaxCls + 2);
-  int* item_off = seq_off + (kMaxCls + 2);
-  int* cursor = item_off + (kMaxCls + 2);
-  int16_t* perm = reinterpret_cast<int16_t*>(smem + kOffPerm);
-  int* s_cu = reinterpret_cast<int*>(smem + kOffPerm + perm_bytes(B));
-
   const int warp = warp_id();
   const int lane = lane_id();
 
@@ -177,56 +103,9 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
   pdl_wait();
   pdl_trigger();
 
-  if (threadIdx.x == 0) {
-    *s_status = device_error_set(err) ? -1 : 0;   // -1: quit without recording
-    *abort_flag = 0;
-  }
-  for (int c = threadIdx.x; c < kMaxCls + 2; c += kThreads) cls_cnt[c] = 0;
-  __syncthreads();
-  if (*s_status) return;
-
-  // ---- item list: tile counts per sequence (all threads), then a stable grouping (warp 0);
-  // cu_seqlens is kept in shared memory for the item decoding of every role
-  for (int b = threadIdx.x; b <= B; b += kThreads) s_cu[b] = __ldg(cu + b);
-  __syncthreads();
-  for (int b = threadIdx.x; b < B; b += kThreads) {
-    const int c0 = s_cu[b], c1 = s_cu[b + 1], len = c1 - c0;
-    if (c0 < 0 || len < 0 || c1 > T_max || len > max_len) {
-      atomicCAS(s_status, 0, len > max_len ? RPP_DERR_LENGTH : RPP_DERR_ROWS);
-    } else {
-      atomicAdd(&cls_cnt[(len + kT - 1) / kT], 1);
-    }
-  }
-  __syncthreads();
-  if (*s_status) {
-    if (threadIdx.x == 0 && *s_status > 0) set_device_error(err, *s_status);
-    return;
-  }
-  if (threadIdx.x == 0) {
-    int so = 0, io = 0;
-    for (int c = n_cls; c >= 1; --c) {   // largest tile count first
-      seq_off[c] = so;
-      item_off[c] = io;
-      cursor[c] = so;
-      so += cls_cnt[c];
-      io += cls_cnt[c] * nh * c;
-    }
-    item_off[0] = io;   // the total, which is also where class 1 ends
-  }
-  __syncthreads();
-  if (warp == 0) {
-    for (int b0 = 0; b0 < B; b0 += 32) {
-      const int b = b0 + lane;
-      int c = -1;
-      if (b < B) c = (s_cu[b + 1] - s_cu[b] + kT - 1) / kT;
-      const unsigned peers = __match_any_sync(0xffffffffu, c);
-      const int rank = __popc(peers & ((1u << lane) - 1u));
-      if (c > 0) perm[cursor[c] + rank] = static_cast<int16_t>(b);
-      __syncwarp();
-      if (c > 0 && rank == 0) cursor[c] += __popc(peers);
-      __syncwarp();
-    }
-  }
+  if (threadIdx.x == 0) *abort_flag = 0;
+  Sched sch;
+  if (!build_items(cu, B, T_max, max_len, nh, n_cls, err, s_status, smem + kOffSched, sch)) return;
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&q_full[i], 1);
@@ -246,7 +125,7 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
     fence_mbarrier_init();
     tma_prefetch_desc(&tm);
   }
-  const int n_items = item_off[0];
+  const int n_items = sch.item_off[0];
   if (static_cast<int>(blockIdx.x) >= n_items) return;   // uniform: nothing allocated yet
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -257,7 +136,6 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int H = nh * kDh;
-  const Sched sch{item_off, seq_off, perm, s_cu, n_cls, nh};
   uint8_t* sQ = smem + kOffQ;
   uint8_t* sK = smem + kOffK;
   uint8_t* sV = smem + kOffV;
