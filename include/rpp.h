@@ -99,6 +99,14 @@ RPP_API rpp_status rpp_set_launch_events(void* const* events, int capacity);
  * fp32 summation order.  Process-wide, not thread-safe; RPP_EINVAL outside 0..2. */
 RPP_API rpp_status rpp_set_gemm_cluster_mode(int mode);
 
+/* TEST / TUNING ONLY -- not part of the method's calls.  Process-wide knob of the
+ * tensor-core GEMMs: 0 (default) lets the per-shape heuristic choose the tile width
+ * (the number of output columns a CTA or CTA pair computes per unit); one of 16, 32, 48,
+ * 64, 96, 128, 144, 192, 256 forces that width wherever it divides N (and is allowed for
+ * the epilogue).  Results are the same for every width.  Process-wide, not thread-safe;
+ * RPP_EINVAL for other values. */
+RPP_API rpp_status rpp_set_gemm_tile_width(int bn);
+
 /* TEST ONLY -- exercises the failure detection of the bounded waits (no counterpart in
  * the pages).  The next fp16 / bf16 / int8 tensor-core GEMM launch of this process issues
  * no operand loads, and its pipeline waits give up after `limit_us` microseconds instead

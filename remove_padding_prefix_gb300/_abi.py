@@ -52,6 +52,7 @@ SIGNATURES = {
     "rpp_set_launch_events": (i32, [C.POINTER(vp), i32]),
     "rpp_set_launch_event_filter": (i32, [C.c_char_p]),
     "rpp_set_gemm_cluster_mode": (i32, [i32]),
+    "rpp_set_gemm_tile_width": (i32, [i32]),
     "rpp_test_stall_next_gemm": (i32, [C.c_uint]),
     "rpp_launch_event_count": (i32, []),
     "rpp_launch_event_label": (C.c_char_p, [i32]),

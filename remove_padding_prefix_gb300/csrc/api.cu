@@ -518,6 +518,16 @@ rpp_status rpp_set_gemm_cluster_mode(int mode) {
   return RPP_OK;
 }
 
+rpp_status rpp_set_gemm_tile_width(int bn) {
+  static const int ok[] = {0, 16, 32, 48, 64, 96, 128, 144, 192, 256};
+  for (int v : ok)
+    if (bn == v) {
+      set_gemm_force_bn(bn);
+      return RPP_OK;
+    }
+  return RPP_EINVAL;
+}
+
 rpp_status rpp_test_stall_next_gemm(unsigned int limit_us) {
   if (limit_us == 0 || limit_us > 1000000u) return RPP_EINVAL;
   set_gemm_stall_next(static_cast<unsigned long long>(limit_us) * 1000ull);

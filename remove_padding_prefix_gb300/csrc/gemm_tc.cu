@@ -129,7 +129,11 @@ TileChoice choose_tiles(int M, int N, int K, int max_bn, int max_splits, int cl 
       // epilogue takes as long as its busiest warp (each of the wpq warps of a lane
       // quadrant takes every wpq-th 32-column slice); with more, it overlaps the next
       // unit's MMAs and only its size counts.
-      const double epi = kps <= 4 ? 6.0 * 32.0 * wpq * ((bn + 32 * wpq - 1) / (32 * wpq)) : 6.0 * bn;
+      double epi = kps <= 4 ? 6.0 * 32.0 * wpq * ((bn + 32 * wpq - 1) / (32 * wpq)) : 6.0 * bn;
+      // a 16-column tail leaves through per-row stores instead of the TMA store: where the
+      // epilogue sets the pace it costs about three 32-column slices (measured on the Swin
+      // QKV GEMM, N = 288, K = 96: 144-column tiles 58.4 us, 96-column tiles 51.3 us)
+      if (kps <= 4 && bn % 32 == 16) epi += 3.0 * 6.0 * 32.0;
       const double cost = static_cast<double>(waves) * (kps * (bn + 32.0) + epi) + (sp - 1) * 64.0;
       if (cost < best_cost - 1e-9) {
         best_cost = cost;
@@ -151,9 +155,11 @@ bool gemm_tc_supported(int N, int K) {
 namespace {
 int g_cluster_mode = 0;   // 0 automatic, 1 never, 2 always (where the GEMM has two row tiles)
 unsigned long long g_stall_next_ns = 0;   // test hook: nonzero = the next launch stalls, waits give up after this
+int g_force_bn = 0;       // tuning hook: nonzero = this tile width wherever it divides N
 }
 
 void set_gemm_cluster_mode(int mode) { g_cluster_mode = mode; }
+void set_gemm_force_bn(int bn) { g_force_bn = bn; }
 void set_gemm_stall_next(unsigned long long limit_ns) { g_stall_next_ns = limit_ns; }
 
 cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t stream) {
@@ -178,6 +184,7 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t stream) {
   const int wpq = g.epi == RPP_EPI_BIAS_GELU ? epi_warps<RPP_EPI_BIAS_GELU>() / 4 : 2;
   TileChoice tc = choose_tiles(rows_hint, g.N, g.K, max_bn, can_split ? g.max_splits : 1, cl, wpq);
   if (g.force_bn) tc.bn = g.force_bn;
+  else if (g_force_bn && g.N % g_force_bn == 0 && g_force_bn <= max_bn) tc.bn = g_force_bn;
   const int bn = tc.bn;
   if (!bn || g.N % bn || bn > max_bn) return cudaErrorNotSupported;
   if (g.splits_out) *g.splits_out = tc.splits;

@@ -118,6 +118,8 @@ bool gemm_tc_supported(int N, int K);
 cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t stream);
 // 0 automatic, 1 never cluster, 2 cluster whenever the GEMM is fp16/bf16
 void set_gemm_cluster_mode(int mode);
+// tuning hook: 0 = the tile-width heuristic, else this width wherever it divides N
+void set_gemm_force_bn(int bn);
 // test hook: the next tensor-core GEMM launch issues no operand loads and its pipeline
 // waits give up after limit_ns (it records RPP_DERR_TIMEOUT and exits cleanly)
 void set_gemm_stall_next(unsigned long long limit_ns);

@@ -117,6 +117,14 @@ def test_patch_merge_size_queries_and_validation(lib):
     assert lib.rpp_patch_merge_forward(C.byref(ok), None, 1, None, None, None, 0, None, None) == -1
 
 
+def test_tile_width_hook_rejects_other_values(lib):
+    """The tuning hook takes 0 or a tile width the GEMM instantiates (no launch here)."""
+    for bad in (-1, 1, 100, 512):
+        assert lib.rpp_set_gemm_tile_width(bad) != 0
+    for ok in (0, 64, 256, 0):
+        assert lib.rpp_set_gemm_tile_width(ok) == 0
+
+
 def test_stall_hook_rejects_out_of_range_limits(lib):
     """The test-only stall hook takes 1 us .. 1 s and nothing else (no launch here)."""
     assert lib.rpp_test_stall_next_gemm(0) == -1
