@@ -129,11 +129,7 @@ TileChoice choose_tiles(int M, int N, int K, int max_bn, int max_splits, int cl 
       // epilogue takes as long as its busiest warp (each of the wpq warps of a lane
       // quadrant takes every wpq-th 32-column slice); with more, it overlaps the next
       // unit's MMAs and only its size counts.
-      double epi = kps <= 4 ? 6.0 * 32.0 * wpq * ((bn + 32 * wpq - 1) / (32 * wpq)) : 6.0 * bn;
-      // a 16-column tail leaves through per-row stores instead of the TMA store: where the
-      // epilogue sets the pace it costs about three 32-column slices (measured on the Swin
-      // QKV GEMM, N = 288, K = 96: 144-column tiles 58.4 us, 96-column tiles 51.3 us)
-      if (kps <= 4 && bn % 32 == 16) epi += 3.0 * 6.0 * 32.0;
+      const double epi = kps <= 4 ? 6.0 * 32.0 * wpq * ((bn + 32 * wpq - 1) / (32 * wpq)) : 6.0 * bn;
       const double cost = static_cast<double>(waves) * (kps * (bn + 32.0) + epi) + (sp - 1) * 64.0;
       if (cost < best_cost - 1e-9) {
         best_cost = cost;
