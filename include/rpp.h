@@ -91,8 +91,8 @@ RPP_API rpp_status rpp_set_launch_events(void* const* events, int capacity);
 /* TEST / TUNING ONLY -- not part of the method's calls.  Process-wide knob of the
  * fp16 / bf16 tensor-core GEMMs (no counterpart in the pages):
  * 0 (default) pairs CTAs into two-CTA clusters running cta_group::2 MMAs on 256-row
- * tiles (each CTA holds its 128 A rows and half of the weight tile) when K >= 1024 and
- * the expected row count is >= 8192; 1 never pairs; 2 always pairs.  The exact int8
+ * tiles (each CTA holds its 128 A rows and half of the weight tile) when K >= 1024, the
+ * expected row count is >= 8192 and N or K is >= 2048; 1 never pairs; 2 always pairs.  The exact int8
  * GEMM always runs unpaired (pairs measured no faster there).
  * The arithmetic per output element is the same in every mode, except that the
  * tile shape and K split are chosen per mode, and a different K split changes the
