@@ -174,7 +174,7 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, cudaStream_t stream) {
   // Pairs pay off when the MMAs dominate (long K, many row tiles, wide N); short-K or
   // few-tile GEMMs are epilogue- or latency-bound and run unpaired, and so does a square
   // 1024 x 1024 GEMM (the BERT-large proj: 33.8 us unpaired against 35.7 paired at
-  // 12 555 rows, bias epilogue).
+  // 12 555 rows, bias epilogue, standalone; inside the step the two are within noise).
   const bool pair_auto = rows_hint >= 8192 && g.K >= 1024 && (g.N >= 2048 || g.K >= 2048);
   int cl = (!is_int && (g_cluster_mode == 2 || (g_cluster_mode == 0 && pair_auto))) ? 2 : 1;
   const int wpq = g.epi == RPP_EPI_BIAS_GELU ? epi_warps<RPP_EPI_BIAS_GELU>() / 4 : 2;
