@@ -396,13 +396,20 @@ rpp_status encoder_layer_run(const rpp_encoder_cfg* c, const void* layer, const 
     RPP_LAUNCH("gemm_qkv_i8", s, linear_i8(cx, at<void>(layer, P.wqkv), bqkv, s0, at<float>(layer, P.sqkv), sqkv,
                                             nullptr, qkv, RPP_BF16, T_max, rows, 3 * H, H, EPI_DQ_BIAS_Q3, err, s,
                                             hint));
-    RPP_LAUNCH("attention_i8", s, launch_attention_sched(qkv, cu, B, T_max, max_len, nh, RPP_BF16, attn, err, s, sqkv));
+    // the attention also writes the codes of its output at s1 (the proj GEMM's input)
+    RPP_LAUNCH("attention_i8", s,
+               launch_attention_sched(qkv, cu, B, T_max, max_len, nh, RPP_BF16, ca, err, s, sqkv, s1));
   } else {
     RPP_LAUNCH("gemm_qkv_i8", s, linear_i8(cx, at<void>(layer, P.wqkv), bqkv, s0, at<float>(layer, P.sqkv), nullptr,
                                             nullptr, qkv, dt, T_max, rows, 3 * H, H, EPI_DQ_BIAS, err, s, hint));
-    RPP_LAUNCH("attention", s, launch_attention_varlen(qkv, cu, B, T_max, max_len, nh, d, dt, attn, err, s));
+    if (d == 64 && attention_sched_supported(B, max_len)) {   // quantisation fused into the attention's output
+      RPP_LAUNCH("attention", s,
+                 launch_attention_sched(qkv, cu, B, T_max, max_len, nh, dt, ca, err, s, nullptr, s1));
+    } else {
+      RPP_LAUNCH("attention", s, launch_attention_varlen(qkv, cu, B, T_max, max_len, nh, d, dt, attn, err, s));
+      RPP_LAUNCH("quantize_attn", s, launch_quantize_codes_bf16(attn, s1, ca, T_max, rows, H, dt, err, s));
+    }
   }
-  RPP_LAUNCH("quantize_attn", s, launch_quantize_codes_bf16(attn, s1, ca, T_max, rows, H, dt, err, s));
   RPP_LAUNCH("gemm_proj_i8", s, linear_i8(ca, at<void>(layer, P.wo), nullptr, s1, at<float>(layer, P.so), nullptr,
                                            nullptr, h, RPP_F32, T_max, rows, H, H, EPI_DQ_ACC, err, s, hint));
   LnArgs l1 = ln_args(g1, be1);

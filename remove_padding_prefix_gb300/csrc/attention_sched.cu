@@ -69,12 +69,14 @@ size_t smem_bytes(int B) { return 1024 + kOffSched + sched_bytes(B); }
 // only the row maxima and sums, the second writes P's codes clamp(rne(127 P), 0, 127)
 // of the normalised softmax into tensor memory; S = Qc Kc^T and O = Pc Vc are then
 // exact integers in the fp32 accumulators, and O is written as fp16 O s_v / 127.
-template <typename T, bool I8>
+// QO: O leaves as the int8 codes clamp(rne(O / s_o), -127, 127) held in bf16, s_o in
+// device memory (the input quantisation of the output projection, fused).
+template <typename T, bool I8, bool QO>
 __global__ void __launch_bounds__(kThreads, 2)
 attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __restrict__ cu, int B, int T_max,
                        int max_len, int nh, int n_cls, void* __restrict__ out_v, float scale_log2,
-                       const float* __restrict__ i8_scales, int32_t* err) {
-  using TOut = typename std::conditional<I8, __half, T>::type;
+                       const float* __restrict__ i8_scales, const float* __restrict__ out_scale, int32_t* err) {
+  using TOut = typename std::conditional<QO, __nv_bfloat16, typename std::conditional<I8, __half, T>::type>::type;
   TOut* out = static_cast<TOut*>(out_v);
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -298,6 +300,8 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
       scale = scale_log2 * __ldg(i8_scales) * __ldg(i8_scales + 1);
       o_scale = __ldg(i8_scales + 2) / 127.0f;
     }
+    float inv_so = 0.f;   // 1 / s_o for the output codes
+    if constexpr (QO) inv_so = __fdiv_rn(1.0f, __ldg(out_scale));
     // this half's row maximum of S (keys past the sequence: -inf), in raw score units
     auto half_max = [&](int nv_h) -> float {
       float pm[4] = {neg_inf(), neg_inf(), neg_inf(), neg_inf()};
@@ -487,9 +491,14 @@ attention_sched_kernel(const __grid_constant__ CUtensorMap tm, const int32_t* __
                                                  32 * hf);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const float* f = reinterpret_cast<const float*>(ov + 8 * u);
-            orow[u] = make_uint4(pack2<TOut>(f[0] * inv, f[1] * inv), pack2<TOut>(f[2] * inv, f[3] * inv),
-                                 pack2<TOut>(f[4] * inv, f[5] * inv), pack2<TOut>(f[6] * inv, f[7] * inv));
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              f[e] = __uint_as_float(ov[8 * u + e]) * inv;
+              if constexpr (QO) f[e] = code_of(f[e], inv_so);
+            }
+            orow[u] = make_uint4(pack2<TOut>(f[0], f[1]), pack2<TOut>(f[2], f[3]), pack2<TOut>(f[4], f[5]),
+                                 pack2<TOut>(f[6], f[7]));
           }
         }
       }
@@ -521,9 +530,9 @@ bool attention_sched_supported(int B, int max_len) {
 
 namespace {
 
-template <typename T, bool I8>
+template <typename T, bool I8, bool QO>
 cudaError_t launch_sched(const CUtensorMap& tm, const int32_t* cu, int B, int T_max, int max_len, int nh, void* out,
-                         const float* i8_scales, int32_t* err, cudaStream_t stream) {
+                         const float* i8_scales, const float* out_scale, int32_t* err, cudaStream_t stream) {
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kDh));
   const int n_cls = (max_len + kT - 1) / kT;
   // persistent: two CTAs per SM, never more CTAs than the largest possible item count
@@ -532,20 +541,20 @@ cudaError_t launch_sched(const CUtensorMap& tm, const int32_t* cu, int B, int T_
   const size_t smem = smem_bytes(B);
   static size_t attr = 0;
   if (attr < smem) {
-    cudaError_t e = cudaFuncSetAttribute(attention_sched_kernel<T, I8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(attention_sched_kernel<T, I8, QO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem_bytes(kMaxB)));
     if (e != cudaSuccess) return e;
     attr = smem_bytes(kMaxB);
   }
-  return launch_pdl(attention_sched_kernel<T, I8>, dim3(grid), dim3(kThreads), smem, stream, tm, cu, B, T_max,
-                    max_len, nh, n_cls, out, scale_log2, i8_scales, err);
+  return launch_pdl(attention_sched_kernel<T, I8, QO>, dim3(grid), dim3(kThreads), smem, stream, tm, cu, B, T_max,
+                    max_len, nh, n_cls, out, scale_log2, i8_scales, out_scale, err);
 }
 
 }  // namespace
 
 cudaError_t launch_attention_sched(const void* qkv, const int32_t* cu, int B, int T_max, int max_len, int nh,
                                    rpp_dtype dtype, void* out, int32_t* err, cudaStream_t stream,
-                                   const float* i8_scales) {
+                                   const float* i8_scales, const float* out_scale) {
   if (B <= 0 || max_len <= 0 || T_max <= 0) return cudaSuccess;
   if (dtype != RPP_F16 && dtype != RPP_BF16) return cudaErrorNotSupported;
   if (i8_scales && dtype != RPP_BF16) return cudaErrorNotSupported;   // codes are held in bf16
@@ -554,9 +563,16 @@ cudaError_t launch_attention_sched(const void* qkv, const int32_t* cu, int B, in
   CUtensorMap tm;
   const CUtensorMapDataType dt = dtype == RPP_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   if (!make_tmap_2d(&tm, qkv, dt, 2, T_max, 3 * H, kT, kDh, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
-  if (i8_scales) return launch_sched<__nv_bfloat16, true>(tm, cu, B, T_max, max_len, nh, out, i8_scales, err, stream);
-  if (dtype == RPP_F16) return launch_sched<__half, false>(tm, cu, B, T_max, max_len, nh, out, nullptr, err, stream);
-  return launch_sched<__nv_bfloat16, false>(tm, cu, B, T_max, max_len, nh, out, nullptr, err, stream);
+  const float* q = i8_scales;
+  const float* so = out_scale;
+  if (q && so) return launch_sched<__nv_bfloat16, true, true>(tm, cu, B, T_max, max_len, nh, out, q, so, err, stream);
+  if (q) return launch_sched<__nv_bfloat16, true, false>(tm, cu, B, T_max, max_len, nh, out, q, so, err, stream);
+  if (dtype == RPP_F16) {
+    if (so) return launch_sched<__half, false, true>(tm, cu, B, T_max, max_len, nh, out, q, so, err, stream);
+    return launch_sched<__half, false, false>(tm, cu, B, T_max, max_len, nh, out, q, so, err, stream);
+  }
+  if (so) return launch_sched<__nv_bfloat16, false, true>(tm, cu, B, T_max, max_len, nh, out, q, so, err, stream);
+  return launch_sched<__nv_bfloat16, false, false>(tm, cu, B, T_max, max_len, nh, out, q, so, err, stream);
 }
 
 }  // namespace rpp

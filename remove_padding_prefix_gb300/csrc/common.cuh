@@ -36,6 +36,13 @@ template <> __device__ __forceinline__ float from_f32<float>(float v) { return v
 template <> __device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
 
+// symmetric int8 code of v at scale 1 / inv_s: clamp(rne(v * inv_s), -127, 127), one fp32
+// multiply (the per-tensor activation quantisation of the int8 flow)
+__device__ __forceinline__ float code_of(float v, float inv_s) {
+  const float q = rintf(__fmul_rn(v, inv_s));   // round half to even
+  return fminf(fmaxf(q, -127.f), 127.f);
+}
+
 // ---- packed fp32 pairs (f32x2: two lanes of one 64-bit register, one instruction)
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
   return static_cast<uint64_t>(__float_as_uint(lo)) | (static_cast<uint64_t>(__float_as_uint(hi)) << 32);

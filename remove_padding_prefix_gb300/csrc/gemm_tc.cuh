@@ -69,12 +69,6 @@ constexpr bool is_int_epi() {
   return (EPI >= EPI_I32 && EPI <= EPI_DQ_BIAS_GELU_Q) || EPI == EPI_DQ_BIAS_Q3;
 }
 
-__device__ __forceinline__ float code_of(float v, float inv_s) {
-  const float t = __fmul_rn(v, inv_s);
-  float q = rintf(t);   // round half to even
-  return fminf(fmaxf(q, -127.f), 127.f);
-}
-
 // TMA store of a 2D box from shared memory (bulk group)
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(

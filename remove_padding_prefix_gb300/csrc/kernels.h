@@ -133,10 +133,11 @@ bool make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dt, in
                   int cols, int box_rows, int box_cols, CUtensorMapSwizzle swz);
 // persistent longest-first tcgen05 varlen attention (S, P, O in tensor memory), head size 64
 bool attention_sched_supported(int B, int max_len);
-// i8_scales: device (s_q, s_k, s_v) for int8 codes held in bf16 (dtype RPP_BF16, fp16 out)
+// i8_scales: device (s_q, s_k, s_v) for int8 codes held in bf16 (dtype RPP_BF16, fp16 out);
+// out_scale: device s_o, the output leaves as bf16-held int8 codes of O / s_o
 cudaError_t launch_attention_sched(const void* qkv, const int32_t* cu, int B, int T_max, int max_len, int nh,
                                    rpp_dtype dtype, void* out, int32_t* err, cudaStream_t stream,
-                                   const float* i8_scales = nullptr);
+                                   const float* i8_scales = nullptr, const float* out_scale = nullptr);
 // tcgen05 varlen attention, head size 64, fp16 / bf16 (one CTA per 128 queries; batches
 // beyond the persistent kernel's limits)
 cudaError_t launch_attention_tc(const void* qkv, const int32_t* cu, int B, int T_max, int max_len, int nh,

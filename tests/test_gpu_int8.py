@@ -1,7 +1,9 @@
 """GPU parity of the INT8 path: weight and activation quantisation bit-exact, int32
 accumulators of the int8 GEMM bit-exact (including adversarial all-extreme inputs at
 the largest K), the calibration pass, the int8 encoder layer within the int8
-tolerance (5e-2 on final outputs), and the all-int8 flow: attention on codes (P's
+tolerance (5e-2 on final outputs; the attention writes the codes of its output, or a
+separate kernel quantises it beyond the persistent attention's limits), and the
+all-int8 flow: attention on codes (P's
 codes read back bit-exact where no code lies near a rounding tie, the output within
 the bound of a few flipped codes elsewhere) and the layer with int8 attention."""
 import numpy as np
@@ -121,6 +123,22 @@ def test_int8_layer_full_config_all_sequences():
     T = int(cu[-1])
     ref = oracle.bert_layer_int8(x[:T], cu, q, s, cfg.nh, cfg.eps)
     assert_close(got[:T], ref, "int8", "int8 layer, all 64 sequences")
+
+
+def test_int8_layer_beyond_persistent_attention_limits():
+    """2050 short sequences (beyond the persistent attention's 2048): the int8 layer takes
+    the one-CTA-per-query-tile attention and a separate quantisation of its output instead
+    of the codes written by the persistent kernel; every sequence against the oracle."""
+    import dataclasses
+    cfg = dataclasses.replace(INT8, H=128, nh=2, F=512)
+    rng = np.random.default_rng(2050)
+    lengths = rng.integers(0, 5, size=2050).astype(np.int32)
+    wl = make_bert_workload(cfg, B=2050, L=4, lengths=lengths, affine=True)
+    s = oracle.calibrate_int8(wl["x_padded"], wl["lengths"], wl["layers"][0], cfg.nh, cfg.eps)
+    got, cu, x = _int8_case(wl, s)
+    T = int(cu[-1])
+    ref = oracle.bert_layer_int8(x[:T], cu, oracle.prepare_int8_layer(wl["layers"][0]), s, cfg.nh, cfg.eps)
+    assert_close(got[:T], ref, "int8", "int8 layer, 2050 sequences")
 
 
 def test_calibration_matches_oracle():
