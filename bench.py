@@ -797,6 +797,19 @@ def main():
             torch.cuda.synchronize()
             return t0.elapsed_time(t1) / 1e3
         pipeline(3)
+
+        def copy_gbs(to_device):   # this host link's rate on one step's buffers, outside the timed region
+            ins, (yd, yh), _ = sets[0]
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            nbytes = 0
+            for hb, db in (ins if to_device else [(yh, yd)]):
+                (db.copy_(hb, non_blocking=True) if to_device else hb.copy_(db, non_blocking=True))
+                nbytes += hb.numel() * hb.element_size()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9
+        link = {"h2d_gbs": round(copy_gbs(True), 1), "d2h_gbs": round(copy_gbs(False), 1)}
         if world > 1:
             torch.distributed.barrier()
         e2e_s = reduce_max(pipeline(args.steps), world, dev)
@@ -804,7 +817,8 @@ def main():
         e2e = {"value": wk.tokens_per_step * args.steps * world / e2e_s, "unit": "tokens/s",
                "h2d_bytes_per_step": int(sum(hb.numel() * hb.element_size() for hb, _ in ins0)),
                "d2h_bytes_per_step": int(yh0.numel() * yh0.element_size()),
-               "copies": "on their own streams, overlapping the neighbouring steps' compute"}
+               "copies": "on their own streams, overlapping the neighbouring steps' compute",
+               "host_link": link}
         if not torch.equal(yh0.to(dev), wk.y):
             raise SystemExit("e2e output mismatch")
 
