@@ -452,7 +452,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (the leader's)
     if (lane == 0 && leader) {
-      uint32_t it = 0, acc_it = 0;
+      // The issuing thread's loop is on the tensor pipe's critical path: the stage and its
+      // phase advance incrementally, and a stage only moves the start-address field
+      // (16-byte units) of the first stage's descriptors.
+      uint32_t s = 0, ph = 0, acc_it = 0;
+      const uint64_t adesc0 = sw128_kmajor_desc(smem_u32(sA));
+      const uint64_t bdesc0 = sw128_kmajor_desc(smem_u32(sB));
       bool ok = true;
       for (int unit = cid; unit < total && ok; unit += ncl, ++acc_it) {
         const int tile = unit / S;
@@ -465,19 +470,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           break;
         }
         tc_fence_after();
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           const int chunk = NCH > 1 ? (kb - kb0) / kChunkBlocks : 0;
           const int kb_in = (kb - kb0) - chunk * kChunkBlocks;
           const uint32_t d_tmem = tmem_base + (a * NCH + chunk) * ACC;
-          const uint32_t s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1u;
           if (!mbar_wait_bounded(&full[s], ph, abort_flag, p.wait_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t adesc = sw128_kmajor_desc(smem_u32(sA + s * A_BYTES));
-          const uint64_t bdesc = sw128_kmajor_desc(smem_u32(sB + s * B_BYTES_AL));
+          const uint64_t adesc = adesc0 + s * (A_BYTES >> 4);
+          const uint64_t bdesc = bdesc0 + s * (B_BYTES_AL >> 4);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             // +32 bytes along K inside the swizzled 128-byte row = +2 in the address field
@@ -485,6 +488,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
           // the stage is free in every CTA of the pair once these MMAs are done
           tc_commit_cg<CL>(&empty[s], kPairMask);
+          if (++s == STAGES) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
         if (ok) tc_commit_cg<CL>(&tfull[a], kPairMask);
       }
