@@ -247,6 +247,14 @@ def test_attention_many_sequences_and_long_tile_counts():
     _attention_case("bf16", [1100, 5, 300], nh=2, seed=24, max_len=1100)
 
 
+def test_attention_at_the_persistent_kernels_key_limit():
+    """One 8192-token sequence, the most the persistent kernel takes (64 query tiles over
+    64 key tiles, lazy rescaling along whole rows), and an 8200-token one, which goes to the
+    one-CTA-per-query-tile kernel; both against the oracle."""
+    _attention_case("bf16", [8192], nh=1, seed=31, max_len=8192)
+    _attention_case("fp16", [8200, 3], nh=1, seed=32, max_len=8200)
+
+
 def test_attention_empty_and_zero_length_sequences():
     _attention_case("fp16", [0, 5, 0, 0, 70], nh=2, seed=3)
     _attention_case("fp16", [0, 0], nh=2, seed=4, max_len=8)
