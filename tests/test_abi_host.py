@@ -60,6 +60,12 @@ def test_argument_validation_returns_without_launching(lib):
     assert lib.rpp_gemm_i8_i32(None, None, None, 1, 16, 16, None, 0, None, None) == -1
     # misaligned activation pointer (odd address) is rejected before any launch
     assert lib.rpp_remove_padding(1, 16, 16, 1, 1, 8, 1, 32, None, None) == -1
+    # the exact int8 GEMM: K beyond four 1024-K chunks, or K / N off the 16 grid, is
+    # unsupported (checked before the pointers are used; these never reach the device)
+    unsupported = -2
+    assert lib.rpp_gemm_i8_i32(256, 256, 256, 1, 16, 4112, 256, 1 << 30, None, None) == unsupported
+    assert lib.rpp_gemm_i8_i32(256, 256, 256, 1, 16, 24, 256, 1 << 30, None, None) == unsupported
+    assert lib.rpp_gemm_i8_i32(256, 256, 256, 1, 24, 16, 256, 1 << 30, None, None) == unsupported
 
 
 def test_size_queries(lib):
