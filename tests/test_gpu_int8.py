@@ -12,11 +12,11 @@ import torch
 
 import oracle
 import remove_padding_prefix_gb300 as rpp
-from workloads import CONFIGS, make_bert_workload, make_calibration_batch, round_to_dtype
+from workloads import make_bert_workload, make_calibration_batch, round_to_dtype, config_by_name
 from gpu_util import dev, up, down, assert_close, check_err
 
 pytestmark = pytest.mark.gpu
-INT8 = CONFIGS[3]
+INT8 = config_by_name("bert_large_int8")
 
 
 @pytest.mark.parametrize("K,N", [(1024, 3072), (4096, 1024), (96, 48)])

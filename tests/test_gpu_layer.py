@@ -11,7 +11,7 @@ import torch
 
 import oracle
 import remove_padding_prefix_gb300 as rpp
-from workloads import CONFIGS, make_bert_workload, round_to_dtype
+from workloads import make_bert_workload, round_to_dtype, config_by_name
 from gpu_util import dev, up, down, assert_close, check_err, TOL
 
 pytestmark = pytest.mark.gpu
@@ -44,13 +44,13 @@ def _run_path(wl, dtype, layers=None, hint=False, poison=None):
 
 
 @pytest.mark.parametrize("hint", [False, True])
-@pytest.mark.parametrize("idx,B,L,lens", [
-    (0, 4, 64, None),                                  # tiny fp32 config as drawn
-    (1, 6, 128, [128, 1, 17, 64, 65, 100]),           # BERT-base shapes, fp16
-    (2, 3, 384, [384, 129, 33]),                       # BERT-large shapes, bf16
+@pytest.mark.parametrize("name,B,L,lens", [
+    ("tiny_fp32", 4, 64, None),                                  # tiny fp32 config as drawn
+    ("bert_base_fp16", 6, 128, [128, 1, 17, 64, 65, 100]),           # BERT-base shapes, fp16
+    ("bert_large_bf16_x24", 3, 384, [384, 129, 33]),                       # BERT-large shapes, bf16
 ])
-def test_layer_small(idx, B, L, lens, hint):
-    cfg = CONFIGS[idx]
+def test_layer_small(name, B, L, lens, hint):
+    cfg = config_by_name(name)
     wl = make_bert_workload(cfg, B=B, L=L, layers=1, lengths=None if lens is None else np.array(lens, np.int32),
                             affine=True)
     got, _ = _run_path(wl, cfg.dtype, hint=hint)
@@ -64,7 +64,7 @@ def test_layer_hidden_not_multiple_of_256(dtype):
     tile, so proj and FC2 (bias + residual epilogue, fp16 pre-LayerNorm sums) take
     narrower column tiles than the BERT shapes."""
     from dataclasses import replace
-    cfg = replace(CONFIGS[2], H=384, nh=6, F=1536, dtype=dtype, layers=1)
+    cfg = replace(config_by_name("bert_large_bf16_x24"), H=384, nh=6, F=1536, dtype=dtype, layers=1)
     wl = make_bert_workload(cfg, B=4, L=200, lengths=np.array([200, 3, 77, 130], np.int32), affine=True)
     for hint in (False, True):
         got, _ = _run_path(wl, dtype, hint=hint)
@@ -73,13 +73,14 @@ def test_layer_hidden_not_multiple_of_256(dtype):
 
 
 @pytest.mark.parametrize("hint", [False, True])
-@pytest.mark.parametrize("idx,lens", [(1, [128, 1, 17, 64, 65, 100]), (2, [384, 129, 33])])
-def test_layer_poisoned_workspace(idx, lens, hint):
+@pytest.mark.parametrize("name,lens", [("bert_base_fp16", [128, 1, 17, 64, 65, 100]),
+                                       ("bert_large_bf16_x24", [384, 129, 33])])
+def test_layer_poisoned_workspace(name, lens, hint):
     """Workspace bytes 0x47 (7.3 in fp16, 5.1e4 in bf16 and fp32) before the call: the
     unwritten capacity rows past the token count feed the attention's out-of-sequence
     query rows large values; the valid outputs match the oracle all the same."""
-    cfg = CONFIGS[idx]
-    wl = make_bert_workload(cfg, B=len(lens), L=max(lens) if idx == 1 else 384, layers=1,
+    cfg = config_by_name(name)
+    wl = make_bert_workload(cfg, B=len(lens), L=max(lens) if name == "bert_base_fp16" else 384, layers=1,
                             lengths=np.array(lens, np.int32), affine=True)
     got, _ = _run_path(wl, cfg.dtype, hint=hint, poison=0x47)
     ref, _, _ = oracle.bert_forward(wl["x_padded"], wl["lengths"], wl["layers"], cfg.nh, cfg.eps)
@@ -89,7 +90,7 @@ def test_layer_poisoned_workspace(idx, lens, hint):
 @pytest.mark.parametrize("mode", [1, 2])
 def test_layer_gemm_cluster_modes(mode):
     """The BERT-base layer with its GEMMs unpaired and always paired into clusters."""
-    cfg = CONFIGS[1]
+    cfg = config_by_name("bert_base_fp16")
     wl = make_bert_workload(cfg, B=6, L=128, layers=1, lengths=np.array([128, 1, 17, 64, 65, 100], np.int32),
                             affine=True)
     assert rpp.lib().rpp_set_gemm_cluster_mode(mode) == 0
@@ -102,7 +103,7 @@ def test_layer_gemm_cluster_modes(mode):
 
 
 def test_layer_all_lengths_zero_gives_zero_output():
-    cfg = CONFIGS[1]
+    cfg = config_by_name("bert_base_fp16")
     wl = make_bert_workload(cfg, B=3, L=16, layers=1, lengths=np.zeros(3, np.int32))
     got, _ = _run_path(wl, "fp16")
     assert np.all(got == 0)
@@ -111,7 +112,7 @@ def test_layer_all_lengths_zero_gives_zero_output():
 def test_bert_base_full_config():
     """The BERT-base-shaped fp16 layer (B=32, L=128) at full size (the bench workload), every
     output against the oracle."""
-    cfg = CONFIGS[1]
+    cfg = config_by_name("bert_base_fp16")
     wl = make_bert_workload(cfg)
     ref, _, _ = oracle.bert_forward(wl["x_padded"], wl["lengths"], wl["layers"], cfg.nh, cfg.eps)
     for hint in (True, False):
@@ -120,7 +121,7 @@ def test_bert_base_full_config():
 
 
 def test_tiny_fp32_full_config():
-    cfg = CONFIGS[0]
+    cfg = config_by_name("tiny_fp32")
     wl = make_bert_workload(cfg)
     got, _ = _run_path(wl, "fp32")
     ref, _, _ = oracle.bert_forward(wl["x_padded"], wl["lengths"], wl["layers"], cfg.nh, cfg.eps)
@@ -152,7 +153,7 @@ def test_bert_large_stack_all_sequences():
     size (max-abs and mean-abs ratios), a first-order bound on the final error is
     E = sum_l delta_l * prod_{k > l} G_k, taken separately for max-abs and mean-abs;
     the test allows 1.25 E for the terms beyond first order."""
-    cfg = CONFIGS[2]
+    cfg = config_by_name("bert_large_bf16_x24")
     wl = make_bert_workload(cfg)
     dtype = "bf16"
     ecfg = rpp.encoder_cfg(cfg.H, cfg.nh, cfg.F, cfg.eps, dtype, tokens_hint=int(wl["lengths"].sum()))
@@ -196,7 +197,7 @@ def test_captured_graph_replays_with_new_lengths():
     layers, rebuild) captured once and replayed with new lengths and new inputs written
     into the captured buffers: the token count lives in device memory, so every replay
     must match the oracle for its own lengths, with zero pad slots."""
-    cfg = CONFIGS[1]
+    cfg = config_by_name("bert_base_fp16")
     B, L = 6, 128
     wl = make_bert_workload(cfg, B=B, L=L, layers=2, affine=True)
     ecfg = rpp.encoder_cfg(cfg.H, cfg.nh, cfg.F, cfg.eps, "fp16", tokens_hint=B * L // 2)

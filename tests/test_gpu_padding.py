@@ -5,7 +5,7 @@ import torch
 
 import oracle
 import remove_padding_prefix_gb300 as rpp
-from workloads import CONFIGS, draw_lengths, make_bert_workload
+from workloads import CONFIGS, draw_lengths, make_bert_workload, config_by_name
 from gpu_util import dev, up, check_err, TDT
 
 pytestmark = pytest.mark.gpu
@@ -70,7 +70,7 @@ def test_remove_rebuild_bit_exact(dtype, H):
 
 
 def test_remove_padding_full_size_config():
-    cfg = CONFIGS[2]   # B=64, L=384, H=1024, bf16: the largest padded batch
+    cfg = config_by_name("bert_large_bf16_x24")   # B=64, L=384, H=1024, bf16: the largest padded batch
     wl = make_bert_workload(cfg, layers=1)
     cu, po, err = _offsets(wl["lengths"], cfg.L)
     x = up(wl["x_padded"].reshape(-1, cfg.H), "bf16")

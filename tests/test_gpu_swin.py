@@ -8,11 +8,11 @@ import torch
 
 import oracle
 import remove_padding_prefix_gb300 as rpp
-from workloads import CONFIGS, make_swin_workload, round_to_dtype
+from workloads import make_swin_workload, round_to_dtype, config_by_name
 from gpu_util import dev, up, down, assert_close, check_err
 
 pytestmark = pytest.mark.gpu
-SWIN = CONFIGS[4]
+SWIN = config_by_name("swin_t_stage1_fp16")
 
 
 def _cfg(I=56, s=3, dtype="fp16"):

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import oracle
-from workloads import CONFIGS, make_bert_workload
+from workloads import make_bert_workload, config_by_name
 
 torch.set_grad_enabled(False)
 
@@ -150,7 +150,7 @@ def _torch_layer(layer, H, nh, F, eps):
 
 @pytest.mark.parametrize("affine", [False, True])
 def test_bert_layer_matches_torch_encoder_layer_on_padded_batch(affine):
-    cfg = CONFIGS[0]
+    cfg = config_by_name("tiny_fp32")
     wl = make_bert_workload(cfg, B=3, L=20, affine=affine, lengths=np.array([20, 7, 1]))
     layer = wl["layers"][0]
     y_pad, cu, po = oracle.bert_forward(wl["x_padded"], wl["lengths"], wl["layers"], cfg.nh, cfg.eps)
@@ -163,7 +163,7 @@ def test_bert_layer_matches_torch_encoder_layer_on_padded_batch(affine):
 
 
 def test_bert_layer_padding_removal_changes_nothing_and_sequences_independent():
-    cfg = CONFIGS[0]
+    cfg = config_by_name("tiny_fp32")
     wl = make_bert_workload(cfg, B=4, L=16, lengths=np.array([16, 3, 9, 12]))
     x = wl["x_padded"].copy()
     valid = np.arange(16)[None, :] < wl["lengths"][:, None]

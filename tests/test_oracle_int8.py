@@ -12,9 +12,9 @@ import numpy as np
 import pytest
 
 import oracle
-from workloads import CONFIGS, make_bert_workload, make_calibration_batch
+from workloads import make_bert_workload, make_calibration_batch, config_by_name
 
-INT8 = CONFIGS[3]
+INT8 = config_by_name("bert_large_int8")
 
 
 def test_weight_quantisation_properties():

@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 import oracle
-from workloads import CONFIGS, make_bert_workload, draw_lengths
+from workloads import CONFIGS, make_bert_workload, draw_lengths, config_by_name
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -86,7 +86,7 @@ def test_remove_rebuild_round_trips():
 
 
 def test_remove_padding_on_a_config_workload():
-    wl = make_bert_workload(CONFIGS[0])
+    wl = make_bert_workload(config_by_name("tiny_fp32"))
     cfg = wl["cfg"]
     cu, po, T = oracle.build_offsets(wl["lengths"], cfg.L)
     packed = oracle.remove_padding(wl["x_padded"], po)

@@ -12,10 +12,10 @@ import pytest
 import torch
 
 import oracle
-from workloads import CONFIGS, make_swin_workload
+from workloads import make_swin_workload, config_by_name
 
 torch.set_grad_enabled(False)
-SWIN = CONFIGS[4]
+SWIN = config_by_name("swin_t_stage1_fp16")
 
 
 def test_shift_matches_torch_roll_and_inverts():
