@@ -752,6 +752,10 @@ cudaError_t dispatch_float(int bn, int epi, rpp_dtype out_dtype, rpp_dtype res_d
     case RPP_EPI_BIAS_RESIDUAL:
       if (out_dtype == RPP_F32 && res_dtype == RPP_F32)
         return dispatch_bn<T, float, float, RPP_EPI_BIAS_RESIDUAL, 1, CL>(bn, ta, tb, p, gr, stream);
+      if constexpr (!std::is_same<T, __half>::value) {
+        if (out_dtype == RPP_F32 && res_dtype == RPP_F16)
+          return dispatch_bn<T, float, __half, RPP_EPI_BIAS_RESIDUAL, 1, CL>(bn, ta, tb, p, gr, stream);
+      }
       if (out_dtype == RPP_F32)
         return dispatch_bn<T, float, T, RPP_EPI_BIAS_RESIDUAL, 1, CL>(bn, ta, tb, p, gr, stream);
       if (out_dtype == RPP_F16 && res_dtype == RPP_F16)

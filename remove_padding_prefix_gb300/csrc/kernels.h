@@ -60,6 +60,7 @@ struct LnArgs {
   void* y = nullptr;
   rpp_dtype out_dtype = RPP_F32;
   float* y32 = nullptr;
+  __half* y16 = nullptr;       // fp16 copy of y (streaming kernel only)
   void* q_codes = nullptr;
   const float* q_scale = nullptr;
   float* amax = nullptr;

@@ -391,7 +391,7 @@ __global__ void amax_kernel(const T* __restrict__ x, int M_max, const int32_t* r
 // (lane l holds the 16-byte vectors l, l + 32, ...), the next row's vectors in flight
 // while this one is normalised, and the arithmetic on packed fp32 pairs (one f32x2
 // instruction per two elements).  Statistics as in the general kernel: fp32, two passes
-// over the registers, biased variance.  Optional fp32 copy of the output, and the
+// over the registers, biased variance.  Optional fp32 or fp16 copy of the output, and the
 // padded-output mode of the general kernel.
 constexpr int kLnsThreads = 256;
 
@@ -535,6 +535,7 @@ __global__ void __launch_bounds__(kLnsThreads) ln_stream_kernel(LnArgs a) {
         for (int j = 0; j < EPV; j += 4)
           *reinterpret_cast<float4*>(yf + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
       }
+      if (a.y16) store_vec<__half, EPV>(a.y16 + static_cast<size_t>(it) * H + col0, o);
     }
     src = src_next;
   }
